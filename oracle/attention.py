@@ -1,0 +1,50 @@
+"""Scaled dot-product causal attention over ONE isolated sequence, float64.
+
+Test infrastructure only.
+
+Definition (Flex, "Request-Adaptive Execution for Efficient Hybrid LLM
+Inference", section 2, Eq. 1: softmax(Q K^T / sqrt(d_h)) V; Flide, section
+3.2.1: in the isolated sequence s (+) q_i a token sees every token at or
+before its position): for query row t and head h,
+
+    o[t, h] = sum_{u <= t} softmax_u( scale * q[t, h] . k[u, g] ) v[u, g]
+
+with g = floor(h / (Hq / Hkv)) (grouped-query heads share a key/value head;
+the pages name grouped heads but no mapping -- consecutive query heads share
+one key/value head).  The softmax subtracts the row maximum before exp.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def causal_attention(q, k, v, scale: float, rows=None, window: int | None = None):
+    """q [n, Hq, d]; k, v [n, Hkv, d]; returns o [len(rows), Hq, d] float64.
+
+    ``rows``: indices t of the query rows to produce (default: all).  A query
+    row t only reads q[t]; keys/values 0..t are read.  ``window``: optional
+    sliding width W (Flide, section 3.2.1: adds t_x - t_y < W).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    assert hq % hkv == 0
+    g = hq // hkv
+    if rows is None:
+        rows = range(n)
+    rows = list(rows)
+    out = np.empty((len(rows), hq, d), dtype=np.float64)
+    for o_i, t in enumerate(rows):
+        lo = 0 if window is None else max(0, t - window + 1)
+        kk = k[lo:t + 1]                         # [u, Hkv, d]
+        vv = v[lo:t + 1]
+        qt = q[t].reshape(hkv, g, d)             # [Hkv, G, d]
+        s = np.einsum("hgd,uhd->hgu", qt, kk) * scale
+        m = s.max(axis=-1, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=-1, keepdims=True)
+        o = np.einsum("hgu,uhd->hgd", p, vv) / l
+        out[o_i] = o.reshape(hq, d)
+    return out
