@@ -1,0 +1,428 @@
+"""Tree-prefill benchmark: ForkAttention + Gated DeltaNet fork prefill on GB300.
+
+One step = one pass of the whole hot path over one round of synthetic input:
+  host round build (C++) -> metadata upload -> KV page write -> ForkAttention
+  -> option log-probs at the readout rows -> GDN chunk-local pass -> GDN
+  level passes (trunk, then branches from the trunk's end state, which is
+  also saved as a checkpoint).
+Workload: the attention tree (trunk 4096 + 8 branches of U[16,64] tokens,
+GQA 32/8, d=128, page 16, bf16, 4 options over the concatenated heads) and
+the GDN tree (trunk 8192 + 16 branches of U[8,128], 16 heads, d=128,
+chunk 64, fp32 state, bf16 inputs).  Tokens = trunk + sum of branches, each
+counted once, for both trees.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Prints ONE JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ATTN = dict(hq=32, hkv=8, d=128, seed=2000)
+GDN = dict(h=16, d=128, seed=3000)
+WORKLOAD = ("fork_attn trunk4096+8br U[16,64] GQA32/8 d128 page16 bf16 + 4-option readout; "
+            "gdn_fork trunk8192+16br U[8,128] H16 d128 chunk64 fp32-state bf16")
+N_OPT = 4
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workload description and algorithmic work
+# ---------------------------------------------------------------------------
+def trees():
+    return synth.attn_tree(), synth.gdn_tree()
+
+
+def attn_pairs(tree) -> int:
+    """Visible (query, key) pairs per head: trunk P(P+1)/2, branch rows see
+    the trunk and their own prefix (Flide Eq. 3)."""
+    tot = 0
+    for req in tree.requests:
+        P = req.n_tok[0]
+        tot += P * (P + 1) // 2
+        for l in req.n_tok[1:]:
+            tot += l * P + l * (l + 1) // 2
+    return tot
+
+
+def attn_flops(tree) -> float:
+    return attn_pairs(tree) * ATTN["hq"] * 4.0 * ATTN["d"]
+
+
+def attn_bytes(tree) -> float:
+    T = tree.useful_tokens()
+    e = 2  # bf16
+    q_o = 2 * T * ATTN["hq"] * ATTN["d"] * e
+    kv = 2 * T * ATTN["hkv"] * ATTN["d"] * e   # pages read once
+    return q_o + kv
+
+
+def gdn_bytes(tree) -> float:
+    T = tree.useful_tokens()
+    h, d = GDN["h"], GDN["d"]
+    n_br = sum(r.n_nodes - 1 for r in tree.requests)
+    qkvo = 4 * T * h * d * 2
+    ab = 2 * T * h * 4
+    states = (n_br + 1) * h * d * d * 4      # branch init reads + the trunk end-state write
+    return qkvo + ab + states
+
+
+# ---------------------------------------------------------------------------
+# clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                out, _ = self.p.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Step:
+    """Device buffers of one input set and the step through the C ABI."""
+
+    def __init__(self, torch, api, rounds, at, gt, a_inp, g_inp, W, n_sets=2):
+        self.torch, self.api, self.rounds = torch, api, rounds
+        dev = "cuda"
+        self.at, self.gt = at, gt
+        # layout once (host) to place inputs in stream order; every step rebuilds the round
+        pool = api.PagePool(at.useful_tokens() // 16 + 64)
+        R, seg = rounds.build_round(at, pool)
+        self.a_T = R.info().n_tokens
+        a_stream = {k: rounds.to_stream(R, seg, a_inp.nodes, k) for k in ("q", "k", "v")}
+        R2, seg2 = rounds.build_round(gt, None, temp_slot0=1, n_temp_slots=4)
+        g_stream = {k: rounds.to_stream(R2, seg2, g_inp.nodes, k) for k in ("q", "k", "v", "alpha", "beta")}
+        self.g_T = R2.info().n_tokens
+        self.a_caps, self.g_caps = R.caps, R2.caps
+        del R, R2
+        bf = torch.bfloat16
+        self.host = {}   # pinned host copies for the end-to-end timing
+        for k, a in a_stream.items():
+            self.host["a_" + k] = torch.from_numpy(a).to(bf).pin_memory()
+        for k, a in g_stream.items():
+            t = torch.from_numpy(a)
+            self.host["g_" + k] = (t if k in ("alpha", "beta") else t.to(bf)).pin_memory()
+        self.sets = []
+        for _ in range(n_sets):
+            s = {k: v.to(dev) for k, v in self.host.items()}
+            s["a_out"] = torch.empty_like(s["a_q"])
+            s["g_out"] = torch.empty_like(s["g_v"])
+            self.sets.append(s)
+        self.n_pages = self.a_T // 16 + 64
+        self.pool = api.PagePool(self.n_pages)
+        self.k_pages = torch.zeros((self.n_pages, ATTN["hkv"], 16, ATTN["d"]), dtype=bf, device=dev)
+        self.v_pages = torch.zeros_like(self.k_pages)
+        self.state = torch.zeros((8, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.float32, device=dev)
+        self.a_meta = torch.empty(api.Round(self.a_caps).meta_bytes() // 4, dtype=torch.int32, device=dev)
+        self.g_meta = torch.empty(api.Round(self.g_caps).meta_bytes() // 4, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(api.gdn_workspace_bytes(self.g_caps, GDN["h"], GDN["d"], GDN["d"]),
+                              dtype=torch.uint8, device=dev)
+        self.W = torch.from_numpy(W).to(dev)
+        n_ro = sum(r.n_nodes - 1 for r in at.requests)
+        self.lp = torch.empty((n_ro, N_OPT), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+        self.ev_attn = []
+
+    def build(self):
+        """Host round build (C++) for both trees; the GDN trunk saves its end
+        state into slot 0 as the checkpoint a later round resumes from."""
+        R_a, _ = self.rounds.build_round(self.at, self.pool, caps=self.a_caps)
+        self.gt.requests[0].save = {0: 0}
+        R_g, _ = self.rounds.build_round(self.gt, None, caps=self.g_caps, temp_slot0=1, n_temp_slots=4)
+        return R_a, R_g
+
+    def run(self, i: int, time_attn: bool = False):
+        api, s = self.api, self.sets[i % len(self.sets)]
+        R_a, R_g = self.build()
+        R_a.upload(self.a_meta)
+        R_g.upload(self.g_meta)
+        api.kv_page_write(self.a_caps, self.a_meta, s["a_k"], s["a_v"], self.k_pages, self.v_pages, self.status)
+        if time_attn:
+            e0 = self.torch.cuda.Event(enable_timing=True)
+            e1 = self.torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+        api.fork_attn(self.a_caps, self.a_meta, s["a_q"], self.k_pages, self.v_pages, s["a_out"], self.status)
+        if time_attn:
+            e1.record(self.stream)
+            self.ev_attn.append((e0, e1))
+        api.choice_logprobs(self.a_caps, self.a_meta, s["a_out"].view(s["a_out"].shape[0], -1), self.W, self.lp,
+                            self.status)
+        api.gdn_fork_prefill(self.g_caps, self.g_meta, s["g_q"], s["g_k"], s["g_v"], s["g_alpha"], s["g_beta"],
+                             self.state, s["g_out"], self.ws, self.status)
+        R_a.release(self.pool)
+        return R_a, R_g
+
+    def run_e2e(self, i: int):
+        """Same step from pinned host buffers: H2D of the inputs, the step,
+        D2H of the outputs (attention rows, GDN rows, log-probs)."""
+        s = self.sets[i % len(self.sets)]
+        h2d = 0
+        for k, v in self.host.items():
+            s[k].copy_(v, non_blocking=True)
+            h2d += v.numel() * v.element_size()
+        self.run(i)
+        outs = [s["a_out"].to("cpu", non_blocking=True), s["g_out"].to("cpu", non_blocking=True),
+                self.lp.to("cpu", non_blocking=True)]
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        return h2d, d2h
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max(torch, x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(values_per_rank, units_per_rank):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return sum(units_per_rank) / max(values_per_rank)
+
+
+def cpu_baseline(at, gt, a_inp, g_inp, budget_s: float = 12.0):
+    """The fp64 oracle timed on a bounded sample of the same workload and
+    extrapolated to the whole step: sampled trunk rows + one branch of the
+    attention tree, and a run of GDN recurrence steps (16 heads); the oracle
+    recomputes the trunk for every branch (isolated passes)."""
+    from oracle import attention as oattn
+    from oracle import forward, gdn as ogdn
+    t_cpu0, t0 = time.process_time(), time.perf_counter()
+    scale = 1 / math.sqrt(ATTN["d"])
+    req = at.requests[0]
+    P = req.n_tok[0]
+    rows = [int(x) for x in np.linspace(0, P - 1, 32)]
+    ta = time.perf_counter()
+    forward.attention_tree(at, a_inp, scale, nodes=[(0, 0)], rows={(0, 0): rows})
+    t_rows = (time.perf_counter() - ta) / len(rows)        # mean over positions ~ uniform
+    tb = time.perf_counter()
+    forward.attention_tree(at, a_inp, scale, nodes=[(0, 1)])
+    t_br = (time.perf_counter() - tb) / req.n_tok[1]       # per branch row (each sees ~P keys)
+    attn_est = t_rows * P + t_br * sum(req.n_tok[1:])
+    g = gt.requests[0]
+    tr = g_inp.nodes[(0, 0)]
+    n_steps = 256
+    tg = time.perf_counter()
+    ogdn.gated_delta_rule(tr["q"][:n_steps], tr["k"][:n_steps], tr["v"][:n_steps], tr["alpha"][:n_steps],
+                          tr["beta"][:n_steps])
+    t_step = (time.perf_counter() - tg) / n_steps
+    gdn_steps = g.n_tok[0] + sum(g.n_tok[0] + l for l in g.n_tok[1:])   # trunk alone + each isolated branch
+    gdn_est = t_step * gdn_steps
+    wall = time.perf_counter() - t0
+    cores = max(1, round((time.process_time() - t_cpu0) / max(wall, 1e-9)))
+    tokens = at.useful_tokens() + gt.useful_tokens()
+    del oattn
+    return {"value": tokens / (attn_est + gdn_est), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 oracle, {len(rows)} trunk rows + all {req.n_tok[1]} rows of one branch of the "
+                       f"attention tree, {n_steps} GDN recurrence steps (16 heads); extrapolated to the step "
+                       f"({attn_est:.1f} s attention + {gdn_est:.1f} s GDN, isolated passes); "
+                       f"sampling took {wall:.1f} s")}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    at, gt = trees()
+    a_inp = synth.attn_inputs(at, ATTN["hq"], ATTN["hkv"], ATTN["d"], seed=ATTN["seed"], bf16=True)
+    g_inp = synth.gdn_inputs(gt, GDN["h"], GDN["d"], GDN["d"], seed=GDN["seed"], bf16=True, law="softplus")
+    vals = []
+    for i in range(args.warmup + args.steps):
+        b = cpu_baseline(at, gt, a_inp, g_inp)
+        if i >= args.warmup:
+            vals.append(b)
+    v = statistics.median(x["value"] for x in vals)
+    line = {"metric": "tree-prefill tokens/s (ForkAttn + GDN)", "value": v, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (at.useful_tokens() +
+                                                                              gt.useful_tokens()) / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"kind": "oracle", "cores": vals[-1]["cores"], "sample": vals[-1]["sample"],
+                             "value": v, "unit": "tokens/s"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    from hybrid_serving_gb300 import _lib, api, rounds
+
+    at, gt = trees()
+    a_inp = synth.attn_inputs(at, ATTN["hq"], ATTN["hkv"], ATTN["d"], seed=ATTN["seed"], bf16=True)
+    g_inp = synth.gdn_inputs(gt, GDN["h"], GDN["d"], GDN["d"], seed=GDN["seed"], bf16=True, law="softplus")
+    W = synth.option_rows(N_OPT, ATTN["hq"] * ATTN["d"], seed=ATTN["seed"] + 1)
+    step = Step(torch, api, rounds, at, gt, a_inp, g_inp, W)
+    tokens = at.useful_tokens() + gt.useful_tokens()
+
+    for i in range(args.warmup):
+        step.run(i)
+    torch.cuda.synchronize()
+    api.check_status(step.status)
+
+    # ---- device-timed region: K steps, inputs resident, 2 rotating input sets ----
+    n0 = _lib.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    step.ev_attn = []
+    barrier(ws)
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(step.stream)
+            step.run(i, time_attn=True)
+            ev[i][1].record(step.stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(ws)
+    launches = _lib.launch_count() - n0          # kernels launched inside the timed region
+    api.check_status(step.status)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in step.ev_attn)
+    total_ms = reduce_max(torch, sum(step_ms), ws)
+    ms_per_step = total_ms / args.steps
+    value = ws * tokens * args.steps / (total_ms / 1e3)
+
+    # ---- end to end from pinned host buffers ----
+    for i in range(2):
+        step.run_e2e(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(step.stream)
+    h2d = d2h = 0
+    for i in range(args.steps):
+        h2d, d2h = step.run_e2e(i)
+    e1.record(step.stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(torch, e0.elapsed_time(e1), ws)
+    e2e_value = ws * tokens * args.steps / (e2e_ms / 1e3)
+
+    pk, pk_kind = peaks()
+    fl = attn_flops(at)
+    achieved = fl / (attn_ms / 1e3) / 1e12
+    peak = pk["bf16_tflops"]
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "kernel": "fork_attn", "peak_kind": f"{pk_kind} bf16 dense burst",
+            "flops_per_launch": fl, "ms_per_launch": round(attn_ms, 4)}
+    line = {"metric": "tree-prefill tokens/s (ForkAttn + GDN)", "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": tokens,
+                       "l2": "inputs > L2: 2 rotating input sets (~0.9 GB touched per step)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": roof,
+            "kernels": {"fork_attn_ms": round(attn_ms, 4),
+                        "gdn_bytes_per_step": gdn_bytes(gt), "attn_bytes_per_step": attn_bytes(at)},
+            "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches), "clocks": clk.summary(), "wall_s": round(wall, 4)}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(at, gt, a_inp, g_inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

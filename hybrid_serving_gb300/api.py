@@ -1,0 +1,211 @@
+"""Python face of the C ABI (include/hs.h), same names without the ``hs_``
+prefix.  Argument marshalling only: tensors are passed as device pointers,
+shapes are read off the tensors, every step runs in libhsfork.so.
+
+Device memory and streams come from PyTorch; nothing here computes.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import Caps, HsError, RoundInfo, SegmentInfo, check, lib
+
+PAGE = 16
+CHUNK = 64
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.HS_BF16
+    if t.dtype == torch.float32:
+        return _lib.HS_F32
+    raise HsError(_lib.HS_EUNSUPPORTED, f"dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _i32arr(xs: Sequence[int]):
+    return (C.c_int32 * max(1, len(xs)))(*xs)
+
+
+def round_caps_for(n_tokens: int, n_segments: int, n_levels: int, n_hist_spans: int = 0,
+                   n_hist_pages: int = 0, page_size: int = PAGE) -> Caps:
+    c = Caps()
+    check(lib.hs_round_caps_for(n_tokens, n_segments, n_levels, n_hist_spans, n_hist_pages, page_size,
+                                C.byref(c)))
+    return c
+
+
+class PagePool:
+    """Host bookkeeping of a caller-owned KV page pool (refcounted pages)."""
+
+    def __init__(self, n_pages: int, page_size: int = PAGE):
+        self._h = C.c_void_p()
+        check(lib.hs_page_pool_create(n_pages, page_size, C.byref(self._h)))
+        self.n_pages = n_pages
+        self.page_size = page_size
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            lib.hs_page_pool_destroy(self._h)
+            self._h = None
+
+    def stats(self):
+        f, l = C.c_int32(), C.c_int32()
+        check(lib.hs_page_pool_stats(self._h, C.byref(f), C.byref(l)))
+        return f.value, l.value
+
+    def refcount(self, page: int) -> int:
+        r = C.c_int32()
+        check(lib.hs_page_pool_refcount(self._h, page, C.byref(r)))
+        return r.value
+
+    def decref(self, pages: Sequence[int]):
+        check(lib.hs_page_pool_decref(self._h, _i32arr(pages), len(pages)))
+
+
+class Round:
+    """A round of request trees flattened into one stream (hs_round)."""
+
+    def __init__(self, caps: Caps):
+        self.caps = caps
+        self._h = C.c_void_p()
+        check(lib.hs_round_create(C.byref(caps), C.byref(self._h)))
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            lib.hs_round_destroy(self._h)
+            self._h = None
+
+    def add_segment(self, parent: int, n_tokens: int, flags: int = 0, save_slot: int = -1) -> int:
+        s = C.c_int32()
+        check(lib.hs_round_add_segment(self._h, parent, n_tokens, flags, save_slot, C.byref(s)))
+        return s.value
+
+    def gdn_state_resume(self, seg: int, ckpt_slot: int, ckpt_pos: int):
+        check(lib.hs_gdn_state_resume(self._h, seg, ckpt_slot, ckpt_pos))
+
+    def attach_history(self, seg: int, ntok: Sequence[int], pages: Sequence[int]):
+        check(lib.hs_round_attach_history(self._h, seg, len(ntok), _i32arr(ntok), _i32arr(pages)))
+
+    def finalize(self, pool: Optional[PagePool], temp_slot0: int = 0, n_temp_slots: int = 0):
+        check(lib.hs_round_finalize(self._h, pool._h if pool is not None else None, temp_slot0, n_temp_slots))
+
+    def meta_bytes(self) -> int:
+        return int(lib.hs_round_meta_bytes(C.byref(self.caps)))
+
+    def pack(self) -> "torch.Tensor":
+        n = self.meta_bytes()
+        out = torch.empty(n // 4, dtype=torch.int32)
+        check(lib.hs_round_pack(self._h, out.data_ptr(), n))
+        return out
+
+    def upload(self, dev_meta: torch.Tensor, stream=None):
+        check(lib.hs_round_upload(self._h, dev_meta.data_ptr(), dev_meta.numel() * dev_meta.element_size(),
+                                  _stream(stream)))
+
+    def info(self) -> RoundInfo:
+        i = RoundInfo()
+        check(lib.hs_round_get_info(self._h, C.byref(i)))
+        return i
+
+    def segment(self, seg: int) -> SegmentInfo:
+        s = SegmentInfo()
+        check(lib.hs_round_segment(self._h, seg, C.byref(s)))
+        return s
+
+    def segment_pages(self, seg: int):
+        n = C.c_int32()
+        check(lib.hs_round_segment_pages(self._h, seg, None, 0, C.byref(n)))
+        buf = (C.c_int32 * max(1, n.value))()
+        check(lib.hs_round_segment_pages(self._h, seg, buf, n.value, C.byref(n)))
+        return list(buf[:n.value])
+
+    def readout_rows(self):
+        n = C.c_int32()
+        check(lib.hs_round_readout_rows(self._h, None, 0, C.byref(n)))
+        buf = (C.c_int32 * max(1, n.value))()
+        check(lib.hs_round_readout_rows(self._h, buf, n.value, C.byref(n)))
+        return list(buf[:n.value])
+
+    def release(self, pool: PagePool, keep: Sequence[int] = ()):
+        check(lib.hs_round_release(self._h, pool._h, _i32arr(keep), len(keep)))
+
+
+# ---------------------------------------------------------------------------
+# hot path
+# ---------------------------------------------------------------------------
+def fork_attn_prefill(caps: Caps, dev_meta: torch.Tensor, q, k_new, v_new, k_pages, v_pages, out,
+                      dev_status: torch.Tensor, scale: Optional[float] = None, stream=None):
+    """q [T,hq,d], k_new/v_new [T,hkv,d], k_pages/v_pages [n_pages,hkv,16,d], out [T,hq,d]."""
+    T, hq, d = q.shape
+    hkv = k_new.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    check(lib.hs_fork_attn_prefill(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, q.data_ptr(),
+                                   k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                   k_pages.shape[0], out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+
+
+def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_pages, dev_status: torch.Tensor,
+                  stream=None):
+    T, hkv, d = k_new.shape
+    check(lib.hs_kv_page_write(C.byref(caps), dev_meta.data_ptr(), _dt(k_new), hkv, d, k_new.data_ptr(),
+                               v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[0],
+                               dev_status.data_ptr(), _stream(stream)))
+
+
+def fork_attn(caps: Caps, dev_meta: torch.Tensor, q, k_pages, v_pages, out, dev_status: torch.Tensor,
+              scale: Optional[float] = None, stream=None):
+    T, hq, d = q.shape
+    hkv = k_pages.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    check(lib.hs_fork_attn(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, q.data_ptr(),
+                           k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[0], out.data_ptr(),
+                           dev_status.data_ptr(), _stream(stream)))
+
+
+def gdn_workspace_bytes(caps: Caps, h: int, dk: int, dv: int) -> int:
+    return int(lib.hs_gdn_workspace_bytes(C.byref(caps), h, dk, dv))
+
+
+def gdn_fork_prefill(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha, beta, state_pool, out, ws,
+                     dev_status: torch.Tensor, chunk: int = CHUNK, stream=None):
+    """q,k [T,h,dk], v [T,h,dv], alpha,beta [T,h] fp32, state_pool [slots,h,dv,dk] fp32, out [T,h,dv]."""
+    T, h, dk = q.shape
+    dv = v.shape[2]
+    check(lib.hs_gdn_fork_prefill(C.byref(caps), dev_meta.data_ptr(), _dt(q), h, dk, dv, chunk, q.data_ptr(),
+                                  k.data_ptr(), v.data_ptr(), alpha.data_ptr(), beta.data_ptr(),
+                                  state_pool.data_ptr(), state_pool.shape[0], out.data_ptr(), ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), dev_status.data_ptr(), _stream(stream)))
+
+
+def gdn_state_checkpoint(state_pool, src_slot: int, dst_slot: int, stream=None):
+    n, h, dv, dk = state_pool.shape
+    check(lib.hs_gdn_state_checkpoint(state_pool.data_ptr(), n, src_slot, dst_slot, h, dk, dv, _stream(stream)))
+
+
+def choice_logprobs(caps: Caps, dev_meta: torch.Tensor, hidden, option_rows, logprobs,
+                    dev_status: torch.Tensor, stream=None):
+    """hidden [T, dim] (a strided 2-D view is fine), option_rows [n_opt, dim] fp32, logprobs [n_ro, n_opt]."""
+    dim = hidden.shape[1]
+    check(lib.hs_choice_logprobs(C.byref(caps), dev_meta.data_ptr(), _dt(hidden), hidden.data_ptr(),
+                                 hidden.stride(0), dim, option_rows.data_ptr(), option_rows.shape[0],
+                                 logprobs.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+
+
+def check_status(dev_status: torch.Tensor):
+    w = C.c_int32(int(dev_status.item()))
+    check(lib.hs_check_status(C.byref(w)))

@@ -1,0 +1,383 @@
+// gdn.cu -- Gated DeltaNet fork prefill in chunks, and state checkpoints.
+//
+// Flide, "Accelerating Decision Inference with Exact State Forking":
+//   section 3.2.2, Eq. 4 -- S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T)
+//     + beta_t v_t k_t^T, o_t = S_t q_t; state segments run first, then each
+//     question continues from its request's end-of-state S_P through an
+//     index, without copying;
+//   section 3.3.1 -- a fixed-length chunk list built per round;
+//   section 3.4 -- the state at a checkpoint is the end state of the first
+//     of two levels, saved during the same pass; a resumed state starts from
+//     the saved slot;
+//   section 3.5 -- every question's chunks start at the fork.
+//
+// Chunked form (gated delta rule regrouped by chunk of C <= 64 tokens, from
+// the state S0 at the chunk start; g = cumulative sum of log alpha inside the
+// chunk):
+//   A_ts = beta_t e^{g_t-g_s} k_t.k_s (s<t),   P_ts = e^{g_t-g_s} q_t.k_s (s<=t)
+//   (I + A) [W | Ut] = [diag(beta e^g) K | diag(beta) V]
+//   U = Ut - W S0^T;  O = diag(e^g) Q S0^T + P U;  S = e^{g_C} S0 + U^T diag(e^{g_C-g}) K
+// Phase A (all chunks of all levels in parallel) builds W, Ut, P, g; phase B
+// walks each node's chunks in order, one launch per tree level, split over
+// d_v slices (rows of S evolve independently, so the split is exact).
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+
+using namespace hsm;
+using hsd::Meta;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDvSlice = 16;
+
+template <int DK, int DV>
+struct WsLayout {
+  static constexpr size_t W = 0;
+  static constexpr size_t UT = W + (size_t)kChunk * DK;
+  static constexpr size_t P = UT + (size_t)kChunk * DV;
+  static constexpr size_t G = P + (size_t)kChunk * kChunk;
+  static constexpr size_t FLOATS = G + kChunk;  // per (chunk, head)
+};
+
+__host__ __device__ inline size_t ws_floats_per(int dk, int dv) {
+  return (size_t)kChunk * dk + (size_t)kChunk * dv + (size_t)kChunk * kChunk + kChunk;
+}
+
+// Load `len` rows of a [T, H, D] tensor (head h) into smem rows of stride
+// `ld` as fp32; rows >= len are zero.
+template <typename T, int D>
+__device__ __forceinline__ void load_rows(float* dst, int ld, const T* __restrict__ src, int row0, int len, int H,
+                                          int h) {
+  constexpr int VEC = 16 / sizeof(T);
+  for (int e = threadIdx.x; e < kChunk * (D / VEC); e += blockDim.x) {
+    const int r = e / (D / VEC), c = (e % (D / VEC)) * VEC;
+    float f[8];
+    if (r < len) {
+      const float4 raw = *reinterpret_cast<const float4*>(src + ((size_t)(row0 + r) * H + h) * D + c);
+      hsd::cvt16(raw, f, T());
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) f[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) dst[r * ld + c + i] = f[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Phase A: chunk-local quantities, one thread block per (chunk, head).
+// ---------------------------------------------------------------------------
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThreads)
+gdn_chunk_local_kernel(const int32_t* __restrict__ meta, int H, const T* __restrict__ q, const T* __restrict__ k,
+                       const T* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
+                       float* __restrict__ ws) {
+  extern __shared__ float sm[];
+  constexpr int LK = DK + 1;
+  float* Ks = sm;                      // [64][LK]
+  float* Qs = Ks + kChunk * LK;        // [64][LK]
+  float* Vs = Qs + kChunk * LK;        // [64][DV]
+  float* As = Vs + kChunk * DV;        // [64][65]
+  float* gs = As + kChunk * (kChunk + 1);
+  float* bs = gs + kChunk;
+
+  Meta M{meta};
+  const int c = blockIdx.x, h = blockIdx.y;
+  if (c >= M.h(H_N_CHUNK)) return;
+  const int32_t* ch = M.chunk(c);
+  const int row0 = ch[C_ROW0], len = ch[C_LEN];
+  load_rows<T, DK>(Ks, LK, k, row0, len, H, h);
+  load_rows<T, DK>(Qs, LK, q, row0, len, H, h);
+  load_rows<T, DV>(Vs, DV, v, row0, len, H, h);
+  if (threadIdx.x < kChunk) {
+    const int t = threadIdx.x;
+    gs[t] = t < len ? logf(alpha[(size_t)(row0 + t) * H + h]) : 0.f;
+    bs[t] = t < len ? beta[(size_t)(row0 + t) * H + h] : 0.f;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // inclusive cumulative sum, fixed order
+    float acc = 0.f;
+    for (int t = 0; t < kChunk; ++t) {
+      acc += gs[t];
+      gs[t] = acc;
+    }
+  }
+  __syncthreads();
+
+  float* wsp = ws + ((size_t)c * H + h) * WsLayout<DK, DV>::FLOATS;
+  // A (strictly lower) into smem, P (lower incl.) straight to the workspace
+  {
+    const int t = threadIdx.x / 4, s0 = (threadIdx.x % 4) * 16;
+    float a[16], p[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) a[j] = p[j] = 0.f;
+    for (int cc = 0; cc < DK; ++cc) {
+      const float kt = Ks[t * LK + cc], qt = Qs[t * LK + cc];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float ks = Ks[(s0 + j) * LK + cc];
+        a[j] = fmaf(kt, ks, a[j]);
+        p[j] = fmaf(qt, ks, p[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int s = s0 + j;
+      const float dec = expf(gs[t] - gs[s]);
+      As[t * (kChunk + 1) + s] = (s < t && t < len) ? bs[t] * dec * a[j] : 0.f;
+      wsp[WsLayout<DK, DV>::P + t * kChunk + s] = (s <= t && t < len) ? dec * p[j] : 0.f;
+    }
+  }
+  if (threadIdx.x < kChunk) wsp[WsLayout<DK, DV>::G + threadIdx.x] = gs[threadIdx.x];
+  __syncthreads();
+  // forward substitution (I + A) X = B, one column per thread, in registers
+  const int col = threadIdx.x;
+  if (col < DK + DV) {
+    float x[kChunk];
+#pragma unroll
+    for (int t = 0; t < kChunk; ++t) {
+      float acc = col < DK ? bs[t] * expf(gs[t]) * Ks[t * LK + col] : bs[t] * Vs[t * DV + (col - DK)];
+      if (t >= len) acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < t; ++s) acc = fmaf(-As[t * (kChunk + 1) + s], x[s], acc);
+      x[t] = acc;
+    }
+    if (col < DK) {
+#pragma unroll
+      for (int t = 0; t < kChunk; ++t) wsp[WsLayout<DK, DV>::W + t * DK + col] = x[t];
+    } else {
+#pragma unroll
+      for (int t = 0; t < kChunk; ++t) wsp[WsLayout<DK, DV>::UT + t * DV + (col - DK)] = x[t];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Phase B: the chunk chain of every node of one tree level, per (node, head,
+// d_v slice).  The state slice lives in shared memory across the chain.
+// ---------------------------------------------------------------------------
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThreads)
+gdn_state_pass_kernel(const int32_t* __restrict__ meta, int level, int H, const T* __restrict__ q,
+                      const T* __restrict__ k, const float* __restrict__ ws, float* __restrict__ state,
+                      int n_slots, T* __restrict__ out, int32_t* status) {
+  extern __shared__ float sm[];
+  constexpr int LK = DK + 1;
+  constexpr int J = kDvSlice;
+  float* Ss = sm;                  // [J][LK]
+  float* Ws = Ss + J * LK;         // [64][LK]
+  float* Qs = Ws + kChunk * LK;    // [64][LK]
+  float* Ks = Qs + kChunk * LK;    // [64][LK]
+  float* Ps = Ks + kChunk * LK;    // [64][65]
+  float* Uts = Ps + kChunk * (kChunk + 1);  // [64][J]
+  float* Us = Uts + kChunk * J;             // [64][J]
+  float* gs = Us + kChunk * J;              // [64]
+  float* dk_s = gs + kChunk;                // [64] e^{g_C - g_t}
+
+  Meta M{meta};
+  if (level >= M.h(H_N_LEVEL)) return;
+  const int lo = M.level_off()[level], hi = M.level_off()[level + 1];
+  if ((int)blockIdx.x >= hi - lo) return;
+  const int seg = M.level_seg()[lo + blockIdx.x];
+  const int32_t* sg = M.seg(seg);
+  const int h = blockIdx.y, j0 = blockIdx.z * J;
+  const int init = sg[S_INIT_SLOT], endslot = sg[S_END_SLOT];
+  if (init >= n_slots || endslot >= n_slots) {
+    hsd::set_status(status, HS_DEV_BAD_SLOT);
+    return;
+  }
+  for (int e = threadIdx.x; e < J * DK; e += blockDim.x) {
+    const int j = e / DK, cc = e % DK;
+    Ss[j * LK + cc] = init >= 0 ? state[(((size_t)init * H + h) * DV + j0 + j) * DK + cc] : 0.f;
+  }
+  const int c_off = sg[S_CHUNK_OFF], n_c = sg[S_N_CHUNK];
+  for (int ci = 0; ci < n_c; ++ci) {
+    const int32_t* ch = M.chunk(c_off + ci);
+    const int row0 = ch[C_ROW0], len = ch[C_LEN];
+    const float* wsp = ws + ((size_t)(c_off + ci) * H + h) * WsLayout<DK, DV>::FLOATS;
+    __syncthreads();  // previous chunk done with every buffer
+    for (int e = threadIdx.x; e < kChunk * DK; e += blockDim.x) {
+      const int t = e / DK, cc = e % DK;
+      Ws[t * LK + cc] = wsp[WsLayout<DK, DV>::W + e];
+    }
+    for (int e = threadIdx.x; e < kChunk * kChunk; e += blockDim.x) {
+      const int t = e / kChunk, s = e % kChunk;
+      Ps[t * (kChunk + 1) + s] = wsp[WsLayout<DK, DV>::P + e];
+    }
+    for (int e = threadIdx.x; e < kChunk * J; e += blockDim.x) {
+      const int t = e / J, j = e % J;
+      Uts[e] = wsp[WsLayout<DK, DV>::UT + t * DV + j0 + j];
+    }
+    if (threadIdx.x < kChunk) gs[threadIdx.x] = wsp[WsLayout<DK, DV>::G + threadIdx.x];
+    load_rows<T, DK>(Qs, LK, q, row0, len, H, h);
+    load_rows<T, DK>(Ks, LK, k, row0, len, H, h);
+    __syncthreads();
+    if (threadIdx.x < kChunk) dk_s[threadIdx.x] = threadIdx.x < len ? expf(gs[len - 1] - gs[threadIdx.x]) : 0.f;
+    // U = Ut - W S^T  (4 outputs per thread: row t, columns jj..jj+3)
+    const int t = threadIdx.x / 4, jj = (threadIdx.x % 4) * 4;
+    {
+      float u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[i] = 0.f;
+      for (int cc = 0; cc < DK; ++cc) {
+        const float w = Ws[t * LK + cc];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = fmaf(w, Ss[(jj + i) * LK + cc], u[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) Us[t * J + jj + i] = t < len ? Uts[t * J + jj + i] - u[i] : 0.f;
+    }
+    __syncthreads();
+    // O = e^g (Q S^T) + P U
+    {
+      float o1[4], o2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o1[i] = o2[i] = 0.f;
+      for (int cc = 0; cc < DK; ++cc) {
+        const float qv = Qs[t * LK + cc];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o1[i] = fmaf(qv, Ss[(jj + i) * LK + cc], o1[i]);
+      }
+      for (int s = 0; s <= t; ++s) {
+        const float p = Ps[t * (kChunk + 1) + s];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o2[i] = fmaf(p, Us[s * J + jj + i], o2[i]);
+      }
+      if (t < len) {
+        const float eg = expf(gs[t]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          out[((size_t)(row0 + t) * H + h) * DV + j0 + jj + i] = hsd::from_f<T>(fmaf(eg, o1[i], o2[i]));
+      }
+    }
+    __syncthreads();
+    // S = e^{g_C} S + U^T diag(e^{g_C - g}) K
+    {
+      const float egc = expf(gs[len - 1]);
+      const int j = threadIdx.x / 16, cl = threadIdx.x % 16;
+      float acc[DK / 16];
+#pragma unroll
+      for (int i = 0; i < DK / 16; ++i) acc[i] = 0.f;
+      for (int s = 0; s < len; ++s) {
+        const float us = Us[s * J + j] * dk_s[s];
+#pragma unroll
+        for (int i = 0; i < DK / 16; ++i) acc[i] = fmaf(us, Ks[s * LK + cl + 16 * i], acc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < DK / 16; ++i) {
+        float* sp = &Ss[j * LK + cl + 16 * i];
+        *sp = fmaf(egc, *sp, acc[i]);
+      }
+    }
+  }
+  __syncthreads();
+  if (endslot >= 0) {
+    for (int e = threadIdx.x; e < J * DK; e += blockDim.x) {
+      const int j = e / DK, cc = e % DK;
+      state[(((size_t)endslot * H + h) * DV + j0 + j) * DK + cc] = Ss[j * LK + cc];
+    }
+  }
+}
+
+__global__ void copy_state_kernel(const float4* __restrict__ src, float4* __restrict__ dst, size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+template <int DK, int DV>
+constexpr size_t smemA() {
+  return sizeof(float) * ((size_t)kChunk * (DK + 1) * 2 + kChunk * DV + kChunk * (kChunk + 1) + 2 * kChunk);
+}
+template <int DK, int DV>
+constexpr size_t smemB() {
+  return sizeof(float) * ((size_t)kDvSlice * (DK + 1) + 3 * (size_t)kChunk * (DK + 1) + kChunk * (kChunk + 1) +
+                          2 * kChunk * kDvSlice + 2 * kChunk);
+}
+
+template <typename T, int D>
+hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
+                  const void* v, const float* alpha, const float* beta, float* state, int n_slots, void* out,
+                  float* ws, int32_t* status, cudaStream_t st) {
+  static bool configured = false;  // per template instance
+  auto ka = gdn_chunk_local_kernel<T, D, D>;
+  auto kb = gdn_state_pass_kernel<T, D, D>;
+  if (!configured) {
+    if (cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemA<D, D>()) != cudaSuccess ||
+        cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemB<D, D>()) != cudaSuccess)
+      return hs::fail(HS_ECUDA, "gdn: cannot raise the shared-memory limit");
+    configured = true;
+  }
+  if (caps->max_chunks > 0) {
+    ka<<<dim3(caps->max_chunks, H), kThreads, smemA<D, D>(), st>>>(meta, H, (const T*)q, (const T*)k, (const T*)v,
+                                                                    alpha, beta, ws);
+    HS_LAUNCH_CHECK("gdn_chunk_local");
+  }
+  for (int lev = 0; lev < caps->max_levels && caps->max_segments > 0; ++lev) {
+    kb<<<dim3(caps->max_segments, H, D / kDvSlice), kThreads, smemB<D, D>(), st>>>(
+        meta, lev, H, (const T*)q, (const T*)k, ws, state, n_slots, (T*)out, status);
+    HS_LAUNCH_CHECK("gdn_state_pass");
+  }
+  return HS_OK;
+}
+
+}  // namespace
+
+extern "C" size_t hs_gdn_workspace_bytes(const hs_round_caps* caps, int32_t h, int32_t dk, int32_t dv) {
+  if (!caps || h <= 0 || dk <= 0 || dv <= 0) return 0;
+  return (size_t)caps->max_chunks * h * ws_floats_per(dk, dv) * sizeof(float);
+}
+
+extern "C" hs_status hs_gdn_fork_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t h,
+                                         int32_t dk, int32_t dv, int32_t chunk, const void* q, const void* k,
+                                         const void* v, const float* alpha, const float* beta, float* state_pool,
+                                         int32_t n_slots, void* out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                         void* stream) {
+  HS_CHECK_ARG(caps && dev_meta && q && k && v && alpha && beta && out && ws, "null argument");
+  HS_CHECK_ARG(h > 0, "h must be > 0");
+  HS_CHECK_ARG(n_slots >= 0 && (n_slots == 0 || state_pool), "bad state pool");
+  if (chunk != kChunk) return hs::fail(HS_EUNSUPPORTED, "chunk %d (built: %d)", chunk, kChunk);
+  if (dk != dv || (dk != 64 && dk != 128)) return hs::fail(HS_EUNSUPPORTED, "dk=%d dv=%d (built: 64, 128)", dk, dv);
+  if (dt != HS_F32 && dt != HS_BF16) return hs::fail(HS_EUNSUPPORTED, "dtype %d", (int)dt);
+  const size_t need = hs_gdn_workspace_bytes(caps, h, dk, dv);
+  HS_CHECK_ARG(ws_bytes >= need, "workspace of %zu bytes < %zu", ws_bytes, need);
+  HS_CHECK_ARG(((uintptr_t)ws & 255) == 0, "workspace must be 256-byte aligned");
+  HS_CHECK_ARG((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out) & 15) == 0,
+               "q, k, v, out must be 16-byte aligned");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return hs::fail(HS_ECUDA, "no CUDA device");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int32_t* meta = (const int32_t*)dev_meta;
+  if (dt == HS_BF16) {
+    if (dk == 128)
+      return run_gdn<__nv_bfloat16, 128>(caps, meta, h, q, k, v, alpha, beta, state_pool, n_slots, out, (float*)ws,
+                                         dev_status, st);
+    return run_gdn<__nv_bfloat16, 64>(caps, meta, h, q, k, v, alpha, beta, state_pool, n_slots, out, (float*)ws,
+                                      dev_status, st);
+  }
+  if (dk == 128)
+    return run_gdn<float, 128>(caps, meta, h, q, k, v, alpha, beta, state_pool, n_slots, out, (float*)ws, dev_status,
+                               st);
+  return run_gdn<float, 64>(caps, meta, h, q, k, v, alpha, beta, state_pool, n_slots, out, (float*)ws, dev_status, st);
+}
+
+extern "C" hs_status hs_gdn_state_checkpoint(float* state_pool, int32_t n_slots, int32_t src, int32_t dst, int32_t h,
+                                             int32_t dk, int32_t dv, void* stream) {
+  HS_CHECK_ARG(state_pool, "null state pool");
+  HS_CHECK_ARG(src >= 0 && src < n_slots && dst >= 0 && dst < n_slots, "slot out of range (src %d, dst %d, n %d)",
+               src, dst, n_slots);
+  HS_CHECK_ARG(h > 0 && dk > 0 && dv > 0 && ((size_t)h * dk * dv) % 4 == 0, "bad state shape");
+  HS_CHECK_ARG(((uintptr_t)state_pool & 15) == 0, "state pool must be 16-byte aligned");
+  if (src == dst) return HS_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return hs::fail(HS_ECUDA, "no CUDA device");
+  const size_t per = (size_t)h * dk * dv;
+  const size_t n4 = per / 4;
+  int grid = (int)((n4 + 255) / 256);
+  if (grid > 1024) grid = 1024;
+  copy_state_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((const float4*)(state_pool + (size_t)src * per),
+                                                             (float4*)(state_pool + (size_t)dst * per), n4);
+  HS_LAUNCH_CHECK("gdn_state_checkpoint");
+  return HS_OK;
+}

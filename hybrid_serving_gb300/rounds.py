@@ -1,0 +1,73 @@
+"""Host helpers around hs_round: build a round from a tree description and
+move per-node arrays into / out of stream order using the library's layout.
+
+A tree description is any object with ``requests``, each request having
+``parents`` (node 0 is the root, parents precede children), ``n_tok``,
+``readout`` (bools), ``hist_len`` and ``save`` ({node: state slot}).
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+
+from . import _lib
+from .api import PagePool, Round, round_caps_for
+
+
+def build_round(tree, pool: Optional[PagePool] = None, caps=None, temp_slot0: int = 0,
+                n_temp_slots: Optional[int] = None, resume: Optional[Dict[int, tuple]] = None):
+    """Returns (Round, {(request, node): segment id}).
+
+    ``resume``: {request: (ckpt_slot, [(ntok, [pages...]), ...])} for roots
+    resumed at ``hist_len`` (the span list may be empty for GDN-only rounds).
+    """
+    resume = resume or {}
+    n_seg = sum(r.n_nodes for r in tree.requests)
+    T = sum(sum(r.n_tok) for r in tree.requests)
+    depth = 1
+    for req in tree.requests:
+        d = [0] * req.n_nodes
+        for i in range(1, req.n_nodes):
+            d[i] = d[req.parents[i]] + 1
+        depth = max(depth, max(d) + 1)
+    n_hs = sum(len(v[1]) for v in resume.values())
+    n_hp = sum(len(p) for v in resume.values() for _, p in v[1])
+    if caps is None:
+        caps = round_caps_for(T, n_seg, depth, n_hs, n_hp)
+    R = Round(caps)
+    seg_of = {}
+    for r, req in enumerate(tree.requests):
+        for i in range(req.n_nodes):
+            parent = -1 if i == 0 else seg_of[(r, req.parents[i])]
+            flags = _lib.HS_SEG_READOUT if req.readout[i] else _lib.HS_SEG_NO_READOUT
+            seg_of[(r, i)] = R.add_segment(parent, req.n_tok[i], flags, req.save.get(i, -1))
+        if req.hist_len:
+            slot, spans = resume.get(r, (None, []))
+            if slot is not None:
+                R.gdn_state_resume(seg_of[(r, 0)], slot, req.hist_len)
+            if spans:
+                R.attach_history(seg_of[(r, 0)], [n for n, _ in spans], [p for _, ps in spans for p in ps])
+    R.finalize(pool, temp_slot0, n_seg if n_temp_slots is None else n_temp_slots)
+    return R, seg_of
+
+
+def to_stream(R: Round, seg_of: Dict[Tuple[int, int], int], per_node, key: Optional[str] = None) -> np.ndarray:
+    """Scatter {(r, node): array [n, ...]} (or {(r,node): {key: array}}) into stream order."""
+    first = next(iter(per_node.values()))
+    first = first[key] if key is not None else first
+    T = R.info().n_tokens
+    out = np.zeros((T,) + tuple(first.shape[1:]), dtype=first.dtype)
+    for node, s in seg_of.items():
+        a = per_node[node][key] if key is not None else per_node[node]
+        info = R.segment(s)
+        out[info.stream_off:info.stream_off + info.n_tokens] = a
+    return out
+
+
+def from_stream(R: Round, seg_of: Dict[Tuple[int, int], int], arr) -> Dict[Tuple[int, int], np.ndarray]:
+    out = {}
+    for node, s in seg_of.items():
+        info = R.segment(s)
+        out[node] = arr[info.stream_off:info.stream_off + info.n_tokens]
+    return out

@@ -1,0 +1,256 @@
+/*
+ * hs.h -- C ABI of the GB300 tree-prefill library (libhsfork.so).
+ *
+ * Exact tree-structured (forked) prefill: one or more requests, each a tree
+ * of a shared trunk and its question branches (or deeper residuals), packed
+ * into ONE flat token stream; two token mixers run over the stream:
+ *
+ *   - ForkAttention: paged causal attention in which a token sees its own
+ *     node's earlier tokens and every token of its ancestors, never a
+ *     sibling's (Flide, "Accelerating Decision Inference with Exact State
+ *     Forking", section 3.2.1, Eq. 3).  Children alias their ancestors' KV
+ *     pages without copying (ForkServe README, "Copy-on-write context tree").
+ *   - Gated DeltaNet fork prefill: the gated delta rule (Flide section 3.2.2,
+ *     Eq. 4) in chunks; each child continues from its parent's end state
+ *     through a state-slot index, never a copy (Flide section 3.2.2, "two
+ *     calls"), and a root may resume from a state saved by an earlier pass
+ *     (Flide section 3.4).
+ *
+ * Conventions
+ *   - Every call returns hs_status: 0 (HS_OK) or a negative code.  The message
+ *     of the last failure on the calling thread is hs_last_error().
+ *   - The CALLER owns all device memory (inputs, outputs, KV page pools,
+ *     state pools, workspaces, the metadata buffer, the status word).  No call
+ *     allocates device memory.  Host objects (page pool, round) are opaque
+ *     handles with create/destroy.
+ *   - Device calls enqueue work on the given cudaStream_t (passed as void*;
+ *     NULL = the legacy default stream) and never synchronise.
+ *   - Kernels never trap.  A kernel that meets inconsistent metadata writes a
+ *     nonzero code into the caller's int32 device status word (first error
+ *     wins) and skips the offending work; read it back after a sync and pass
+ *     the host copy to hs_check_status().
+ *   - There is no CPU fallback: without a usable CUDA device, device calls
+ *     fail with HS_ECUDA.
+ *   - Layouts are row-major, last index fastest.  T = stream tokens.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t hs_status;
+#define HS_OK 0
+#define HS_EINVAL (-1)        /* bad argument or tree (cycle, unknown parent, empty node, bad slot) */
+#define HS_ECAPACITY (-2)     /* a round exceeds one of its hs_round_caps */
+#define HS_EUNSUPPORTED (-3)  /* dtype / head size / chunk size not built */
+#define HS_ECUDA (-4)         /* a CUDA runtime call failed (including: no device) */
+#define HS_EDEVICE (-5)       /* the device status word reports an error */
+#define HS_ENOPAGES (-6)      /* page pool exhausted (refcounts are left unchanged) */
+
+typedef enum { HS_F32 = 0, HS_BF16 = 1 } hs_dtype;
+
+/* Device status codes (values of the int32 status word). */
+#define HS_DEV_OK 0
+#define HS_DEV_BAD_PAGE 1     /* a page id outside [0, n_pages) */
+#define HS_DEV_BAD_SLOT 2     /* a state slot outside [0, n_slots) */
+#define HS_DEV_BAD_META 3     /* counts above capacity or inconsistent records */
+
+/* ------------------------------------------------------------------------ */
+/* Fixed capacities of a round.  They size the device metadata buffer and   */
+/* every launch grid, so rounds with the same caps reuse the same launch    */
+/* shapes (Flide section 3.3.2: launches fixed by capacity, the tree lives  */
+/* in GPU-resident metadata).                                               */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t max_tokens;      /* stream tokens T */
+  int32_t max_segments;    /* tree nodes over all requests */
+  int32_t max_hist_spans;  /* KV history spans of resumed roots */
+  int32_t max_tiles;       /* attention query tiles (128 rows each) */
+  int32_t max_tile_spans;  /* total span references over all tiles */
+  int32_t max_chunks;      /* GDN chunks (64 tokens, per segment) */
+  int32_t max_readouts;    /* readout rows */
+  int32_t max_page_refs;   /* page-table entries (own pages + history pages) */
+  int32_t max_levels;      /* tree depth + 1 */
+} hs_round_caps;
+
+/* Capacities sufficient for a round of the given totals (tokens, segments,
+ * tree depth, history spans and history pages). */
+hs_status hs_round_caps_for(int32_t n_tokens, int32_t n_segments, int32_t n_levels,
+                            int32_t n_hist_spans, int32_t n_hist_pages, int32_t page_size,
+                            hs_round_caps* out);
+
+/* ------------------------------------------------------------------------ */
+/* KV page pool (host bookkeeping of a caller-owned device page pool).       */
+/* ForkServe README, "Copy-on-write context tree": a node's writes allocate  */
+/* pages for its own tokens; children alias ancestors' pages; abort decrefs. */
+/* Device pools are K and V arrays [n_pages][Hkv][page_size][d].             */
+/* ------------------------------------------------------------------------ */
+typedef struct hs_page_pool hs_page_pool;
+
+hs_status hs_page_pool_create(int32_t n_pages, int32_t page_size, hs_page_pool** out);
+void hs_page_pool_destroy(hs_page_pool* pool);
+/* number of free pages and of pages with refcount > 0 */
+hs_status hs_page_pool_stats(const hs_page_pool* pool, int32_t* n_free, int32_t* n_live);
+hs_status hs_page_pool_refcount(const hs_page_pool* pool, int32_t page, int32_t* ref);
+/* drop one reference of each page (pages reaching 0 return to the free list) */
+hs_status hs_page_pool_decref(hs_page_pool* pool, const int32_t* pages, int32_t n);
+
+/* ------------------------------------------------------------------------ */
+/* Round: a set of request trees flattened into one stream (Flide Eq. 2).    */
+/* ------------------------------------------------------------------------ */
+typedef struct hs_round hs_round;
+
+#define HS_SEG_READOUT 1       /* the node's last token is a readout row (default for leaves) */
+#define HS_SEG_NO_READOUT 2    /* suppress the default readout of a leaf */
+
+hs_status hs_round_create(const hs_round_caps* caps, hs_round** out);
+void hs_round_destroy(hs_round* r);
+
+/* Add a node.  parent_seg = -1 starts a new request (its trunk).  Nodes of
+ * one request must be added after their parent.  save_slot >= 0 persists the
+ * node's end-of-node GDN state into that state slot (a checkpoint, Flide
+ * section 3.4); -1 = no persistent save.  The new node's id (dense, in add
+ * order) is written to *seg_out. */
+hs_status hs_round_add_segment(hs_round* r, int32_t parent_seg, int32_t n_tokens, int32_t flags,
+                               int32_t save_slot, int32_t* seg_out);
+
+/* Resume a ROOT node from a checkpoint (Flide section 3.4): its first stream
+ * token sits at position ckpt_pos and its GDN state starts from ckpt_slot. */
+hs_status hs_gdn_state_resume(hs_round* r, int32_t seg, int32_t ckpt_slot, int32_t ckpt_pos);
+
+/* Attach the cached KV history of a resumed root: n_spans spans, span i
+ * holding ntok[i] tokens on ceil(ntok[i]/page_size) pages taken in order
+ * from `pages`.  The spans precede the root's own keys (Flide section 3.4:
+ * cached keys and values precede new ones).  sum(ntok) must equal ckpt_pos.
+ * The round takes one reference on each page and drops it at release. */
+hs_status hs_round_attach_history(hs_round* r, int32_t seg, int32_t n_spans, const int32_t* ntok,
+                                  const int32_t* pages);
+
+/* Lay out the stream, allocate each node's own KV pages from `pool` (may be
+ * NULL for GDN-only rounds), assign temporary GDN state slots
+ * [temp_slot0, temp_slot0 + n_temp_slots) to inner nodes, and build the
+ * metadata.  Errors leave the pool unchanged. */
+hs_status hs_round_finalize(hs_round* r, hs_page_pool* pool, int32_t temp_slot0, int32_t n_temp_slots);
+
+/* Bytes of the device metadata buffer for these caps (fixed per caps). */
+size_t hs_round_meta_bytes(const hs_round_caps* caps);
+/* Copy the packed metadata (int32 words) into a host buffer. */
+hs_status hs_round_pack(const hs_round* r, void* host, size_t bytes);
+/* One cudaMemcpyAsync of the packed metadata into the device buffer. */
+hs_status hs_round_upload(const hs_round* r, void* dev_meta, size_t bytes, void* stream);
+
+typedef struct {
+  int32_t n_tokens, n_segments, n_tiles, n_chunks, n_readouts, n_levels, n_pages_allocated;
+  int32_t n_spans, n_tile_spans, n_page_refs;
+} hs_round_info;
+hs_status hs_round_get_info(const hs_round* r, hs_round_info* out);
+
+typedef struct {
+  int32_t stream_off, n_tokens, pos0, request, parent, level;
+  int32_t init_slot, end_slot, readout_row, n_pages;
+} hs_segment_info;
+hs_status hs_round_segment(const hs_round* r, int32_t seg, hs_segment_info* out);
+/* the node's own pages (cap entries at most; *n = count) */
+hs_status hs_round_segment_pages(const hs_round* r, int32_t seg, int32_t* pages, int32_t cap, int32_t* n);
+/* the readout rows in readout order (stream row of each readout node's last token) */
+hs_status hs_round_readout_rows(const hs_round* r, int32_t* rows, int32_t cap, int32_t* n);
+
+/* Commit/abort (ForkServe README: commit keeps one path, abort decrefs the
+ * residuals).  Drops the round's page references for every node NOT listed
+ * in keep_segs and for the history pages; kept nodes' own pages stay live
+ * (one reference each, now owned by the caller). */
+hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep_segs, int32_t n_keep);
+
+/* ------------------------------------------------------------------------ */
+/* Hot path                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* ForkAttention prefill (Flide section 3.2.1, Eq. 3; scaled dot-product
+ * attention, Flex "Request-Adaptive Execution ..." section 2, Eq. 1).
+ * Writes the stream's new K/V into each node's own pages, then for every
+ * stream row and query head h computes
+ *   out[t,h] = sum_{y visible to t} softmax(scale * q[t,h].k[y,g]) v[y,g],
+ * g = h / (hq/hkv), the visible keys being the resumed history, every
+ * ancestor's tokens and the row's own node up to itself.
+ *   q      [T, hq, d]     dt        k_new, v_new [T, hkv, d] dt
+ *   k_pages, v_pages [n_pages, hkv, page_size, d] dt (written: own pages only)
+ *   out    [T, hq, d]     dt        (bf16 outputs are round-to-nearest-even)
+ * Supported: dt in {HS_F32, HS_BF16}; d in {64, 128}; hq % hkv == 0;
+ * page_size 16.  Inputs must be 16-byte aligned.  Accumulation is fp32;
+ * the result of a row does not depend on what else is in the round. */
+hs_status hs_fork_attn_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt,
+                               int32_t hq, int32_t hkv, int32_t d, float scale, const void* q,
+                               const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                               int32_t n_pages, void* out, int32_t* dev_status, void* stream);
+
+/* The two halves of hs_fork_attn_prefill, for callers that write the pages
+ * themselves or time the halves apart:
+ *   hs_kv_page_write -- k_new/v_new rows into each node's own pages (and
+ *     zeroes the unused rows of each node's last page);
+ *   hs_fork_attn     -- the attention over pages already written.
+ * Arguments as for hs_fork_attn_prefill. */
+hs_status hs_kv_page_write(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hkv, int32_t d,
+                           const void* k_new, const void* v_new, void* k_pages, void* v_pages, int32_t n_pages,
+                           int32_t* dev_status, void* stream);
+hs_status hs_fork_attn(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hq, int32_t hkv,
+                       int32_t d, float scale, const void* q, const void* k_pages, const void* v_pages,
+                       int32_t n_pages, void* out, int32_t* dev_status, void* stream);
+
+/* Workspace bytes hs_gdn_fork_prefill needs for these caps and shapes. */
+size_t hs_gdn_workspace_bytes(const hs_round_caps* caps, int32_t h, int32_t dk, int32_t dv);
+
+/* Gated DeltaNet fork prefill (Flide section 3.2.2, Eq. 4):
+ *   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t
+ * per head, over chunks of `chunk` tokens that start at every node's first
+ * token.  Level by level: a root starts from zero (or its resume slot), a
+ * child from its parent's end state (read through the slot index), and
+ * every node that has children or a save slot writes its end state.
+ *   q, k   [T, h, dk] dt    v [T, h, dv] dt    alpha, beta [T, h] fp32
+ *   state_pool [n_slots, h, dv, dk] fp32 (read: init slots; written: end slots)
+ *   out    [T, h, dv] dt
+ *   ws     >= hs_gdn_workspace_bytes(), 256-byte aligned, contents scratch
+ * Supported: dt in {HS_F32, HS_BF16}; dk == dv in {64, 128}; chunk == 64. */
+hs_status hs_gdn_fork_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t h,
+                              int32_t dk, int32_t dv, int32_t chunk, const void* q, const void* k,
+                              const void* v, const float* alpha, const float* beta, float* state_pool,
+                              int32_t n_slots, void* out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                              void* stream);
+
+/* Snapshot one GDN state slot into another (Flide section 3.4, checkpoint):
+ * state_pool[dst] = state_pool[src], [h, dv, dk] fp32 each. */
+hs_status hs_gdn_state_checkpoint(float* state_pool, int32_t n_slots, int32_t src_slot, int32_t dst_slot,
+                                  int32_t h, int32_t dk, int32_t dv, void* stream);
+
+/* Option log-probabilities at the readout rows (Flide section 3.1, Eq. 1;
+ * section 3.3.3, selective readout through an index buffer):
+ *   logprobs[i, o] = log softmax_o( option_rows[o] . hidden[row_i] )
+ *   hidden      [T, hidden_dim] dt with row stride hidden_stride elements
+ *   option_rows [n_opt, hidden_dim] fp32
+ *   logprobs    [n_readouts, n_opt] fp32
+ * Dot products accumulate in fp32 in a fixed order.  n_opt <= 32. */
+hs_status hs_choice_logprobs(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt,
+                             const void* hidden, int64_t hidden_stride, int32_t hidden_dim,
+                             const float* option_rows, int32_t n_opt, float* logprobs,
+                             int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and diagnostics                                                    */
+/* ------------------------------------------------------------------------ */
+/* Map a host copy of the device status word to HS_OK / HS_EDEVICE. */
+hs_status hs_check_status(const int32_t* host_status_word);
+/* Thread-local message of the last failing call on this thread. */
+const char* hs_last_error(void);
+/* Number of kernels this library has launched in this process. */
+int64_t hs_launch_count(void);
+/* Library version string. */
+const char* hs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HS_H_ */

@@ -1,0 +1,140 @@
+"""ForkAttention parity: the CUDA path through the C ABI vs the fp64 oracle.
+
+Tolerances (max-abs over every compared element): 1e-4 for fp32 inputs,
+2e-2 for bf16 inputs with fp32 accumulation; choice distributions within
+1e-3 total variation.  Batch invariance is checked bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import choice as ochoice
+from oracle import forward, numerics
+
+pytestmark = pytest.mark.gpu
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+from harness import AttnRun, max_abs  # noqa: E402
+from hybrid_serving_gb300 import _lib, api  # noqa: E402
+
+TOL_F32, TOL_BF16, TOL_TV = 1e-4, 2e-2, 1e-3
+
+
+def _check(tree, inp, dtype, tol, **kw):
+    run = AttnRun(tree, inp, dtype, **kw).run()
+    api.check_status(run.status)
+    got = run.outputs()
+    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(inp.d))
+    err = max_abs(got, ref)
+    assert err <= tol, f"max abs err {err}"
+    return run, got, ref
+
+
+def test_tiny_fp32():
+    tree = synth.tiny_tree()
+    inp = synth.attn_inputs(tree, 2, 2, 64, seed=1000, bf16=False, sigma=1 / 8)
+    _check(tree, inp, torch.float32, TOL_F32)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ragged_multi_request(d, dtype):
+    tree = synth.Tree([synth.fork_tree(300, [17, 1, 128, 129]), synth.fork_tree(5, [40, 3]),
+                       synth.fork_tree(129, [64, 65, 1])])
+    inp = synth.attn_inputs(tree, 8, 2, d, seed=1100 + d, bf16=dtype == torch.bfloat16)
+    _check(tree, inp, dtype, TOL_BF16 if dtype == torch.bfloat16 else TOL_F32)
+
+
+def test_deep_tree_bf16():
+    tree = synth.Tree([synth.fanout_tree(70, 9, 3, 3), synth.Request(parents=[-1, 0, 1, 1, 0, 4],
+                                                                     n_tok=[33, 20, 5, 100, 9, 2])])
+    inp = synth.attn_inputs(tree, 4, 4, 128, seed=1200, bf16=True)
+    _check(tree, inp, torch.bfloat16, TOL_BF16)
+
+
+def test_resumed_history_bf16():
+    """Round A computes a 200-token trunk; round B resumes at 200 with the
+    trunk's pages as history, 37 new trunk tokens and two branches.  The
+    oracle recomputes every path from position 0."""
+    full = synth.Tree([synth.fork_tree(237, [11, 30])])
+    inp = synth.attn_inputs(full, 8, 2, 128, seed=1300, bf16=True)
+    a_tree = synth.Tree([synth.fork_tree(200, [4])])
+    a_inp = synth.remap_inputs(full, inp, synth.Tree([synth.fork_tree(200, [11, 30])]))
+    a_inp.nodes = {(0, 0): a_inp.nodes[(0, 0)], (0, 1): {k: v[:4] for k, v in a_inp.nodes[(0, 1)].items()}}
+    A = AttnRun(a_tree, a_inp, torch.bfloat16, n_pages=64).run()
+    pages = A.R.segment_pages(A.seg_of[(0, 0)])
+    A.R.release(A.pool, keep=[A.seg_of[(0, 0)]])
+    b_tree = synth.Tree([synth.fork_tree(37, [11, 30], hist_len=200)])
+    b_inp = synth.remap_inputs(full, inp, b_tree)
+    B = AttnRun(b_tree, b_inp, torch.bfloat16, pool=A.pool, k_pages=A.k_pages, v_pages=A.v_pages,
+                resume={0: (None, [(200, pages)])}).run()
+    api.check_status(B.status)
+    got = B.outputs()
+    ref = forward.attention_tree(b_tree, b_inp, 1 / math.sqrt(128))
+    assert max_abs(got, ref) <= TOL_BF16
+
+
+def test_full_size_sampled_and_choices():
+    """The attention workload at full size (trunk 4096, 8 branches of
+    U[16,64], GQA 32/8, d=128, bf16): sampled trunk rows, every row of two
+    branches, and the 4-option distribution of every branch."""
+    tree = synth.attn_tree()
+    inp = synth.attn_inputs(tree, 32, 8, 128, seed=2000, bf16=True)
+    run = AttnRun(tree, inp, torch.bfloat16).run()
+    api.check_status(run.status)
+    got = run.outputs()
+    req = tree.requests[0]
+    rows = {(0, 0): [0, 1, 15, 16, 127, 128, 129, 1000, 2047, 2048, 4094, 4095]}
+    nodes = [(0, 0), (0, 1), (0, req.n_nodes - 1)]
+    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(128), nodes=nodes, rows=rows)
+    err = max(float(np.abs(got[(0, 0)][rows[(0, 0)]] - ref[(0, 0)]).max()),
+              max_abs(got, ref, keys=nodes[1:]))
+    assert err <= TOL_BF16, err
+    # choices: logits over the concatenated head outputs of each branch's last token
+    W = synth.option_rows(4, 32 * 128, seed=2001)
+    Wd = torch.from_numpy(W).cuda()
+    lp = torch.empty((run.R.info().n_readouts, 4), dtype=torch.float32, device="cuda")
+    api.choice_logprobs(run.R.caps, run.meta, run.out.view(run.out.shape[0], -1), Wd, lp, run.status)
+    torch.cuda.synchronize()
+    api.check_status(run.status)
+    last = {(0, b): [req.n_tok[b] - 1] for b in range(1, req.n_nodes)}
+    ref_last = forward.attention_tree(tree, inp, 1 / math.sqrt(128), nodes=list(last), rows=last)
+    h = np.stack([numerics.round_bf16(ref_last[(0, b)][0].reshape(-1)) for b in range(1, req.n_nodes)])
+    p_ref = np.exp(ochoice.option_logprobs(h, W))
+    p_gpu = np.exp(lp.cpu().numpy().astype(np.float64))
+    tv = ochoice.total_variation(p_gpu, p_ref)
+    assert tv.max() <= TOL_TV, tv
+    assert (ochoice.top1(p_gpu) == ochoice.top1(p_ref)).all()
+    # the kernel alone, on the GPU's own hidden rows
+    hg = np.stack([got[(0, b)][-1].reshape(-1) for b in range(1, req.n_nodes)])
+    assert ochoice.total_variation(p_gpu, np.exp(ochoice.option_logprobs(hg, W))).max() <= 1e-5
+
+
+def test_batch_invariance_bitwise():
+    """A branch's bits do not depend on its siblings or on other requests
+    in the round (Flide section 3.5)."""
+    base = synth.fork_tree(777, [20, 50, 13, 100])
+    other = synth.fork_tree(300, [9, 9])
+    tree = synth.Tree([other, base])
+    inp = synth.attn_inputs(tree, 8, 2, 128, seed=1400, bf16=True)
+    mixed = AttnRun(tree, inp, torch.bfloat16).run().raw_outputs()
+    for b in range(1, 5):
+        alone_tree = synth.Tree([synth.fork_tree(777, [base.n_tok[b]])])
+        alone_inp = synth.AttnInputs(8, 2, 128, True, {(0, 0): inp.nodes[(1, 0)], (0, 1): inp.nodes[(1, b)]},
+                                     {0: inp.hist[1]})
+        alone = AttnRun(alone_tree, alone_inp, torch.bfloat16).run().raw_outputs()
+        assert torch.equal(alone[(0, 1)], mixed[(1, b)]), f"branch {b} differs"
+        assert torch.equal(alone[(0, 0)], mixed[(1, 0)])
+
+
+def test_bad_page_sets_status_without_fault():
+    tree = synth.Tree([synth.fork_tree(64, [8])])
+    inp = synth.attn_inputs(tree, 2, 2, 64, seed=1500, bf16=True)
+    run = AttnRun(tree, inp, torch.bfloat16, n_pages=32, n_pages_kernel=2).run()
+    assert int(run.status.item()) == 1  # HS_DEV_BAD_PAGE
+    with pytest.raises(_lib.HsError):
+        api.check_status(run.status)

@@ -1,0 +1,275 @@
+"""Host-side tests of the round builder and page pool (no GPU).
+
+The packed metadata is decoded here from its documented record layout and
+compared, bit for bit, with the oracle's layout (Flide Eq. 2), positions,
+token metadata and -- for every query row -- the key set of Eq. 3, after
+mapping each physical page row the attention kernel would read back to
+the token written there.
+"""
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import layout
+
+api = pytest.importorskip("hybrid_serving_gb300.api")
+from hybrid_serving_gb300 import _lib, rounds  # noqa: E402
+
+PAGE = 16
+# record layouts (words) of the metadata blob
+H = dict(N_TOK=1, N_SEG=2, N_SPAN=3, N_TILE=4, N_TILE_SPAN=5, N_CHUNK=6, N_READOUT=7, N_LEVEL=8, N_PAGE_REF=9,
+         OFF_SEG=10, OFF_TOK=11, OFF_SPAN=12, OFF_TILE=13, OFF_TILE_SPAN=14, OFF_CHUNK=15, OFF_READOUT=16,
+         OFF_LEVEL=17, OFF_LEVEL_SEG=18, OFF_PAGE_REF=19)
+SEGW, TOKW, SPANW, TILEW, CHUNKW = 16, 2, 4, 8, 4
+
+
+class Blob:
+    def __init__(self, words):
+        self.w = np.asarray(words, dtype=np.int64)
+
+    def h(self, k):
+        return int(self.w[H[k]])
+
+    def arr(self, off, n, width):
+        o = self.h(off)
+        return self.w[o:o + n * width].reshape(n, width) if width > 1 else self.w[o:o + n]
+
+    @property
+    def segs(self):
+        return self.arr("OFF_SEG", self.h("N_SEG"), SEGW)
+
+    @property
+    def toks(self):
+        return self.arr("OFF_TOK", self.h("N_TOK"), TOKW)
+
+    @property
+    def spans(self):
+        return self.arr("OFF_SPAN", self.h("N_SPAN"), SPANW)
+
+    @property
+    def tiles(self):
+        return self.arr("OFF_TILE", self.h("N_TILE"), TILEW)
+
+    @property
+    def tile_spans(self):
+        return self.arr("OFF_TILE_SPAN", self.h("N_TILE_SPAN"), 1)
+
+    @property
+    def chunks(self):
+        return self.arr("OFF_CHUNK", self.h("N_CHUNK"), CHUNKW)
+
+    @property
+    def page_ref(self):
+        return self.arr("OFF_PAGE_REF", self.h("N_PAGE_REF"), 1)
+
+    @property
+    def readouts(self):
+        return self.arr("OFF_READOUT", self.h("N_READOUT"), 1)
+
+
+def make(tree, n_pages=4096, resume=None, pool=None):
+    pool = pool or api.PagePool(n_pages)
+    R, seg_of = rounds.build_round(tree, pool, resume=resume)
+    return R, seg_of, pool, Blob(R.pack().numpy())
+
+
+TREES = [
+    synth.Tree([synth.fork_tree(64, [8, 8, 8])]),
+    synth.Tree([synth.fork_tree(300, [17, 1, 128, 129]), synth.fork_tree(5, [40, 3])]),
+    synth.Tree([synth.fanout_tree(40, 7, 3, 3)]),
+    synth.Tree([synth.Request(parents=[-1, 0, 1, 1, 0, 4], n_tok=[33, 20, 5, 100, 9, 2]),
+                synth.fork_tree(129, [64, 65, 1])]),
+]
+
+
+def test_abi_exports_every_declared_symbol():
+    hdr = open(__import__("os").path.join(__import__("os").path.dirname(__file__), "..", "include", "hs.h")).read()
+    declared = set(re.findall(r"\b(hs_[a-z0-9_]+)\s*\(", hdr))
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (hs_[a-z0-9_]+)$", out, re.M))
+    assert declared, "no declarations parsed"
+    assert declared <= exported, f"not exported: {sorted(declared - exported)}"
+    assert declared <= set(_lib.EXPORTED), f"not bound: {sorted(declared - set(_lib.EXPORTED))}"
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+def test_layout_positions_tokens_match_oracle(ti):
+    tree = TREES[ti]
+    R, seg_of, pool, B = make(tree)
+    lay = layout.stream_layout(tree)
+    for (r, i), s in seg_of.items():
+        info = R.segment(s)
+        assert info.stream_off == lay[(r, i)]
+        assert info.pos0 == layout.positions(tree.requests[r])[i]
+        assert info.request == r and info.n_tokens == tree.requests[r].n_tok[i]
+        assert info.level == layout.depth(tree.requests[r])[i]
+    j, c, t, ix = layout.token_metadata(tree)
+    node_of = {s: rn for rn, s in seg_of.items()}
+    toks = B.toks
+    assert B.h("N_TOK") == layout.stream_length(tree)
+    for row in range(B.h("N_TOK")):
+        r, i = node_of[int(toks[row, 0])]
+        assert (r, i, int(toks[row, 1])) == (j[row], c[row], ix[row])
+
+
+def _phys_of_tokens(R, seg_of, B):
+    """(page, row) -> (node, index) for every token the KV write puts in a page."""
+    where = {}
+    segs = B.segs
+    pref = B.page_ref
+    for (r, i), s in seg_of.items():
+        n = int(segs[s, 1])
+        for u in range(n):
+            where[(int(pref[int(segs[s, 12]) + u // PAGE]), u % PAGE)] = ((r, i), u)
+    return where
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+def test_visible_keys_match_eq3(ti):
+    """For every query row: the keys the tiles make visible (shared spans in
+    full, own spans up to the row's index for the row's own node) map back
+    to exactly the oracle's Eq. 3 set."""
+    tree = TREES[ti]
+    R, seg_of, pool, B = make(tree)
+    where = _phys_of_tokens(R, seg_of, B)
+    node_of = {s: rn for rn, s in seg_of.items()}
+    toks, spans, tiles, ts, pref = B.toks, B.spans, B.tiles, B.tile_spans, B.page_ref
+    covered = np.zeros(B.h("N_TOK"), int)
+    for tl in tiles:
+        row0, n_rows, soff, n_sh, n_own = (int(x) for x in tl[:5])
+        for row in range(row0, row0 + n_rows):
+            covered[row] += 1
+            seg, idx = int(toks[row, 0]), int(toks[row, 1])
+            got = []
+            for k in range(n_sh + n_own):
+                sp = spans[int(ts[soff + k])]
+                off, ntok, owner = int(sp[0]), int(sp[1]), int(sp[2])
+                if k < n_sh:
+                    nvis = ntok
+                else:
+                    nvis = idx + 1 if owner == seg else 0
+                for key in range(nvis):
+                    (rn, u) = where[(int(pref[off + key // PAGE]), key % PAGE)]
+                    got.append((rn[1], u))
+            r, i = node_of[seg]
+            assert sorted(got) == layout.visible_keys(tree, r, i, idx), (row, seg, idx)
+    assert (covered == 1).all()
+
+
+def test_history_spans_and_resume():
+    full = synth.Tree([synth.fork_tree(70, [5, 9])])
+    pool = api.PagePool(256)
+    R0, s0, _, B0 = make(full, pool=pool)
+    pages = R0.segment_pages(s0[(0, 0)])
+    R0.release(pool, keep=[s0[(0, 0)]])
+    assert pool.stats()[1] == len(pages) == 5
+    res = synth.Tree([synth.fork_tree(11, [5, 9], hist_len=70)])
+    R1, s1, _, B1 = make(res, pool=pool, resume={0: (3, [(70, pages)])})
+    assert R1.segment(s1[(0, 0)]).pos0 == 70 and R1.segment(s1[(0, 0)]).init_slot == 3
+    assert R1.segment(s1[(0, 1)]).pos0 == 81
+    # history pages gained the round's reference
+    assert all(pool.refcount(p) == 2 for p in pages)
+    # visible keys of the first branch token: history 0..69, root tail 0..10, itself
+    toks, spans, tiles, ts = B1.toks, B1.spans, B1.tiles, B1.tile_spans
+    row = R1.segment(s1[(0, 1)]).stream_off
+    tl = [t for t in tiles if t[0] <= row < t[0] + t[1]][0]
+    n_keys = sum(int(spans[int(ts[int(tl[2]) + k])][1]) for k in range(int(tl[3])))
+    assert n_keys == 70 + 11
+    R1.release(pool)
+    assert all(pool.refcount(p) == 1 for p in pages)
+
+
+def test_chunks_slots_readouts():
+    tree = TREES[1]
+    R, seg_of, pool, B = make(tree)
+    ch = B.chunks
+    for (r, i), s in seg_of.items():
+        info = R.segment(s)
+        mine = [c for c in ch if c[0] == s]
+        assert [int(c[3]) for c in mine] == list(range(len(mine)))
+        assert int(mine[0][1]) == info.stream_off                       # starts at the node
+        assert sum(int(c[2]) for c in mine) == info.n_tokens
+        assert all(1 <= int(c[2]) <= 64 for c in mine)
+        p = tree.requests[r].parents[i]
+        if p >= 0:
+            assert info.init_slot == R.segment(seg_of[(r, p)]).end_slot >= 0
+        else:
+            assert info.init_slot == -1
+        if tree.requests[r].readout[i]:
+            assert info.readout_row == info.stream_off + info.n_tokens - 1
+    assert list(B.readouts) == [R.segment(s).readout_row for s in sorted(seg_of.values())
+                                if R.segment(s).readout_row >= 0]
+
+
+def test_forkserve_pages_fork_and_commit():
+    """ForkServe cost model: 10 sessions x (trunk 256 + 4 x 32), page 16:
+    240 pages live at fork; keeping each session's winner (index 0) leaves
+    the spine, 10 x (16 + 2) = 180 pages."""
+    pool = api.PagePool(1024)
+    tree = synth.Tree([synth.fork_tree(256, [32] * 4) for _ in range(10)])
+    R, seg_of = rounds.build_round(tree, pool)
+    assert pool.stats()[1] == 240
+    keep = [seg_of[(r, i)] for r in range(10) for i in (0, 1)]
+    R.release(pool, keep=keep)
+    assert pool.stats()[1] == 180
+
+
+def test_deep_tree_pages():
+    pool = api.PagePool(4096)
+    tree = synth.Tree([synth.fanout_tree(256, 32, 4, 3) for _ in range(10)])
+    R, seg_of = rounds.build_round(tree, pool)
+    assert pool.stats()[1] == 1840 == layout.live_pages(tree, 16)
+    assert R.info().n_tokens == 29440
+
+
+def test_errors_leave_state_unchanged():
+    caps = api.round_caps_for(100, 4, 2)
+    R = api.Round(caps)
+    with pytest.raises(_lib.HsError) as e:
+        R.add_segment(-1, 0)
+    assert e.value.code == _lib.HS_EINVAL
+    with pytest.raises(_lib.HsError):
+        R.add_segment(5, 3)                          # unknown parent
+    root = R.add_segment(-1, 60)
+    R.add_segment(root, 50)
+    pool = api.PagePool(64)
+    with pytest.raises(_lib.HsError) as e:
+        R.finalize(pool)                             # 110 tokens > 100
+    assert e.value.code == _lib.HS_ECAPACITY
+    assert pool.stats() == (64, 0)
+    # pool exhaustion: nothing allocated
+    small = api.PagePool(3)
+    R2, _ = None, None
+    tree = synth.Tree([synth.fork_tree(40, [8])])
+    with pytest.raises(_lib.HsError) as e:
+        rounds.build_round(tree, small)
+    assert e.value.code == _lib.HS_ENOPAGES and small.stats() == (3, 0)
+    # two nodes saving into one slot
+    R3 = api.Round(api.round_caps_for(100, 4, 2))
+    a = R3.add_segment(-1, 10, save_slot=2)
+    R3.add_segment(a, 5, save_slot=2)
+    with pytest.raises(_lib.HsError):
+        R3.finalize(None, 0, 4)
+    # depth above max_levels
+    R4 = api.Round(api.round_caps_for(100, 4, 1))
+    a = R4.add_segment(-1, 10)
+    R4.add_segment(a, 5)
+    with pytest.raises(_lib.HsError) as e:
+        R4.finalize(None)
+    assert e.value.code == _lib.HS_ECAPACITY
+
+
+def test_device_calls_fail_without_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    caps = api.round_caps_for(10, 1, 1)
+    st = _lib.lib.hs_gdn_state_checkpoint(None, 1, 0, 0, 1, 4, 4, None)
+    assert st == _lib.HS_EINVAL
+    import ctypes
+    buf = (ctypes.c_float * 64)()
+    st = _lib.lib.hs_gdn_state_checkpoint(ctypes.cast(buf, ctypes.c_void_p), 2, 0, 1, 1, 4, 4, None)
+    assert st == _lib.HS_ECUDA
