@@ -175,7 +175,7 @@ class Step:
             self.sets.append(s)
         self.n_pages = self.a_T // 16 + 64
         self.pool = api.PagePool(self.n_pages)
-        self.k_pages = torch.zeros((self.n_pages, ATTN["hkv"], 16, ATTN["d"]), dtype=bf, device=dev)
+        self.k_pages = torch.zeros((ATTN["hkv"], self.n_pages, 16, ATTN["d"]), dtype=bf, device=dev)
         self.v_pages = torch.zeros_like(self.k_pages)
         self.state = torch.zeros((8, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.float32, device=dev)
         self.a_meta = torch.empty(api.Round(self.a_caps).meta_bytes() // 4, dtype=torch.int32, device=dev)

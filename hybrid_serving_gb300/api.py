@@ -150,30 +150,30 @@ class Round:
 # ---------------------------------------------------------------------------
 def fork_attn_prefill(caps: Caps, dev_meta: torch.Tensor, q, k_new, v_new, k_pages, v_pages, out,
                       dev_status: torch.Tensor, scale: Optional[float] = None, stream=None):
-    """q [T,hq,d], k_new/v_new [T,hkv,d], k_pages/v_pages [n_pages,hkv,16,d], out [T,hq,d]."""
+    """q [T,hq,d], k_new/v_new [T,hkv,d], k_pages/v_pages [hkv,n_pages,16,d], out [T,hq,d]."""
     T, hq, d = q.shape
     hkv = k_new.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     check(lib.hs_fork_attn_prefill(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, q.data_ptr(),
                                    k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
-                                   k_pages.shape[0], out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+                                   k_pages.shape[1], out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
 
 
 def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_pages, dev_status: torch.Tensor,
                   stream=None):
     T, hkv, d = k_new.shape
     check(lib.hs_kv_page_write(C.byref(caps), dev_meta.data_ptr(), _dt(k_new), hkv, d, k_new.data_ptr(),
-                               v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[0],
+                               v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[1],
                                dev_status.data_ptr(), _stream(stream)))
 
 
 def fork_attn(caps: Caps, dev_meta: torch.Tensor, q, k_pages, v_pages, out, dev_status: torch.Tensor,
               scale: Optional[float] = None, stream=None):
     T, hq, d = q.shape
-    hkv = k_pages.shape[1]
+    hkv = k_pages.shape[0]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     check(lib.hs_fork_attn(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, q.data_ptr(),
-                           k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[0], out.data_ptr(),
+                           k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[1], out.data_ptr(),
                            dev_status.data_ptr(), _stream(stream)))
 
 

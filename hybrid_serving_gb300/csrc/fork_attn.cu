@@ -57,7 +57,7 @@ kv_page_write_kernel(const int32_t* __restrict__ meta, int hkv, int d, const T* 
       const int e = jj * VEC;
       const int h = e / d, c = e % d;
       const T* src = (which ? v_new : k_new) + (size_t)t * hkv * d + e;
-      T* dst = (which ? vp : kp) + (((size_t)page * hkv + h) * kPage + row) * d + c;
+      T* dst = (which ? vp : kp) + (((size_t)h * n_pages + page) * kPage + row) * d + c;
       *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
       if (last)
         for (int rr = row + 1; rr < kPage; ++rr)
@@ -144,7 +144,7 @@ fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float s
           const int ref = sp_off + key / kPage;
           const int page = ref < n_ref ? refs[ref] : -1;
           if (page >= 0 && page < n_pages) {
-            const size_t base = (((size_t)page * hkv + kvh) * kPage + key % kPage) * D + c4;
+            const size_t base = (((size_t)kvh * n_pages + page) * kPage + key % kPage) * D + c4;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               kv[i] = hsd::to_f(kp[base + i]);

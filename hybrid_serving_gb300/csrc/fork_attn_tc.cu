@@ -1,9 +1,491 @@
-// fork_attn_tc.cu -- tensor-core ForkAttention (bf16, d = 128) for sm_103a.
-// Placeholder until the tcgen05 kernel lands: declines every call so that
-// the CUDA-core path runs.
-#include "device.cuh"
+// fork_attn_tc.cu -- tensor-core ForkAttention for sm_103a (bf16, d = 128).
+//
+// Flide, "Accelerating Decision Inference with Exact State Forking":
+// section 3.2.1, Eq. 3 (visibility), section 3.3.1 (keys from the shared
+// state and the query's own question; fully visible key blocks read without
+// a mask, only partial blocks masked), section 3.5 (a question's reductions
+// start at the fork and do not depend on the rest of the round).  The scale
+// is 1/sqrt(d) (Flex, "Request-Adaptive Execution ...", section 2, Eq. 1).
+//
+// One CTA = one attention tile (up to 128 consecutive stream rows: a run of
+// one node, or sibling nodes packed together) x one query head.  The CTA
+// walks the tile's key spans (ancestors first, then the tile's own nodes) in
+// blocks of 128 keys starting at each span's first key, so a row's sequence
+// of blocks depends only on its own tree path:
+//
+//   warp 4      TMA producer: Q once; per block K and V pages into a 2-stage
+//               ring (one 128-row box per 64-column half when the 8 pages of
+//               a block are consecutive, else one 16-row box per page; pages
+//               past the span are loaded from out of range, i.e. zeros).
+//   warp 5      allocates TMEM and issues tcgen05.mma from one thread:
+//               S_j = Q K_j^T into one of two TMEM score buffers, then
+//               O += P_{j-1} V_{j-1} once the softmax has written P.
+//   warps 0..3  softmax, thread t <-> TMEM lane t <-> query row t: reads S_j,
+//               masks partial blocks, keeps the running max in log2 units,
+//               rescales O and l only when the max grows by more than 2^8
+//               (a per-row decision), writes P into shared memory in the
+//               128-byte-swizzled K-major layout the MMA reads, and at the
+//               end writes O / l.  P is split into a bf16 high part and a
+//               bf16 low part (p - high), both multiplied into O, so P enters
+//               the product with ~16 significant bits instead of 8.
+//
+// TMEM: columns [0,128) and [128,256) = S ping-pong, [256,384) = O.
+// Shared memory: Q 32 KB | K 2 x 32 KB | V 2 x 32 KB | P hi, lo 2 x 32 KB (SW128).
+// Every wait is bounded; a wait that runs out records HS_DEV_TIMEOUT in the
+// status word, and the CTA drains its own copies and MMAs before leaving.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
-hs_status hs_fork_attn_tc_launch(const hs_round_caps*, const void*, int, int, int, float, const void*, const void*,
-                                 const void*, int, void*, int32_t*, cudaStream_t) {
-  return HS_EUNSUPPORTED;
+#include "device.cuh"
+#include "tc_ptx.cuh"
+
+using namespace hsm;
+using hsd::Meta;
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBlk = 128;                    // keys per block
+constexpr int kSlab = 128 * 128;             // bytes of one [128 rows][64 cols] bf16 slab
+constexpr int kTile = 2 * kSlab;             // 32 KB: 128 x 128 bf16
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;         // 2 stages
+constexpr int kOffV = kOffK + 2 * kTile;     // 2 stages
+constexpr int kOffP = kOffV + 2 * kTile;
+constexpr int kSmemBytes = kOffP + 2 * kTile;  // 224 KB (P as bf16 high and low parts)
+constexpr int kThreads = 192;
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr int HS_DEV_TIMEOUT = 4;
+
+constexpr uint32_t kIdescQK = tc::idesc_bf16(128, 128, 0, 0);  // A = Q (K-major), B = K (K-major)
+constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, 0, 1);  // A = P (K-major), B = V (N-major)
+
+struct Params {
+  const int32_t* meta;
+  int hq, hkv, n_pages;
+  float scale_log2e;
+  __nv_bfloat16* out;
+  int32_t* status;
+};
+
+// The key blocks of a tile in the order every role walks them.
+struct Cursor {
+  Meta M;
+  const int32_t* tspans;
+  int n_shared, n_spans, n_own, tile_lo, tile_hi;
+  int si, b0, kmax;
+  int sp_off, sp_n, owner, own, first_idx;
+  __device__ void init(Meta m, const int32_t* tl) {
+    M = m;
+    tspans = m.tile_spans() + tl[TL_SPAN_OFF];
+    n_shared = tl[TL_N_SHARED];
+    n_own = tl[TL_N_OWN];
+    n_spans = n_shared + n_own;
+    tile_lo = tl[TL_ROW0];
+    tile_hi = tl[TL_ROW0] + tl[TL_N_ROWS];
+    si = -1;
+    b0 = 0;
+    kmax = 0;
+  }
+  // advance to the next block; false when the tile has no more
+  __device__ bool next() {
+    b0 += kBlk;
+    while (b0 >= kmax) {
+      if (++si >= n_spans) return false;
+      const int32_t* sp = M.span(tspans[si]);
+      sp_off = sp[SP_PAGE_REF_OFF];
+      sp_n = sp[SP_N_TOK];
+      owner = sp[SP_OWNER];
+      own = si >= n_shared;
+      kmax = sp_n;
+      first_idx = 0;
+      if (own) {
+        const int32_t* og = M.seg(owner);
+        const int lo = max(tile_lo, og[S_STREAM_OFF]);
+        const int hi = min(tile_hi, og[S_STREAM_OFF] + og[S_LEN]);
+        kmax = hi > lo ? hi - og[S_STREAM_OFF] : 0;
+        first_idx = lo - og[S_STREAM_OFF];
+      }
+      b0 = 0;
+    }
+    return true;
+  }
+  __device__ int valid() const { return min(kBlk, sp_n - b0); }
+  // every row of the tile sees every key of the block
+  __device__ bool full() const {
+    return own ? (n_own == 1 && b0 + kBlk <= first_idx && b0 + kBlk <= sp_n) : (sp_n - b0 >= kBlk);
+  }
+};
+
+__device__ __forceinline__ void record(int32_t* status, int* abort_flag, int code) {
+  hsd::set_status(status, code);
+  atomicExch(abort_flag, 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
+                    const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
+                    const __grid_constant__ CUtensorMap tm_v128, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_kve[2], bar_sf[2], bar_pf, bar_pv, bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  Meta M{p.meta};
+  const int tile = blockIdx.x;
+  if (tile >= M.h(H_N_TILE)) return;
+  const int32_t* tl = M.tile(tile);
+  const int h = blockIdx.y;
+  const int kvh = h / (p.hq / p.hkv);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tc::mbar_init(&bar_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&bar_kf[s], 1);
+      tc::mbar_init(&bar_vf[s], 1);
+      tc::mbar_init(&bar_kve[s], 1);
+      tc::mbar_init(&bar_sf[s], 1);
+    }
+    tc::mbar_init(&bar_pf, 128);
+    tc::mbar_init(&bar_pv, 1);
+    tc::mbar_init(&bar_done, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(&tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  Cursor cur;
+  cur.init(M, tl);
+  const int n_ref = M.h(H_N_PAGE_REF);
+  const int32_t* refs = M.page_ref();
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k16);
+      tc::prefetch_tmap(&tm_v16);
+      tc::mbar_expect_tx(&bar_q, kTile);
+      tc::tma_load_3d(smem + kOffQ, &tm_q, 0, h, tl[TL_ROW0], &bar_q);
+      tc::tma_load_3d(smem + kOffQ + kSlab, &tm_q, 64, h, tl[TL_ROW0], &bar_q);
+      const int oob_y = p.hkv * p.n_pages * kPage;  // first row past the pool: zero fill
+      int j = 0;
+      while (cur.next()) {
+        const int st = j & 1;
+        if (j >= 2 && !tc::mbar_wait(&bar_kve[st], ((j >> 1) - 1) & 1, kWaitCycles)) {
+          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+          break;
+        }
+        if (*(volatile int*)&abort_flag) break;
+        const int npg = (cur.valid() + kPage - 1) / kPage;
+        int pg[8];
+        bool consecutive = npg == 8;
+        for (int i = 0; i < 8; ++i) {
+          pg[i] = -1;
+          if (i < npg) {
+            const int ref = cur.sp_off + cur.b0 / kPage + i;
+            const int page = ref < n_ref ? refs[ref] : -1;
+            if (page >= 0 && page < p.n_pages) {
+              pg[i] = page;
+            } else {
+              hsd::set_status(p.status, ref < n_ref ? HS_DEV_BAD_PAGE : HS_DEV_BAD_META);
+            }
+          }
+          if (i > 0 && (pg[i] < 0 || pg[i] != pg[i - 1] + 1)) consecutive = false;
+        }
+        if (pg[0] < 0) consecutive = false;
+        uint8_t* ks = smem + kOffK + st * kTile;
+        uint8_t* vs = smem + kOffV + st * kTile;
+        tc::mbar_expect_tx(&bar_kf[st], kTile);
+        tc::mbar_expect_tx(&bar_vf[st], kTile);
+        if (consecutive) {
+          const int y = (kvh * p.n_pages + pg[0]) * kPage;
+          for (int half = 0; half < 2; ++half) tc::tma_load_2d(ks + half * kSlab, &tm_k128, half * 64, y, &bar_kf[st]);
+          for (int half = 0; half < 2; ++half) tc::tma_load_2d(vs + half * kSlab, &tm_v128, half * 64, y, &bar_vf[st]);
+        } else {
+          for (int i = 0; i < 8; ++i) {
+            const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
+            for (int half = 0; half < 2; ++half)
+              tc::tma_load_2d(ks + half * kSlab + i * 2048, &tm_k16, half * 64, y, &bar_kf[st]);
+          }
+          for (int i = 0; i < 8; ++i) {
+            const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
+            for (int half = 0; half < 2; ++half)
+              tc::tma_load_2d(vs + half * kSlab + i * 2048, &tm_v16, half * 64, y, &bar_vf[st]);
+          }
+        }
+        ++j;
+      }
+      // drain: every copy this thread issued has landed before the CTA leaves
+      tc::mbar_wait(&bar_q, 0, kWaitCycles);
+      for (int i = (j >= 2 ? j - 2 : 0); i < j; ++i) {
+        tc::mbar_wait(&bar_kf[i & 1], (i >> 1) & 1, kWaitCycles);
+        tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t sq = tc::smem_u32(smem + kOffQ);
+      const uint32_t sp = tc::smem_u32(smem + kOffP);
+      bool ok = tc::mbar_wait(&bar_q, 0, kWaitCycles);
+      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      auto pv = [&](int i) -> bool {
+        if (!tc::mbar_wait(&bar_pf, i & 1, kWaitCycles) ||
+            !tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t sv = tc::smem_u32(smem + kOffV + (i & 1) * kTile);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t a = tc::sdesc_sw128(sp + part * kTile + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+            const uint64_t b = tc::sdesc_sw128(sv + k * 2048, kSlab, 1024);
+            tc::mma_bf16_ss(tmem + 256, a, b, kIdescPV, (i > 0 || part > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&bar_pv);
+        tc::mma_commit(&bar_kve[i & 1]);
+        return true;
+      };
+      int j = 0;
+      while (ok && cur.next()) {
+        const int st = j & 1;
+        if (!tc::mbar_wait(&bar_kf[st], (j >> 1) & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (*(volatile int*)&abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint32_t sk = tc::smem_u32(smem + kOffK + st * kTile);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = tc::sdesc_sw128(sq + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+          const uint64_t b = tc::sdesc_sw128(sk + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+          tc::mma_bf16_ss(tmem + st * 128, a, b, kIdescQK, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bar_sf[st]);
+        if (j >= 1 && !pv(j - 1)) {
+          ok = false;
+          break;
+        }
+        ++j;
+      }
+      if (ok && j >= 1 && !pv(j - 1)) ok = false;
+      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      // drain: all MMAs issued by this thread complete before TMEM is freed
+      tc::mma_commit(&bar_done);
+      tc::mbar_wait(&bar_done, 0, kWaitCycles);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = threadIdx.x;  // row of the tile == TMEM lane
+    const int row = tl[TL_ROW0] + t;
+    const bool active = t < tl[TL_N_ROWS];
+    int my_seg = -1, my_idx = 0;
+    if (active) {
+      my_seg = M.tok(row)[T_SEG];
+      my_idx = M.tok(row)[T_IDX];
+    }
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    const float sl2 = p.scale_log2e;
+    uint8_t* ps = smem + kOffP;
+    int j = 0;
+    bool ok = true;
+    while (cur.next()) {
+      const int st = j & 1;
+      if (!tc::mbar_wait(&bar_sf[st], (j >> 1) & 1, kWaitCycles)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + lane_base + st * 128 + c * 32, r[c]);
+      tc::tmem_wait_ld();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
+      if (!cur.full()) {
+        const int lim = !active ? 0 : !cur.own ? cur.sp_n - cur.b0 : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = i < lim ? s[i] : -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_used, mx * sl2);
+      float factor = 1.f;
+      const bool rescale = m_new > m_used + 8.f;
+      if (rescale) {
+        factor = exp2f(m_used - m_new);
+        m_used = m_new;
+      }
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = exp2f(fmaf(s[i], sl2, -mref));
+        rs += s[i];
+      }
+      l = l * factor + rs;
+      // the previous P.V must be done before P is overwritten or O rescaled
+      if (j >= 1) {
+        if (!tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (rescale) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+            tc::tmem_st32(tmem + lane_base + 256 + c * 32, o);
+          }
+          tc::tmem_wait_st();
+        }
+      }
+      // P row t, K-major, 128-byte swizzle: 16-byte chunk c of a slab row lands at chunk c ^ (t % 8).
+      // High part bf16(p) at ps, low part bf16(p - high) at ps + kTile.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int k0 = half * 64 + c * 8;
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = s[k0 + 2 * e], b = s[k0 + 2 * e + 1];
+            hi[e] = tc::pack_bf16x2(a, b);
+            const float ah = __uint_as_float(hi[e] << 16), bh = __uint_as_float(hi[e] & 0xFFFF0000u);
+            lo[e] = tc::pack_bf16x2(a - ah, b - bh);
+          }
+          const int off = half * kSlab + t * 128 + ((c ^ (t & 7)) << 4);
+          *reinterpret_cast<uint4*>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(ps + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bar_pf);
+      ++j;
+    }
+    if (ok && j >= 1) {
+      if (tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles)) {
+        tc::fence_after_sync();
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = p.out + ((size_t)row * p.hq + h) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+          tc::tmem_wait_ld();
+          if (active) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
+              v.y = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
+              v.z = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
+              v.w = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+            }
+          }
+        }
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 5) tc::tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Runs the tensor-core kernel when it applies (bf16, d = 128); returns
+// HS_EUNSUPPORTED otherwise so the caller takes the CUDA-core kernel.
+hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, int hq, int hkv, int d, float scale,
+                                 const void* q, const void* kp, const void* vp, int n_pages, void* out,
+                                 int32_t* status, cudaStream_t st) {
+  if (d != kD) return HS_EUNSUPPORTED;
+  if (caps->max_tiles <= 0) return HS_OK;
+  // the pool rows must be addressable by 32-bit TMA coordinates
+  if ((long long)hkv * n_pages * kPage + kPage >= (1LL << 31)) return HS_EUNSUPPORTED;
+  const long long T = caps->max_tokens;
+  CUtensorMap m_q, m_k16, m_k128, m_v16, m_v128;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)hq, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)hq * kD * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    if (!make_map(&m_q, q, 3, dims, strides, box)) return hs::fail(HS_ECUDA, "tensor map for q");
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)hkv * n_pages * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t b16[2] = {64, 16}, b128[2] = {64, 128};
+    if (!make_map(&m_k16, kp, 2, dims, strides, b16) || !make_map(&m_k128, kp, 2, dims, strides, b128) ||
+        !make_map(&m_v16, vp, 2, dims, strides, b16) || !make_map(&m_v128, vp, 2, dims, strides, b128))
+      return hs::fail(HS_ECUDA, "tensor map for the page pools");
+  }
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(fork_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024) !=
+        cudaSuccess)
+      return hs::fail(HS_ECUDA, "fork_attn_tc: cannot raise the shared-memory limit");
+    configured = true;
+  }
+  Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status};
+  fork_attn_tc_kernel<<<dim3(caps->max_tiles, hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
+                                                                                        m_v128, prm);
+  HS_LAUNCH_CHECK("fork_attn_tc");
+  return HS_OK;
 }

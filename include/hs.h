@@ -88,7 +88,7 @@ hs_status hs_round_caps_for(int32_t n_tokens, int32_t n_segments, int32_t n_leve
 /* KV page pool (host bookkeeping of a caller-owned device page pool).       */
 /* ForkServe README, "Copy-on-write context tree": a node's writes allocate  */
 /* pages for its own tokens; children alias ancestors' pages; abort decrefs. */
-/* Device pools are K and V arrays [n_pages][Hkv][page_size][d].             */
+/* Device pools are K and V arrays [Hkv][n_pages][page_size][d].             */
 /* ------------------------------------------------------------------------ */
 typedef struct hs_page_pool hs_page_pool;
 
@@ -177,9 +177,13 @@ hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep_
  *   out[t,h] = sum_{y visible to t} softmax(scale * q[t,h].k[y,g]) v[y,g],
  * g = h / (hq/hkv), the visible keys being the resumed history, every
  * ancestor's tokens and the row's own node up to itself.
- *   q      [T, hq, d]     dt        k_new, v_new [T, hkv, d] dt
- *   k_pages, v_pages [n_pages, hkv, page_size, d] dt (written: own pages only)
- *   out    [T, hq, d]     dt        (bf16 outputs are round-to-nearest-even)
+ *   q      [Tcap, hq, d]  dt        k_new, v_new [Tcap, hkv, d] dt
+ *   (Tcap = caps->max_tokens: buffers are sized by capacity; rows past the
+ *   round's stream are read as padding and never written)
+ *   k_pages, v_pages [hkv, n_pages, page_size, d] dt (head-major: one head's
+ *                    pages are contiguous; written: own pages only; every
+ *                    row must hold finite values -- zero the pools once)
+ *   out    [Tcap, hq, d]  dt        (bf16 outputs are round-to-nearest-even)
  * Supported: dt in {HS_F32, HS_BF16}; d in {64, 128}; hq % hkv == 0;
  * page_size 16.  Inputs must be 16-byte aligned.  Accumulation is fp32;
  * the result of a row does not depend on what else is in the round. */

@@ -28,7 +28,7 @@ class AttnRun:
         if pool is None:
             n_pages = n_pages or (T // 16 + sum(r.n_nodes for r in tree.requests) + 16)
             pool = api.PagePool(n_pages)
-            k_pages = torch.zeros((n_pages, inp.hkv, 16, inp.d), dtype=dtype, device=DEV)
+            k_pages = torch.zeros((inp.hkv, n_pages, 16, inp.d), dtype=dtype, device=DEV)
             v_pages = torch.zeros_like(k_pages)
         self.pool, self.k_pages, self.v_pages = pool, k_pages, v_pages
         self.R, self.seg_of = rounds.build_round(tree, pool, resume=resume)
@@ -44,7 +44,7 @@ class AttnRun:
     def run(self, scale=None):
         kp = self.k_pages
         if self.n_pages_kernel is not None:
-            kp = self.k_pages[: self.n_pages_kernel]
+            kp = self.k_pages[:, : self.n_pages_kernel]
         api.fork_attn_prefill(self.R.caps, self.meta, self.q, self.k, self.v, kp, self.v_pages, self.out,
                               self.status, scale=scale)
         torch.cuda.synchronize()
