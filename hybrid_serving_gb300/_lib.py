@@ -76,6 +76,7 @@ _SIGS = {
     "hs_gdn_workspace_bytes": (C.c_size_t, [CAPSP, I32, I32, I32]),
     "hs_gdn_fork_prefill": (I32, [CAPSP, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, I32, P, P, C.c_size_t,
                                   P, P]),
+    "hs_gdn_fork_prefill_noalloc": (I32, [CAPSP, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, I32, P, P, P]),
     "hs_gdn_state_checkpoint": (I32, [P, I32, I32, I32, I32, I32, I32, P]),
     "hs_choice_logprobs": (I32, [CAPSP, P, I32, P, C.c_int64, I32, P, I32, P, P, P]),
     "hs_check_status": (I32, [I32P]),

@@ -192,6 +192,18 @@ def gdn_fork_prefill(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha, beta, s
                                   ws.numel() * ws.element_size(), dev_status.data_ptr(), _stream(stream)))
 
 
+def gdn_fork_prefill_noalloc(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha, beta, state_pool, out,
+                             dev_status: torch.Tensor, chunk: int = CHUNK, stream=None):
+    """hs_gdn_fork_prefill without a workspace argument: for callers that
+    cannot allocate device memory (the library's built-in scratch is used)."""
+    T, h, dk = q.shape
+    dv = v.shape[2]
+    check(lib.hs_gdn_fork_prefill_noalloc(C.byref(caps), dev_meta.data_ptr(), _dt(q), h, dk, dv, chunk,
+                                          q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
+                                          beta.data_ptr(), state_pool.data_ptr(), state_pool.shape[0],
+                                          out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+
+
 def gdn_state_checkpoint(state_pool, src_slot: int, dst_slot: int, stream=None):
     n, h, dv, dk = state_pool.shape
     check(lib.hs_gdn_state_checkpoint(state_pool.data_ptr(), n, src_slot, dst_slot, h, dk, dv, _stream(stream)))

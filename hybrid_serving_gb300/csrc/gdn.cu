@@ -22,6 +22,8 @@
 // d_v slices (rows of S evolve independently, so the split is exact).
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "device.cuh"
 
 using namespace hsm;
@@ -380,4 +382,48 @@ extern "C" hs_status hs_gdn_state_checkpoint(float* state_pool, int32_t n_slots,
                                                              (float4*)(state_pool + (size_t)dst * per), n4);
   HS_LAUNCH_CHECK("gdn_state_checkpoint");
   return HS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace-free variant for callers that cannot allocate device memory:
+// the scratch lives in a file-scope device array (HS_GDN_NOALLOC_SCRATCH_BYTES
+// per GPU that loads the library, held until exit).  Host code cannot use the
+// array's name as a device address, so each device's address is looked up
+// once with cudaGetSymbolAddress while that device is current.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_gdn_noalloc_scratch[HS_GDN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" hs_status hs_gdn_fork_prefill_noalloc(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt,
+                                                 int32_t h, int32_t dk, int32_t dv, int32_t chunk, const void* q,
+                                                 const void* k, const void* v, const float* alpha, const float* beta,
+                                                 float* state_pool, int32_t n_slots, void* out, int32_t* dev_status,
+                                                 void* stream) {
+  HS_CHECK_ARG(caps, "null caps");
+  const size_t need = hs_gdn_workspace_bytes(caps, h, dk, dv);
+  if (need > HS_GDN_NOALLOC_SCRATCH_BYTES)
+    return hs::fail(HS_ECAPACITY, "round needs %zu bytes of GDN scratch; the built-in scratch holds %zu", need,
+                    (size_t)HS_GDN_NOALLOC_SCRATCH_BYTES);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return hs::fail(HS_ECUDA, "no CUDA device");
+  if (dev < 0 || dev >= kMaxDevices) return hs::fail(HS_EUNSUPPORTED, "device ordinal %d", dev);
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      cudaError_t e = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_gdn_noalloc_scratch);
+      if (e != cudaSuccess) {
+        g_scratch_ptr[dev] = nullptr;
+        return hs::fail(HS_ECUDA, "scratch address on device %d: %s", dev, cudaGetErrorString(e));
+      }
+    }
+    ptr = g_scratch_ptr[dev];
+  }
+  return hs_gdn_fork_prefill(caps, dev_meta, dt, h, dk, dv, chunk, q, k, v, alpha, beta, state_pool, n_slots, out,
+                             ptr, HS_GDN_NOALLOC_SCRATCH_BYTES, dev_status, stream);
 }

@@ -225,6 +225,31 @@ hs_status hs_gdn_fork_prefill(const hs_round_caps* caps, const void* dev_meta, h
                               int32_t n_slots, void* out, void* ws, size_t ws_bytes, int32_t* dev_status,
                               void* stream);
 
+/* Gated DeltaNet fork prefill for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this is a library convenience.)  Some
+ * callers have no allocator to hand a workspace from -- code running where
+ * cudaMalloc is forbidden or unavailable, e.g. inside a host framework that
+ * owns all device memory, or a plug-in that may only touch the buffers it
+ * is given.  This entry point takes the same arguments as
+ * hs_gdn_fork_prefill minus the workspace and uses a scratch array compiled
+ * into the library instead: HS_GDN_NOALLOC_SCRATCH_BYTES of device memory
+ * that every GPU loading the library holds until the process exits.
+ *   - A round whose hs_gdn_workspace_bytes() exceeds that size is rejected
+ *     with HS_ECAPACITY before anything is launched.
+ *   - It allocates nothing: no cudaMalloc / cudaFree, no allocating library.
+ *   - The first call on a device looks up that device's scratch address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     the kernels fully rewrite every entry they read, so nothing needs
+ *     clearing, but calls that overlap on the GPU (other streams, other
+ *     threads) race on it: serialise them. */
+#define HS_GDN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+hs_status hs_gdn_fork_prefill_noalloc(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t h,
+                                      int32_t dk, int32_t dv, int32_t chunk, const void* q, const void* k,
+                                      const void* v, const float* alpha, const float* beta, float* state_pool,
+                                      int32_t n_slots, void* out, int32_t* dev_status, void* stream);
+
 /* Snapshot one GDN state slot into another (Flide section 3.4, checkpoint):
  * state_pool[dst] = state_pool[src], [h, dv, dk] fp32 each. */
 hs_status hs_gdn_state_checkpoint(float* state_pool, int32_t n_slots, int32_t src_slot, int32_t dst_slot,
