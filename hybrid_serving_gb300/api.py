@@ -98,6 +98,9 @@ class Round:
     def gdn_state_resume(self, seg: int, ckpt_slot: int, ckpt_pos: int):
         check(lib.hs_gdn_state_resume(self._h, seg, ckpt_slot, ckpt_pos))
 
+    def set_conv_window(self, seg: int, window_row0: int):
+        check(lib.hs_round_set_conv_window(self._h, seg, window_row0))
+
     def attach_history(self, seg: int, ntok: Sequence[int], pages: Sequence[int]):
         check(lib.hs_round_attach_history(self._h, seg, len(ntok), _i32arr(ntok), _i32arr(pages)))
 

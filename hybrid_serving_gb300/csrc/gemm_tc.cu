@@ -1,0 +1,221 @@
+// gemm_tc.cu -- batch-invariant bf16 GEMM on tcgen05 for sm_103a.
+//
+//   C[M, N] = A[M, K] . B[N, K]^T  (+ R[M, N])      bf16 in, fp32 accumulate, bf16 out
+//
+// Flide, "Accelerating Decision Inference with Exact State Forking",
+// section 3.5: every matrix product sums each output element in a fixed
+// order whatever the number of rows.  Here every output tile is 128 x 128,
+// there is no split-K, and the K loop runs in the same 64-wide stages and
+// 16-wide MMA steps for any M, so a row's result does not depend on which
+// other rows share the launch.
+//
+// One CTA per output tile.  Warp 0 streams A and B tiles with TMA into a
+// 3-stage ring (128-byte swizzle); warp 1 owns 128 TMEM columns and issues
+// tcgen05.mma (M=128, N=128, K=16) from one thread; warps 2..5 read the
+// accumulator back (thread = row), add the optional residual and store
+// bf16.  Waits are bounded and report HS_DEV_TIMEOUT through the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int kStages = 3;
+constexpr int kStageA = BM * BK * 2;  // 16 KB
+constexpr int kStageB = BN * BK * 2;  // 16 KB
+constexpr int kSmem = kStages * (kStageA + kStageB);
+constexpr int kThreads = 192;
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr int HS_DEV_TIMEOUT = 4;
+constexpr uint32_t kIdesc = tc::idesc_bf16(BM, BN, 0, 0);
+
+struct GemmParams {
+  int M, N, K;
+  __nv_bfloat16* C;
+  long long ldc;
+  const __nv_bfloat16* R;  // optional residual, same layout as C
+  long long ldr;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc;
+  __shared__ uint32_t tmem_slot;
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int nk = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&bar_full[s], 1);
+      tc::mbar_init(&bar_empty[s], 1);
+    }
+    tc::mbar_init(&bar_acc, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&tmem_slot, 128);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_a);
+      tc::prefetch_tmap(&tm_b);
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages && !tc::mbar_wait(&bar_empty[s], ((kb / kStages) - 1) & 1, kWaitCycles)) {
+          hsd::set_status(p.status, HS_DEV_TIMEOUT);
+          break;
+        }
+        uint8_t* sa = smem + s * (kStageA + kStageB);
+        uint8_t* sb = sa + kStageA;
+        tc::mbar_expect_tx(&bar_full[s], kStageA + kStageB);
+        tc::tma_load_2d(sa, &tm_a, kb * BK, m0, &bar_full[s]);
+        tc::tma_load_2d(sb, &tm_b, kb * BK, n0, &bar_full[s]);
+        ++issued;
+      }
+      // drain: the last copies have landed before the CTA leaves
+      for (int kb = issued > kStages ? issued - kStages : 0; kb < issued; ++kb)
+        tc::mbar_wait(&bar_full[kb % kStages], (kb / kStages) & 1, kWaitCycles);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (!tc::mbar_wait(&bar_full[s], (kb / kStages) & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t sa = tc::smem_u32(smem + s * (kStageA + kStageB));
+        const uint32_t sb = sa + kStageA;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t a = tc::sdesc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t b = tc::sdesc_sw128(sb + k * 32, 16, 1024);
+          tc::mma_bf16_ss(tmem, a, b, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&bar_empty[s]);
+      }
+      if (!ok) hsd::set_status(p.status, HS_DEV_TIMEOUT);
+      tc::mma_commit(&bar_acc);  // also drains every MMA before TMEM is freed
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp % 4;  // TMEM lanes this warp may read
+    const int r = quarter * 32 + lane;
+    const int row = m0 + r;
+    if (tc::mbar_wait(&bar_acc, 0, kWaitCycles)) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
+        tc::tmem_wait_ld();
+        if (row < p.M) {
+          const int col0 = n0 + c * 32;
+          __nv_bfloat16* dst = p.C + (size_t)row * p.ldc + col0;
+          const __nv_bfloat16* res = p.R ? p.R + (size_t)row * p.ldr + col0 : nullptr;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[q * 8 + i]);
+            if (res) {
+              float rr[8];
+              hsd::cvt16(*reinterpret_cast<const float4*>(res + q * 8), rr, __nv_bfloat16());
+#pragma unroll
+              for (int i = 0; i < 8; ++i) f[i] += rr[i];
+            }
+            uint4 o;
+            o.x = tc::pack_bf16x2(f[0], f[1]);
+            o.y = tc::pack_bf16x2(f[2], f[3]);
+            o.z = tc::pack_bf16x2(f[4], f[5]);
+            o.w = tc::pack_bf16x2(f[6], f[7]);
+            *reinterpret_cast<uint4*>(dst + q * 8) = o;
+          }
+        }
+      }
+    } else {
+      hsd::set_status(p.status, HS_DEV_TIMEOUT);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tmem, 128);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+bool map_2d(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B,
+                                  int64_t ldb, void* C, int64_t ldc, const void* R, int64_t ldr, int32_t* dev_status,
+                                  void* stream) {
+  HS_CHECK_ARG(A && B && C, "null argument");
+  HS_CHECK_ARG(M >= 0 && N > 0 && K > 0, "bad shape %d x %d x %d", M, N, K);
+  if (N % BN != 0 || K % BK != 0)
+    return hs::fail(HS_EUNSUPPORTED, "N (%d) must be a multiple of %d and K (%d) of %d", N, BN, K, BK);
+  HS_CHECK_ARG(lda >= K && ldb >= K && ldc >= N && (!R || ldr >= N), "leading dimensions too small");
+  HS_CHECK_ARG(lda % 8 == 0 && ldb % 8 == 0 && ldc % 8 == 0 && (!R || ldr % 8 == 0),
+               "leading dimensions must be multiples of 8 elements");
+  HS_CHECK_ARG((((uintptr_t)A | (uintptr_t)B | (uintptr_t)C | (uintptr_t)R) & 15) == 0,
+               "pointers must be 16-byte aligned");
+  if (M == 0) return HS_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return hs::fail(HS_ECUDA, "no CUDA device");
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, A, M, K, lda, BM) || !map_2d(&mb, B, N, K, ldb, BN))
+    return hs::fail(HS_ECUDA, "gemm: tensor map encoding failed");
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
+        cudaSuccess)
+      return hs::fail(HS_ECUDA, "gemm: cannot raise the shared-memory limit");
+    configured = true;
+  }
+  GemmParams prm{M, N, K, (__nv_bfloat16*)C, ldc, (const __nv_bfloat16*)R, ldr, dev_status};
+  dim3 grid(N / BN, (M + BM - 1) / BM);
+  gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
+  HS_LAUNCH_CHECK("gemm_bf16");
+  return HS_OK;
+}

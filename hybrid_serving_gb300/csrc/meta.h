@@ -51,6 +51,7 @@ enum : int {
   H_CAP_PAGE_REF,
   H_TOTAL_WORDS,
   H_MAX_SEG_CHUNKS,  // largest number of chunks in one segment
+  H_OFF_PRED,        // per token: kConvTaps-1 predecessor rows for the causal conv
 };
 
 // segment record
@@ -71,6 +72,14 @@ enum : int {
   S_PAGE_REF_OFF,    // first own page in the page-ref array
   S_N_PAGES,
 };
+
+// Causal-conv predecessors of a token (Flide section 3.2.2: the convolution
+// reads a token's predecessors through an index, so a question's first tokens
+// see its state's last tokens).  pred[k-1] = the token k steps back in the
+// isolated sequence: >= 0 a stream row; -1 none (before the sequence);
+// <= -2 row (-2 - value) of the caller's conv-window buffer (a resumed root).
+constexpr int kConvTaps = 4;
+constexpr int kPredWords = kConvTaps - 1;
 
 // token record: the node a stream row belongs to and its index inside it
 constexpr int kTokWords = 2;
@@ -93,7 +102,7 @@ enum : int { C_SEG = 0, C_ROW0, C_LEN, C_IDX };
 
 struct Layout {
   int32_t off_seg, off_tok, off_span, off_tile, off_tile_span, off_chunk, off_readout, off_level,
-      off_level_seg, off_page_ref, total_words;
+      off_level_seg, off_page_ref, off_pred, total_words;
 };
 
 inline int32_t align16(int32_t x) { return (x + 15) & ~15; }
@@ -114,6 +123,7 @@ inline Layout layout_for(int32_t cap_tok, int32_t cap_seg, int32_t cap_span, int
   L.off_level = o;      o = align16(o + cap_level + 1);
   L.off_level_seg = o;  o = align16(o + cap_seg);
   L.off_page_ref = o;   o = align16(o + cap_page_ref);
+  L.off_pred = o;       o = align16(o + cap_tok * kPredWords);
   L.total_words = o;
   return L;
 }

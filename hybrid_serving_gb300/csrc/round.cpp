@@ -132,7 +132,7 @@ namespace {
 
 struct Seg {
   int32_t parent = -1, n_tok = 0, flags = 0, save_slot = -1, request = 0;
-  int32_t resume_slot = -1, resume_pos = -1;
+  int32_t resume_slot = -1, resume_pos = -1, conv_window = -1;
   std::vector<int32_t> hist_ntok, hist_pages;
   std::vector<int32_t> children;
   // computed at finalize
@@ -198,7 +198,7 @@ extern "C" hs_status hs_round_create(const hs_round_caps* caps, hs_round** out) 
   int64_t words = (int64_t)kHeaderWords + (int64_t)c.max_segments * kSegWords + (int64_t)c.max_tokens * kTokWords +
                   (int64_t)(c.max_segments + c.max_hist_spans) * kSpanWords + (int64_t)c.max_tiles * kTileWords +
                   c.max_tile_spans + (int64_t)c.max_chunks * kChunkWords + c.max_readouts + c.max_levels +
-                  c.max_segments + c.max_page_refs + 200;
+                  c.max_segments + c.max_page_refs + (int64_t)c.max_tokens * kPredWords + 200;
   HS_CHECK_ARG(words < (int64_t)1 << 30, "capacities too large");
   auto* r = new hs_round;
   r->caps = c;
@@ -244,6 +244,16 @@ extern "C" hs_status hs_gdn_state_resume(hs_round* r, int32_t seg, int32_t ckpt_
   HS_CHECK_ARG(ckpt_pos >= 0, "bad checkpoint position %d", ckpt_pos);
   r->segs[seg].resume_slot = ckpt_slot;
   r->segs[seg].resume_pos = ckpt_pos;
+  return HS_OK;
+}
+
+extern "C" hs_status hs_round_set_conv_window(hs_round* r, int32_t seg, int32_t window_row0) {
+  HS_CHECK_ARG(r, "null round");
+  HS_CHECK_ARG(!r->finalized, "round already finalized");
+  HS_CHECK_ARG(seg >= 0 && seg < (int32_t)r->segs.size(), "unknown node %d", seg);
+  HS_CHECK_ARG(r->segs[seg].parent < 0, "only a root has a conv window (node %d has a parent)", seg);
+  HS_CHECK_ARG(window_row0 >= 0, "bad window row %d", window_row0);
+  r->segs[seg].conv_window = window_row0;
   return HS_OK;
 }
 
@@ -570,6 +580,27 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
   memcpy(h + L.off_chunk, chunks.data(), chunks.size() * 4);
   memcpy(h + L.off_readout, r->readouts.data(), r->readouts.size() * 4);
   memcpy(h + L.off_page_ref, page_ref.data(), page_ref.size() * 4);
+  h[H_OFF_PRED] = L.off_pred;
+  // conv predecessors: walk back through the node, then its ancestors' last tokens
+  for (int32_t i = 0; i < n; ++i) {
+    const Seg& s = S[i];
+    for (int32_t u = 0; u < s.n_tok; ++u) {
+      int32_t* pr = h + L.off_pred + (s.stream_off + u) * kPredWords;
+      for (int32_t k = 1; k <= kPredWords; ++k) {
+        int32_t node = i, idx = u - k, val = -1;
+        while (idx < 0 && S[node].parent >= 0) {
+          node = S[node].parent;
+          idx += S[node].n_tok;
+        }
+        if (idx >= 0) {
+          val = S[node].stream_off + idx;
+        } else if (S[node].conv_window >= 0) {  // idx in [-kPredWords, -1] of a resumed root
+          if (idx >= -kPredWords) val = -2 - (S[node].conv_window + kPredWords + idx);
+        }
+        pr[k - 1] = val;
+      }
+    }
+  }
   {
     int32_t k = 0;
     for (int32_t lev = 0; lev < n_levels; ++lev) {

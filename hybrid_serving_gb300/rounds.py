@@ -19,8 +19,10 @@ def build_round(tree, pool: Optional[PagePool] = None, caps=None, temp_slot0: in
                 n_temp_slots: Optional[int] = None, resume: Optional[Dict[int, tuple]] = None):
     """Returns (Round, {(request, node): segment id}).
 
-    ``resume``: {request: (ckpt_slot, [(ntok, [pages...]), ...])} for roots
-    resumed at ``hist_len`` (the span list may be empty for GDN-only rounds).
+    ``resume``: {request: (ckpt_slot, [(ntok, [pages...]), ...][, window_row0])}
+    for roots resumed at ``hist_len`` (the span list may be empty for
+    GDN-only rounds; window_row0 = the root's conv window in the caller's
+    window buffer).
     """
     resume = resume or {}
     n_seg = sum(r.n_nodes for r in tree.requests)
@@ -43,7 +45,10 @@ def build_round(tree, pool: Optional[PagePool] = None, caps=None, temp_slot0: in
             flags = _lib.HS_SEG_READOUT if req.readout[i] else _lib.HS_SEG_NO_READOUT
             seg_of[(r, i)] = R.add_segment(parent, req.n_tok[i], flags, req.save.get(i, -1))
         if req.hist_len:
-            slot, spans = resume.get(r, (None, []))
+            res = resume.get(r, (None, []))
+            slot, spans = res[0], res[1]
+            if len(res) > 2 and res[2] is not None:
+                R.set_conv_window(seg_of[(r, 0)], res[2])
             if slot is not None:
                 R.gdn_state_resume(seg_of[(r, 0)], slot, req.hist_len)
             if spans:

@@ -1,0 +1,174 @@
+"""Hybrid attention / Gated DeltaNet stack over a forked round, on the C ABI.
+
+Sequencing and argument marshalling only: every operation is a kernel of
+libhsfork.so (tcgen05 GEMMs with the residual fused into the epilogue,
+RMSNorm, rotary embedding at standalone positions, the GDN front end with
+predecessors across the fork, ForkAttention, Gated DeltaNet fork prefill,
+SwiGLU, option log-probs).  PyTorch only allocates device memory.
+
+Layer definition (the pages give none; see the oracle for the same text):
+pre-norm residual blocks of a token mixer ('A' attention, 'G' Gated
+DeltaNet) and a SwiGLU MLP; final RMSNorm; option logits against embedding
+rows of the option tokens (Flide section 3.1, Eq. 1).  Every tensor between
+operations is stored in bf16 (gates fp32).
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+from . import api
+from ._lib import check, lib
+
+DEV = "cuda"
+
+
+@dataclass
+class StackShape:
+    hidden: int = 2048
+    pattern: str = "GGGAGGGA"
+    attn_hq: int = 16
+    attn_hkv: int = 4
+    head_d: int = 128
+    gdn_h: int = 16
+    gdn_d: int = 128
+    ffn: int = 4096
+    vocab: int = 32768
+    rope_theta: float = 1e4
+    eps: float = 1e-6
+    option_ids: List[int] = field(default_factory=lambda: [11, 12, 13, 14])
+
+
+def _s(stream=None) -> int:
+    return (stream or torch.cuda.current_stream()).cuda_stream
+
+
+def gemm(A, B, Cout, M: int, R=None, status=None, stream=None):
+    """Cout[:M] = A[:M] @ B^T (+ R[:M]) through hs_gemm_bf16."""
+    N, K = B.shape
+    check(lib.hs_gemm_bf16(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), Cout.data_ptr(),
+                           Cout.stride(0), R.data_ptr() if R is not None else None,
+                           R.stride(0) if R is not None else 0, status.data_ptr(), _s(stream)))
+
+
+class HybridStack:
+    def __init__(self, shape: StackShape, weights: Dict[str, np.ndarray], max_pos: int):
+        self.sh = shape
+        self.W = {k: torch.from_numpy(np.ascontiguousarray(v)).to(DEV).to(torch.bfloat16)
+                  for k, v in weights.items()}
+        opt = np.asarray(weights["embed"], np.float32)[list(shape.option_ids)]
+        self.opt = torch.from_numpy(np.ascontiguousarray(opt)).to(DEV)
+        tab = np.empty((max_pos, shape.head_d // 2, 2), np.float32)
+        check(lib.hs_rope_table(tab.ctypes.data, max_pos, shape.head_d, shape.rope_theta))
+        self.rope = torch.from_numpy(tab).to(DEV)
+        self.max_pos = max_pos
+        self.n_attn = shape.pattern.count("A")
+        self.n_gdn = shape.pattern.count("G")
+        self.status = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    # ------------------------------------------------------------------ pools
+    def alloc(self, Tcap: int, n_pages: int, n_slots: int, n_windows: int = 0, caps=None):
+        sh = self.sh
+        bf = torch.bfloat16
+        self.Tcap = Tcap
+        self.h = torch.zeros((Tcap, sh.hidden), dtype=bf, device=DEV)
+        self.a = torch.zeros_like(self.h)
+        wp_n = max(v.shape[0] for k, v in self.W.items() if k.endswith("wp")) if self.n_gdn else 0
+        self.proj = torch.zeros((Tcap, max(wp_n, 2 * sh.ffn)), dtype=bf, device=DEV)
+        self.q = torch.zeros((Tcap, sh.attn_hq, sh.head_d), dtype=bf, device=DEV)
+        self.k = torch.zeros((Tcap, sh.attn_hkv, sh.head_d), dtype=bf, device=DEV)
+        self.v = torch.zeros_like(self.k)
+        self.o = torch.zeros((Tcap, max(sh.attn_hq * sh.head_d, sh.gdn_h * sh.gdn_d)), dtype=bf, device=DEV)
+        self.gq = torch.zeros((Tcap, sh.gdn_h, sh.gdn_d), dtype=bf, device=DEV)
+        self.gk = torch.zeros_like(self.gq)
+        self.gv = torch.zeros_like(self.gq)
+        self.ga = torch.zeros((Tcap, sh.gdn_h), dtype=torch.float32, device=DEV)
+        self.gb = torch.zeros_like(self.ga)
+        self.m = torch.zeros((Tcap, sh.ffn), dtype=bf, device=DEV)
+        self.kp = [torch.zeros((sh.attn_hkv, n_pages, 16, sh.head_d), dtype=bf, device=DEV) for _ in range(self.n_attn)]
+        self.vp = [torch.zeros_like(t) for t in self.kp]
+        self.state = [torch.zeros((n_slots, sh.gdn_h, sh.gdn_d, sh.gdn_d), dtype=torch.float32, device=DEV)
+                      for _ in range(self.n_gdn)]
+        self.win = [torch.zeros((max(n_windows, 1), wp_n), dtype=bf, device=DEV) for _ in range(self.n_gdn)]
+        self.n_windows = n_windows
+        self.ws = None
+
+    def _ws(self, caps):
+        nb = api.gdn_workspace_bytes(caps, self.sh.gdn_h, self.sh.gdn_d, self.sh.gdn_d)
+        if self.ws is None or self.ws.numel() < nb:
+            self.ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=DEV)
+        return self.ws
+
+    # ---------------------------------------------------------------- forward
+    def forward(self, R: api.Round, meta: torch.Tensor, ids: torch.Tensor, n_readout: int,
+                save_windows: Optional[List[tuple]] = None, stream=None):
+        """One forked prefill round.  ``ids`` device int32 [Tcap] in stream
+        order.  ``save_windows``: [(device src rows int32, device dst rows
+        int32, n)] -- after each GDN layer's projection, copy those stream rows
+        into the layer's conv-window buffer (a checkpoint's window).
+        Returns (final hidden [T, hidden] view, option logprobs [n_readout, n_opt])."""
+        sh, st = self.sh, self.status
+        caps = R.caps
+        T = R.info().n_tokens
+        s = _s(stream)
+        check(lib.hs_embed(ids.data_ptr(), T, self.W["embed"].data_ptr(), sh.vocab, sh.hidden, self.h.data_ptr(),
+                           st.data_ptr(), s))
+        ai = gi = 0
+        for li, kind in enumerate(sh.pattern):
+            p = f"l{li}."
+            check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
+                                 sh.hidden, s))
+            if kind == "A":
+                qv = self.q.view(self.Tcap, -1)
+                kv = self.k.view(self.Tcap, -1)
+                vv = self.v.view(self.Tcap, -1)
+                gemm(self.a, self.W[p + "wq"], qv, T, status=st, stream=stream)
+                gemm(self.a, self.W[p + "wk"], kv, T, status=st, stream=stream)
+                gemm(self.a, self.W[p + "wv"], vv, T, status=st, stream=stream)
+                check(lib.hs_rope_apply(C.byref(caps), meta.data_ptr(), qv.data_ptr(), qv.stride(0), 0, sh.attn_hq,
+                                        sh.head_d, self.rope.data_ptr(), self.max_pos, st.data_ptr(), s))
+                check(lib.hs_rope_apply(C.byref(caps), meta.data_ptr(), kv.data_ptr(), kv.stride(0), 0, sh.attn_hkv,
+                                        sh.head_d, self.rope.data_ptr(), self.max_pos, st.data_ptr(), s))
+                ov = self.o[:, :sh.attn_hq * sh.head_d].view(self.Tcap, sh.attn_hq, sh.head_d)
+                api.fork_attn_prefill(caps, meta, self.q, self.k, self.v, self.kp[ai], self.vp[ai], ov, st,
+                                      stream=stream)
+                gemm(self.o[:, :sh.attn_hq * sh.head_d], self.W[p + "wo"], self.h, T, R=self.h, status=st,
+                     stream=stream)
+                ai += 1
+            else:
+                wp = self.W[p + "wp"]
+                pv = self.proj[:, :wp.shape[0]]
+                gemm(self.a, wp, pv, T, status=st, stream=stream)
+                if save_windows:
+                    for src_rows, dst_rows, n in save_windows:
+                        check(lib.hs_copy_rows(pv.data_ptr(), pv.stride(0) * 2, src_rows.data_ptr(),
+                                               self.win[gi].data_ptr(), self.win[gi].stride(0) * 2,
+                                               dst_rows.data_ptr(), n, wp.shape[0] * 2, s))
+                win = self.win[gi] if self.n_windows else None
+                check(lib.hs_gdn_prep(C.byref(caps), meta.data_ptr(), pv.data_ptr(), pv.stride(0),
+                                      win.data_ptr() if win is not None else None,
+                                      win.stride(0) if win is not None else 0, self.n_windows,
+                                      self.W[p + "conv"].data_ptr(), sh.gdn_h, sh.gdn_d, self.gq.data_ptr(),
+                                      self.gk.data_ptr(), self.gv.data_ptr(), self.ga.data_ptr(), self.gb.data_ptr(),
+                                      st.data_ptr(), s))
+                ov = self.o[:, :sh.gdn_h * sh.gdn_d].view(self.Tcap, sh.gdn_h, sh.gdn_d)
+                api.gdn_fork_prefill(caps, meta, self.gq, self.gk, self.gv, self.ga, self.gb, self.state[gi], ov,
+                                     self._ws(caps), st, stream=stream)
+                gemm(self.o[:, :sh.gdn_h * sh.gdn_d], self.W[p + "wo"], self.h, T, R=self.h, status=st,
+                     stream=stream)
+                gi += 1
+            check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
+                                 sh.hidden, s))
+            gu = self.proj[:, :2 * sh.ffn]
+            gemm(self.a, self.W[p + "wgu"], gu, T, status=st, stream=stream)
+            check(lib.hs_swiglu(gu.data_ptr(), gu.stride(0), T, sh.ffn, self.m.data_ptr(), sh.ffn, s))
+            gemm(self.m, self.W[p + "wd"], self.h, T, R=self.h, status=st, stream=stream)
+        check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(), sh.hidden,
+                             s))
+        lp = torch.empty((max(n_readout, 1), len(sh.option_ids)), dtype=torch.float32, device=DEV)
+        api.choice_logprobs(caps, meta, self.a, self.opt, lp, st, stream=stream)
+        return self.a[:T], lp[:n_readout]

@@ -131,6 +131,13 @@ hs_status hs_gdn_state_resume(hs_round* r, int32_t seg, int32_t ckpt_slot, int32
 hs_status hs_round_attach_history(hs_round* r, int32_t seg, int32_t n_spans, const int32_t* ntok,
                                   const int32_t* pages);
 
+/* Give a resumed ROOT the causal-conv window it continues from: its
+ * kConvTaps-1 = 3 predecessor tokens (oldest first) are rows
+ * window_row0 .. window_row0+2 of the caller's conv-window buffer passed to
+ * hs_gdn_prep (Flide section 3.4: a checkpoint keeps the convolution window).
+ * Without a window, a root's first tokens see zeros before them. */
+hs_status hs_round_set_conv_window(hs_round* r, int32_t seg, int32_t window_row0);
+
 /* Lay out the stream, allocate each node's own KV pages from `pool` (may be
  * NULL for GDN-only rounds), assign temporary GDN state slots
  * [temp_slot0, temp_slot0 + n_temp_slots) to inner nodes, and build the
@@ -266,6 +273,55 @@ hs_status hs_choice_logprobs(const hs_round_caps* caps, const void* dev_meta, hs
                              const void* hidden, int64_t hidden_stride, int32_t hidden_dim,
                              const float* option_rows, int32_t n_opt, float* logprobs,
                              int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Building blocks of a hybrid attention / Gated DeltaNet stack (the        */
+/* per-token parts; Flide section 3.2: pointwise work ignores the tree).     */
+/* All bf16 tensors are row-major with the given leading dimension          */
+/* (elements); every row is computed alone, in a fixed reduction order.     */
+/* ------------------------------------------------------------------------ */
+
+/* C[M,N] = A[M,K] . B[N,K]^T (+ R[M,N]), bf16 in/out, fp32 accumulation in a
+ * fixed order for any M (one 128x128 tile per CTA, no split-K; Flide
+ * section 3.5).  N % 128 == 0, K % 64 == 0, leading dimensions % 8 == 0,
+ * 16-byte aligned pointers.  R may be NULL; R may alias C. */
+hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       void* C, int64_t ldc, const void* R, int64_t ldr, int32_t* dev_status, void* stream);
+/* out[t] = table[ids[t]] (ids: device int32 [T]; an id outside [0,vocab)
+ * gives a zero row and HS_DEV_BAD_META). */
+hs_status hs_embed(const int32_t* ids, int32_t T, const void* table, int32_t vocab, int32_t dim, void* out,
+                   int32_t* dev_status, void* stream);
+/* out = x / sqrt(mean(x^2) + eps) * w   (w bf16 [dim] or NULL for ones) */
+hs_status hs_rmsnorm(const void* x, int64_t ldx, int32_t T, int32_t dim, const void* w, float eps, void* out,
+                     int64_t ldo, void* stream);
+/* Host: cos/sin table [max_pos][d/2][2] fp32 of angle p * theta^(-2i/d),
+ * computed in double. */
+hs_status hs_rope_table(float* host_table, int32_t max_pos, int32_t d, double theta);
+/* In place: rotate-half rotary embedding of n_heads heads of width d at
+ * column col0 of x [Tcap, ldx], each token at its standalone position
+ * (node pos0 + index; Flide section 3.2).  table: device copy of
+ * hs_rope_table. */
+hs_status hs_rope_apply(const hs_round_caps* caps, const void* dev_meta, void* x, int64_t ldx, int32_t col0,
+                        int32_t n_heads, int32_t d, const float* table, int32_t max_pos, int32_t* dev_status,
+                        void* stream);
+/* Gated DeltaNet front end per token: proj [Tcap, ldp] holds q | k | v
+ * (h*d columns each) then a | b (h columns each).  The q, k, v channels go
+ * through a depthwise causal convolution of 4 taps, y_t = sum_k w[ch][k] x_{t-k},
+ * whose predecessors come from the round metadata (across the fork; from
+ * `window` rows [n_window_rows, ldw] for a resumed root), then SiLU; q and k
+ * heads are L2-normalised (eps 1e-6).  alpha = exp(-0.1 softplus(a)),
+ * beta = sigmoid(b).  conv_w bf16 [3*h*d][4]; q, k, v bf16 [Tcap, h, d];
+ * alpha, beta fp32 [Tcap, h]. */
+hs_status hs_gdn_prep(const hs_round_caps* caps, const void* dev_meta, const void* proj, int64_t ldp,
+                      const void* window, int64_t ldw, int32_t n_window_rows, const void* conv_w, int32_t h, int32_t d,
+                      void* q, void* k, void* v, float* alpha, float* beta, int32_t* dev_status, void* stream);
+/* out[t, i] = silu(gu[t, i]) * gu[t, F + i] */
+hs_status hs_swiglu(const void* gu, int64_t ldg, int32_t T, int32_t F, void* out, int64_t ldo, void* stream);
+/* dst row dst_rows[i] = src row src_rows[i] (device int32 row lists; row
+ * strides lds, ldd and width_bytes in BYTES, multiples of 16; a
+ * checkpoint's convolution window, for instance). */
+hs_status hs_copy_rows(const void* src, int64_t lds, const int32_t* src_rows, void* dst, int64_t ldd,
+                       const int32_t* dst_rows, int32_t n, int32_t width_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status and diagnostics                                                    */

@@ -21,7 +21,7 @@ def round_bf16(x) -> np.ndarray:
     r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
     r = np.where(np.abs(x) < 2.0 ** -126, 0.0, r)
     big = 2.0 ** 127 * (2 - 2.0 ** -7)
-    r = np.where(np.abs(r) > big, np.sign(r) * np.inf, r)
+    r = np.where(np.abs(r) > big, np.copysign(np.inf, r), r)
     return r
 
 

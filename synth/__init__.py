@@ -276,3 +276,90 @@ def remap_inputs(src_tree: Tree, src: "GdnInputs | AttnInputs", dst_tree: Tree):
             out_nodes[(r, bd)] = src.nodes[(r, bs)]
     kw = {k: v for k, v in src.__dict__.items() if k not in ("nodes", "hist")}
     return type(src)(nodes=out_nodes, hist=out_hist, **kw)
+
+
+# --------------------------------------------------------------------------
+# hybrid stack workloads (random-init weights, token ids)
+# --------------------------------------------------------------------------
+def _bf16n(rng, shape, std=0.02):
+    return to_bf16_values(rng.standard_normal(shape, dtype=np.float32) * std)
+
+
+def stack_weights(hidden: int, pattern: str, hq: int, hkv: int, d: int, gh: int, gd: int, ffn: int, vocab: int,
+                  taps: int = 4, seed: int = 4100, pad: int = 128) -> Dict[str, np.ndarray]:
+    """All weights N(0, 0.02), rounded to bf16; [out, in] layout.  The fused
+    GDN projection (q | k | v | a | b) is padded with zero rows to a multiple
+    of ``pad``."""
+    rng = np.random.default_rng(seed)
+    W = {"embed": _bf16n(rng, (vocab, hidden))}
+    for li, kind in enumerate(pattern):
+        p = f"l{li}."
+        if kind == "A":
+            W[p + "wq"] = _bf16n(rng, (hq * d, hidden))
+            W[p + "wk"] = _bf16n(rng, (hkv * d, hidden))
+            W[p + "wv"] = _bf16n(rng, (hkv * d, hidden))
+            W[p + "wo"] = _bf16n(rng, (hidden, hq * d))
+        else:
+            n = 3 * gh * gd + 2 * gh
+            npad = -(-n // pad) * pad
+            wp = np.zeros((npad, hidden), np.float32)
+            wp[:n] = _bf16n(rng, (n, hidden))
+            W[p + "wp"] = wp
+            W[p + "conv"] = _bf16n(rng, (3 * gh * gd, taps))
+            W[p + "wo"] = _bf16n(rng, (hidden, gh * gd))
+        W[p + "wgu"] = _bf16n(rng, (2 * ffn, hidden))
+        W[p + "wd"] = _bf16n(rng, (hidden, ffn))
+    return W
+
+
+def token_ids(tree: Tree, vocab: int, seed: int):
+    """Uniform token ids per (request, node) and for each request's history."""
+    nodes, hist = {}, {}
+    for r, req in enumerate(tree.requests):
+        rng = np.random.default_rng(seed + r)
+        n = req.hist_len + sum(req.n_tok)
+        ids = rng.integers(0, vocab, size=n).astype(np.int32)
+        hist[r] = ids[:req.hist_len]
+        for i, part in enumerate(_split_nodes(req, ids, req.hist_len)):
+            nodes[(r, i)] = part
+    return nodes, hist
+
+
+def mixed_tree(seed: int = 4000, n_req: int = 64, lo: int = 512, hi: int = 16384, bmin: int = 2, bmax: int = 12,
+               lmin: int = 8, lmax: int = 128) -> Tree:
+    """Requests with log-uniform trunks in [lo, hi], bmin..bmax branches of U[lmin, lmax] tokens."""
+    rng = np.random.default_rng(seed)
+    reqs = []
+    for _ in range(n_req):
+        P = int(round(np.exp(rng.uniform(np.log(lo), np.log(hi)))))
+        k = int(rng.integers(bmin, bmax + 1))
+        reqs.append(fork_tree(P, [int(x) for x in rng.integers(lmin, lmax + 1, size=k)]))
+    return Tree(reqs)
+
+
+def agent_tree(n_sessions: int = 10, trunk: int = 256, residual: int = 32, fanout: int = 4, depth: int = 3,
+               spine_slot: int = 0) -> Tree:
+    """Sessions of a trunk plus ``depth`` levels of ``fanout`` residuals; the
+    committed spine follows child 0 at every level, and its leaf saves its
+    end state into ``spine_slot + session``."""
+    reqs = []
+    for s in range(n_sessions):
+        r = fanout_tree(trunk, residual, fanout, depth)
+        leaf = spine_leaf(r)
+        r.save = {leaf: spine_slot + s}
+        reqs.append(r)
+    return Tree(reqs)
+
+
+def spine_path(req: Request) -> List[int]:
+    """Root-to-leaf path through child 0 at every level (the committed spine)."""
+    path = [0]
+    while True:
+        kids = [i for i, p in enumerate(req.parents) if p == path[-1]]
+        if not kids:
+            return path
+        path.append(kids[0])
+
+
+def spine_leaf(req: Request) -> int:
+    return spine_path(req)[-1]
