@@ -61,12 +61,13 @@ def _oracle_node(oc, W, tree, ids_nodes, hist, r, node, both=False):
 
 
 def _assert_tv(lp_gpu, oc, W, h64, h32, what):
-    """Option distributions within max(1e-3, twice the fp32 forward's TV)."""
+    """Option distributions within the stated 1e-3 plus twice the fp32
+    forward's TV over the same rows (Flide App. G's rounding-level bar)."""
     p64 = np.exp(ostack.option_logprobs(oc, W, h64))
     p32 = np.exp(ostack.option_logprobs(oc, W, h32))
     tv_ref = float(ochoice.total_variation(p32, p64).max())
     tv = float(ochoice.total_variation(np.exp(lp_gpu), p64).max())
-    assert tv <= max(TV, 2 * tv_ref), (what, tv, tv_ref)
+    assert tv <= TV + 2 * tv_ref, (what, tv, tv_ref)
 
 
 def _assert_rounding_level(got, ref, ref32, what):
@@ -121,11 +122,12 @@ def _agent_round_trip(dims, n_sessions, trunk, residual, depth, extra, check_lea
     ids, hist = synth.token_ids(tree, dims["vocab"], seed=seed)
     T = tree.useful_tokens()
     n_pages = layout.live_pages(tree, 16) + n_sessions * (-(-extra // 16)) + 16
+    n_slots = 32 + sum(r.n_nodes for r in tree.requests) + 8
     stk = HybridStack(sh, W, max_pos=4096)
-    stk.alloc(Tcap=max(T, n_sessions * extra), n_pages=n_pages, n_slots=128, n_windows=3 * n_sessions)
+    stk.alloc(Tcap=max(T, n_sessions * extra), n_pages=n_pages, n_slots=n_slots, n_windows=3 * n_sessions)
     pool = api.PagePool(n_pages)
     # conv windows: the spine leaf's last 3 stream rows -> window rows 3s..3s+2
-    R0, seg0 = rounds.build_round(tree, pool, temp_slot0=32, n_temp_slots=96)
+    R0, seg0 = rounds.build_round(tree, pool, temp_slot0=32, n_temp_slots=n_slots - 32)
     src, dst = [], []
     for s, req in enumerate(tree.requests):
         leaf = synth.spine_leaf(req)
@@ -136,7 +138,7 @@ def _agent_round_trip(dims, n_sessions, trunk, residual, depth, extra, check_lea
     pool = api.PagePool(n_pages)
     sw = [(torch.tensor(src, dtype=torch.int32, device="cuda"), torch.tensor(dst, dtype=torch.int32, device="cuda"),
            len(src))]
-    RA, segA, hidA, lpA = _run(stk, tree, ids, pool=pool, n_slots=128, save_windows=sw)
+    RA, segA, hidA, lpA = _run(stk, tree, ids, pool=pool, n_slots=n_slots, save_windows=sw)
     gotA = rounds.from_stream(RA, segA, hidA)
     for (s, leaf) in check_leaves:
         ref, ref32 = _oracle_node(oc, W, tree, ids, hist, s, leaf, both=True)
@@ -156,17 +158,80 @@ def _agent_round_trip(dims, n_sessions, trunk, residual, depth, extra, check_lea
     for s in range(n_sessions):
         idsB[(s, 0)] = rng.integers(0, dims["vocab"], size=extra).astype(np.int32)
     resume = {s: (s, spans[s], 3 * s) for s in range(n_sessions)}
-    RB, segB, hidB, lpB = _run(stk, treeB, idsB, pool=pool, n_slots=128, resume=resume)
+    RB, segB, hidB, lpB = _run(stk, treeB, idsB, pool=pool, n_slots=n_slots, resume=resume)
     gotB = rounds.from_stream(RB, segB, hidB)
-    for s in range(min(n_sessions, 2)):
+    last64, last32 = [], []
+    n_chk = min(n_sessions, 2)
+    for s in range(n_chk):
         req = tree.requests[s]
         seq = np.concatenate([ids[(s, n)] for n in synth.spine_path(req)] + [idsB[(s, 0)]])
         ref = ostack.forward(oc, W, seq)[-extra:]
         ref32 = ostack.forward(oc, W, seq, gemm_dtype=np.float32)[-extra:]
         _assert_rounding_level(gotB[(s, 0)], ref, ref32, ("B", s))
-        _assert_tv(lpB[s:s + 1], oc, W, ref[-1:], ref32[-1:], ("B", s))
+        last64.append(ref[-1])
+        last32.append(ref32[-1])
+    _assert_tv(lpB[:n_chk], oc, W, np.stack(last64), np.stack(last32), "B")
 
 
 def test_small_agent_tree_commit_and_resume():
     _agent_round_trip(SMALL, n_sessions=3, trunk=64, residual=8, depth=3, extra=48,
                       check_leaves=[(0, 21), (1, 40), (2, 84)], seed=4400)
+
+
+FULL = dict(hidden=2048, pattern="GGGAGGGA", attn_hq=16, attn_hkv=4, head_d=128, gdn_h=16, gdn_d=128, ffn=4096,
+            vocab=32768)
+
+
+def test_agent_tree_full_width_commit_and_resume():
+    """The deep agent tree at full width: 10 sessions, trunk 256, three
+    levels of fan-out 4 of 32-token residuals (multi-level page aliasing),
+    then every committed spine extended by 512 resumed tokens."""
+    _agent_round_trip(FULL, n_sessions=10, trunk=256, residual=32, depth=3, extra=512,
+                      check_leaves=[(0, 21), (7, 84)], seed=5000)
+
+
+def test_mixed_batch_full_width_invariance_and_sampled_parity():
+    """64 requests, trunks log-uniform in [512, 16384], 2-12 branches of
+    U[8,128], 8 layers at width 2048.  Every sampled request re-run alone
+    gives bit-identical rows; the shortest request's trunk and two branches
+    match the oracle at the rounding level."""
+    sh, oc, W = _cfgs(FULL)
+    tree = synth.mixed_tree(seed=4000)
+    ids, hist = synth.token_ids(tree, FULL["vocab"], seed=4500)
+    T = tree.useful_tokens()
+    n_pages = layout.live_pages(tree, 16) + 64
+    n_seg = sum(r.n_nodes for r in tree.requests)
+    stk = HybridStack(sh, W, max_pos=20000)
+    stk.alloc(Tcap=T, n_pages=n_pages, n_slots=n_seg + 8)
+    R, seg_of = rounds.build_round(tree, api.PagePool(n_pages), temp_slot0=0, n_temp_slots=n_seg + 8)
+    meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+    R.upload(meta)
+    idd = torch.from_numpy(rounds.to_stream(R, seg_of, ids)).cuda()
+    hid, lp = stk.forward(R, meta, idd, R.info().n_readouts)
+    torch.cuda.synchronize()
+    api.check_status(stk.status)
+    mixed = hid.clone()
+    rows = {k: (R.segment(s).stream_off, R.segment(s).n_tokens) for k, s in seg_of.items()}
+    lens = [sum(r.n_tok) for r in tree.requests]
+    order = sorted(range(len(lens)), key=lambda r: lens[r])
+    sample = sorted(set(order[:4] + order[-2:] + [7, 31]))
+    for r in sample:
+        req = tree.requests[r]
+        t1 = synth.Tree([synth.Request(parents=req.parents, n_tok=req.n_tok)])
+        ids1 = {(0, i): ids[(r, i)] for i in range(req.n_nodes)}
+        R1, s1 = rounds.build_round(t1, api.PagePool(n_pages), temp_slot0=0, n_temp_slots=8)
+        m1 = torch.empty(R1.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+        R1.upload(m1)
+        i1 = torch.zeros(T, dtype=torch.int32, device="cuda")
+        i1[:R1.info().n_tokens] = torch.from_numpy(rounds.to_stream(R1, s1, ids1)).cuda()
+        h1, _ = stk.forward(R1, m1, i1, R1.info().n_readouts)
+        torch.cuda.synchronize()
+        for i in range(req.n_nodes):
+            a0, n = rows[(r, i)]
+            b0 = R1.segment(s1[(0, i)]).stream_off
+            assert torch.equal(h1[b0:b0 + n], mixed[a0:a0 + n]), ("request", r, "node", i)
+    r = order[0]
+    for i in (0, 1, tree.requests[r].n_nodes - 1):
+        a0, n = rows[(r, i)]
+        ref, ref32 = _oracle_node(oc, W, tree, ids, hist, r, i, both=True)
+        _assert_rounding_level(mixed[a0:a0 + n].float().cpu().numpy(), ref, ref32, ("mixed", r, i))
