@@ -38,6 +38,19 @@ GDN = dict(h=16, d=128, seed=3000)
 WORKLOAD = ("fork_attn trunk4096+8br U[16,64] GQA32/8 d128 page16 bf16 + 4-option readout; "
             "gdn_fork trunk8192+16br U[8,128] H16 d128 chunk64 fp32-state bf16")
 N_OPT = 4
+# DRAM traffic per launch from one ncu capture (profiles/fork_attn_tc_attention_tree.md),
+# valid only while the kernel source still has the hash it was captured with.
+NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "b6fed49680ddae60", 57.80e6)}
+
+
+def ncu_traffic(kernel: str):
+    import hashlib
+    path, sha, nbytes = NCU_TRAFFIC[kernel]
+    try:
+        h = hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return nbytes if h == sha else None
 
 
 def peaks():
@@ -104,7 +117,7 @@ class Clocks:
     def __enter__(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
@@ -188,6 +201,7 @@ class Step:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream()
         self.ev_attn = []
+        self.ev_gdn = []
 
     def build(self):
         """Host round build (C++) for both trees; the GDN trunk saves its end
@@ -213,8 +227,15 @@ class Step:
             self.ev_attn.append((e0, e1))
         api.choice_logprobs(self.a_caps, self.a_meta, s["a_out"].view(s["a_out"].shape[0], -1), self.W, self.lp,
                             self.status)
+        if time_attn:
+            g0 = self.torch.cuda.Event(enable_timing=True)
+            g1 = self.torch.cuda.Event(enable_timing=True)
+            g0.record(self.stream)
         api.gdn_fork_prefill(self.g_caps, self.g_meta, s["g_q"], s["g_k"], s["g_v"], s["g_alpha"], s["g_beta"],
                              self.state, s["g_out"], self.ws, self.status)
+        if time_attn:
+            g1.record(self.stream)
+            self.ev_gdn.append((g0, g1))
         R_a.release(self.pool)
         return R_a, R_g
 
@@ -269,7 +290,7 @@ def cpu_baseline(at, gt, a_inp, g_inp, budget_s: float = 12.0):
     scale = 1 / math.sqrt(ATTN["d"])
     req = at.requests[0]
     P = req.n_tok[0]
-    rows = [int(x) for x in np.linspace(0, P - 1, 32)]
+    rows = [int(x) for x in np.linspace(0, P - 1, 96)]
     ta = time.perf_counter()
     forward.attention_tree(at, a_inp, scale, nodes=[(0, 0)], rows={(0, 0): rows})
     t_rows = (time.perf_counter() - ta) / len(rows)        # mean over positions ~ uniform
@@ -279,7 +300,7 @@ def cpu_baseline(at, gt, a_inp, g_inp, budget_s: float = 12.0):
     attn_est = t_rows * P + t_br * sum(req.n_tok[1:])
     g = gt.requests[0]
     tr = g_inp.nodes[(0, 0)]
-    n_steps = 256
+    n_steps = 1024
     tg = time.perf_counter()
     ogdn.gated_delta_rule(tr["q"][:n_steps], tr["k"][:n_steps], tr["v"][:n_steps], tr["alpha"][:n_steps],
                           tr["beta"][:n_steps])
@@ -326,8 +347,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -359,6 +380,7 @@ def main():
     n0 = _lib.launch_count()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     step.ev_attn = []
+    step.ev_gdn = []
     barrier(ws)
     torch.cuda.synchronize()
     with Clocks(torch.cuda.current_device()) as clk:
@@ -374,6 +396,7 @@ def main():
     api.check_status(step.status)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in step.ev_attn)
+    gdn_ms = statistics.mean(a.elapsed_time(b) for a, b in step.ev_gdn)
     total_ms = reduce_max(torch, sum(step_ms), ws)
     ms_per_step = total_ms / args.steps
     value = ws * tokens * args.steps / (total_ms / 1e3)
@@ -397,8 +420,9 @@ def main():
     fl = attn_flops(at)
     achieved = fl / (attn_ms / 1e3) / 1e12
     peak = pk["bf16_tflops"]
+    tr = ncu_traffic("fork_attn")
     roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": tr,
             "kernel": "fork_attn", "peak_kind": f"{pk_kind} bf16 dense burst",
             "flops_per_launch": fl, "ms_per_launch": round(attn_ms, 4)}
     line = {"metric": "tree-prefill tokens/s (ForkAttn + GDN)", "value": round(value, 1), "unit": "tokens/s",
@@ -409,8 +433,13 @@ def main():
                        "l2": "inputs > L2: 2 rotating input sets (~0.9 GB touched per step)",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof,
-            "kernels": {"fork_attn_ms": round(attn_ms, 4),
-                        "gdn_bytes_per_step": gdn_bytes(gt), "attn_bytes_per_step": attn_bytes(at)},
+            "kernels": {"fork_attn_ms": round(attn_ms, 4), "attn_bytes_per_step": attn_bytes(at),
+                        "gdn_fork_prefill": {
+                            "bound": "hbm", "ms_per_launch": round(gdn_ms, 4), "bytes_per_launch": gdn_bytes(gt),
+                            "achieved": round(gdn_bytes(gt) / (gdn_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+                            "peak": pk["hbm_gbs"],
+                            "frac": round(gdn_bytes(gt) / (gdn_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                            "launches": "chunk-local pass + one state pass per tree level"}},
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clk.summary(), "wall_s": round(wall, 4)}
