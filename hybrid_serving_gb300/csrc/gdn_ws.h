@@ -1,0 +1,26 @@
+// gdn_ws.h -- compact per-(chunk, head) GDN workspace shared by the
+// chunk-local pass and the tensor-core state pass (bf16 inputs, d = 128).
+//
+//   W   [64 tokens][128] bf16, the 128-byte-swizzled K-major shared-memory
+//       image (two [64][64] slabs), ready for a bulk copy into an MMA operand
+//   U   [64 tokens][128] bf16, plain row-major (Ut of the chunked form)
+//   P   [64][64] bf16, swizzled K-major image (one slab)
+//   g   [64] fp32 cumulative log-decay inside the chunk
+#pragma once
+
+namespace gdnws {
+constexpr int kW = 0;
+constexpr int kU = 16384;
+constexpr int kP = 32768;
+constexpr int kG = 40960;
+constexpr int kBytes = 41216;  // per (chunk, head); multiple of 16
+constexpr int kFloats = kBytes / 4;
+
+// Byte offset of bf16 element (row, col) in a 128-byte-swizzled K-major image
+// made of [rows][64]-element slabs (one slab per 64 columns): 16-byte chunk c
+// of a 128-byte row lands at chunk c ^ (row % 8).
+__host__ __device__ inline int sw128_off(int row, int col, int rows) {
+  const int slab = col >> 6, c = col & 63;
+  return slab * rows * 128 + row * 128 + (((c >> 3) ^ (row & 7)) << 4) + (c & 7) * 2;
+}
+}  // namespace gdnws
