@@ -2,9 +2,10 @@
 
 Test infrastructure only.
 
-The pages never define the layer of their hybrid models (parity of the
-stack as a whole is pinned only by this definition and its component
-tests).  The definition taken here: pre-norm residual blocks, each a token
+PARITY UNPINNED as a whole: the pages never define the layer of their
+hybrid models, so the composition below is this oracle's own definition;
+only its components are pinned (tests/test_oracle_stack.py) and the
+mixers it calls (attention, gdn) are pinned on their own.  The definition taken here: pre-norm residual blocks, each a token
 mixer followed by a SwiGLU MLP.
 
 * RMSNorm: x / sqrt(mean(x^2) + eps), weight one.
