@@ -13,23 +13,28 @@
 // blocks of 128 keys starting at each span's first key, so a row's sequence
 // of blocks depends only on its own tree path:
 //
-//   warp 4      TMA producer: Q once; per block K and V pages into a 2-stage
+//   warp 8      TMA producer: Q once; per block K and V pages into a 2-stage
 //               ring (one 128-row box per 64-column half when the 8 pages of
 //               a block are consecutive, else one 16-row box per page; pages
 //               past the span are loaded from out of range, i.e. zeros).
-//   warp 5      allocates TMEM and issues tcgen05.mma from one thread:
+//   warp 9      allocates TMEM and issues tcgen05.mma from one thread:
 //               S_j = Q K_j^T into one of two TMEM score buffers, then
-//               O += P_{j-1} V_{j-1} once the softmax has written P.
-//   warps 0..3  softmax, thread t <-> TMEM lane t <-> query row t: reads S_j,
-//               masks partial blocks, keeps the running max in log2 units,
-//               rescales O and l only when the max grows by more than 2^8
-//               (a per-row decision), writes P into shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads, and at the
-//               end writes O / l.  P is split into a bf16 high part and a
-//               bf16 low part (p - high), both multiplied into O, so P enters
-//               the product with ~16 significant bits instead of 8.
+//               O_c += P_{j-1,c} V_{j-1,c} for the two key halves c once the
+//               softmax has written P.
+//   warps 0..7  softmax.  Warp w serves TMEM lanes 32 (w % 4) .. +31 (query
+//               rows) and key half c = w / 4 (keys 64 c .. 64 c + 63 of every
+//               block): each (row, half) runs its own online softmax over its
+//               half of the keys into its own accumulator O_c, with the
+//               running max in log2 units, rescaling O_c and l_c only when
+//               the max grows by more than 2^8 (a per-(row, half) decision).
+//               P goes to shared memory in the 128-byte-swizzled K-major
+//               layout the MMA reads, split into a bf16 high part and a bf16
+//               low part (p - high), both multiplied into O_c, so P enters
+//               the product with ~16 significant bits.  At the end the two
+//               halves of a row combine (m = max m_c, O = sum 2^(m_c - m) O_c,
+//               l likewise, in a fixed order) and write O / l.
 //
-// TMEM: columns [0,128) and [128,256) = S ping-pong, [256,384) = O.
+// TMEM: columns [0,128) and [128,256) = S ping-pong, [256,384) = O_0, [384,512) = O_1.
 // Shared memory: Q 32 KB | K 2 x 32 KB | V 2 x 32 KB | P hi, lo 2 x 32 KB (SW128).
 // Every wait is bounded; a wait that runs out records HS_DEV_TIMEOUT in the
 // status word, and the CTA drains its own copies and MMAs before leaving.
@@ -54,7 +59,8 @@ constexpr int kOffK = kOffQ + kTile;         // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;     // 2 stages
 constexpr int kOffP = kOffV + 2 * kTile;
 constexpr int kSmemBytes = kOffP + 2 * kTile;  // 224 KB (P as bf16 high and low parts)
-constexpr int kThreads = 192;
+constexpr int kSoftWarps = 8, kWarpProd = 8, kWarpMma = 9;
+constexpr int kThreads = 320;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int HS_DEV_TIMEOUT = 4;
 
@@ -128,15 +134,16 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                     const __grid_constant__ CUtensorMap tm_v128, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_kve[2], bar_sf[2], bar_pf, bar_pv, bar_done;
+  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_kve[2], bar_sf[2], bar_pf, bar_pv, bar_done, bar_x;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   Meta M{p.meta};
-  const int tile = blockIdx.x;
+  // tile-major order: every head of the heaviest tiles first (tiles are sorted by work)
+  const int tile = blockIdx.x / p.hq;
   if (tile >= M.h(H_N_TILE)) return;
   const int32_t* tl = M.tile(tile);
-  const int h = blockIdx.y;
+  const int h = blockIdx.x % p.hq;
   const int kvh = h / (p.hq / p.hkv);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -150,12 +157,13 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc::mbar_init(&bar_kve[s], 1);
       tc::mbar_init(&bar_sf[s], 1);
     }
-    tc::mbar_init(&bar_pf, 128);
+    tc::mbar_init(&bar_pf, 32 * kSoftWarps);
+    tc::mbar_init(&bar_x, 32 * kSoftWarps);
     tc::mbar_init(&bar_pv, 1);
     tc::mbar_init(&bar_done, 1);
     tc::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc::tmem_alloc(&tmem_slot, 512);
     tc::tmem_relinquish();
   }
@@ -169,7 +177,7 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int n_ref = M.h(H_N_PAGE_REF);
   const int32_t* refs = M.page_ref();
 
-  if (warp == 4) {
+  if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
@@ -233,7 +241,7 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t sq = tc::smem_u32(smem + kOffQ);
@@ -247,12 +255,15 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tc::fence_after_sync();
         const uint32_t sv = tc::smem_u32(smem + kOffV + (i & 1) * kTile);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        for (int c = 0; c < 2; ++c) {        // key half c -> accumulator O_c
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t a = tc::sdesc_sw128(sp + part * kTile + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-            const uint64_t b = tc::sdesc_sw128(sv + k * 2048, kSlab, 1024);
-            tc::mma_bf16_ss(tmem + 256, a, b, kIdescPV, (i > 0 || part > 0 || k > 0) ? 1u : 0u);
+          for (int part = 0; part < 2; ++part) {  // P high part, then low part
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = tc::sdesc_sw128(sp + part * kTile + c * kSlab + k * 32, 16, 1024);
+              const uint64_t b = tc::sdesc_sw128(sv + c * 8192 + k * 2048, kSlab, 1024);
+              tc::mma_bf16_ss(tmem + 256 + 128 * c, a, b, kIdescPV, (i > 0 || part > 0 || k > 0) ? 1u : 0u);
+            }
           }
         }
         tc::mma_commit(&bar_pv);
@@ -294,7 +305,8 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;  // row of the tile == TMEM lane
+    const int quarter = warp % 4, hc = warp / 4;  // TMEM lane quarter, key half
+    const int t = quarter * 32 + lane;            // row of the tile == TMEM lane
     const int row = tl[TL_ROW0] + t;
     const bool active = t < tl[TL_N_ROWS];
     int my_seg = -1, my_idx = 0;
@@ -302,7 +314,8 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       my_seg = M.tok(row)[T_SEG];
       my_idx = M.tok(row)[T_IDX];
     }
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t col_s = 64 * hc, col_o = 256 + 128 * hc;
     float m_used = -INFINITY, l = 0.f;
     const float sl2 = p.scale_log2e;
     uint8_t* ps = smem + kOffP;
@@ -310,28 +323,34 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     bool ok = true;
     while (cur.next()) {
       const int st = j & 1;
-      if (!tc::mbar_wait(&bar_sf[st], (j >> 1) & 1, kWaitCycles)) {
+      // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[st], (j >> 1) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + lane_base + st * 128 + c * 32, r[c]);
+      uint32_t r[2][32];
+      tc::tmem_ld32(tmem + lane_base + st * 128 + col_s, r[0]);
+      tc::tmem_ld32(tmem + lane_base + st * 128 + col_s + 32, r[1]);
       tc::tmem_wait_ld();
-      float s[128];
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
       if (!cur.full()) {
-        const int lim = !active ? 0 : !cur.own ? cur.sp_n - cur.b0 : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0);
+        const int lim = (!active ? 0 : !cur.own ? cur.sp_n - cur.b0 : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0)) -
+                        64 * hc;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = i < lim ? s[i] : -INFINITY;
+        for (int i = 0; i < 64; ++i) s[i] = i < lim ? s[i] : -INFINITY;
       }
-      float mx = s[0];
+      // row max of this half: 8 partial maxima, then a fixed tree
+      float mp[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      for (int a = 0; a < 8; ++a) mp[a] = s[a];
+#pragma unroll
+      for (int i = 8; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_new = fmaxf(m_used, mx * sl2);
       float factor = 1.f;
       const bool rescale = m_new > m_used + 8.f;
@@ -340,52 +359,53 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         m_used = m_new;
       }
       const float mref = m_used == -INFINITY ? 0.f : m_used;
-      float rs = 0.f;
+      float rp[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
+      for (int a = 0; a < 8; ++a) rp[a] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
         s[i] = exp2f(fmaf(s[i], sl2, -mref));
-        rs += s[i];
+        rp[i & 7] += s[i];
       }
+      const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       l = l * factor + rs;
-      // the previous P.V must be done before P is overwritten or O rescaled
+      // the previous P.V must be done before P is overwritten or O_c rescaled
       if (j >= 1) {
-        if (!tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles)) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (rescale) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(tmem + lane_base + 256 + c * 32, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-            tc::tmem_st32(tmem + lane_base + 256 + c * 32, o);
-          }
-          tc::tmem_wait_st();
-        }
       }
-      // P row t, K-major, 128-byte swizzle: 16-byte chunk c of a slab row lands at chunk c ^ (t % 8).
-      // High part bf16(p) at ps, low part bf16(p - high) at ps + kTile.
+      // P row t, keys of half hc = slab hc, K-major, 128-byte swizzle: 16-byte chunk c of a slab
+      // row lands at chunk c ^ (t % 8).  High part bf16(p) at ps, low part bf16(p - high) at ps + kTile.
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int c = 0; c < 8; ++c) {
+        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int k0 = half * 64 + c * 8;
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = s[k0 + 2 * e], b = s[k0 + 2 * e + 1];
-            hi[e] = tc::pack_bf16x2(a, b);
-            const float ah = __uint_as_float(hi[e] << 16), bh = __uint_as_float(hi[e] & 0xFFFF0000u);
-            lo[e] = tc::pack_bf16x2(a - ah, b - bh);
-          }
-          const int off = half * kSlab + t * 128 + ((c ^ (t & 7)) << 4);
-          *reinterpret_cast<uint4*>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(ps + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int e = 0; e < 4; ++e) {
+          const float a = s[c * 8 + 2 * e], b = s[c * 8 + 2 * e + 1];
+          hi[e] = tc::pack_bf16x2(a, b);
+          const float ah = __uint_as_float(hi[e] << 16), bh = __uint_as_float(hi[e] & 0xFFFF0000u);
+          lo[e] = tc::pack_bf16x2(a - ah, b - bh);
         }
+        const int off = hc * kSlab + t * 128 + ((c ^ (t & 7)) << 4);
+        *reinterpret_cast<uint4*>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(ps + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      // O_c after the previous P.V, rescaled to the new max (P is written first so s is dead);
+      // the rows of the warp that keep their max multiply by factor = 1, which is exact
+      if (j >= 1 && __any_sync(~0u, rescale)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(tmem + lane_base + col_o + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+          tc::tmem_st32(tmem + lane_base + col_o + c * 32, o);
+        }
+        tc::tmem_wait_st();
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -393,23 +413,43 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       ++j;
     }
     if (ok && j >= 1) {
-      if (tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles)) {
+      // combine the two halves of the row: once the last P.V is done (so every MMA has
+      // read Q), exchange (m, l) through the Q buffer
+      float* xm = reinterpret_cast<float*>(smem + kOffQ);  // [2][128] maxima, then [2][128] sums
+      bool got = __all_sync(~0u, tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles));
+      if (got) {
+        xm[hc * 128 + t] = m_used;
+        xm[256 + hc * 128 + t] = l;
+        tc::mbar_arrive(&bar_x);
+        got = __all_sync(~0u, tc::mbar_wait(&bar_x, 0, kWaitCycles));
+      }
+      if (got) {
         tc::fence_after_sync();
-        const float inv = 1.f / l;
-        __nv_bfloat16* dst = p.out + ((size_t)row * p.hq + h) * kD;
+        const float m0 = xm[t], m1 = xm[128 + t];
+        const float m = fmaxf(m0, m1);
+        const float c0 = m0 == -INFINITY ? 0.f : exp2f(m0 - m);
+        const float c1 = m1 == -INFINITY ? 0.f : exp2f(m1 - m);
+        const float inv = 1.f / (c0 * xm[256 + t] + c1 * xm[384 + t]);
+        const float w0 = c0 * inv, w1 = c1 * inv;
+        __nv_bfloat16* dst = p.out + ((size_t)row * p.hq + h) * kD + 64 * hc;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+        for (int c = 0; c < 2; ++c) {  // output columns 64 hc + 32 c .. +31
+          uint32_t o0[32], o1[32];
+          tc::tmem_ld32(tmem + lane_base + 256 + 64 * hc + 32 * c, o0);
+          tc::tmem_ld32(tmem + lane_base + 384 + 64 * hc + 32 * c, o1);
           tc::tmem_wait_ld();
           if (active) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                f[e] = fmaf(w0, __uint_as_float(o0[q * 8 + e]), w1 * __uint_as_float(o1[q * 8 + e]));
               uint4 v;
-              v.x = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
-              v.y = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
-              v.z = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
-              v.w = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+              v.x = tc::pack_bf16x2(f[0], f[1]);
+              v.y = tc::pack_bf16x2(f[2], f[3]);
+              v.z = tc::pack_bf16x2(f[4], f[5]);
+              v.w = tc::pack_bf16x2(f[6], f[7]);
               *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
             }
           }
@@ -423,7 +463,7 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 5) tc::tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tc::tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -484,7 +524,7 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
     configured = true;
   }
   Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status};
-  fork_attn_tc_kernel<<<dim3(caps->max_tiles, hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
+  fork_attn_tc_kernel<<<dim3(caps->max_tiles * hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
                                                                                         m_v128, prm);
   HS_LAUNCH_CHECK("fork_attn_tc");
   return HS_OK;

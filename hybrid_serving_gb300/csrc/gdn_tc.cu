@@ -229,7 +229,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int ci = 0; ci < n_c; ++ci) {
       const int st = ci & 1, par = ci & 1;
       const uint8_t* sb = smem + kOffStage + st * kStageBytes;
-      if (!tc::mbar_wait(&bar_full[st], (ci >> 1) & 1, kWaitCycles)) {
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[st], (ci >> 1) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
@@ -243,7 +243,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (j == 0) egc[par] = expf(gC);
       }
       tc::named_sync(1, 128);
-      if (!tc::mbar_wait(&bar_d12, par, kWaitCycles)) {
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_d12, par, kWaitCycles))) {
         ok = false;
         break;
       }
@@ -281,7 +281,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       tc::mbar_arrive(&bar_u);
-      if (!tc::mbar_wait(&bar_d34, par, kWaitCycles)) {
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_d34, par, kWaitCycles))) {
         ok = false;
         break;
       }

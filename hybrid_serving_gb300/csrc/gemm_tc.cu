@@ -120,7 +120,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     const int quarter = warp % 4;  // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
     const int row = m0 + r;
-    if (tc::mbar_wait(&bar_acc, 0, kWaitCycles)) {
+    if (__all_sync(~0u, tc::mbar_wait(&bar_acc, 0, kWaitCycles))) {  // warp-wide: tcgen05.ld is collective
       tc::fence_after_sync();
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
