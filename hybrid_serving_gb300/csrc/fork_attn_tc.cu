@@ -13,31 +13,36 @@
 // blocks of 128 keys starting at each span's first key, so a row's sequence
 // of blocks depends only on its own tree path:
 //
-//   warp 8      TMA producer: Q once; per block K and V pages into a 2-stage
+//   warp 8      TMA producer: Q once; per block K and V pages into a 3-stage
 //               ring (one 128-row box per 64-column half when the 8 pages of
 //               a block are consecutive, else one 16-row box per page; pages
-//               past the span are loaded from out of range, i.e. zeros).
+//               past the span are loaded from out of range, i.e. zeros).  A
+//               K stage is refilled once its S has been computed, a V stage
+//               once its P.V has.
 //   warp 9      allocates TMEM and issues tcgen05.mma from one thread:
-//               S_j = Q K_j^T into one of two TMEM score buffers, then
+//               S_j = Q K_j^T into one of two TMEM buffers, then
 //               O_c += P_{j-1,c} V_{j-1,c} for the two key halves c once the
-//               softmax has written P.
+//               softmax has written P_{j-1}, with P read from TMEM.
 //   warps 0..7  softmax.  Warp w serves TMEM lanes 32 (w % 4) .. +31 (query
 //               rows) and key half c = w / 4 (keys 64 c .. 64 c + 63 of every
 //               block): each (row, half) runs its own online softmax over its
 //               half of the keys into its own accumulator O_c, with the
 //               running max in log2 units, rescaling O_c and l_c only when
-//               the max grows by more than 2^8 (a per-(row, half) decision).
-//               P goes to shared memory in the 128-byte-swizzled K-major
-//               layout the MMA reads, split into a bf16 high part and a bf16
-//               low part (p - high), both multiplied into O_c, so P enters
-//               the product with ~16 significant bits.  At the end the two
-//               halves of a row combine (m = max m_c, O = sum 2^(m_c - m) O_c,
-//               l likewise, in a fixed order) and write O / l.
+//               the max grows by more than 2^8 (a per-(row, half) decision;
+//               only then does it wait for the previous P.V).  P_j overwrites
+//               S_j in place, split into a bf16 high part and a bf16 low part
+//               (p - high), both multiplied into O_c, so P enters the product
+//               with ~16 significant bits.  At the end the two halves of a
+//               row combine (m = max m_c, O = sum 2^(m_c - m) O_c, l likewise,
+//               in a fixed order) and write O / l.
 //
-// TMEM: columns [0,128) and [128,256) = S ping-pong, [256,384) = O_0, [384,512) = O_1.
-// Shared memory: Q 32 KB | K 2 x 32 KB | V 2 x 32 KB | P hi, lo 2 x 32 KB (SW128).
-// Every wait is bounded; a wait that runs out records HS_DEV_TIMEOUT in the
-// status word, and the CTA drains its own copies and MMAs before leaving.
+// TMEM: columns [0,128) and [128,256) = S/P ping-pong (half c of a row: S in
+// columns 64c..64c+63, then P high in the first 32 and P low in the next 32),
+// [256,384) = O_0, [384,512) = O_1.  Shared memory: Q 32 KB | K 3 x 32 KB |
+// V 3 x 32 KB (SW128).  MMAs issued by one thread run in issue order, so S_{j+2}
+// overwrites P_j only after P.V_j has read it.  Every wait is bounded; a wait
+// that runs out records HS_DEV_TIMEOUT in the status word, and the CTA drains
+// its own copies and MMAs before leaving.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -54,13 +59,14 @@ constexpr int kD = 128;
 constexpr int kBlk = 128;                    // keys per block
 constexpr int kSlab = 128 * 128;             // bytes of one [128 rows][64 cols] bf16 slab
 constexpr int kTile = 2 * kSlab;             // 32 KB: 128 x 128 bf16
+constexpr int kStages = 3;                   // K/V ring depth
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;         // 2 stages
-constexpr int kOffV = kOffK + 2 * kTile;     // 2 stages
-constexpr int kOffP = kOffV + 2 * kTile;
-constexpr int kSmemBytes = kOffP + 2 * kTile;  // 224 KB (P as bf16 high and low parts)
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kSmemBytes = kOffV + kStages * kTile;  // 224 KB
 constexpr int kSoftWarps = 8, kWarpProd = 8, kWarpMma = 9;
 constexpr int kThreads = 320;
+constexpr uint32_t kTmO = 256;               // O_0 at 256, O_1 at 384
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int HS_DEV_TIMEOUT = 4;
 
@@ -134,7 +140,8 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                     const __grid_constant__ CUtensorMap tm_v128, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_kve[2], bar_sf[2], bar_pf, bar_pv, bar_done, bar_x;
+  __shared__ uint64_t bar_q, bar_kf[kStages], bar_vf[kStages], bar_ke[kStages], bar_ve[kStages];
+  __shared__ uint64_t bar_sf[2], bar_pf[2], bar_pv[2], bar_done, bar_x;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -151,16 +158,19 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (threadIdx.x == 0) {
     abort_flag = 0;
     tc::mbar_init(&bar_q, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&bar_kf[s], 1);
       tc::mbar_init(&bar_vf[s], 1);
-      tc::mbar_init(&bar_kve[s], 1);
-      tc::mbar_init(&bar_sf[s], 1);
+      tc::mbar_init(&bar_ke[s], 1);
+      tc::mbar_init(&bar_ve[s], 1);
     }
-    tc::mbar_init(&bar_pf, 32 * kSoftWarps);
-    tc::mbar_init(&bar_x, 32 * kSoftWarps);
-    tc::mbar_init(&bar_pv, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bar_sf[b], 1);
+      tc::mbar_init(&bar_pf[b], 32 * kSoftWarps);
+      tc::mbar_init(&bar_pv[b], 1);
+    }
     tc::mbar_init(&bar_done, 1);
+    tc::mbar_init(&bar_x, 32 * kSoftWarps);
     tc::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -187,14 +197,8 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc::tma_load_3d(smem + kOffQ, &tm_q, 0, h, tl[TL_ROW0], &bar_q);
       tc::tma_load_3d(smem + kOffQ + kSlab, &tm_q, 64, h, tl[TL_ROW0], &bar_q);
       const int oob_y = p.hkv * p.n_pages * kPage;  // first row past the pool: zero fill
-      int j = 0;
+      int j = 0, s = 0, n = 0;                      // block, its stage, uses of the stage before it
       while (cur.next()) {
-        const int st = j & 1;
-        if (j >= 2 && !tc::mbar_wait(&bar_kve[st], ((j >> 1) - 1) & 1, kWaitCycles)) {
-          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
-          break;
-        }
-        if (*(volatile int*)&abort_flag) break;
         const int npg = (cur.valid() + kPage - 1) / kPage;
         int pg[8];
         bool consecutive = npg == 8;
@@ -212,68 +216,89 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (i > 0 && (pg[i] < 0 || pg[i] != pg[i - 1] + 1)) consecutive = false;
         }
         if (pg[0] < 0) consecutive = false;
-        uint8_t* ks = smem + kOffK + st * kTile;
-        uint8_t* vs = smem + kOffV + st * kTile;
-        tc::mbar_expect_tx(&bar_kf[st], kTile);
-        tc::mbar_expect_tx(&bar_vf[st], kTile);
+        uint8_t* ks = smem + kOffK + s * kTile;
+        uint8_t* vs = smem + kOffV + s * kTile;
+        // K stage s is free once S of block j - kStages is computed
+        if (n > 0 && !tc::mbar_wait(&bar_ke[s], (n - 1) & 1, kWaitCycles)) {
+          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+          break;
+        }
+        if (*(volatile int*)&abort_flag) break;
+        tc::mbar_expect_tx(&bar_kf[s], kTile);
         if (consecutive) {
           const int y = (kvh * p.n_pages + pg[0]) * kPage;
-          for (int half = 0; half < 2; ++half) tc::tma_load_2d(ks + half * kSlab, &tm_k128, half * 64, y, &bar_kf[st]);
-          for (int half = 0; half < 2; ++half) tc::tma_load_2d(vs + half * kSlab, &tm_v128, half * 64, y, &bar_vf[st]);
+          for (int half = 0; half < 2; ++half) tc::tma_load_2d(ks + half * kSlab, &tm_k128, half * 64, y, &bar_kf[s]);
         } else {
           for (int i = 0; i < 8; ++i) {
             const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
             for (int half = 0; half < 2; ++half)
-              tc::tma_load_2d(ks + half * kSlab + i * 2048, &tm_k16, half * 64, y, &bar_kf[st]);
+              tc::tma_load_2d(ks + half * kSlab + i * 2048, &tm_k16, half * 64, y, &bar_kf[s]);
           }
+        }
+        // V stage s is free once P.V of block j - kStages is done
+        if (n > 0 && !tc::mbar_wait(&bar_ve[s], (n - 1) & 1, kWaitCycles)) {
+          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+          ++j;  // the K copy of this block is in flight: drain it below
+          break;
+        }
+        tc::mbar_expect_tx(&bar_vf[s], kTile);
+        if (consecutive) {
+          const int y = (kvh * p.n_pages + pg[0]) * kPage;
+          for (int half = 0; half < 2; ++half) tc::tma_load_2d(vs + half * kSlab, &tm_v128, half * 64, y, &bar_vf[s]);
+        } else {
           for (int i = 0; i < 8; ++i) {
             const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
             for (int half = 0; half < 2; ++half)
-              tc::tma_load_2d(vs + half * kSlab + i * 2048, &tm_v16, half * 64, y, &bar_vf[st]);
+              tc::tma_load_2d(vs + half * kSlab + i * 2048, &tm_v16, half * 64, y, &bar_vf[s]);
           }
         }
         ++j;
+        if (++s == kStages) {
+          s = 0;
+          ++n;
+        }
       }
       // drain: every copy this thread issued has landed before the CTA leaves
       tc::mbar_wait(&bar_q, 0, kWaitCycles);
-      for (int i = (j >= 2 ? j - 2 : 0); i < j; ++i) {
-        tc::mbar_wait(&bar_kf[i & 1], (i >> 1) & 1, kWaitCycles);
-        tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles);
+      for (int i = (j >= kStages ? j - kStages : 0); i < j; ++i) {
+        tc::mbar_wait(&bar_kf[i % kStages], (i / kStages) & 1, kWaitCycles);
+        tc::mbar_wait(&bar_vf[i % kStages], (i / kStages) & 1, kWaitCycles);
       }
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t sq = tc::smem_u32(smem + kOffQ);
-      const uint32_t sp = tc::smem_u32(smem + kOffP);
       bool ok = tc::mbar_wait(&bar_q, 0, kWaitCycles);
       if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
       auto pv = [&](int i) -> bool {
-        if (!tc::mbar_wait(&bar_pf, i & 1, kWaitCycles) ||
-            !tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles))
+        const int si = i % kStages;
+        if (!tc::mbar_wait(&bar_pf[i & 1], (i >> 1) & 1, kWaitCycles) ||
+            !tc::mbar_wait(&bar_vf[si], (i / kStages) & 1, kWaitCycles))
           return false;
         tc::fence_after_sync();
-        const uint32_t sv = tc::smem_u32(smem + kOffV + (i & 1) * kTile);
+        const uint32_t sv = tc::smem_u32(smem + kOffV + si * kTile);
+        const uint32_t pt = tmem + (uint32_t)(i & 1) * 128;  // P_i sits where S_i was
 #pragma unroll
         for (int c = 0; c < 2; ++c) {        // key half c -> accumulator O_c
 #pragma unroll
           for (int part = 0; part < 2; ++part) {  // P high part, then low part
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t a = tc::sdesc_sw128(sp + part * kTile + c * kSlab + k * 32, 16, 1024);
               const uint64_t b = tc::sdesc_sw128(sv + c * 8192 + k * 2048, kSlab, 1024);
-              tc::mma_bf16_ss(tmem + 256 + 128 * c, a, b, kIdescPV, (i > 0 || part > 0 || k > 0) ? 1u : 0u);
+              tc::mma_bf16_ts(tmem + kTmO + 128 * c, pt + 64 * c + 32 * part + 8 * k, b, kIdescPV,
+                              (i > 0 || part > 0 || k > 0) ? 1u : 0u);
             }
           }
         }
-        tc::mma_commit(&bar_pv);
-        tc::mma_commit(&bar_kve[i & 1]);
+        tc::mma_commit(&bar_pv[i & 1]);
+        tc::mma_commit(&bar_ve[si]);
         return true;
       };
       int j = 0;
       while (ok && cur.next()) {
-        const int st = j & 1;
-        if (!tc::mbar_wait(&bar_kf[st], (j >> 1) & 1, kWaitCycles)) {
+        const int s = j % kStages;
+        if (!tc::mbar_wait(&bar_kf[s], (j / kStages) & 1, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -282,14 +307,15 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           ok = false;
           break;
         }
-        const uint32_t sk = tc::smem_u32(smem + kOffK + st * kTile);
+        const uint32_t sk = tc::smem_u32(smem + kOffK + s * kTile);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t a = tc::sdesc_sw128(sq + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
           const uint64_t b = tc::sdesc_sw128(sk + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + st * 128, a, b, kIdescQK, k > 0 ? 1u : 0u);
+          tc::mma_bf16_ss(tmem + (uint32_t)(j & 1) * 128, a, b, kIdescQK, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&bar_sf[st]);
+        tc::mma_commit(&bar_ke[s]);
+        tc::mma_commit(&bar_sf[j & 1]);
         if (j >= 1 && !pv(j - 1)) {
           ok = false;
           break;
@@ -298,7 +324,7 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       if (ok && j >= 1 && !pv(j - 1)) ok = false;
       if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
-      // drain: all MMAs issued by this thread complete before TMEM is freed
+      // every MMA issued by this thread completes before O is read and TMEM is freed
       tc::mma_commit(&bar_done);
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
     }
@@ -315,23 +341,23 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       my_idx = M.tok(row)[T_IDX];
     }
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t col_s = 64 * hc, col_o = 256 + 128 * hc;
+    const uint32_t col_o = kTmO + 128 * hc;
     float m_used = -INFINITY, l = 0.f;
     const float sl2 = p.scale_log2e;
-    uint8_t* ps = smem + kOffP;
     int j = 0;
     bool ok = true;
     while (cur.next()) {
-      const int st = j & 1;
+      const int b = j & 1;
       // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[st], (j >> 1) & 1, kWaitCycles))) {
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[b], (j >> 1) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
+      const uint32_t sb = tmem + lane_base + (uint32_t)b * 128 + 64 * hc;
       uint32_t r[2][32];
-      tc::tmem_ld32(tmem + lane_base + st * 128 + col_s, r[0]);
-      tc::tmem_ld32(tmem + lane_base + st * 128 + col_s + 32, r[1]);
+      tc::tmem_ld32(sb, r[0]);
+      tc::tmem_ld32(sb + 32, r[1]);
       tc::tmem_wait_ld();
       float s[64];
 #pragma unroll
@@ -369,33 +395,24 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       l = l * factor + rs;
-      // the previous P.V must be done before P is overwritten or O_c rescaled
-      if (j >= 1) {
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles))) {
+      // P_j over S_j: keys 2i, 2i+1 of this half in column i (high part), 32 + i (low part)
+      uint32_t hi[32], lo[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float a = s[2 * i], c = s[2 * i + 1];
+        hi[i] = tc::pack_bf16x2(a, c);
+        lo[i] = tc::pack_bf16x2(a - __uint_as_float(hi[i] << 16), c - __uint_as_float(hi[i] & 0xFFFF0000u));
+      }
+      tc::tmem_st32(sb, hi);
+      tc::tmem_st32(sb + 32, lo);
+      // O_c rescaled to the new max once P.V_{j-1} is done; rows of the warp that keep
+      // their max multiply by factor = 1, which is exact
+      if (j >= 1 && __any_sync(~0u, rescale)) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_pv[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-      }
-      // P row t, keys of half hc = slab hc, K-major, 128-byte swizzle: 16-byte chunk c of a slab
-      // row lands at chunk c ^ (t % 8).  High part bf16(p) at ps, low part bf16(p - high) at ps + kTile.
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = s[c * 8 + 2 * e], b = s[c * 8 + 2 * e + 1];
-          hi[e] = tc::pack_bf16x2(a, b);
-          const float ah = __uint_as_float(hi[e] << 16), bh = __uint_as_float(hi[e] & 0xFFFF0000u);
-          lo[e] = tc::pack_bf16x2(a - ah, b - bh);
-        }
-        const int off = hc * kSlab + t * 128 + ((c ^ (t & 7)) << 4);
-        *reinterpret_cast<uint4*>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(ps + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      // O_c after the previous P.V, rescaled to the new max (P is written first so s is dead);
-      // the rows of the warp that keep their max multiply by factor = 1, which is exact
-      if (j >= 1 && __any_sync(~0u, rescale)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -405,18 +422,17 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
           tc::tmem_st32(tmem + lane_base + col_o + c * 32, o);
         }
-        tc::tmem_wait_st();
       }
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bar_pf);
+      tc::mbar_arrive(&bar_pf[b]);
       ++j;
     }
     if (ok && j >= 1) {
-      // combine the two halves of the row: once the last P.V is done (so every MMA has
-      // read Q), exchange (m, l) through the Q buffer
+      // combine the two halves of the row once every MMA is done (so none still reads Q):
+      // exchange (m, l) through the Q buffer
       float* xm = reinterpret_cast<float*>(smem + kOffQ);  // [2][128] maxima, then [2][128] sums
-      bool got = __all_sync(~0u, tc::mbar_wait(&bar_pv, (j - 1) & 1, kWaitCycles));
+      bool got = __all_sync(~0u, tc::mbar_wait(&bar_done, 0, kWaitCycles));
       if (got) {
         xm[hc * 128 + t] = m_used;
         xm[256 + hc * 128 + t] = l;
@@ -435,8 +451,8 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
         for (int c = 0; c < 2; ++c) {  // output columns 64 hc + 32 c .. +31
           uint32_t o0[32], o1[32];
-          tc::tmem_ld32(tmem + lane_base + 256 + 64 * hc + 32 * c, o0);
-          tc::tmem_ld32(tmem + lane_base + 384 + 64 * hc + 32 * c, o1);
+          tc::tmem_ld32(tmem + lane_base + kTmO + 64 * hc + 32 * c, o0);
+          tc::tmem_ld32(tmem + lane_base + kTmO + 128 + 64 * hc + 32 * c, o1);
           tc::tmem_wait_ld();
           if (active) {
 #pragma unroll
