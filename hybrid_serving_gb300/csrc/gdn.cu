@@ -436,7 +436,14 @@ gdn_chunk_local_v2(const int32_t* __restrict__ meta, int H, const T* __restrict_
     uint8_t* dstb = reinterpret_cast<uint8_t*>(wsp);
     for (int e = tid; e < gdnws::kG / 16; e += blockDim.x)
       reinterpret_cast<uint4*>(dstb)[e] = reinterpret_cast<const uint4*>(stg)[e];
-    if (tid < kChunk) reinterpret_cast<float*>(dstb + gdnws::kG)[tid] = gs[tid];
+    float* gd = reinterpret_cast<float*>(dstb + gdnws::kG);
+    const float gC = gs[len - 1];
+    if (tid < kChunk) {
+      gd[tid] = tid < len ? expf(gs[tid]) : 0.f;
+      gd[kChunk + tid] = tid < len ? expf(gC - gs[tid]) : 0.f;
+    } else if (tid == kChunk) {
+      gd[2 * kChunk] = expf(gC);
+    }
   }
 }
 

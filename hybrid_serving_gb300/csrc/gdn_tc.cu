@@ -7,19 +7,29 @@
 //
 // One CTA walks one node's chunks for one head, carrying the whole state S
 // (d_v = 128 rows x d_k = 128) with d_v as the MMA M dimension.  For a chunk
-// with inputs W, Ut, P, g (chunk-local pass) and Q, K (the stream):
+// with inputs W, Ut, P and the decay factors (chunk-local pass) and Q, K (the
+// stream):
 //
 //   D1 = S W^T            U  = Ut^T - D1         (U[j][t], j = row of S)
 //   D2 = S Q^T            U' = U diag(e^{gC-g})
 //   D3 = U P^T            O  = D2 diag(e^g) + D3   -> out[t][h][j]
 //   D4 = U' K             S <- e^{gC} S + D4
 //
-// Warp 4 prefetches the next chunk (bulk copies of W, Ut, P, g from the
-// workspace; TMA boxes of Q and K), warp 5 issues the MMAs from one thread,
-// warps 0..3 (thread j = TMEM lane j = row j of S) keep S in fp32 registers,
-// form U, O and the new S, and write the bf16 MMA operands (S, U, U') into
-// shared memory.  Operands are bf16, accumulation fp32.  Every wait is
-// bounded (HS_DEV_TIMEOUT).
+// S lives in tensor memory twice: in fp32 as the accumulator of D4 (scaled
+// by e^{gC} in place before D4 adds to it) and in bf16 as the A operand of
+// D1 and D2; U and U' are bf16 A operands in tensor memory too, so shared
+// memory holds only the chunk inputs, in a 3-stage ring.  Roles:
+//
+//   warp 8      producer: bulk copies of W, Ut, P and the decay factors from
+//               the workspace, TMA boxes of Q and K, up to 3 chunks ahead;
+//   warp 9      issues the MMAs from one thread, the state chain first
+//               (D1, then D4 as soon as U' is written), the outputs after;
+//   warps 0..3  rows of the state (thread j = TMEM lane j = row j of S):
+//               U and U', the scaling of S, the bf16 copy of S;
+//   warps 4..7  outputs: O for chunk c while the rows already work on c + 1.
+//
+// Operands are bf16, accumulation fp32.  Every wait is bounded
+// (HS_DEV_TIMEOUT).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -34,18 +44,23 @@ using hsd::Meta;
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kWarpProd = 8, kWarpMma = 9;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int HS_DEV_TIMEOUT = 4;
-// shared memory (offsets from a 1024-aligned base)
-constexpr int kOffS = 0;          // S  bf16 [128][128]: 2 slabs of [128][64]
-constexpr int kOffU = 32768;      // U  bf16 [128][64]
-constexpr int kOffUp = 49152;     // U' bf16 [128][64]
-constexpr int kOffStage = 65536;  // 2 stages
+// one stage of chunk inputs (offsets from the stage base)
 constexpr int kStW = 0, kStQ = 16384, kStK = 32768, kStP = 49152, kStUt = 57344, kStG = 73728;
-constexpr int kStageBytes = 74752;  // 73728 + 1024 (g padded)
-constexpr int kSmem = kOffStage + 2 * kStageBytes;
-constexpr uint32_t kStageTx = 16384 * 3 + 8192 + 16384 + 256;
+constexpr int kStageBytes = 74752;  // 73728 + the 1 KB decay block
+constexpr int kStages = 3;
+constexpr int kSmem = kStages * kStageBytes;
+constexpr uint32_t kStageTx = 16384 * 4 + 8192 + 1024;
+static_assert(kStG + (gdnws::kBytes - gdnws::kG) == kStageBytes, "stage layout");
+// tensor-memory columns
+constexpr uint32_t kTS32 = 0;    // S fp32 [128][128]
+constexpr uint32_t kTS16 = 128;  // S bf16, two per column (64)
+constexpr uint32_t kTU = 192;    // U bf16 (32)
+constexpr uint32_t kTUp = 224;   // U' bf16 (32)
+constexpr uint32_t kTD1 = 256, kTD2 = 320, kTD3 = 384;  // fp32 [128][64] each
 
 constexpr uint32_t kIdesc64 = tc::idesc_bf16(128, 64, 0, 0);     // D[128x64], A, B K-major
 constexpr uint32_t kIdesc128mn = tc::idesc_bf16(128, 128, 0, 1); // D[128x128], B N-major (K)
@@ -62,9 +77,8 @@ struct Prm {
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_empty[2], bar_s, bar_u, bar_d12, bar_d34, bar_done;
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_s, bar_u, bar_d1, bar_d4, bar_d23, bar_of, bar_done;
   __shared__ uint32_t tmem_slot;
-  __shared__ float egs[2][64], dks[2][64], egc[2];
   __shared__ int abort_flag;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
@@ -85,18 +99,20 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&bar_full[s], 1);
-      tc::mbar_init(&bar_empty[s], 1);
+      tc::mbar_init(&bar_empty[s], 1 + 8);  // the MMA commit + one arrival per row and output warp
     }
     tc::mbar_init(&bar_s, 128);
     tc::mbar_init(&bar_u, 128);
-    tc::mbar_init(&bar_d12, 1);
-    tc::mbar_init(&bar_d34, 1);
+    tc::mbar_init(&bar_of, 128);
+    tc::mbar_init(&bar_d1, 1);
+    tc::mbar_init(&bar_d4, 1);
+    tc::mbar_init(&bar_d23, 1);
     tc::mbar_init(&bar_done, 1);
     tc::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc::tmem_alloc(&tmem_slot, 512);
     tc::tmem_relinquish();
   }
@@ -104,54 +120,51 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  // TMEM columns: D1 [0,64) D2 [64,128) D3 [128,192) D4 [256,384)
   auto fail = [&]() {
     hsd::set_status(p.status, HS_DEV_TIMEOUT);
     atomicExch(&abort_flag, 1);
   };
+  auto stage = [&](int ci) { return smem + (ci % kStages) * kStageBytes; };
 
-  if (warp == 4) {
+  if (warp == kWarpProd) {
     // ----------------------------------------------------------- producer
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
       int issued = 0;
       for (int ci = 0; ci < n_c; ++ci) {
-        const int st = ci & 1;
-        if (ci >= 2 && !tc::mbar_wait(&bar_empty[st], ((ci >> 1) - 1) & 1, kWaitCycles)) {
+        const int s = ci % kStages, n = ci / kStages;
+        if (n >= 1 && !tc::mbar_wait(&bar_empty[s], (n - 1) & 1, kWaitCycles)) {
           fail();
           break;
         }
         if (*(volatile int*)&abort_flag) break;
-        const int32_t* ch = M.chunk(c_off + ci);
-        const int row0 = ch[C_ROW0];
+        const int row0 = M.chunk(c_off + ci)[C_ROW0];
         const uint8_t* w = p.ws + ((size_t)(c_off + ci) * p.H + h) * gdnws::kBytes;
-        uint8_t* sb = smem + kOffStage + st * kStageBytes;
-        tc::mbar_expect_tx(&bar_full[st], kStageTx);
-        tc::bulk_load(sb + kStW, w + gdnws::kW, 16384, &bar_full[st]);
-        tc::bulk_load(sb + kStUt, w + gdnws::kU, 16384, &bar_full[st]);
-        tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[st]);
-        tc::bulk_load(sb + kStG, w + gdnws::kG, 256, &bar_full[st]);
+        uint8_t* sb = stage(ci);
+        tc::mbar_expect_tx(&bar_full[s], kStageTx);
+        tc::bulk_load(sb + kStW, w + gdnws::kW, 16384, &bar_full[s]);
         for (int half = 0; half < 2; ++half) {
-          tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[st]);
-          tc::tma_load_3d(sb + kStK + half * 8192, &tm_k, half * 64, h, row0, &bar_full[st]);
+          tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
+          tc::tma_load_3d(sb + kStK + half * 8192, &tm_k, half * 64, h, row0, &bar_full[s]);
         }
+        tc::bulk_load(sb + kStUt, w + gdnws::kU, 16384, &bar_full[s]);
+        tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[s]);
+        tc::bulk_load(sb + kStG, w + gdnws::kG, gdnws::kBytes - gdnws::kG, &bar_full[s]);
         ++issued;
       }
-      for (int ci = issued >= 2 ? issued - 2 : 0; ci < issued; ++ci)
-        tc::mbar_wait(&bar_full[ci & 1], (ci >> 1) & 1, kWaitCycles);
+      for (int ci = issued >= kStages ? issued - kStages : 0; ci < issued; ++ci)
+        tc::mbar_wait(&bar_full[ci % kStages], (ci / kStages) & 1, kWaitCycles);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t sS = tc::smem_u32(smem + kOffS);
-      const uint32_t sU = tc::smem_u32(smem + kOffU);
-      const uint32_t sUp = tc::smem_u32(smem + kOffUp);
       bool ok = true;
       for (int ci = 0; ci < n_c && ok; ++ci) {
-        const int st = ci & 1;
-        const uint32_t sb = tc::smem_u32(smem + kOffStage + st * kStageBytes);
-        if (!tc::mbar_wait(&bar_s, ci & 1, kWaitCycles) || !tc::mbar_wait(&bar_full[st], (ci >> 1) & 1, kWaitCycles)) {
+        const int s = ci % kStages;
+        const uint32_t sb = tc::smem_u32(stage(ci));
+        if (!tc::mbar_wait(&bar_s, ci & 1, kWaitCycles) ||
+            !tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) {
           ok = false;
           break;
         }
@@ -161,89 +174,94 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           break;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // D1 = S W^T, D2 = S Q^T   (K = d_k, 16 per step)
-          const uint64_t a = tc::sdesc_sw128(sS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+        for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
           const uint64_t bw = tc::sdesc_sw128(sb + kStW + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-          const uint64_t bq = tc::sdesc_sw128(sb + kStQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + 0, a, bw, kIdesc64, k > 0 ? 1u : 0u);
-          tc::mma_bf16_ss(tmem + 64, a, bq, kIdesc64, k > 0 ? 1u : 0u);
+          tc::mma_bf16_ts(tmem + kTD1, tmem + kTS16 + 8 * k, bw, kIdesc64, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&bar_d12);
+        tc::mma_commit(&bar_d1);
+        // D2 = S Q^T once the output warps have read the previous D2, D3
+        if (ci >= 1 && !tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t bq = tc::sdesc_sw128(sb + kStQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
+          tc::mma_bf16_ts(tmem + kTD2, tmem + kTS16 + 8 * k, bq, kIdesc64, k > 0 ? 1u : 0u);
+        }
         if (!tc::mbar_wait(&bar_u, ci & 1, kWaitCycles)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // D3 = U P^T, D4 = U' K   (K = tokens, 16 per step)
-          const uint64_t au = tc::sdesc_sw128(sU + k * 32, 16, 1024);
-          const uint64_t aup = tc::sdesc_sw128(sUp + k * 32, 16, 1024);
-          const uint64_t bp = tc::sdesc_sw128(sb + kStP + k * 32, 16, 1024);
+        for (int k = 0; k < 4; ++k) {  // S += U' K   (K = tokens; S already scaled by e^{gC})
           const uint64_t bk = tc::sdesc_sw128(sb + kStK + k * 2048, 8192, 1024);
-          tc::mma_bf16_ss(tmem + 128, au, bp, kIdesc64, k > 0 ? 1u : 0u);
-          tc::mma_bf16_ss(tmem + 256, aup, bk, kIdesc128mn, k > 0 ? 1u : 0u);
+          tc::mma_bf16_ts(tmem + kTS32, tmem + kTUp + 8 * k, bk, kIdesc128mn, 1u);
         }
-        tc::mma_commit(&bar_d34);
-        tc::mma_commit(&bar_empty[st]);
+        tc::mma_commit(&bar_d4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // D3 = U P^T
+          const uint64_t bp = tc::sdesc_sw128(sb + kStP + k * 32, 16, 1024);
+          tc::mma_bf16_ts(tmem + kTD3, tmem + kTU + 8 * k, bp, kIdesc64, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bar_d23);
+        tc::mma_commit(&bar_empty[s]);
       }
       if (!ok) fail();
       tc::mma_commit(&bar_done);
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     // ---------------------------------------------------- rows of the state
     const int j = threadIdx.x;  // row of S == TMEM lane
     const uint32_t lb = (uint32_t)(warp * 32) << 16;
-    float S[kD];
-    if (init >= 0) {
-      const float4* src = reinterpret_cast<const float4*>(p.state + (((size_t)init * p.H + h) * kD + j) * kD);
+    // the initial state, in fp32 and as the bf16 operand
+    {
+      const float4* src =
+          init >= 0 ? reinterpret_cast<const float4*>(p.state + (((size_t)init * p.H + h) * kD + j) * kD) : nullptr;
 #pragma unroll
-      for (int i = 0; i < kD / 4; ++i) {
-        const float4 v = src[i];
-        S[4 * i] = v.x;
-        S[4 * i + 1] = v.y;
-        S[4 * i + 2] = v.z;
-        S[4 * i + 3] = v.w;
+      for (int q = 0; q < 4; ++q) {
+        uint32_t f[32], b[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = src ? src[q * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+          f[4 * i] = __float_as_uint(v.x);
+          f[4 * i + 1] = __float_as_uint(v.y);
+          f[4 * i + 2] = __float_as_uint(v.z);
+          f[4 * i + 3] = __float_as_uint(v.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+        tc::tmem_st32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_st16(tmem + lb + kTS16 + q * 16, b);
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kD; ++i) S[i] = 0.f;
-    }
-    auto write_S = [&]() {  // bf16 row j of the A operand, 128-byte swizzle
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint4 v;
-        v.x = tc::pack_bf16x2(S[c * 8 + 0], S[c * 8 + 1]);
-        v.y = tc::pack_bf16x2(S[c * 8 + 2], S[c * 8 + 3]);
-        v.z = tc::pack_bf16x2(S[c * 8 + 4], S[c * 8 + 5]);
-        v.w = tc::pack_bf16x2(S[c * 8 + 6], S[c * 8 + 7]);
-        *reinterpret_cast<uint4*>(smem + kOffS + gdnws::sw128_off(j, c * 8, 128)) = v;
-      }
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bar_s);
-    };
-    write_S();
+    }
     bool ok = true;
     for (int ci = 0; ci < n_c; ++ci) {
-      const int st = ci & 1, par = ci & 1;
-      const uint8_t* sb = smem + kOffStage + st * kStageBytes;
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[st], (ci >> 1) & 1, kWaitCycles))) {
+      const int s = ci % kStages;
+      const uint8_t* sb = stage(ci);
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
-      const int32_t* ch = M.chunk(c_off + ci);
-      const int row0 = ch[C_ROW0], len = ch[C_LEN];
-      const float* g = reinterpret_cast<const float*>(sb + kStG);
-      if (j < 64) {
-        const float gC = g[len - 1];
-        egs[par][j] = j < len ? expf(g[j]) : 0.f;
-        dks[par][j] = j < len ? expf(gC - g[j]) : 0.f;
-        if (j == 0) egc[par] = expf(gC);
+      const float* gblk = reinterpret_cast<const float*>(sb + kStG);  // e^g [64] | e^{gC-g} [64] | e^{gC}
+      // S <- e^{gC} S in place (overlaps D1; D4 adds to it)
+      const float ec = gblk[128];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t f[32];
+        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = __float_as_uint(ec * __uint_as_float(f[e]));
+        tc::tmem_st32(tmem + lb + kTS32 + q * 32, f);
       }
-      tc::named_sync(1, 128);
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_d12, par, kWaitCycles))) {
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_d1, ci & 1, kWaitCycles))) {
         ok = false;
         break;
       }
@@ -252,79 +270,104 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const __nv_bfloat16* ut = reinterpret_cast<const __nv_bfloat16*>(sb + kStUt);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t d1[32];
-        tc::tmem_ld32(tmem + lb + half * 32, d1);
+        uint32_t d1[32], u2[16], up2[16];
+        tc::tmem_ld32(tmem + lb + kTD1 + half * 32, d1);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float u[8], up[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int t = half * 32 + c * 8 + e;
-            u[e] = __bfloat162float(ut[t * kD + j]) - __uint_as_float(d1[c * 8 + e]);
-            up[e] = u[e] * dks[par][t];
-          }
-          const int off = gdnws::sw128_off(j, half * 32 + c * 8, 128);
-          uint4 a, b;
-          a.x = tc::pack_bf16x2(u[0], u[1]);
-          a.y = tc::pack_bf16x2(u[2], u[3]);
-          a.z = tc::pack_bf16x2(u[4], u[5]);
-          a.w = tc::pack_bf16x2(u[6], u[7]);
-          b.x = tc::pack_bf16x2(up[0], up[1]);
-          b.y = tc::pack_bf16x2(up[2], up[3]);
-          b.z = tc::pack_bf16x2(up[4], up[5]);
-          b.w = tc::pack_bf16x2(up[6], up[7]);
-          *reinterpret_cast<uint4*>(smem + kOffU + off) = a;
-          *reinterpret_cast<uint4*>(smem + kOffUp + off) = b;
+        for (int e = 0; e < 16; ++e) {
+          const int t = half * 32 + 2 * e;
+          const float ua = __bfloat162float(ut[t * kD + j]) - __uint_as_float(d1[2 * e]);
+          const float ub = __bfloat162float(ut[(t + 1) * kD + j]) - __uint_as_float(d1[2 * e + 1]);
+          u2[e] = tc::pack_bf16x2(ua, ub);
+          up2[e] = tc::pack_bf16x2(ua * gblk[64 + t], ub * gblk[64 + t + 1]);
         }
+        tc::tmem_st16(tmem + lb + kTU + half * 16, u2);
+        tc::tmem_st16(tmem + lb + kTUp + half * 16, up2);
       }
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bar_u);
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_d34, par, kWaitCycles))) {
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // Ut and the decay block are read
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_d4, ci & 1, kWaitCycles))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      // O = D2 diag(e^g) + D3  -> out[row0 + t][h][j]
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t d2[32], d3[32];
-        tc::tmem_ld32(tmem + lb + 64 + half * 32, d2);
-        tc::tmem_ld32(tmem + lb + 128 + half * 32, d3);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = half * 32 + e;
-          if (t < len)
-            p.out[((size_t)(row0 + t) * p.H + h) * kD + j] =
-                __float2bfloat16_rn(fmaf(egs[par][t], __uint_as_float(d2[e]), __uint_as_float(d3[e])));
-        }
-      }
-      // S <- e^{gC} S + D4
-      const float ec = egc[par];
+      // the bf16 operand of the new state
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t d4[32];
-        tc::tmem_ld32(tmem + lb + 256 + q * 32, d4);
+        uint32_t f[32], b[16];
+        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) S[q * 32 + e] = fmaf(ec, S[q * 32 + e], __uint_as_float(d4[e]));
+        for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+        tc::tmem_st16(tmem + lb + kTS16 + q * 16, b);
       }
-      write_S();
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bar_s);
     }
     if (!ok) {
       fail();
     } else if (endslot >= 0) {
       float4* dst = reinterpret_cast<float4*>(p.state + (((size_t)endslot * p.H + h) * kD + j) * kD);
 #pragma unroll
-      for (int i = 0; i < kD / 4; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+      for (int q = 0; q < 4; ++q) {
+        uint32_t f[32];
+        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[q * 8 + i] = make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]),
+                                       __uint_as_float(f[4 * i + 2]), __uint_as_float(f[4 * i + 3]));
+      }
     }
+  } else {
+    // ------------------------------------------------------------- outputs
+    const int j = threadIdx.x - 128;  // TMEM lane j
+    const uint32_t lb = (uint32_t)((warp - 4) * 32) << 16;
+    bool ok = true;
+    for (int ci = 0; ci < n_c; ++ci) {
+      const int s = ci % kStages;
+      const float* egs = reinterpret_cast<const float*>(stage(ci) + kStG);
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
+          !__all_sync(~0u, tc::mbar_wait(&bar_d23, ci & 1, kWaitCycles))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const int32_t* ch = M.chunk(c_off + ci);
+      const int row0 = ch[C_ROW0], len = ch[C_LEN];
+      __nv_bfloat16* dst = p.out + ((size_t)row0 * p.H + h) * kD + j;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t d2[32], d3[32];
+        tc::tmem_ld32(tmem + lb + kTD2 + half * 32, d2);
+        tc::tmem_ld32(tmem + lb + kTD3 + half * 32, d3);
+        tc::tmem_wait_ld();
+        if (half == 1) {
+          tc::fence_before_sync();
+          tc::mbar_arrive(&bar_of);  // D2, D3 may be overwritten
+        }
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = fmaf(egs[half * 32 + e], __uint_as_float(d2[e]), __uint_as_float(d3[e]));
+        if (half == 1) {
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // e^g is read
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (half * 32 + e < len) dst[(size_t)(half * 32 + e) * p.H * kD] = __float2bfloat16_rn(o[e]);
+      }
+    }
+    if (!ok) fail();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 5) tc::tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tc::tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

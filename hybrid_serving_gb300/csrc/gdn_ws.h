@@ -5,7 +5,9 @@
 //       image (two [64][64] slabs), ready for a bulk copy into an MMA operand
 //   U   [64 tokens][128] bf16, plain row-major (Ut of the chunked form)
 //   P   [64][64] bf16, swizzled K-major image (one slab)
-//   g   [64] fp32 cumulative log-decay inside the chunk
+//   G   decay factors, fp32: e^{g_t} [64] | e^{g_C - g_t} [64] | e^{g_C} [1],
+//       padded to 1 KB (g = cumulative log-decay inside the chunk, C = its
+//       last token; zero past the chunk's length)
 #pragma once
 
 namespace gdnws {
@@ -13,7 +15,7 @@ constexpr int kW = 0;
 constexpr int kU = 16384;
 constexpr int kP = 32768;
 constexpr int kG = 40960;
-constexpr int kBytes = 41216;  // per (chunk, head); multiple of 16
+constexpr int kBytes = 41984;  // per (chunk, head); multiple of 1024
 constexpr int kFloats = kBytes / 4;
 
 // Byte offset of bf16 element (row, col) in a 128-byte-swizzled K-major image
