@@ -25,7 +25,6 @@
 #include <mutex>
 
 #include "device.cuh"
-#include "gdn_ws.h"
 
 using namespace hsm;
 using hsd::Meta;
@@ -306,12 +305,11 @@ __device__ __forceinline__ float dot4(const float4& a, const float4& b) {
 // K, Q, V are staged in fp32 with a 4-float pad so that float4 reads of 8
 // different rows hit 32 different banks.
 // ---------------------------------------------------------------------------
-template <typename T, int D, bool kCompact = false>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chunk_local_v2(const int32_t* __restrict__ meta, int H, const T* __restrict__ q, const T* __restrict__ k,
                    const T* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
                    float* __restrict__ ws) {
-  static_assert(!kCompact || D == 128, "the compact workspace is laid out for d = 128");
   constexpr int L = D + 4;
   constexpr int LA = kChunk + 4;
   extern __shared__ __align__(16) float smA[];
@@ -373,8 +371,8 @@ gdn_chunk_local_v2(const int32_t* __restrict__ meta, int H, const T* __restrict_
     }
   }
   __syncthreads();
-  float* wsp = ws + ((size_t)c * H + h) * (kCompact ? (size_t)gdnws::kFloats : WsLayout<D, D>::FLOATS);
-  if (!kCompact) {
+  float* wsp = ws + ((size_t)c * H + h) * WsLayout<D, D>::FLOATS;
+  {
     for (int e = tid; e < kChunk * (kChunk / 4); e += blockDim.x) {
       const int t = e / (kChunk / 4), s4 = (e % (kChunk / 4)) * 4;
       *reinterpret_cast<float4*>(wsp + WsLayout<D, D>::P + t * kChunk + s4) =
@@ -404,46 +402,9 @@ gdn_chunk_local_v2(const int32_t* __restrict__ meta, int H, const T* __restrict_
       }
       x[t] = acc;
     }
-    if (!kCompact) {
-      float* dst = wsp + (isW ? WsLayout<D, D>::W : WsLayout<D, D>::UT) + cc;
+    float* dst = wsp + (isW ? WsLayout<D, D>::W : WsLayout<D, D>::UT) + cc;
 #pragma unroll
-      for (int t = 0; t < kChunk; ++t) dst[t * D] = x[t];
-    } else {
-      // bf16 images in shared memory (K, Q, V are no longer read), then one coalesced copy out
-      __syncthreads();
-      uint8_t* stg = reinterpret_cast<uint8_t*>(Ks);
-      if (isW) {
-#pragma unroll
-        for (int t = 0; t < kChunk; ++t)
-          *reinterpret_cast<__nv_bfloat16*>(stg + gdnws::kW + gdnws::sw128_off(t, cc, kChunk)) = __float2bfloat16_rn(x[t]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < kChunk; ++t)
-          *reinterpret_cast<__nv_bfloat16*>(stg + gdnws::kU + (t * D + cc) * 2) = __float2bfloat16_rn(x[t]);
-      }
-    }
-  } else if (kCompact) {
-    __syncthreads();
-  }
-  if (kCompact) {
-    uint8_t* stg = reinterpret_cast<uint8_t*>(Ks);
-    for (int e = tid; e < kChunk * kChunk; e += blockDim.x) {
-      const int t = e / kChunk, s = e % kChunk;
-      *reinterpret_cast<__nv_bfloat16*>(stg + gdnws::kP + gdnws::sw128_off(t, s, kChunk)) =
-          __float2bfloat16_rn(Ps[t * LA + s]);
-    }
-    __syncthreads();
-    uint8_t* dstb = reinterpret_cast<uint8_t*>(wsp);
-    for (int e = tid; e < gdnws::kG / 16; e += blockDim.x)
-      reinterpret_cast<uint4*>(dstb)[e] = reinterpret_cast<const uint4*>(stg)[e];
-    float* gd = reinterpret_cast<float*>(dstb + gdnws::kG);
-    const float gC = gs[len - 1];
-    if (tid < kChunk) {
-      gd[tid] = tid < len ? expf(gs[tid]) : 0.f;
-      gd[kChunk + tid] = tid < len ? expf(gC - gs[tid]) : 0.f;
-    } else if (tid == kChunk) {
-      gd[2 * kChunk] = expf(gC);
-    }
+    for (int t = 0; t < kChunk; ++t) dst[t * D] = x[t];
   }
 }
 
@@ -659,6 +620,9 @@ constexpr size_t smemB() {
 hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
                                  const uint8_t* ws, float* state, int n_slots, void* out, int32_t* status,
                                  cudaStream_t st);
+hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
+                                const void* v, const float* alpha, const float* beta, uint8_t* ws, int32_t* status,
+                                cudaStream_t st);
 
 namespace {
 
@@ -676,19 +640,9 @@ hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const v
                   const void* v, const float* alpha, const float* beta, float* state, int n_slots, void* out,
                   float* ws, int32_t* status, cudaStream_t st) {
   if constexpr (sizeof(T) == 2 && D == 128) {
-    // tensor-core state pass over the compact bf16 workspace
-    static bool cfg_tc = false;
-    auto ka = gdn_chunk_local_v2<T, D, true>;
-    if (!cfg_tc) {
-      if (cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemA2<D>()) != cudaSuccess)
-        return hs::fail(HS_ECUDA, "gdn: cannot raise the shared-memory limit");
-      cfg_tc = true;
-    }
-    if (caps->max_chunks > 0) {
-      ka<<<dim3(caps->max_chunks, H), kThreads, smemA2<D>(), st>>>(meta, H, (const T*)q, (const T*)k, (const T*)v,
-                                                                   alpha, beta, ws);
-      HS_LAUNCH_CHECK("gdn_chunk_local");
-    }
+    // tensor cores for both passes, through the compact bf16 workspace
+    const hs_status s = hs_gdn_prep_tc_launch(caps, meta, H, q, k, v, alpha, beta, (uint8_t*)ws, status, st);
+    if (s != HS_OK) return s;
     return hs_gdn_chain_tc_launch(caps, meta, H, q, k, (const uint8_t*)ws, state, n_slots, out, status, st);
   }
   // bf16 inputs take the pipelined state pass; fp32 rows do not fit its double buffer at d=128

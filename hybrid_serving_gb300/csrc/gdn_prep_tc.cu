@@ -1,0 +1,359 @@
+// gdn_prep_tc.cu -- chunk-local pass of the Gated DeltaNet prefill on tcgen05
+// (bf16 inputs, d_k = d_v = 128, chunks of 64 tokens).
+//
+// Flide, "Accelerating Decision Inference with Exact State Forking", section
+// 3.2.2 (Eq. 4, the gated delta rule) regrouped by chunk, every node's chunks
+// starting at its first token (section 3.5).  For one chunk of one head, with
+// g = cumulative sum of log alpha inside the chunk:
+//
+//   A_ts = beta_t e^{g_t - g_s} k_t.k_s  (s < t)      T = (I + A)^{-1}
+//   P_ts = e^{g_t - g_s} q_t.k_s          (s <= t)
+//   W  = T diag(beta e^g) K,   Ut = T diag(beta) V
+//
+// and the decay factors e^{g_t}, e^{g_C - g_t}, e^{g_C} (C = last token).  The
+// results go to the compact workspace that the tensor-core state pass reads
+// (layout in gdn_ws.h).
+//
+// One CTA = one chunk x two heads, so that the two heads' 64 tokens stack
+// into the 128 rows of an MMA:
+//   warp 4      TMA of Q, K, V (both heads), tensor-memory allocation, and the
+//               MMAs from one thread: K K^T and Q K^T (128 x 128, the two
+//               64 x 64 diagonal blocks are used), then per head
+//               W^T = K^T (T diag(beta e^g))^T and Ut^T = V^T (T diag(beta))^T
+//               with K and V read as MN-major A operands straight from their
+//               TMA tiles and T split into a bf16 high and low part.
+//   warps 0..3  thread r = (head r / 64, token r % 64): the decay factors, the
+//               masked rows of A and P, then column r % 64 of T by forward
+//               substitution in fp32, then (as thread = row k of W^T, Ut^T)
+//               the bf16 images of W and Ut, copied out in bulk.
+// Every wait is bounded (HS_DEV_TIMEOUT in the status word).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+#include "gdn_ws.h"
+#include "tc_ptx.cuh"
+
+using namespace hsm;
+using hsd::Meta;
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kThreads = 160;
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr int HS_DEV_TIMEOUT = 4;
+// shared memory (from a 1024-aligned base).  Q, K, V: two [128][64] slabs each
+// (slab = 64 columns of d; rows 0..63 head a, 64..127 head b).
+constexpr int kOffQ = 0, kOffK = 32768, kOffV = 65536;
+constexpr int kOffA = 98304;   // A, fp32 [2][64][64], 16-byte chunks swizzled by row
+constexpr int kOffB = 131072;  // per head: T1 hi, T1 lo, T2 hi, T2 lo, each [64 s][64 t] bf16 (MN-major)
+constexpr int kSmem = kOffB + 2 * 4 * 8192;  // 192 KB
+constexpr uint32_t kInTx = 3 * 32768;
+// tensor-memory columns
+constexpr uint32_t kTKK = 0, kTQK = 128;  // [128][128] fp32 each
+constexpr uint32_t kTW = 256, kTU = 384;  // [128 (d)][64 (t)] per head, heads side by side
+
+constexpr uint32_t kIdescSq = tc::idesc_bf16(128, 128, 0, 0);  // A, B K-major
+constexpr uint32_t kIdescWU = tc::idesc_bf16(128, 64, 1, 1);   // A, B MN-major
+
+struct Prm {
+  const int32_t* meta;
+  int H;
+  const float* alpha;
+  const float* beta;
+  uint8_t* ws;
+  int32_t* status;
+};
+
+__device__ __forceinline__ int a_off(int t, int s) {  // byte offset of A[t][s] in one head's block
+  return t * 256 + ((((s >> 2) ^ (t & 15))) << 4) + (s & 3) * 4;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const Prm p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_in, bar_d, bar_b, bar_w;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float gsh[2][64], bsh[2][64];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+
+  Meta M{p.meta};
+  const int c = blockIdx.x, hp = blockIdx.y;
+  if (c >= M.h(H_N_CHUNK)) return;
+  const int32_t* ch = M.chunk(c);
+  const int row0 = ch[C_ROW0], len = ch[C_LEN];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar_in, 1);
+    tc::mbar_init(&bar_d, 1);
+    tc::mbar_init(&bar_b, 128);
+    tc::mbar_init(&bar_w, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 4) {
+    tc::tmem_alloc(&tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------- copies and MMAs
+    if (lane == 0) {
+      tc::mbar_expect_tx(&bar_in, kInTx);
+      for (int i = 0; i < 2; ++i) {
+        const int hh = 2 * hp + i;  // head H (odd H) is out of range: zero fill
+        for (int half = 0; half < 2; ++half) {
+          const int o = half * 16384 + i * 8192;
+          tc::tma_load_3d(smem + kOffQ + o, &tm_q, half * 64, hh, row0, &bar_in);
+          tc::tma_load_3d(smem + kOffK + o, &tm_k, half * 64, hh, row0, &bar_in);
+          tc::tma_load_3d(smem + kOffV + o, &tm_v, half * 64, hh, row0, &bar_in);
+        }
+      }
+      bool ok = tc::mbar_wait(&bar_in, 0, kWaitCycles);
+      if (ok) {
+        tc::fence_after_sync();
+        const uint32_t sq = tc::smem_u32(smem + kOffQ), sk = tc::smem_u32(smem + kOffK);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // K K^T, Q K^T over d (16 per step)
+          const uint64_t bk = tc::sdesc_sw128(sk + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t aq = tc::sdesc_sw128(sq + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          tc::mma_bf16_ss(tmem + kTKK, bk, bk, kIdescSq, k > 0 ? 1u : 0u);
+          tc::mma_bf16_ss(tmem + kTQK, aq, bk, kIdescSq, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bar_d);
+        ok = tc::mbar_wait(&bar_b, 0, kWaitCycles);
+      }
+      if (ok) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t ak = tc::smem_u32(smem + kOffK + i * 8192);
+          const uint32_t av = tc::smem_u32(smem + kOffV + i * 8192);
+          const uint32_t bb = tc::smem_u32(smem + kOffB + i * 4 * 8192);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // over the chunk's tokens s, 16 per step
+              const uint64_t a_k = tc::sdesc_sw128(ak + k * 2048, 16384, 1024);
+              const uint64_t a_v = tc::sdesc_sw128(av + k * 2048, 16384, 1024);
+              const uint64_t b1 = tc::sdesc_sw128(bb + part * 8192 + k * 2048, 8192, 1024);
+              const uint64_t b2 = tc::sdesc_sw128(bb + (2 + part) * 8192 + k * 2048, 8192, 1024);
+              const uint32_t acc = (part > 0 || k > 0) ? 1u : 0u;
+              tc::mma_bf16_ss(tmem + kTW + 64 * i, a_k, b1, kIdescWU, acc);
+              tc::mma_bf16_ss(tmem + kTU + 64 * i, a_v, b2, kIdescWU, acc);
+            }
+          }
+        }
+      } else {
+        hsd::set_status(p.status, HS_DEV_TIMEOUT);
+      }
+      // every MMA (or none) is complete before anyone reads tensor memory or leaves
+      tc::mma_commit(&bar_w);
+      tc::mbar_wait(&bar_w, 0, kWaitCycles);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- rows
+    const int r = threadIdx.x;  // TMEM lane
+    const int i = r >> 6, t = r & 63;
+    const int hh = 2 * hp + i;
+    const bool valid = hh < p.H;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    uint8_t* wsi = p.ws + ((size_t)c * p.H + (valid ? hh : 0)) * gdnws::kBytes;
+    {
+      const size_t a = (size_t)(row0 + t) * p.H + hh;
+      gsh[i][t] = (valid && t < len) ? logf(p.alpha[a]) : 0.f;
+      bsh[i][t] = (valid && t < len) ? p.beta[a] : 0.f;
+    }
+    tc::named_sync(1, 128);
+    if (t == 0) {  // inclusive cumulative sum, fixed order
+      float acc = 0.f;
+      for (int s = 0; s < 64; ++s) {
+        acc += gsh[i][s];
+        gsh[i][s] = acc;
+      }
+    }
+    tc::named_sync(1, 128);
+    const float gt = gsh[i][t], bt = bsh[i][t];
+    const float gC = gsh[i][len - 1];
+    if (valid) {
+      float* gd = reinterpret_cast<float*>(wsi + gdnws::kG);
+      gd[t] = t < len ? expf(gt) : 0.f;
+      gd[64 + t] = t < len ? expf(gC - gt) : 0.f;
+      if (t == 0) gd[128] = expf(gC);
+    }
+    bool ok = __all_sync(~0u, tc::mbar_wait(&bar_d, 0, kWaitCycles));
+    if (ok) {
+      tc::fence_after_sync();
+      // row t of A (fp32, shared) and of P (bf16, straight to the workspace)
+      uint8_t* Ai = smem + kOffA + i * 16384;
+      uint8_t* Pi = wsi + gdnws::kP;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t kk[32], qk[32];
+        tc::tmem_ld32(tmem + lb + kTKK + 64 * i + 32 * half, kk);
+        tc::tmem_ld32(tmem + lb + kTQK + 64 * i + 32 * half, qk);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          float av[4], pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = half * 32 + c4 * 4 + e;
+            const bool low = s <= t && t < len;
+            const float dec = low ? expf(gt - gsh[i][s]) : 0.f;
+            av[e] = (low && s < t) ? bt * dec * __uint_as_float(kk[c4 * 4 + e]) : 0.f;
+            pv[e] = low ? dec * __uint_as_float(qk[c4 * 4 + e]) : 0.f;
+          }
+          *reinterpret_cast<float4*>(Ai + a_off(t, half * 32 + c4 * 4)) = make_float4(av[0], av[1], av[2], av[3]);
+          if (valid)  // four consecutive s: one half of a 16-byte chunk of P's swizzled row
+            *reinterpret_cast<uint2*>(Pi + gdnws::sw128_off(t, half * 32 + c4 * 4, 64)) =
+                make_uint2(tc::pack_bf16x2(pv[0], pv[1]), tc::pack_bf16x2(pv[2], pv[3]));
+        }
+      }
+    }
+    tc::named_sync(1, 128);
+    // column j = t of T = (I + A)^{-1} by forward substitution: x_u = [u == j] - sum_{s<u} A_us x_s
+    const uint8_t* Ai = smem + kOffA + i * 16384;
+    float x[64];
+#pragma unroll
+    for (int u = 0; u < 64; ++u) {
+      float acc = u == t ? 1.f : 0.f;
+#pragma unroll
+      for (int s = 0; s < u; s += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(Ai + a_off(u, s));
+        acc = fmaf(-a4.x, x[s], acc);
+        if (s + 1 < u) acc = fmaf(-a4.y, x[s + 1], acc);
+        if (s + 2 < u) acc = fmaf(-a4.z, x[s + 2], acc);
+        if (s + 3 < u) acc = fmaf(-a4.w, x[s + 3], acc);
+      }
+      x[u] = acc;
+    }
+    // row j of the MN-major B operands: T1 = T diag(beta e^g), T2 = T diag(beta), high and low bf16 parts
+    {
+      const float s1 = t < len ? bt * expf(gt) : 0.f, s2 = bt;
+      uint8_t* Bi = smem + kOffB + i * 4 * 8192;
+      const int rowb = (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = x[c8 * 8 + 2 * e] * s1, b = x[c8 * 8 + 2 * e + 1] * s1;
+          h1[e] = tc::pack_bf16x2(a, b);
+          l1[e] = tc::pack_bf16x2(a - __uint_as_float(h1[e] << 16), b - __uint_as_float(h1[e] & 0xFFFF0000u));
+          const float a2 = x[c8 * 8 + 2 * e] * s2, b2 = x[c8 * 8 + 2 * e + 1] * s2;
+          h2[e] = tc::pack_bf16x2(a2, b2);
+          l2[e] = tc::pack_bf16x2(a2 - __uint_as_float(h2[e] << 16), b2 - __uint_as_float(h2[e] & 0xFFFF0000u));
+        }
+        const int off = rowb + ((c8 ^ (t & 7)) << 4);
+        *reinterpret_cast<uint4*>(Bi + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+        *reinterpret_cast<uint4*>(Bi + 8192 + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+        *reinterpret_cast<uint4*>(Bi + 16384 + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+        *reinterpret_cast<uint4*>(Bi + 24576 + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    tc::mbar_arrive(&bar_b);
+    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w, 0, kWaitCycles));
+    if (ok) {
+      tc::fence_after_sync();
+      // thread r = row r of W^T and Ut^T (column r of W and Ut): bf16 images in the Q and K buffers
+      const int kd = r;
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint8_t* stg = smem + (which == 0 ? kOffQ : kOffK) + i2 * 16384;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
+            tc::tmem_ld32(tmem + lb + (which == 0 ? kTW : kTU) + 64 * i2 + 32 * half, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int tt = half * 32 + e;
+              const int off = which == 0 ? gdnws::sw128_off(tt, kd, 64) : (tt * kD + kd) * 2;
+              *reinterpret_cast<__nv_bfloat16*>(stg + off) = __float2bfloat16_rn(__uint_as_float(v[e]));
+            }
+          }
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::named_sync(1, 128);
+      if (r == 0) {
+        for (int i2 = 0; i2 < 2; ++i2) {
+          if (2 * hp + i2 >= p.H) continue;
+          uint8_t* dst = p.ws + ((size_t)c * p.H + 2 * hp + i2) * gdnws::kBytes;
+          tc::bulk_store(dst + gdnws::kW, smem + kOffQ + i2 * 16384, 16384);
+          tc::bulk_store(dst + gdnws::kU, smem + kOffK + i2 * 16384, 16384);
+        }
+        tc::bulk_commit();
+        tc::bulk_wait_all();
+      }
+    } else {
+      hsd::set_status(p.status, HS_DEV_TIMEOUT);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 4) tc::tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+bool map_rows(CUtensorMap* m, const void* base, int H, long long T) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Chunk-local pass of every chunk and head into the compact workspace.
+hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
+                                const void* v, const float* alpha, const float* beta, uint8_t* ws, int32_t* status,
+                                cudaStream_t st) {
+  if (caps->max_chunks <= 0) return HS_OK;
+  CUtensorMap mq, mk, mv;
+  if (!map_rows(&mq, q, H, caps->max_tokens) || !map_rows(&mk, k, H, caps->max_tokens) ||
+      !map_rows(&mv, v, H, caps->max_tokens))
+    return hs::fail(HS_ECUDA, "gdn: tensor map encoding failed");
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(gdn_chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
+        cudaSuccess)
+      return hs::fail(HS_ECUDA, "gdn_chunk_prep_tc: cannot raise the shared-memory limit");
+    configured = true;
+  }
+  Prm prm{meta, H, alpha, beta, ws, status};
+  gdn_chunk_prep_tc_kernel<<<dim3(caps->max_chunks, (H + 1) / 2), kThreads, kSmem + 1024, st>>>(mq, mk, mv, prm);
+  HS_LAUNCH_CHECK("gdn_chunk_prep_tc");
+  return HS_OK;
+}
