@@ -617,7 +617,7 @@ constexpr size_t smemB() {
 
 }  // namespace
 
-hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
+hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q,
                                  const uint8_t* ws, float* state, int n_slots, void* out, int32_t* status,
                                  cudaStream_t st);
 hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
@@ -643,7 +643,7 @@ hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const v
     // tensor cores for both passes, through the compact bf16 workspace
     const hs_status s = hs_gdn_prep_tc_launch(caps, meta, H, q, k, v, alpha, beta, (uint8_t*)ws, status, st);
     if (s != HS_OK) return s;
-    return hs_gdn_chain_tc_launch(caps, meta, H, q, k, (const uint8_t*)ws, state, n_slots, out, status, st);
+    return hs_gdn_chain_tc_launch(caps, meta, H, q, (const uint8_t*)ws, state, n_slots, out, status, st);
   }
   // bf16 inputs take the pipelined state pass; fp32 rows do not fit its double buffer at d=128
   constexpr bool kPipelined = sizeof(T) == 2;

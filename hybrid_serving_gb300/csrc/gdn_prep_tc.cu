@@ -10,7 +10,8 @@
 //   P_ts = e^{g_t - g_s} q_t.k_s          (s <= t)
 //   W  = T diag(beta e^g) K,   Ut = T diag(beta) V
 //
-// and the decay factors e^{g_t}, e^{g_C - g_t}, e^{g_C} (C = last token).  The
+// K' = diag(e^{g_C - g}) K, and the decay factors e^{g_t}, e^{g_C - g_t}, e^{g_C}
+// (C = last token).  The
 // results go to the compact workspace that the tensor-core state pass reads
 // (layout in gdn_ws.h).
 //
@@ -24,8 +25,9 @@
 //               TMA tiles and T split into a bf16 high and low part.
 //   warps 0..3  thread r = (head r / 64, token r % 64): the decay factors, the
 //               masked rows of A and P, then column r % 64 of T by forward
-//               substitution in fp32, then (as thread = row k of W^T, Ut^T)
-//               the bf16 images of W and Ut, copied out in bulk.
+//               substitution in fp32, then its row of K' = diag(e^{g_C-g}) K,
+//               then (as thread = row k of W^T, Ut^T) the swizzled bf16 images
+//               of W^T and Ut^T; the three images are copied out in bulk.
 // Every wait is bounded (HS_DEV_TIMEOUT in the status word).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -266,7 +268,30 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
     ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w, 0, kWaitCycles));
     if (ok) {
       tc::fence_after_sync();
-      // thread r = row r of W^T and Ut^T (column r of W and Ut): bf16 images in the Q and K buffers
+      // K' = diag(e^{gC-g}) K: thread r = (head i, token t) scales its row of the K tile into the V buffer
+      // (the wait on the copy barrier, long complete, makes the TMA-written tile visible to this thread)
+      if (__all_sync(~0u, tc::mbar_wait(&bar_in, 0, kWaitCycles))) {
+        const float dk = t < len ? expf(gC - gt) : 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int rowoff = hf * 16384 + i * 8192 + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int off = ((c ^ (t & 7)) << 4);
+            const uint4 kv = *reinterpret_cast<const uint4*>(smem + kOffK + rowoff + off);
+            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o4[e] = tc::pack_bf16x2(dk * __uint_as_float(w4[e] << 16), dk * __uint_as_float(w4[e] & 0xFFFF0000u));
+            *reinterpret_cast<uint4*>(smem + kOffV + i * 16384 + hf * 8192 + t * 128 + off) =
+                make_uint4(o4[0], o4[1], o4[2], o4[3]);
+          }
+        }
+      }
+      tc::named_sync(1, 128);  // every row of the K tile is read before the Ut images overwrite it
+      // thread r = row r of W^T and Ut^T: its 64 tokens as one swizzled 128-byte row of each image
+      // (W images in the Q buffer, Ut images in the K buffer; every MMA is done with both)
       const int kd = r;
 #pragma unroll
       for (int i2 = 0; i2 < 2; ++i2) {
@@ -279,10 +304,13 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
             tc::tmem_ld32(tmem + lb + (which == 0 ? kTW : kTU) + 64 * i2 + 32 * half, v);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int tt = half * 32 + e;
-              const int off = which == 0 ? gdnws::sw128_off(tt, kd, 64) : (tt * kD + kd) * 2;
-              *reinterpret_cast<__nv_bfloat16*>(stg + off) = __float2bfloat16_rn(__uint_as_float(v[e]));
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint4 u;
+              u.x = tc::pack_bf16x2(__uint_as_float(v[c4 * 8 + 0]), __uint_as_float(v[c4 * 8 + 1]));
+              u.y = tc::pack_bf16x2(__uint_as_float(v[c4 * 8 + 2]), __uint_as_float(v[c4 * 8 + 3]));
+              u.z = tc::pack_bf16x2(__uint_as_float(v[c4 * 8 + 4]), __uint_as_float(v[c4 * 8 + 5]));
+              u.w = tc::pack_bf16x2(__uint_as_float(v[c4 * 8 + 6]), __uint_as_float(v[c4 * 8 + 7]));
+              *reinterpret_cast<uint4*>(stg + gdnws::sw128_off(kd, half * 32 + c4 * 8, 128)) = u;
             }
           }
         }
@@ -295,6 +323,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
           uint8_t* dst = p.ws + ((size_t)c * p.H + 2 * hp + i2) * gdnws::kBytes;
           tc::bulk_store(dst + gdnws::kW, smem + kOffQ + i2 * 16384, 16384);
           tc::bulk_store(dst + gdnws::kU, smem + kOffK + i2 * 16384, 16384);
+          tc::bulk_store(dst + gdnws::kK, smem + kOffV + i2 * 16384, 16384);
         }
         tc::bulk_commit();
         tc::bulk_wait_all();

@@ -11,25 +11,30 @@
 // stream):
 //
 //   D1 = S W^T            U  = Ut^T - D1         (U[j][t], j = row of S)
-//   D2 = S Q^T            U' = U diag(e^{gC-g})
+//   D2 = S Q^T
 //   D3 = U P^T            O  = D2 diag(e^g) + D3   -> out[t][h][j]
-//   D4 = U' K             S <- e^{gC} S + D4
+//   D4 = U K'             S <- e^{gC} S + D4,   K' = diag(e^{gC-g}) K
 //
 // S lives in tensor memory twice: in fp32 as the accumulator of D4 (scaled
 // by e^{gC} in place before D4 adds to it) and in bf16 as the A operand of
-// D1 and D2; U and U' are bf16 A operands in tensor memory too, so shared
-// memory holds only the chunk inputs, in a 3-stage ring.  Roles:
+// D1 and D2; U is a bf16 A operand in tensor memory too, so shared memory
+// holds only the chunk inputs, in a 3-stage ring.  Roles:
 //
-//   warp 8      producer: bulk copies of W, Ut, P and the decay factors from
-//               the workspace, TMA boxes of Q and K, up to 3 chunks ahead;
-//   warp 9      issues the MMAs from one thread, the state chain first
-//               (D1, then D4 as soon as U' is written), the outputs after;
+//   warp 8      producer: bulk copies of W^T, Ut^T, P, K' and the decay
+//               factors from the workspace, TMA boxes of Q, up to 3 chunks
+//               ahead;
+//   warp 9      issues the state chain's MMAs (D1, then D4 as soon as U is
+//               written) from one thread;
+//   warp 10     issues the output MMAs (D2, D3) from one thread, so that they
+//               never queue in front of the chain's;
 //   warps 0..3  rows of the state (thread j = TMEM lane j = row j of S):
-//               U and U', the scaling of S, the bf16 copy of S;
-//   warps 4..7  outputs: O for chunk c while the rows already work on c + 1.
+//               U, the scaling of S, the bf16 copy of S;
+//   warps 4..7  outputs: O for chunk c (staged in the chunk's Q buffer, then
+//               written out in 16-byte pieces) while the rows work on c + 1.
 //
-// Operands are bf16, accumulation fp32.  Every wait is bounded
-// (HS_DEV_TIMEOUT).
+// Operands are bf16, accumulation fp32.  The four hand-offs of the state chain
+// (S -> D1 -> U -> D4 -> S) poll their barriers without suspending.  Every
+// wait is bounded (HS_DEV_TIMEOUT).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,8 +49,8 @@ using hsd::Meta;
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 320;
-constexpr int kWarpProd = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+constexpr int kWarpProd = 8, kWarpMma = 9, kWarpOmma = 10;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int HS_DEV_TIMEOUT = 4;
 // one stage of chunk inputs (offsets from the stage base)
@@ -59,11 +64,11 @@ static_assert(kStG + (gdnws::kBytes - gdnws::kG) == kStageBytes, "stage layout")
 constexpr uint32_t kTS32 = 0;    // S fp32 [128][128]
 constexpr uint32_t kTS16 = 128;  // S bf16, two per column (64)
 constexpr uint32_t kTU = 192;    // U bf16 (32)
-constexpr uint32_t kTUp = 224;   // U' bf16 (32)
 constexpr uint32_t kTD1 = 256, kTD2 = 320, kTD3 = 384;  // fp32 [128][64] each
 
-constexpr uint32_t kIdesc64 = tc::idesc_bf16(128, 64, 0, 0);     // D[128x64], A, B K-major
-constexpr uint32_t kIdesc128mn = tc::idesc_bf16(128, 128, 0, 1); // D[128x128], B N-major (K)
+constexpr uint32_t kIdesc64 = tc::idesc_bf16(128, 64, 0, 0);      // D[128x64], B K-major
+constexpr uint32_t kIdesc64mn = tc::idesc_bf16(128, 64, 0, 1);    // D[128x64], B N-major
+constexpr uint32_t kIdesc128mn = tc::idesc_bf16(128, 128, 0, 1);  // D[128x128], B N-major
 
 struct Prm {
   const int32_t* meta;
@@ -75,9 +80,10 @@ struct Prm {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, const Prm p) {
+gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_s, bar_u, bar_d1, bar_d4, bar_d23, bar_of, bar_done;
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_s, bar_u, bar_of;
+  __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -101,15 +107,17 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&bar_full[s], 1);
-      tc::mbar_init(&bar_empty[s], 1 + 8);  // the MMA commit + one arrival per row and output warp
+      tc::mbar_init(&bar_empty[s], 2 + 8);  // two MMA commits + one arrival per row and output warp
     }
     tc::mbar_init(&bar_s, 128);
     tc::mbar_init(&bar_u, 128);
     tc::mbar_init(&bar_of, 128);
     tc::mbar_init(&bar_d1, 1);
     tc::mbar_init(&bar_d4, 1);
+    tc::mbar_init(&bar_d2, 1);
     tc::mbar_init(&bar_d23, 1);
     tc::mbar_init(&bar_done, 1);
+    tc::mbar_init(&bar_done2, 1);
     tc::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -130,7 +138,6 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // ----------------------------------------------------------- producer
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_k);
       int issued = 0;
       for (int ci = 0; ci < n_c; ++ci) {
         const int s = ci % kStages, n = ci / kStages;
@@ -144,62 +151,80 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         uint8_t* sb = stage(ci);
         tc::mbar_expect_tx(&bar_full[s], kStageTx);
         tc::bulk_load(sb + kStW, w + gdnws::kW, 16384, &bar_full[s]);
-        for (int half = 0; half < 2; ++half) {
-          tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
-          tc::tma_load_3d(sb + kStK + half * 8192, &tm_k, half * 64, h, row0, &bar_full[s]);
-        }
         tc::bulk_load(sb + kStUt, w + gdnws::kU, 16384, &bar_full[s]);
-        tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[s]);
         tc::bulk_load(sb + kStG, w + gdnws::kG, gdnws::kBytes - gdnws::kG, &bar_full[s]);
+        tc::bulk_load(sb + kStK, w + gdnws::kK, 16384, &bar_full[s]);
+        for (int half = 0; half < 2; ++half)
+          tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
+        tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[s]);
         ++issued;
       }
       for (int ci = issued >= kStages ? issued - kStages : 0; ci < issued; ++ci)
         tc::mbar_wait(&bar_full[ci % kStages], (ci / kStages) & 1, kWaitCycles);
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- MMA
+    // ------------------------------------------------ MMA: the state chain
+    if (lane == 0) {
+      bool ok = true;
+      for (int ci = 0; ci < n_c && ok; ++ci) {
+        const int s = ci % kStages;
+        const uint32_t sb = tc::smem_u32(stage(ci));
+        if (!tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles) ||
+            !tc::mbar_wait_spin(&bar_s, ci & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
+          const uint64_t bw = tc::sdesc_sw128(sb + kStW + k * 2048, 16384, 1024);
+          tc::mma_bf16_ts(tmem + kTD1, tmem + kTS16 + 8 * k, bw, kIdesc64mn, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bar_d1);
+        if (!tc::mbar_wait_spin(&bar_u, ci & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // S += U K'   (K = tokens; S already scaled by e^{gC})
+          const uint64_t bk = tc::sdesc_sw128(sb + kStK + k * 2048, 8192, 1024);
+          tc::mma_bf16_ts(tmem + kTS32, tmem + kTU + 8 * k, bk, kIdesc128mn, 1u);
+        }
+        tc::mma_commit(&bar_d4);
+        tc::mma_commit(&bar_empty[s]);
+        if (*(volatile int*)&abort_flag) ok = false;
+      }
+      if (!ok) fail();
+      tc::mma_commit(&bar_done);
+      tc::mbar_wait(&bar_done, 0, kWaitCycles);
+    }
+    __syncwarp();
+  } else if (warp == kWarpOmma) {
+    // -------------------------------------------------- MMA: the outputs
     if (lane == 0) {
       bool ok = true;
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
         if (!tc::mbar_wait(&bar_s, ci & 1, kWaitCycles) ||
-            !tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) {
+            !tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles) ||
+            (ci >= 1 && !tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (*(volatile int*)&abort_flag) {
-          ok = false;
-          break;
-        }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
-          const uint64_t bw = tc::sdesc_sw128(sb + kStW + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ts(tmem + kTD1, tmem + kTS16 + 8 * k, bw, kIdesc64, k > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(&bar_d1);
-        // D2 = S Q^T once the output warps have read the previous D2, D3
-        if (ci >= 1 && !tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 8; ++k) {  // D2 = S Q^T
           const uint64_t bq = tc::sdesc_sw128(sb + kStQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
           tc::mma_bf16_ts(tmem + kTD2, tmem + kTS16 + 8 * k, bq, kIdesc64, k > 0 ? 1u : 0u);
         }
+        tc::mma_commit(&bar_d2);
         if (!tc::mbar_wait(&bar_u, ci & 1, kWaitCycles)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // S += U' K   (K = tokens; S already scaled by e^{gC})
-          const uint64_t bk = tc::sdesc_sw128(sb + kStK + k * 2048, 8192, 1024);
-          tc::mma_bf16_ts(tmem + kTS32, tmem + kTUp + 8 * k, bk, kIdesc128mn, 1u);
-        }
-        tc::mma_commit(&bar_d4);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // D3 = U P^T
           const uint64_t bp = tc::sdesc_sw128(sb + kStP + k * 32, 16, 1024);
@@ -207,10 +232,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         tc::mma_commit(&bar_d23);
         tc::mma_commit(&bar_empty[s]);
+        if (*(volatile int*)&abort_flag) ok = false;
       }
       if (!ok) fail();
-      tc::mma_commit(&bar_done);
-      tc::mbar_wait(&bar_done, 0, kWaitCycles);
+      tc::mma_commit(&bar_done2);
+      tc::mbar_wait(&bar_done2, 0, kWaitCycles);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -261,35 +287,41 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         for (int e = 0; e < 32; ++e) f[e] = __float_as_uint(ec * __uint_as_float(f[e]));
         tc::tmem_st32(tmem + lb + kTS32 + q * 32, f);
       }
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_d1, ci & 1, kWaitCycles))) {
+      // D1 done; D3 of the previous chunk (which reads U) done
+      if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d1, ci & 1, kWaitCycles)) ||
+          (ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_d23, (ci - 1) & 1, kWaitCycles)))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      // U = Ut^T - D1,  U' = U diag(e^{gC-g})
-      const __nv_bfloat16* ut = reinterpret_cast<const __nv_bfloat16*>(sb + kStUt);
+      // U = Ut^T - D1;  row j of Ut^T is one swizzled 128-byte row
+      const uint8_t* utj = sb + kStUt + j * 128;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t d1[32], u2[16], up2[16];
+        uint32_t d1[32], u2[16];
         tc::tmem_ld32(tmem + lb + kTD1 + half * 32, d1);
+        uint4 uv[4];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) uv[c4] = *reinterpret_cast<const uint4*>(utj + (((half * 4 + c4) ^ (j & 7)) << 4));
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int t = half * 32 + 2 * e;
-          const float ua = __bfloat162float(ut[t * kD + j]) - __uint_as_float(d1[2 * e]);
-          const float ub = __bfloat162float(ut[(t + 1) * kD + j]) - __uint_as_float(d1[2 * e + 1]);
-          u2[e] = tc::pack_bf16x2(ua, ub);
-          up2[e] = tc::pack_bf16x2(ua * gblk[64 + t], ub * gblk[64 + t + 1]);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t w4[4] = {uv[c4].x, uv[c4].y, uv[c4].z, uv[c4].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            u2[c4 * 4 + e] = tc::pack_bf16x2(__uint_as_float(w4[e] << 16) - __uint_as_float(d1[c4 * 8 + 2 * e]),
+                                             __uint_as_float(w4[e] & 0xFFFF0000u) - __uint_as_float(d1[c4 * 8 + 2 * e + 1]));
         }
         tc::tmem_st16(tmem + lb + kTU + half * 16, u2);
-        tc::tmem_st16(tmem + lb + kTUp + half * 16, up2);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bar_u);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // Ut and the decay block are read
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_d4, ci & 1, kWaitCycles))) {
+      // D4 done (new S), D2 done (the bf16 S may be overwritten)
+      if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d4, ci & 1, kWaitCycles)) ||
+          !__all_sync(~0u, tc::mbar_wait(&bar_d2, ci & 1, kWaitCycles))) {
         ok = false;
         break;
       }
@@ -330,7 +362,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     bool ok = true;
     for (int ci = 0; ci < n_c; ++ci) {
       const int s = ci % kStages;
-      const float* egs = reinterpret_cast<const float*>(stage(ci) + kStG);
+      uint8_t* sb = stage(ci);
+      const float* egs = reinterpret_cast<const float*>(sb + kStG);
       if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
           !__all_sync(~0u, tc::mbar_wait(&bar_d23, ci & 1, kWaitCycles))) {
         ok = false;
@@ -339,28 +372,41 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc::fence_after_sync();
       const int32_t* ch = M.chunk(c_off + ci);
       const int row0 = ch[C_ROW0], len = ch[C_LEN];
-      __nv_bfloat16* dst = p.out + ((size_t)row0 * p.H + h) * kD + j;
+      // D2, D3 and e^g into registers first, so that D2, D3 are released at once and the
+      // staging stores below do not wait on loads from the same buffer
+      uint32_t d2[64], d3[64];
+      tc::tmem_ld32(tmem + lb + kTD2, *reinterpret_cast<uint32_t(*)[32]>(d2));
+      tc::tmem_ld32(tmem + lb + kTD2 + 32, *reinterpret_cast<uint32_t(*)[32]>(d2 + 32));
+      tc::tmem_ld32(tmem + lb + kTD3, *reinterpret_cast<uint32_t(*)[32]>(d3));
+      tc::tmem_ld32(tmem + lb + kTD3 + 32, *reinterpret_cast<uint32_t(*)[32]>(d3 + 32));
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bar_of);  // D2, D3 may be overwritten
+      float o[64];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t d2[32], d3[32];
-        tc::tmem_ld32(tmem + lb + kTD2 + half * 32, d2);
-        tc::tmem_ld32(tmem + lb + kTD3 + half * 32, d3);
-        tc::tmem_wait_ld();
-        if (half == 1) {
-          tc::fence_before_sync();
-          tc::mbar_arrive(&bar_of);  // D2, D3 may be overwritten
-        }
-        float o[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = fmaf(egs[half * 32 + e], __uint_as_float(d2[e]), __uint_as_float(d3[e]));
-        if (half == 1) {
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // e^g is read
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (half * 32 + e < len) dst[(size_t)(half * 32 + e) * p.H * kD] = __float2bfloat16_rn(o[e]);
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 e = *reinterpret_cast<const float4*>(egs + 4 * c4);
+        o[4 * c4] = fmaf(e.x, __uint_as_float(d2[4 * c4]), __uint_as_float(d3[4 * c4]));
+        o[4 * c4 + 1] = fmaf(e.y, __uint_as_float(d2[4 * c4 + 1]), __uint_as_float(d3[4 * c4 + 1]));
+        o[4 * c4 + 2] = fmaf(e.z, __uint_as_float(d2[4 * c4 + 2]), __uint_as_float(d3[4 * c4 + 2]));
+        o[4 * c4 + 3] = fmaf(e.w, __uint_as_float(d2[4 * c4 + 3]), __uint_as_float(d3[4 * c4 + 3]));
       }
+      // O[t][j] into the chunk's Q buffer (D2 has read it), plain [64][128] bf16
+      __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sb + kStQ);
+#pragma unroll
+      for (int t = 0; t < 64; ++t) stg[t * kD + j] = __float2bfloat16_rn(o[t]);
+      tc::named_sync(2, 128);
+      __nv_bfloat16* dst = p.out + ((size_t)row0 * p.H + h) * kD;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = j + 128 * i, t = e >> 4, c16 = e & 15;
+        if (t < len)
+          *reinterpret_cast<uint4*>(dst + (size_t)t * p.H * kD + c16 * 8) =
+              *reinterpret_cast<const uint4*>(sb + kStQ + t * 256 + c16 * 16);
+      }
+      tc::fence_proxy_async_smem();  // the Q buffer is refilled by TMA after this
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar_empty[s]);
     }
     if (!ok) fail();
   }
@@ -399,11 +445,11 @@ bool map_rows(CUtensorMap* m, const void* base, int H, long long T) {
 
 // State passes of every tree level on tensor cores, reading the compact
 // workspace written by the chunk-local pass.
-hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
+hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q,
                                  const uint8_t* ws, float* state, int n_slots, void* out, int32_t* status,
                                  cudaStream_t st) {
-  CUtensorMap mq, mk;
-  if (!map_rows(&mq, q, H, caps->max_tokens) || !map_rows(&mk, k, H, caps->max_tokens))
+  CUtensorMap mq;
+  if (!map_rows(&mq, q, H, caps->max_tokens))
     return hs::fail(HS_ECUDA, "gdn: tensor map encoding failed");
   static bool configured = false;
   if (!configured) {
@@ -414,7 +460,7 @@ hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta,
   }
   for (int lev = 0; lev < caps->max_levels && caps->max_segments > 0; ++lev) {
     Prm prm{meta, lev, H, n_slots, ws, state, (__nv_bfloat16*)out, status};
-    gdn_chain_tc_kernel<<<dim3(caps->max_segments, H), kThreads, kSmem + 1024, st>>>(mq, mk, prm);
+    gdn_chain_tc_kernel<<<dim3(caps->max_segments, H), kThreads, kSmem + 1024, st>>>(mq, prm);
     HS_LAUNCH_CHECK("gdn_chain_tc");
   }
   return HS_OK;

@@ -1,10 +1,14 @@
 // gdn_ws.h -- compact per-(chunk, head) GDN workspace shared by the
 // chunk-local pass and the tensor-core state pass (bf16 inputs, d = 128).
 //
-//   W   [64 tokens][128] bf16, the 128-byte-swizzled K-major shared-memory
-//       image (two [64][64] slabs), ready for a bulk copy into an MMA operand
-//   U   [64 tokens][128] bf16, plain row-major (Ut of the chunked form)
+//   W   bf16, the 128-byte-swizzled image of W^T: row k (128 rows, d_k) holds
+//       W[t][k] for the 64 tokens t (one [128][64] slab) -- the MN-major
+//       B operand of S W^T, and one row per thread for the writer
+//   U   bf16, Ut^T in the same layout: row j (d_v) holds Ut[t][j]
 //   P   [64][64] bf16, swizzled K-major image (one slab)
+//   K'  bf16, diag(e^{g_C - g}) K: [64 tokens][128] as two swizzled [64][64]
+//       slabs (the image a TMA box of K would give), the MN-major B operand
+//       of the state update
 //   G   decay factors, fp32: e^{g_t} [64] | e^{g_C - g_t} [64] | e^{g_C} [1],
 //       padded to 1 KB (g = cumulative log-decay inside the chunk, C = its
 //       last token; zero past the chunk's length)
@@ -14,8 +18,9 @@ namespace gdnws {
 constexpr int kW = 0;
 constexpr int kU = 16384;
 constexpr int kP = 32768;
-constexpr int kG = 40960;
-constexpr int kBytes = 41984;  // per (chunk, head); multiple of 1024
+constexpr int kK = 40960;
+constexpr int kG = 57344;
+constexpr int kBytes = 58368;  // per (chunk, head); multiple of 1024
 constexpr int kFloats = kBytes / 4;
 
 // Byte offset of bf16 element (row, col) in a 128-byte-swizzled K-major image
