@@ -16,19 +16,23 @@
 // (layout in gdn_ws.h).
 //
 // One CTA = one chunk x two heads, so that the two heads' 64 tokens stack
-// into the 128 rows of an MMA:
+// into the 128 rows of an MMA; two CTAs share an SM (96 KB of shared memory,
+// 256 tensor-memory columns each), so one's copies and waits overlap the
+// other's arithmetic:
 //   warp 4      TMA of Q, K, V (both heads), tensor-memory allocation, and the
 //               MMAs from one thread: K K^T and Q K^T (128 x 128, the two
 //               64 x 64 diagonal blocks are used), then per head
-//               W^T = K^T (T diag(beta e^g))^T and Ut^T = V^T (T diag(beta))^T
-//               with K and V read as MN-major A operands straight from their
-//               TMA tiles and T split into a bf16 high and low part.
+//               W^T = K^T (T diag(beta e^g))^T and, once those are done,
+//               Ut^T = V^T (T diag(beta))^T, with K and V read as MN-major A
+//               operands straight from their TMA tiles and T split into a
+//               bf16 high and low part.
 //   warps 0..3  thread r = (head r / 64, token r % 64): the decay factors, the
 //               masked rows of A and P, then column r % 64 of T by forward
 //               substitution in fp32, then its row of K' = diag(e^{g_C-g}) K,
 //               then (as thread = row k of W^T, Ut^T) the swizzled bf16 images
 //               of W^T and Ut^T; the three images are copied out in bulk.
-// Every wait is bounded (HS_DEV_TIMEOUT in the status word).
+// Shared memory: Q | K | V, 32 KB each.  The Q buffer is reused for A (fp32)
+// once Q K^T is done, then for the T operands, then for the W^T images.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -49,13 +53,13 @@ constexpr int HS_DEV_TIMEOUT = 4;
 // shared memory (from a 1024-aligned base).  Q, K, V: two [128][64] slabs each
 // (slab = 64 columns of d; rows 0..63 head a, 64..127 head b).
 constexpr int kOffQ = 0, kOffK = 32768, kOffV = 65536;
-constexpr int kOffA = 98304;   // A, fp32 [2][64][64], 16-byte chunks swizzled by row
-constexpr int kOffB = 131072;  // per head: T1 hi, T1 lo, T2 hi, T2 lo, each [64 s][64 t] bf16 (MN-major)
-constexpr int kSmem = kOffB + 2 * 4 * 8192;  // 192 KB
+constexpr int kSmem = 98304;
+constexpr int kOffA = kOffQ;  // A, fp32 [2][64][64], 16-byte chunks swizzled by row (after Q K^T)
+constexpr int kOffT = kOffQ;  // per head: T hi, T lo, each [64 s][64 t] bf16 MN-major (after the solve)
 constexpr uint32_t kInTx = 3 * 32768;
-// tensor-memory columns
+// tensor-memory columns (256): K K^T and Q K^T, then W^T and Ut^T over them
 constexpr uint32_t kTKK = 0, kTQK = 128;  // [128][128] fp32 each
-constexpr uint32_t kTW = 256, kTU = 384;  // [128 (d)][64 (t)] per head, heads side by side
+constexpr uint32_t kTW = 0, kTU = 128;    // [128 (d)][64 (t)] per head, heads side by side
 
 constexpr uint32_t kIdescSq = tc::idesc_bf16(128, 128, 0, 0);  // A, B K-major
 constexpr uint32_t kIdescWU = tc::idesc_bf16(128, 64, 1, 1);   // A, B MN-major
@@ -73,11 +77,30 @@ __device__ __forceinline__ int a_off(int t, int s) {  // byte offset of A[t][s] 
   return t * 256 + ((((s >> 2) ^ (t & 15))) << 4) + (s & 3) * 4;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Row j of T diag(scale) as the MN-major B operand of one head: high part at
+// `bt`, low part at `bt + 8192`.
+__device__ __forceinline__ void write_t_operand(uint8_t* bt, int j, const float (&x)[64], float scale) {
+  const int rowb = (j >> 3) * 1024 + (j & 7) * 128;
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = x[c8 * 8 + 2 * e] * scale, b = x[c8 * 8 + 2 * e + 1] * scale;
+      hi[e] = tc::pack_bf16x2(a, b);
+      lo[e] = tc::pack_bf16x2(a - __uint_as_float(hi[e] << 16), b - __uint_as_float(hi[e] & 0xFFFF0000u));
+    }
+    const int off = rowb + ((c8 ^ (j & 7)) << 4);
+    *reinterpret_cast<uint4*>(bt + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(bt + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
 gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_in, bar_d, bar_b, bar_w;
+  __shared__ uint64_t bar_in, bar_d, bar_b1, bar_w1, bar_b2, bar_w2;
   __shared__ uint32_t tmem_slot;
   __shared__ float gsh[2][64], bsh[2][64];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -92,12 +115,14 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar_in, 1);
     tc::mbar_init(&bar_d, 1);
-    tc::mbar_init(&bar_b, 128);
-    tc::mbar_init(&bar_w, 1);
+    tc::mbar_init(&bar_b1, 128);
+    tc::mbar_init(&bar_w1, 1);
+    tc::mbar_init(&bar_b2, 128);
+    tc::mbar_init(&bar_w2, 1);
     tc::fence_mbar_init();
   }
   if (warp == 4) {
-    tc::tmem_alloc(&tmem_slot, 512);
+    tc::tmem_alloc(&tmem_slot, 256);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -130,35 +155,30 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
           tc::mma_bf16_ss(tmem + kTQK, aq, bk, kIdescSq, k > 0 ? 1u : 0u);
         }
         tc::mma_commit(&bar_d);
-        ok = tc::mbar_wait(&bar_b, 0, kWaitCycles);
       }
-      if (ok) {
+      // W^T, then Ut^T, each from its T operand in the Q buffer
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        ok = tc::mbar_wait(pass == 0 ? &bar_b1 : &bar_b2, 0, kWaitCycles);
+        if (!ok) break;
         tc::fence_after_sync();
+        const int src = pass == 0 ? kOffK : kOffV;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          const uint32_t ak = tc::smem_u32(smem + kOffK + i * 8192);
-          const uint32_t av = tc::smem_u32(smem + kOffV + i * 8192);
-          const uint32_t bb = tc::smem_u32(smem + kOffB + i * 4 * 8192);
+          const uint32_t a0 = tc::smem_u32(smem + src + i * 8192);
+          const uint32_t bb = tc::smem_u32(smem + kOffT + i * 16384);
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {  // over the chunk's tokens s, 16 per step
-              const uint64_t a_k = tc::sdesc_sw128(ak + k * 2048, 16384, 1024);
-              const uint64_t a_v = tc::sdesc_sw128(av + k * 2048, 16384, 1024);
-              const uint64_t b1 = tc::sdesc_sw128(bb + part * 8192 + k * 2048, 8192, 1024);
-              const uint64_t b2 = tc::sdesc_sw128(bb + (2 + part) * 8192 + k * 2048, 8192, 1024);
-              const uint32_t acc = (part > 0 || k > 0) ? 1u : 0u;
-              tc::mma_bf16_ss(tmem + kTW + 64 * i, a_k, b1, kIdescWU, acc);
-              tc::mma_bf16_ss(tmem + kTU + 64 * i, a_v, b2, kIdescWU, acc);
+              const uint64_t a = tc::sdesc_sw128(a0 + k * 2048, 16384, 1024);
+              const uint64_t b = tc::sdesc_sw128(bb + part * 8192 + k * 2048, 8192, 1024);
+              tc::mma_bf16_ss(tmem + (pass == 0 ? kTW : kTU) + 64 * i, a, b, kIdescWU, (part > 0 || k > 0) ? 1u : 0u);
             }
           }
         }
-      } else {
-        hsd::set_status(p.status, HS_DEV_TIMEOUT);
+        tc::mma_commit(pass == 0 ? &bar_w1 : &bar_w2);
       }
-      // every MMA (or none) is complete before anyone reads tensor memory or leaves
-      tc::mma_commit(&bar_w);
-      tc::mbar_wait(&bar_w, 0, kWaitCycles);
+      if (!ok) hsd::set_status(p.status, HS_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -194,7 +214,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
     bool ok = __all_sync(~0u, tc::mbar_wait(&bar_d, 0, kWaitCycles));
     if (ok) {
       tc::fence_after_sync();
-      // row t of A (fp32, shared) and of P (bf16, straight to the workspace)
+      // row t of A (fp32, in the Q buffer: Q K^T is done) and of P (bf16, straight to the workspace)
       uint8_t* Ai = smem + kOffA + i * 16384;
       uint8_t* Pi = wsi + gdnws::kP;
 #pragma unroll
@@ -223,54 +243,44 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
     }
     tc::named_sync(1, 128);
     // column j = t of T = (I + A)^{-1} by forward substitution: x_u = [u == j] - sum_{s<u} A_us x_s
-    const uint8_t* Ai = smem + kOffA + i * 16384;
     float x[64];
-#pragma unroll
-    for (int u = 0; u < 64; ++u) {
-      float acc = u == t ? 1.f : 0.f;
-#pragma unroll
-      for (int s = 0; s < u; s += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(Ai + a_off(u, s));
-        acc = fmaf(-a4.x, x[s], acc);
-        if (s + 1 < u) acc = fmaf(-a4.y, x[s + 1], acc);
-        if (s + 2 < u) acc = fmaf(-a4.z, x[s + 2], acc);
-        if (s + 3 < u) acc = fmaf(-a4.w, x[s + 3], acc);
-      }
-      x[u] = acc;
-    }
-    // row j of the MN-major B operands: T1 = T diag(beta e^g), T2 = T diag(beta), high and low bf16 parts
     {
-      const float s1 = t < len ? bt * expf(gt) : 0.f, s2 = bt;
-      uint8_t* Bi = smem + kOffB + i * 4 * 8192;
-      const int rowb = (t >> 3) * 1024 + (t & 7) * 128;
+      const uint8_t* Ai = smem + kOffA + i * 16384;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint32_t h1[4], l1[4], h2[4], l2[4];
+      for (int u = 0; u < 64; ++u) {
+        float acc = u == t ? 1.f : 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = x[c8 * 8 + 2 * e] * s1, b = x[c8 * 8 + 2 * e + 1] * s1;
-          h1[e] = tc::pack_bf16x2(a, b);
-          l1[e] = tc::pack_bf16x2(a - __uint_as_float(h1[e] << 16), b - __uint_as_float(h1[e] & 0xFFFF0000u));
-          const float a2 = x[c8 * 8 + 2 * e] * s2, b2 = x[c8 * 8 + 2 * e + 1] * s2;
-          h2[e] = tc::pack_bf16x2(a2, b2);
-          l2[e] = tc::pack_bf16x2(a2 - __uint_as_float(h2[e] << 16), b2 - __uint_as_float(h2[e] & 0xFFFF0000u));
+        for (int s = 0; s < u; s += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(Ai + a_off(u, s));
+          acc = fmaf(-a4.x, x[s], acc);
+          if (s + 1 < u) acc = fmaf(-a4.y, x[s + 1], acc);
+          if (s + 2 < u) acc = fmaf(-a4.z, x[s + 2], acc);
+          if (s + 3 < u) acc = fmaf(-a4.w, x[s + 3], acc);
         }
-        const int off = rowb + ((c8 ^ (t & 7)) << 4);
-        *reinterpret_cast<uint4*>(Bi + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-        *reinterpret_cast<uint4*>(Bi + 8192 + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-        *reinterpret_cast<uint4*>(Bi + 16384 + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-        *reinterpret_cast<uint4*>(Bi + 24576 + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+        x[u] = acc;
       }
+    }
+    tc::named_sync(1, 128);  // A is read by every thread before the T operands overwrite it
+    // row j of T diag(beta e^g) for W, then (once the W products are done) of T diag(beta) for Ut
+    uint8_t* bt_i = smem + kOffT + i * 16384;
+    write_t_operand(bt_i, t, x, t < len ? bt * expf(gt) : 0.f);
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    tc::mbar_arrive(&bar_b1);
+    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w1, 0, kWaitCycles));
+    if (ok) {
+      tc::fence_after_sync();
+      write_t_operand(bt_i, t, x, bt);
     }
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
-    tc::mbar_arrive(&bar_b);
-    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w, 0, kWaitCycles));
+    tc::mbar_arrive(&bar_b2);
+    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w2, 0, kWaitCycles)) &&
+         __all_sync(~0u, tc::mbar_wait(&bar_in, 0, kWaitCycles));  // (makes the TMA-written K tile visible here)
     if (ok) {
       tc::fence_after_sync();
       // K' = diag(e^{gC-g}) K: thread r = (head i, token t) scales its row of the K tile into the V buffer
-      // (the wait on the copy barrier, long complete, makes the TMA-written tile visible to this thread)
-      if (__all_sync(~0u, tc::mbar_wait(&bar_in, 0, kWaitCycles))) {
+      {
         const float dk = t < len ? expf(gC - gt) : 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -335,7 +345,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 4) tc::tmem_dealloc(tmem, 512);
+  if (warp == 4) tc::tmem_dealloc(tmem, 256);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
