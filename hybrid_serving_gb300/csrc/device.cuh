@@ -61,6 +61,8 @@ struct Meta {
   __device__ __forceinline__ const int32_t* readout() const { return m + m[hsm::H_OFF_READOUT]; }
   __device__ __forceinline__ const int32_t* level_off() const { return m + m[hsm::H_OFF_LEVEL]; }
   __device__ __forceinline__ const int32_t* level_seg() const { return m + m[hsm::H_OFF_LEVEL_SEG]; }
+  __device__ __forceinline__ const int32_t* scan() const { return m + m[hsm::H_OFF_SCAN]; }
+  __device__ __forceinline__ const int32_t* scan_level_off() const { return m + m[hsm::H_OFF_SCAN_LEVEL]; }
 };
 
 }  // namespace hsd

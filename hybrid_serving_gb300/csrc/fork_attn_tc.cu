@@ -29,10 +29,12 @@
 //               half of the keys into its own accumulator O_c, with the
 //               running max in log2 units, rescaling O_c and l_c only when
 //               the max grows by more than 2^8 (a per-(row, half) decision;
-//               only then does it wait for the previous P.V).  P_j overwrites
-//               S_j in place, split into a bf16 high part and a bf16 low part
-//               (p - high), both multiplied into O_c, so P enters the product
-//               with ~16 significant bits.  At the end the two halves of a
+//               only then does it wait for the previous P.V).  The exponent
+//               is the hardware 2^x approximation (relative error ~2^-22).
+//               P_j overwrites S_j in place, split into a bf16 high part (the
+//               top 16 bits of p) and a bf16 low part (p - high, rounded),
+//               both multiplied into O_c, so P enters the product with ~16
+//               significant bits.  At the end the two halves of a
 //               row combine (m = max m_c, O = sum 2^(m_c - m) O_c, l likewise,
 //               in a fixed order) and write O / l.
 //
@@ -390,7 +392,7 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       for (int a = 0; a < 8; ++a) rp[a] = 0.f;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        s[i] = exp2f(fmaf(s[i], sl2, -mref));
+        s[i] = tc::ex2_approx(fmaf(s[i], sl2, -mref));
         rp[i & 7] += s[i];
       }
       const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
@@ -400,7 +402,7 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float a = s[2 * i], c = s[2 * i + 1];
-        hi[i] = tc::pack_bf16x2(a, c);
+        hi[i] = tc::pack_bf16x2_trunc(a, c);
         lo[i] = tc::pack_bf16x2(a - __uint_as_float(hi[i] << 16), c - __uint_as_float(hi[i] & 0xFFFF0000u));
       }
       tc::tmem_st32(sb, hi);

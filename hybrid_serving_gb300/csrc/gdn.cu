@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "device.cuh"
+#include "gdn_ws.h"
 
 using namespace hsm;
 using hsd::Meta;
@@ -618,8 +619,9 @@ constexpr size_t smemB() {
 }  // namespace
 
 hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q,
-                                 const uint8_t* ws, float* state, int n_slots, void* out, int32_t* status,
-                                 cudaStream_t st);
+                                 const uint8_t* ws, uint8_t* scan, float* state, int n_slots, void* out,
+                                 int32_t* status, cudaStream_t st);
+static size_t scan_region_offset(const hs_round_caps* caps, int32_t h, int32_t dk, int32_t dv);
 hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q, const void* k,
                                 const void* v, const float* alpha, const float* beta, uint8_t* ws, int32_t* status,
                                 cudaStream_t st);
@@ -643,7 +645,8 @@ hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const v
     // tensor cores for both passes, through the compact bf16 workspace
     const hs_status s = hs_gdn_prep_tc_launch(caps, meta, H, q, k, v, alpha, beta, (uint8_t*)ws, status, st);
     if (s != HS_OK) return s;
-    return hs_gdn_chain_tc_launch(caps, meta, H, q, (const uint8_t*)ws, state, n_slots, out, status, st);
+    uint8_t* scan = (uint8_t*)ws + scan_region_offset(caps, H, D, D);
+    return hs_gdn_chain_tc_launch(caps, meta, H, q, (const uint8_t*)ws, scan, state, n_slots, out, status, st);
   }
   // bf16 inputs take the pipelined state pass; fp32 rows do not fit its double buffer at d=128
   constexpr bool kPipelined = sizeof(T) == 2;
@@ -682,9 +685,16 @@ hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const v
 
 }  // namespace
 
+// Per-chunk blocks, then (d = 128) the buffers of the two-level state scan.
+static size_t scan_region_offset(const hs_round_caps* caps, int32_t h, int32_t dk, int32_t dv) {
+  return ((size_t)caps->max_chunks * h * ws_floats_per(dk, dv) * sizeof(float) + 255) & ~(size_t)255;
+}
+
 extern "C" size_t hs_gdn_workspace_bytes(const hs_round_caps* caps, int32_t h, int32_t dk, int32_t dv) {
   if (!caps || h <= 0 || dk <= 0 || dv <= 0) return 0;
-  return (size_t)caps->max_chunks * h * ws_floats_per(dk, dv) * sizeof(float);
+  size_t n = scan_region_offset(caps, h, dk, dv);
+  if (dk == 128 && dv == 128) n += (size_t)scan_cap(caps->max_chunks) * h * gdnws::kScanBytes;
+  return n;
 }
 
 extern "C" hs_status hs_gdn_fork_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t h,

@@ -64,6 +64,7 @@ static_assert(kStG + (gdnws::kBytes - gdnws::kG) == kStageBytes, "stage layout")
 constexpr uint32_t kTS32 = 0;    // S fp32 [128][128]
 constexpr uint32_t kTS16 = 128;  // S bf16, two per column (64)
 constexpr uint32_t kTU = 192;    // U bf16 (32)
+constexpr uint32_t kTSlo = 192;  // S bf16 low part (64), only while a later group forms its start state
 constexpr uint32_t kTD1 = 256, kTD2 = 320, kTD3 = 384;  // fp32 [128][64] each
 
 constexpr uint32_t kIdesc64 = tc::idesc_bf16(128, 64, 0, 0);      // D[128x64], B K-major
@@ -73,26 +74,47 @@ constexpr uint32_t kIdesc128mn = tc::idesc_bf16(128, 128, 0, 1);  // D[128x128],
 struct Prm {
   const int32_t* meta;
   int level, H, n_slots;
+  int pass;  // 0: group 0 of every node, and N, M of the later groups; 1: the later groups
   const uint8_t* ws;
+  uint8_t* scan;  // per (extra scan group, head) buffers (gdn_ws.h)
   float* state;
   __nv_bfloat16* out;
   int32_t* status;
 };
 
+// What one CTA does with its group of chunks.
+enum InitKind { kInitSlot, kInitZero, kInitIdentity, kInitScan };
+enum EndKind { kEndNone, kEndSlot, kEndScanS, kEndScanN, kEndScanM };
+
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_s, bar_u, bar_of;
-  __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2;
+  __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2, bar_pm, bar_ps, bar_pd;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
   Meta M{p.meta};
   if (p.level >= M.h(H_N_LEVEL)) return;
-  const int lo = M.level_off()[p.level], hi = M.level_off()[p.level + 1];
-  if ((int)blockIdx.x >= hi - lo) return;
-  const int seg = M.level_seg()[lo + blockIdx.x];
+  // the task: (node, group g, part) -- part 1 = the group's transition M (pass 0 only)
+  const int n_lev_seg = M.level_off()[p.level + 1] - M.level_off()[p.level];
+  const int scan_lo = M.scan_level_off()[p.level];
+  const int n_lev_scan = M.scan_level_off()[p.level + 1] - scan_lo;
+  const int cap_seg = M.h(H_CAP_SEG), cap_scan = scan_cap(M.h(H_CAP_CHUNK));
+  int seg, g = 0, part = 0, e = -1;
+  if (p.pass == 0 && (int)blockIdx.x < cap_seg) {
+    if ((int)blockIdx.x >= n_lev_seg) return;
+    seg = M.level_seg()[M.level_off()[p.level] + blockIdx.x];
+  } else {
+    const int y = p.pass == 0 ? (int)blockIdx.x - cap_seg : (int)blockIdx.x;
+    part = y / cap_scan;
+    const int t = y % cap_scan;
+    if (part > (p.pass == 0 ? 1 : 0) || t >= n_lev_scan) return;
+    e = scan_lo + t;
+    seg = M.scan()[2 * e];
+    g = M.scan()[2 * e + 1];
+  }
   const int32_t* sg = M.seg(seg);
   const int h = blockIdx.y;
   const int init = sg[S_INIT_SLOT], endslot = sg[S_END_SLOT];
@@ -100,7 +122,18 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     if (threadIdx.x == 0) hsd::set_status(p.status, HS_DEV_BAD_SLOT);
     return;
   }
-  const int c_off = sg[S_CHUNK_OFF], n_c = sg[S_N_CHUNK];
+  const int n_all = sg[S_N_CHUNK], G = scan_groups(n_all), e1 = sg[S_SCAN1];
+  const int c_off = sg[S_CHUNK_OFF] + (int)((long long)g * n_all / G);
+  const int n_c = sg[S_CHUNK_OFF] + (int)((long long)(g + 1) * n_all / G) - c_off;
+  const bool outputs = p.pass == 1 || g == 0;
+  const bool zero_ut = part == 1;
+  const InitKind ik = p.pass == 1 ? kInitScan : g == 0 ? (init >= 0 ? kInitSlot : kInitZero)
+                                              : part == 0 ? kInitZero : kInitIdentity;
+  const EndKind ek = p.pass == 1 ? (g == G - 1 && endslot >= 0 ? kEndSlot : kEndNone)
+                     : g == 0    ? (G > 1 ? kEndScanS : endslot >= 0 ? kEndSlot : kEndNone)
+                                 : (part == 0 ? kEndScanN : kEndScanM);
+  const int n_comb = p.pass == 1 ? g - 1 : 0;  // products S <- S M_q + N_q before the chain (groups 1 .. g-1)
+  auto scanbuf = [&](int entry) { return p.scan + ((size_t)entry * p.H + h) * gdnws::kScanBytes; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -118,6 +151,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     tc::mbar_init(&bar_d23, 1);
     tc::mbar_init(&bar_done, 1);
     tc::mbar_init(&bar_done2, 1);
+    tc::mbar_init(&bar_pm, 1);
+    tc::mbar_init(&bar_ps, 128);
+    tc::mbar_init(&bar_pd, 1);
     tc::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -138,8 +174,22 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     // ----------------------------------------------------------- producer
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
+      // the start state of a later group: the images of M_1 .. M_{g-1}, one at a time, in stage 0
+      bool pro_ok = true;
+      for (int q = 1; q <= n_comb && pro_ok; ++q) {
+        if (q >= 2 && !tc::mbar_wait(&bar_pd, (q - 2) & 1, kWaitCycles)) {
+          pro_ok = false;
+          break;
+        }
+        const uint8_t* sbq = scanbuf(e1 + q - 1);
+        tc::mbar_expect_tx(&bar_pm, 65536);
+        tc::bulk_load(smem, sbq + gdnws::kScanMhi, 32768, &bar_pm);
+        tc::bulk_load(smem + 32768, sbq + gdnws::kScanMlo, 32768, &bar_pm);
+      }
+      if (pro_ok && n_comb > 0 && !tc::mbar_wait(&bar_pd, (n_comb - 1) & 1, kWaitCycles)) pro_ok = false;
+      if (!pro_ok) fail();
       int issued = 0;
-      for (int ci = 0; ci < n_c; ++ci) {
+      for (int ci = 0; ci < n_c && pro_ok; ++ci) {
         const int s = ci % kStages, n = ci / kStages;
         if (n >= 1 && !tc::mbar_wait(&bar_empty[s], (n - 1) & 1, kWaitCycles)) {
           fail();
@@ -166,6 +216,25 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     // ------------------------------------------------ MMA: the state chain
     if (lane == 0) {
       bool ok = true;
+      // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi into the fp32 state columns
+      for (int q = 1; q <= n_comb && ok; ++q) {
+        if (!tc::mbar_wait(&bar_pm, (q - 1) & 1, kWaitCycles) || !tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t sm = tc::smem_u32(smem);
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t b = tc::sdesc_sw128(sm + (pr == 1 ? 32768 : 0) + k * 2048, 16384, 1024);
+            tc::mma_bf16_ts(tmem + kTS32, tmem + (pr == 2 ? kTSlo : kTS16) + 8 * k, b, kIdesc128mn,
+                            (pr > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&bar_pd);
+      }
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
@@ -214,10 +283,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           break;
         }
         tc::fence_after_sync();
+        if (outputs) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // D2 = S Q^T
-          const uint64_t bq = tc::sdesc_sw128(sb + kStQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ts(tmem + kTD2, tmem + kTS16 + 8 * k, bq, kIdesc64, k > 0 ? 1u : 0u);
+          for (int k = 0; k < 8; ++k) {  // D2 = S Q^T
+            const uint64_t bq = tc::sdesc_sw128(sb + kStQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
+            tc::mma_bf16_ts(tmem + kTD2, tmem + kTS16 + 8 * k, bq, kIdesc64, k > 0 ? 1u : 0u);
+          }
         }
         tc::mma_commit(&bar_d2);
         if (!tc::mbar_wait(&bar_u, ci & 1, kWaitCycles)) {
@@ -225,10 +296,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           break;
         }
         tc::fence_after_sync();
+        if (outputs) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // D3 = U P^T
-          const uint64_t bp = tc::sdesc_sw128(sb + kStP + k * 32, 16, 1024);
-          tc::mma_bf16_ts(tmem + kTD3, tmem + kTU + 8 * k, bp, kIdesc64, k > 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // D3 = U P^T
+            const uint64_t bp = tc::sdesc_sw128(sb + kStP + k * 32, 16, 1024);
+            tc::mma_bf16_ts(tmem + kTD3, tmem + kTU + 8 * k, bp, kIdesc64, k > 0 ? 1u : 0u);
+          }
         }
         tc::mma_commit(&bar_d23);
         tc::mma_commit(&bar_empty[s]);
@@ -243,31 +316,87 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     // ---------------------------------------------------- rows of the state
     const int j = threadIdx.x;  // row of S == TMEM lane
     const uint32_t lb = (uint32_t)(warp * 32) << 16;
-    // the initial state, in fp32 and as the bf16 operand
+    bool ok = true;
+    // the initial state into the fp32 columns: a slot, zero, the identity (a transition), or a scan buffer
     {
-      const float4* src =
-          init >= 0 ? reinterpret_cast<const float4*>(p.state + (((size_t)init * p.H + h) * kD + j) * kD) : nullptr;
+      const float* src = ik == kInitSlot   ? p.state + (((size_t)init * p.H + h) * kD + j) * kD
+                         : ik == kInitScan ? reinterpret_cast<const float*>(scanbuf(e1) + gdnws::kScanS) + j * kD
+                                           : nullptr;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t f[32], b[16];
+        uint32_t f[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 v = src ? src[q * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 v = src ? reinterpret_cast<const float4*>(src)[q * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
           f[4 * i] = __float_as_uint(v.x);
           f[4 * i + 1] = __float_as_uint(v.y);
           f[4 * i + 2] = __float_as_uint(v.z);
           f[4 * i + 3] = __float_as_uint(v.w);
         }
+        if (ik == kInitIdentity) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+          for (int i = 0; i < 32; ++i) f[i] = __float_as_uint(q * 32 + i == j ? 1.f : 0.f);
+        }
         tc::tmem_st32(tmem + lb + kTS32 + q * 32, f);
-        tc::tmem_st16(tmem + lb + kTS16 + q * 16, b);
+      }
+      tc::tmem_wait_st();
+    }
+    // a later group's start state: S <- S M_q + N_q for q = 1 .. g-1, on tensor cores with S and M split into
+    // bf16 high and low parts (S_hi M_hi + S_hi M_lo + S_lo M_hi), N_q added in fp32
+    for (int q = 1; q <= n_comb && ok; ++q) {
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t f[32], bh[16], bl[16];
+        tc::tmem_ld32(tmem + lb + kTS32 + c4 * 32, f);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = __uint_as_float(f[2 * i]), b = __uint_as_float(f[2 * i + 1]);
+          bh[i] = tc::pack_bf16x2(a, b);
+          bl[i] = tc::pack_bf16x2(a - __uint_as_float(bh[i] << 16), b - __uint_as_float(bh[i] & 0xFFFF0000u));
+        }
+        tc::tmem_st16(tmem + lb + kTS16 + c4 * 16, bh);
+        tc::tmem_st16(tmem + lb + kTSlo + c4 * 16, bl);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bar_s);
+      tc::mbar_arrive(&bar_ps);
+      if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_pd, (q - 1) & 1, kWaitCycles))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const float4* nq = reinterpret_cast<const float4*>(scanbuf(e1 + q - 1) + gdnws::kScanN) + j * (kD / 4);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t f[32];
+        tc::tmem_ld32(tmem + lb + kTS32 + c4 * 32, f);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = nq[c4 * 8 + i];
+          f[4 * i] = __float_as_uint(__uint_as_float(f[4 * i]) + v.x);
+          f[4 * i + 1] = __float_as_uint(__uint_as_float(f[4 * i + 1]) + v.y);
+          f[4 * i + 2] = __float_as_uint(__uint_as_float(f[4 * i + 2]) + v.z);
+          f[4 * i + 3] = __float_as_uint(__uint_as_float(f[4 * i + 3]) + v.w);
+        }
+        tc::tmem_st32(tmem + lb + kTS32 + c4 * 32, f);
+      }
+      tc::tmem_wait_st();
     }
-    bool ok = true;
+    // the bf16 operand of the start state
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t f[32], b[16];
+      tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+      tc::tmem_st16(tmem + lb + kTS16 + q * 16, b);
+    }
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+    tc::mbar_arrive(&bar_s);
     for (int ci = 0; ci < n_c; ++ci) {
       const int s = ci % kStages;
       const uint8_t* sb = stage(ci);
@@ -302,7 +431,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         tc::tmem_ld32(tmem + lb + kTD1 + half * 32, d1);
         uint4 uv[4];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) uv[c4] = *reinterpret_cast<const uint4*>(utj + (((half * 4 + c4) ^ (j & 7)) << 4));
+        for (int c4 = 0; c4 < 4; ++c4)  // (a transition M runs with Ut = 0)
+          uv[c4] = zero_ut ? make_uint4(0u, 0u, 0u, 0u)
+                           : *reinterpret_cast<const uint4*>(utj + (((half * 4 + c4) ^ (j & 7)) << 4));
         tc::tmem_wait_ld();
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
@@ -342,8 +473,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     }
     if (!ok) {
       fail();
-    } else if (endslot >= 0) {
-      float4* dst = reinterpret_cast<float4*>(p.state + (((size_t)endslot * p.H + h) * kD + j) * kD);
+    } else if (ek == kEndSlot || ek == kEndScanS || ek == kEndScanN) {
+      float4* dst = reinterpret_cast<float4*>(
+          ek == kEndSlot    ? p.state + (((size_t)endslot * p.H + h) * kD + j) * kD
+          : ek == kEndScanS ? reinterpret_cast<float*>(scanbuf(e1) + gdnws::kScanS) + j * kD
+                            : reinterpret_cast<float*>(scanbuf(e) + gdnws::kScanN) + j * kD);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t f[32];
@@ -353,6 +487,31 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         for (int i = 0; i < 8; ++i)
           dst[q * 8 + i] = make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]),
                                        __uint_as_float(f[4 * i + 2]), __uint_as_float(f[4 * i + 3]));
+      }
+    } else if (ek == kEndScanM) {
+      // row j of the transition M as the bf16 high and low images of an MN-major B operand:
+      // element (j, n) in slab n / 64, 128-byte row j, 16-byte chunk (n % 64) / 8 swizzled by j % 8
+      uint8_t* mh = scanbuf(e) + gdnws::kScanMhi;
+      uint8_t* ml = scanbuf(e) + gdnws::kScanMlo;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t f[32];
+        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int n0 = q * 32 + c * 8;
+          const int off = (n0 >> 6) * 16384 + (j >> 3) * 1024 + (j & 7) * 128 + ((((n0 & 63) >> 3) ^ (j & 7)) << 4);
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float a = __uint_as_float(f[c * 8 + 2 * i]), b = __uint_as_float(f[c * 8 + 2 * i + 1]);
+            hw[i] = tc::pack_bf16x2(a, b);
+            lw[i] = tc::pack_bf16x2(a - __uint_as_float(hw[i] << 16), b - __uint_as_float(hw[i] & 0xFFFF0000u));
+          }
+          *reinterpret_cast<uint4*>(mh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(ml + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
       }
     }
   } else {
@@ -370,6 +529,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         break;
       }
       tc::fence_after_sync();
+      if (!outputs) {  // no D2, D3 were formed: keep the hand-offs only
+        tc::mbar_arrive(&bar_of);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar_empty[s]);
+        continue;
+      }
       const int32_t* ch = M.chunk(c_off + ci);
       const int row0 = ch[C_ROW0], len = ch[C_LEN];
       // D2, D3 and e^g into registers first, so that D2, D3 are released at once and the
@@ -446,8 +611,8 @@ bool map_rows(CUtensorMap* m, const void* base, int H, long long T) {
 // State passes of every tree level on tensor cores, reading the compact
 // workspace written by the chunk-local pass.
 hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta, int H, const void* q,
-                                 const uint8_t* ws, float* state, int n_slots, void* out, int32_t* status,
-                                 cudaStream_t st) {
+                                 const uint8_t* ws, uint8_t* scan, float* state, int n_slots, void* out,
+                                 int32_t* status, cudaStream_t st) {
   CUtensorMap mq;
   if (!map_rows(&mq, q, H, caps->max_tokens))
     return hs::fail(HS_ECUDA, "gdn: tensor map encoding failed");
@@ -458,10 +623,16 @@ hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta,
       return hs::fail(HS_ECUDA, "gdn_chain_tc: cannot raise the shared-memory limit");
     configured = true;
   }
+  // per level: group 0 of every node (and the later groups' N and M), then the later groups of the long nodes
+  const int cap_scan = scan_cap(caps->max_chunks);
+  const bool any_scan = caps->max_chunks >= 2 * kScanMinChunks;
   for (int lev = 0; lev < caps->max_levels && caps->max_segments > 0; ++lev) {
-    Prm prm{meta, lev, H, n_slots, ws, state, (__nv_bfloat16*)out, status};
-    gdn_chain_tc_kernel<<<dim3(caps->max_segments, H), kThreads, kSmem + 1024, st>>>(mq, prm);
-    HS_LAUNCH_CHECK("gdn_chain_tc");
+    for (int pass = 0; pass < (any_scan ? 2 : 1); ++pass) {
+      Prm prm{meta, lev, H, n_slots, pass, ws, scan, state, (__nv_bfloat16*)out, status};
+      const int gx = pass == 0 ? caps->max_segments + (any_scan ? 2 * cap_scan : 0) : cap_scan;
+      gdn_chain_tc_kernel<<<dim3(gx, H), kThreads, kSmem + 1024, st>>>(mq, prm);
+      HS_LAUNCH_CHECK("gdn_chain_tc");
+    }
   }
   return HS_OK;
 }

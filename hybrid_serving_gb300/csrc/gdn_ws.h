@@ -23,6 +23,17 @@ constexpr int kG = 57344;
 constexpr int kBytes = 58368;  // per (chunk, head); multiple of 1024
 constexpr int kFloats = kBytes / 4;
 
+// Per (extra scan group, head) buffers of the two-level state scan, after the
+// per-chunk blocks: the group's start state S (fp32 [128][128], rows d_v),
+// its zero-start end state N (fp32 [128][128]) and its transition M (d_k x
+// d_k) as the bf16 high and low images of the MN-major B operand of S M
+// (two [128][64] slabs each: row k holds M[k][n]).
+constexpr int kScanS = 0;
+constexpr int kScanN = 65536;
+constexpr int kScanMhi = 131072;
+constexpr int kScanMlo = 163840;
+constexpr int kScanBytes = 196608;
+
 // Byte offset of bf16 element (row, col) in a 128-byte-swizzled K-major image
 // made of [rows][64]-element slabs (one slab per 64 columns): 16-byte chunk c
 // of a 128-byte row lands at chunk c ^ (row % 8).

@@ -8,6 +8,12 @@
 #pragma once
 #include <stdint.h>
 
+#ifdef __CUDACC__
+#define HSM_HD __host__ __device__
+#else
+#define HSM_HD
+#endif
+
 namespace hsm {
 
 constexpr int32_t kMagic = 0x48534d31;  // "HSM1"
@@ -52,7 +58,24 @@ enum : int {
   H_TOTAL_WORDS,
   H_MAX_SEG_CHUNKS,  // largest number of chunks in one segment
   H_OFF_PRED,        // per token: kConvTaps-1 predecessor rows for the causal conv
+  H_N_SCAN,          // extra scan groups (group 1 and up of the long nodes), all levels
+  H_OFF_SCAN,        // [segment, group] per extra scan group, grouped by level
+  H_OFF_SCAN_LEVEL,  // [max_levels + 1] prefix offsets into SCAN
 };
+
+// The GDN state chain of a long node is split into groups of consecutive
+// chunks that run side by side (a two-level scan of the affine chunk map
+// S -> S M_c + N_c): group g of a node with n chunks holds chunks
+// [g n / G, (g + 1) n / G).  G depends on the node's own length only.
+constexpr int kScanMinChunks = 24;
+constexpr int kScanMaxGroups = 5;
+HSM_HD inline int32_t scan_groups(int32_t n_chunks) {
+  if (n_chunks < 2 * kScanMinChunks) return 1;
+  const int32_t g = n_chunks / kScanMinChunks;
+  return g < kScanMaxGroups ? g : kScanMaxGroups;
+}
+// bound on the number of extra groups of a round with cap_chunk chunks
+HSM_HD inline int32_t scan_cap(int32_t cap_chunk) { return cap_chunk / kScanMinChunks + 1; }
 
 // segment record
 constexpr int kSegWords = 16;
@@ -71,6 +94,7 @@ enum : int {
   S_READOUT_ROW,     // stream row of the readout (-1 = none)
   S_PAGE_REF_OFF,    // first own page in the page-ref array
   S_N_PAGES,
+  S_SCAN1,           // scan-table entry of the node's group 1 (-1 = one group); groups 2.. follow it
 };
 
 // Causal-conv predecessors of a token (Flide section 3.2.2: the convolution
@@ -102,7 +126,7 @@ enum : int { C_SEG = 0, C_ROW0, C_LEN, C_IDX };
 
 struct Layout {
   int32_t off_seg, off_tok, off_span, off_tile, off_tile_span, off_chunk, off_readout, off_level,
-      off_level_seg, off_page_ref, off_pred, total_words;
+      off_level_seg, off_page_ref, off_pred, off_scan, off_scan_level, total_words;
 };
 
 inline int32_t align16(int32_t x) { return (x + 15) & ~15; }
@@ -124,6 +148,8 @@ inline Layout layout_for(int32_t cap_tok, int32_t cap_seg, int32_t cap_span, int
   L.off_level_seg = o;  o = align16(o + cap_seg);
   L.off_page_ref = o;   o = align16(o + cap_page_ref);
   L.off_pred = o;       o = align16(o + cap_tok * kPredWords);
+  L.off_scan = o;       o = align16(o + scan_cap(cap_chunk) * 2);
+  L.off_scan_level = o; o = align16(o + cap_level + 1);
   L.total_words = o;
   return L;
 }

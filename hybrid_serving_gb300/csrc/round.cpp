@@ -540,6 +540,8 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
   h[H_OFF_LEVEL] = L.off_level;
   h[H_OFF_LEVEL_SEG] = L.off_level_seg;
   h[H_OFF_PAGE_REF] = L.off_page_ref;
+  h[H_OFF_SCAN] = L.off_scan;
+  h[H_OFF_SCAN_LEVEL] = L.off_scan_level;
   h[H_CAP_TOK] = C.max_tokens;
   h[H_CAP_SEG] = C.max_segments;
   h[H_CAP_SPAN] = C.max_segments + C.max_hist_spans;
@@ -609,6 +611,25 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
         if (S[id].level == lev) h[L.off_level_seg + k++] = id;
     }
     for (int32_t lev = n_levels; lev <= C.max_levels; ++lev) h[L.off_level + lev] = k;
+  }
+  {  // extra scan groups of the long nodes, by level, in segment order then group order
+    int32_t k = 0;
+    for (int32_t lev = 0; lev < n_levels; ++lev) {
+      h[L.off_scan_level + lev] = k;
+      for (int32_t id : order) {
+        if (S[id].level != lev) continue;
+        const int32_t G = scan_groups(S[id].n_chunk);
+        h[L.off_seg + id * kSegWords + S_SCAN1] = G > 1 ? k : -1;
+        for (int32_t g = 1; g < G; ++g) {
+          if (k >= scan_cap(C.max_chunks)) return hs::fail(HS_ECAPACITY, "scan group table full");
+          h[L.off_scan + 2 * k] = id;
+          h[L.off_scan + 2 * k + 1] = g;
+          ++k;
+        }
+      }
+    }
+    for (int32_t lev = n_levels; lev <= C.max_levels; ++lev) h[L.off_scan_level + lev] = k;
+    h[H_N_SCAN] = k;
   }
 
   hs_round_info& I = r->info;

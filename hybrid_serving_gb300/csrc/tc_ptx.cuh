@@ -214,6 +214,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, 
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz: relative error about
+// 2^-22, subnormal results flushed to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// The bf16 high parts of two floats, by truncation (their top 16 bits), packed
+// with the first in the low half; a - high is exact in fp32.
+__device__ __forceinline__ uint32_t pack_bf16x2_trunc(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
