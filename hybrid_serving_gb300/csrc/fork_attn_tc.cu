@@ -484,6 +484,379 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (warp == kWarpMma) tc::tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------------------
+// Two query heads per CTA (heads 2p and 2p + 1 of a KV-head group of even size
+// share every K and V page): the heads' online softmaxes run in two warp
+// groups while the MMA warp alternates between them, so one head's softmax
+// overlaps the other head's products and each K/V block is loaded once.
+//
+//   warp 8      TMA: Q of both heads once; per block K and V into a 2-stage
+//               ring (a K stage is refilled once both heads' S are computed,
+//               a V stage once both heads' P.V are).
+//   warp 9      TMEM (512 columns: S_A, S_B, O_A, O_B) and the MMAs, in the
+//               order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...;
+//               S_X(j+1) overwrites P_X(j) only after P.V_X(j) is issued
+//               (MMAs of one thread run in issue order).
+//   warps 0..3  softmax of head A, warps 4..7 of head B: thread t = query row
+//               t = TMEM lane t over all 128 keys of a block (a first pass
+//               over the scores for the row max, a second for the
+//               exponentials, 32 keys at a time); P overwrites S in place:
+//               the 32 score columns of keys 32g .. 32g+31 become 16 columns
+//               of bf16 high parts (top 16 bits) and 16 of rounded low parts.
+//               Since S_X(j) is computed after P.V_X(j-1) is issued, O_X is
+//               final for block j-1 when S_X(j) is seen, so a lazy rescale
+//               (running max grown by more than 2^8) never waits.
+// ---------------------------------------------------------------------------
+namespace pair {
+constexpr int kOffQ = 0;                  // Q_A, Q_B: 32 KB each
+constexpr int kOffK = 2 * kTile;          // 2 stages
+constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
+constexpr int kSmemBytes = kOffV + 2 * kTile;  // 192 KB
+constexpr uint32_t kTmS = 0, kTmO = 256;  // S_X at 128 X, O_X at 256 + 128 X
+}  // namespace pair
+
+__global__ void __launch_bounds__(kThreads, 1)
+fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
+                     const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
+                     const __grid_constant__ CUtensorMap tm_v128, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2], bar_sf[2], bar_pf[2], bar_pv[2], bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  Meta M{p.meta};
+  const int np = p.hq / 2;
+  const int tile = blockIdx.x / np;  // tile-major: both heads of the heaviest tiles first
+  if (tile >= M.h(H_N_TILE)) return;
+  const int32_t* tl = M.tile(tile);
+  const int h0 = 2 * (blockIdx.x % np);
+  const int kvh = h0 / (p.hq / p.hkv);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tc::mbar_init(&bar_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&bar_kf[s], 1);
+      tc::mbar_init(&bar_vf[s], 1);
+      tc::mbar_init(&bar_ke[s], 1);
+      tc::mbar_init(&bar_ve[s], 1);
+      tc::mbar_init(&bar_sf[s], 1);   // [X]: S_X done
+      tc::mbar_init(&bar_pf[s], 128); // [X]: P_X written
+      tc::mbar_init(&bar_pv[s], 1);   // [X]: P.V_X done
+    }
+    tc::mbar_init(&bar_done, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tc::tmem_alloc(&tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  Cursor cur;
+  cur.init(M, tl);
+  const int n_ref = M.h(H_N_PAGE_REF);
+  const int32_t* refs = M.page_ref();
+
+  if (warp == kWarpProd) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k16);
+      tc::prefetch_tmap(&tm_v16);
+      tc::mbar_expect_tx(&bar_q, 2 * kTile);
+      for (int x = 0; x < 2; ++x) {
+        tc::tma_load_3d(smem + pair::kOffQ + x * kTile, &tm_q, 0, h0 + x, tl[TL_ROW0], &bar_q);
+        tc::tma_load_3d(smem + pair::kOffQ + x * kTile + kSlab, &tm_q, 64, h0 + x, tl[TL_ROW0], &bar_q);
+      }
+      const int oob_y = p.hkv * p.n_pages * kPage;  // first row past the pool: zero fill
+      int j = 0;
+      while (cur.next()) {
+        const int s = j & 1, n = j >> 1;
+        const int npg = (cur.valid() + kPage - 1) / kPage;
+        int pg[8];
+        bool consecutive = npg == 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          pg[i] = -1;
+          if (i < npg) {
+            const int ref = cur.sp_off + cur.b0 / kPage + i;
+            const int page = ref < n_ref ? refs[ref] : -1;
+            if (page >= 0 && page < p.n_pages) {
+              pg[i] = page;
+            } else {
+              hsd::set_status(p.status, ref < n_ref ? HS_DEV_BAD_PAGE : HS_DEV_BAD_META);
+            }
+          }
+          if (i > 0 && (pg[i] < 0 || pg[i] != pg[i - 1] + 1)) consecutive = false;
+        }
+        if (pg[0] < 0) consecutive = false;
+        uint8_t* ks = smem + pair::kOffK + s * kTile;
+        uint8_t* vs = smem + pair::kOffV + s * kTile;
+        if (n > 0 && !tc::mbar_wait(&bar_ke[s], (n - 1) & 1, kWaitCycles)) {
+          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+          break;
+        }
+        if (*(volatile int*)&abort_flag) break;
+        tc::mbar_expect_tx(&bar_kf[s], kTile);
+        if (consecutive) {
+          const int y = (kvh * p.n_pages + pg[0]) * kPage;
+          for (int half = 0; half < 2; ++half) tc::tma_load_2d(ks + half * kSlab, &tm_k128, half * 64, y, &bar_kf[s]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
+            for (int half = 0; half < 2; ++half)
+              tc::tma_load_2d(ks + half * kSlab + i * 2048, &tm_k16, half * 64, y, &bar_kf[s]);
+          }
+        }
+        if (n > 0 && !tc::mbar_wait(&bar_ve[s], (n - 1) & 1, kWaitCycles)) {
+          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+          ++j;  // the K copy of this block is in flight: drain it below
+          break;
+        }
+        tc::mbar_expect_tx(&bar_vf[s], kTile);
+        if (consecutive) {
+          const int y = (kvh * p.n_pages + pg[0]) * kPage;
+          for (int half = 0; half < 2; ++half) tc::tma_load_2d(vs + half * kSlab, &tm_v128, half * 64, y, &bar_vf[s]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
+            for (int half = 0; half < 2; ++half)
+              tc::tma_load_2d(vs + half * kSlab + i * 2048, &tm_v16, half * 64, y, &bar_vf[s]);
+          }
+        }
+        ++j;
+      }
+      // drain: every copy this thread issued has landed before the CTA leaves
+      tc::mbar_wait(&bar_q, 0, kWaitCycles);
+      for (int i = (j >= 2 ? j - 2 : 0); i < j; ++i) {
+        tc::mbar_wait(&bar_kf[i & 1], (i >> 1) & 1, kWaitCycles);
+        tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      bool ok = tc::mbar_wait(&bar_q, 0, kWaitCycles);
+      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      auto s_mma = [&](int x, int jj) {  // S_X(jj) = Q_X K_jj^T
+        const uint32_t sq = tc::smem_u32(smem + pair::kOffQ + x * kTile);
+        const uint32_t sk = tc::smem_u32(smem + pair::kOffK + (jj & 1) * kTile);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = tc::sdesc_sw128(sq + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+          const uint64_t b = tc::sdesc_sw128(sk + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+          tc::mma_bf16_ss(tmem + pair::kTmS + 128 * x, a, b, kIdescQK, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&bar_sf[x]);
+      };
+      auto pv_mma = [&](int x, int jj) {  // O_X += P_X(jj) V_jj, per 32 keys: high parts, then low parts
+        const uint32_t sv = tc::smem_u32(smem + pair::kOffV + (jj & 1) * kTile);
+        const uint32_t pt = tmem + pair::kTmS + 128 * x;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {  // keys 32 g4 + 16 k .. +15
+              const uint64_t b = tc::sdesc_sw128(sv + g4 * 4096 + k * 2048, kSlab, 1024);
+              tc::mma_bf16_ts(tmem + pair::kTmO + 128 * x, pt + 32 * g4 + 16 * part + 8 * k, b, kIdescPV,
+                              (jj > 0 || g4 > 0 || part > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+        }
+        tc::mma_commit(&bar_pv[x]);
+      };
+      // the number of blocks of the tile, counted once (the loop then needs no cursor)
+      int n_blk = 0;
+      while (cur.next()) ++n_blk;
+      if (ok && n_blk > 0) {
+        if (!tc::mbar_wait(&bar_kf[0], 0, kWaitCycles)) {
+          ok = false;
+        } else {
+          tc::fence_after_sync();
+          s_mma(0, 0);
+          s_mma(1, 0);
+          tc::mma_commit(&bar_ke[0]);
+        }
+      }
+      for (int j = 0; ok && j < n_blk; ++j) {
+        const bool more = j + 1 < n_blk;
+        for (int x = 0; x < 2 && ok; ++x) {
+          // (polling waits: a suspended MMA thread would notice the softmax late)
+          if (!tc::mbar_wait_spin(&bar_pf[x], j & 1, kWaitCycles) ||
+              (x == 0 && !tc::mbar_wait_spin(&bar_vf[j & 1], (j >> 1) & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          if (*(volatile int*)&abort_flag) {
+            ok = false;
+            break;
+          }
+          pv_mma(x, j);
+          if (x == 1) tc::mma_commit(&bar_ve[j & 1]);
+          if (more) {
+            if (x == 0 && !tc::mbar_wait_spin(&bar_kf[(j + 1) & 1], ((j + 1) >> 1) & 1, kWaitCycles)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            s_mma(x, j + 1);
+            if (x == 1) tc::mma_commit(&bar_ke[(j + 1) & 1]);
+          }
+        }
+      }
+      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      // every MMA issued by this thread completes before O is read and TMEM is freed
+      tc::mma_commit(&bar_done);
+      tc::mbar_wait(&bar_done, 0, kWaitCycles);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = warp / 4;                      // head A or B
+    const int t = (warp % 4) * 32 + lane;        // row of the tile == TMEM lane
+    const int row = tl[TL_ROW0] + t;
+    const bool active = t < tl[TL_N_ROWS];
+    int my_seg = -1, my_idx = 0;
+    if (active) {
+      my_seg = M.tok(row)[T_SEG];
+      my_idx = M.tok(row)[T_IDX];
+    }
+    const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t sbuf = tmem + lane_base + pair::kTmS + 128 * x, obuf = tmem + lane_base + pair::kTmO + 128 * x;
+    float m_used = -INFINITY, l = 0.f;
+    const float sl2 = p.scale_log2e;
+    int j = 0;
+    bool ok = true;
+    while (cur.next()) {
+      // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[x], j & 1, kWaitCycles))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const int lim = cur.full() ? kBlk
+                                 : (!active ? 0 : !cur.own ? cur.sp_n - cur.b0
+                                                           : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0));
+      // pass 1: the row max of the block, 32 scores at a time (scores past the row's visible keys read as -inf)
+      const bool masked = __any_sync(~0u, lim < kBlk);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(sbuf + 32 * c, r);
+        tc::tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 32 * c + i < lim ? r[i] : 0xFF800000u;
+        }
+        float m2[2] = {mx, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        mx = fmaxf(m2[0], m2[1]);
+      }
+      const float m_new = fmaxf(m_used, mx * sl2);
+      float factor = 1.f;
+      const bool rescale = m_new > m_used + 8.f;
+      if (rescale) {
+        factor = exp2f(m_used - m_new);
+        m_used = m_new;
+      }
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
+      // pass 2, 32 keys at a time: P = 2^(s log2e scale - m) over S in place; pairs of keys in fp32x2
+      const uint64_t sc2 = tc::f2_pack(sl2, sl2), mm2 = tc::f2_pack(-mref, -mref);
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {  // keys 32 g4 .. +31: P words in the same 32 columns (16 high, 16 low)
+        uint32_t r[32], hi[16], lo[16];
+        tc::tmem_ld32(sbuf + 32 * g4, r);
+        tc::tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 32 * g4 + i < lim ? r[i] : 0xFF800000u;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float ya, yb;
+          tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
+          const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
+          const uint64_t ab = tc::f2_pack(a, b);
+          acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
+          hi[i] = tc::pack_bf16x2_trunc(a, b);
+          float da, db;
+          tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
+          lo[i] = tc::pack_bf16x2(da, db);
+        }
+        tc::tmem_st16(sbuf + 32 * g4, hi);
+        tc::tmem_st16(sbuf + 32 * g4 + 16, lo);
+      }
+      float rp[8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) tc::f2_unpack(acc2[a], rp[2 * a], rp[2 * a + 1]);
+      const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+      l = l * factor + rs;
+      // O_X after P.V_X(j-1) (already complete: S_X(j) was issued after it), rescaled to the new max; rows of
+      // the warp that keep their max multiply by factor = 1, which is exact
+      if (j >= 1 && __any_sync(~0u, rescale)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(obuf + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+          tc::tmem_st32(obuf + c * 32, o);
+        }
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bar_pf[x]);
+      ++j;
+    }
+    if (ok && j >= 1) {
+      // O_X / l once the last P.V_X is done
+      if (__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (j - 1) & 1, kWaitCycles))) {
+        tc::fence_after_sync();
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = p.out + ((size_t)row * p.hq + h0 + x) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(obuf + c * 32, o);
+          tc::tmem_wait_ld();
+          if (active) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
+              v.y = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
+              v.z = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
+              v.w = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+            }
+          }
+        }
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == kWarpMma) tc::tmem_dealloc(tmem, 512);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -537,13 +910,20 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(fork_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(fork_attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair::kSmemBytes + 1024) != cudaSuccess)
       return hs::fail(HS_ECUDA, "fork_attn_tc: cannot raise the shared-memory limit");
     configured = true;
   }
   Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status};
-  fork_attn_tc_kernel<<<dim3(caps->max_tiles * hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
-                                                                                        m_v128, prm);
+  if ((hq / hkv) % 2 == 0) {  // two query heads that share a KV head per CTA
+    fork_attn_tc2_kernel<<<dim3(caps->max_tiles * (hq / 2)), kThreads, pair::kSmemBytes + 1024, st>>>(
+        m_q, m_k16, m_k128, m_v16, m_v128, prm);
+  } else {
+    fork_attn_tc_kernel<<<dim3(caps->max_tiles * hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
+                                                                                          m_v128, prm);
+  }
   HS_LAUNCH_CHECK("fork_attn_tc");
   return HS_OK;
 }
