@@ -248,16 +248,17 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       const uint8_t* Ai = smem + kOffA + i * 16384;
 #pragma unroll
       for (int u = 0; u < 64; ++u) {
-        float acc = u == t ? 1.f : 0.f;
+        // four partial sums (s mod 4) so the products do not wait on one another, combined in a fixed order
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int s = 0; s < u; s += 4) {
           const float4 a4 = *reinterpret_cast<const float4*>(Ai + a_off(u, s));
-          acc = fmaf(-a4.x, x[s], acc);
-          if (s + 1 < u) acc = fmaf(-a4.y, x[s + 1], acc);
-          if (s + 2 < u) acc = fmaf(-a4.z, x[s + 2], acc);
-          if (s + 3 < u) acc = fmaf(-a4.w, x[s + 3], acc);
+          acc[0] = fmaf(a4.x, x[s], acc[0]);
+          if (s + 1 < u) acc[1] = fmaf(a4.y, x[s + 1], acc[1]);
+          if (s + 2 < u) acc[2] = fmaf(a4.z, x[s + 2], acc[2]);
+          if (s + 3 < u) acc[3] = fmaf(a4.w, x[s + 3], acc[3]);
         }
-        x[u] = acc;
+        x[u] = (u == t ? 1.f : 0.f) - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       }
     }
     tc::named_sync(1, 128);  // A is read by every thread before the T operands overwrite it
