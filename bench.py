@@ -38,9 +38,9 @@ GDN = dict(h=16, d=128, seed=3000)
 WORKLOAD = ("fork_attn trunk4096+8br U[16,64] GQA32/8 d128 page16 bf16 + 4-option readout; "
             "gdn_fork trunk8192+16br U[8,128] H16 d128 chunk64 fp32-state bf16")
 N_OPT = 4
-# DRAM traffic per launch from one ncu capture (profiles/fork_attn_tc_attention_tree.md),
+# DRAM traffic per launch from one ncu capture (profiles/fork_attn_tc2_attention_tree.md),
 # valid only while the kernel source still has the hash it was captured with.
-NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "b6fed49680ddae60", 57.80e6)}
+NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "36ab6286050e07b6", 57.02e6)}
 
 
 def ncu_traffic(kernel: str):
