@@ -159,7 +159,7 @@ class Clocks:
 class Step:
     """Device buffers of one input set and the step through the C ABI."""
 
-    def __init__(self, torch, api, rounds, at, gt, a_inp, g_inp, W, n_sets=2):
+    def __init__(self, torch, api, rounds, at, gt, a_inp, g_inp, W, n_sets=3):
         self.torch, self.api, self.rounds = torch, api, rounds
         dev = "cuda"
         self.at, self.gt = at, gt
@@ -174,34 +174,79 @@ class Step:
         self.a_caps, self.g_caps = R.caps, R2.caps
         del R, R2
         bf = torch.bfloat16
+        n_ro = sum(r.n_nodes - 1 for r in at.requests)
+        # Each group of tensors that crosses the host link together lives in one byte buffer
+        # (attention inputs, GDN inputs, attention results + log-probs, GDN results), so a step
+        # moves it with one copy; the tensors are views into it.
+        a_in = [("a_" + k, a.shape, bf) for k, a in a_stream.items()]
+        g_in = [("g_" + k, a.shape, torch.float32 if k in ("alpha", "beta") else bf) for k, a in g_stream.items()]
+        a_res = [("a_out", a_stream["q"].shape, bf), ("lp", (n_ro, N_OPT), torch.float32)]
+        g_res = [("g_out", g_stream["v"].shape, bf)]
+        self.groups = {"a_in": a_in, "g_in": g_in, "a_res": a_res, "g_res": g_res}
+
+        def packed(spec, device, pin):
+            offs, n = [], 0
+            for _, shape, dt in spec:
+                offs.append(n)
+                n += -(-int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size() // 256) * 256
+            buf = torch.empty(n, dtype=torch.uint8, device=device)
+            if pin:
+                buf = buf.pin_memory()
+            views = {}
+            for (name, shape, dt), o in zip(spec, offs):
+                nb = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+                views[name] = buf[o:o + nb].view(dt).view(shape)
+            return buf, views
+
+        self.host_buf = {}
         self.host = {}   # pinned host copies for the end-to-end timing
+        for g in ("a_in", "g_in"):
+            self.host_buf[g], v = packed(self.groups[g], "cpu", True)
+            self.host.update(v)
         for k, a in a_stream.items():
-            self.host["a_" + k] = torch.from_numpy(a).to(bf).pin_memory()
+            self.host["a_" + k].copy_(torch.from_numpy(a))
         for k, a in g_stream.items():
-            t = torch.from_numpy(a)
-            self.host["g_" + k] = (t if k in ("alpha", "beta") else t.to(bf)).pin_memory()
-        self.sets = []
+            self.host["g_" + k].copy_(torch.from_numpy(a))
+        self.sets, self.set_bufs = [], []
         for _ in range(n_sets):
-            s = {k: v.to(dev) for k, v in self.host.items()}
-            s["a_out"] = torch.empty_like(s["a_q"])
-            s["g_out"] = torch.empty_like(s["g_v"])
+            s, bufs = {}, {}
+            for g in self.groups:
+                bufs[g], v = packed(self.groups[g], dev, False)
+                s.update(v)
+            bufs["a_in"].copy_(self.host_buf["a_in"])
+            bufs["g_in"].copy_(self.host_buf["g_in"])
             self.sets.append(s)
+            self.set_bufs.append(bufs)
         self.n_pages = self.a_T // 16 + 64
         self.pool = api.PagePool(self.n_pages)
         self.k_pages = torch.zeros((ATTN["hkv"], self.n_pages, 16, ATTN["d"]), dtype=bf, device=dev)
         self.v_pages = torch.zeros_like(self.k_pages)
         self.state = torch.zeros((8, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.float32, device=dev)
-        self.a_meta = torch.empty(api.Round(self.a_caps).meta_bytes() // 4, dtype=torch.int32, device=dev)
-        self.g_meta = torch.empty(api.Round(self.g_caps).meta_bytes() // 4, dtype=torch.int32, device=dev)
+        # device metadata per input set, so a step's upload never overwrites what an earlier step still reads
+        self.metas = [(torch.empty(api.Round(self.a_caps).meta_bytes() // 4, dtype=torch.int32, device=dev),
+                       torch.empty(api.Round(self.g_caps).meta_bytes() // 4, dtype=torch.int32, device=dev))
+                      for _ in range(n_sets)]
+        self.a_meta, self.g_meta = self.metas[0]
         self.ws = torch.empty(api.gdn_workspace_bytes(self.g_caps, GDN["h"], GDN["d"], GDN["d"]),
                               dtype=torch.uint8, device=dev)
         self.W = torch.from_numpy(W).to(dev)
-        n_ro = sum(r.n_nodes - 1 for r in at.requests)
-        self.lp = torch.empty((n_ro, N_OPT), dtype=torch.float32, device=dev)
+        self.lp = self.sets[0]["lp"]  # (per input set, so a step's results are not overwritten while they copy back)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream()
         self.ev_attn = []
         self.ev_gdn = []
+        # end to end: one stream per copy direction (the link is full duplex), pinned result buffers
+        # per input set, and per-set events
+        self.copy_stream = torch.cuda.Stream()
+        self.d2h_stream = torch.cuda.Stream()
+        self.host_out = [{g: packed(self.groups[g], "cpu", True)[0] for g in ("a_res", "g_res")} for _ in self.sets]
+        self.set_free = [None] * len(self.sets)
+        self.e2e_events = [[torch.cuda.Event() for _ in range(5)] for _ in self.sets]
+        # metadata goes up from pinned buffers (one pair per input set) so the upload never waits
+        # behind input copies on the copy engine; an event says when a buffer may be refilled
+        self.meta_host = [(torch.empty(self.a_meta.numel(), dtype=torch.int32).pin_memory(),
+                           torch.empty(self.g_meta.numel(), dtype=torch.int32).pin_memory()) for _ in self.sets]
+        self.meta_sent = [None] * len(self.sets)
 
     def build(self):
         """Host round build (C++) for both trees; the GDN trunk saves its end
@@ -211,27 +256,58 @@ class Step:
         R_g, _ = self.rounds.build_round(self.gt, None, caps=self.g_caps, temp_slot0=1, n_temp_slots=4)
         return R_a, R_g
 
-    def run(self, i: int, time_attn: bool = False):
+    def _inputs_h2d(self, bufs, ev):
+        cs = self.copy_stream
+        with self.torch.cuda.stream(cs):
+            bufs["a_in"].copy_(self.host_buf["a_in"], non_blocking=True)
+            ev[0].record(cs)
+            bufs["g_in"].copy_(self.host_buf["g_in"], non_blocking=True)
+            ev[1].record(cs)
+
+    def run(self, i: int, time_attn: bool = False, ev_a_in=None, ev_g_in=None, ev_a_done=None, up=None,
+            inputs=None):
+        """One step on the compute stream.  `up` (a stream) carries the metadata
+        upload instead of the compute stream; the caller's ev_a_in then orders it."""
         api, s = self.api, self.sets[i % len(self.sets)]
+        k_set = i % len(self.sets)
         R_a, R_g = self.build()
-        R_a.upload(self.a_meta)
-        R_g.upload(self.g_meta)
-        api.kv_page_write(self.a_caps, self.a_meta, s["a_k"], s["a_v"], self.k_pages, self.v_pages, self.status)
+        ha, hg = self.meta_host[k_set]
+        if self.meta_sent[k_set] is not None:
+            self.meta_sent[k_set].synchronize()   # this pinned buffer's previous upload is done
+        R_a.pack(ha)
+        R_g.pack(hg)
+        us = up if up is not None else self.stream
+        a_meta, g_meta = self.metas[k_set]
+        with self.torch.cuda.stream(us):
+            a_meta.copy_(ha, non_blocking=True)
+            g_meta.copy_(hg, non_blocking=True)
+            if self.meta_sent[k_set] is None:
+                self.meta_sent[k_set] = self.torch.cuda.Event()
+            self.meta_sent[k_set].record(us)
+        if inputs is not None:
+            inputs()
+        if ev_a_in is not None:
+            self.stream.wait_event(ev_a_in)
+        api.kv_page_write(self.a_caps, a_meta, s["a_k"], s["a_v"], self.k_pages, self.v_pages, self.status)
         if time_attn:
             e0 = self.torch.cuda.Event(enable_timing=True)
             e1 = self.torch.cuda.Event(enable_timing=True)
             e0.record(self.stream)
-        api.fork_attn(self.a_caps, self.a_meta, s["a_q"], self.k_pages, self.v_pages, s["a_out"], self.status)
+        api.fork_attn(self.a_caps, a_meta, s["a_q"], self.k_pages, self.v_pages, s["a_out"], self.status)
         if time_attn:
             e1.record(self.stream)
             self.ev_attn.append((e0, e1))
-        api.choice_logprobs(self.a_caps, self.a_meta, s["a_out"].view(s["a_out"].shape[0], -1), self.W, self.lp,
+        api.choice_logprobs(self.a_caps, a_meta, s["a_out"].view(s["a_out"].shape[0], -1), self.W, s["lp"],
                             self.status)
+        if ev_a_done is not None:
+            ev_a_done.record(self.stream)
+        if ev_g_in is not None:
+            self.stream.wait_event(ev_g_in)
         if time_attn:
             g0 = self.torch.cuda.Event(enable_timing=True)
             g1 = self.torch.cuda.Event(enable_timing=True)
             g0.record(self.stream)
-        api.gdn_fork_prefill(self.g_caps, self.g_meta, s["g_q"], s["g_k"], s["g_v"], s["g_alpha"], s["g_beta"],
+        api.gdn_fork_prefill(self.g_caps, g_meta, s["g_q"], s["g_k"], s["g_v"], s["g_alpha"], s["g_beta"],
                              self.state, s["g_out"], self.ws, self.status)
         if time_attn:
             g1.record(self.stream)
@@ -241,16 +317,31 @@ class Step:
 
     def run_e2e(self, i: int):
         """Same step from pinned host buffers: H2D of the inputs, the step,
-        D2H of the outputs (attention rows, GDN rows, log-probs)."""
-        s = self.sets[i % len(self.sets)]
-        h2d = 0
-        for k, v in self.host.items():
-            s[k].copy_(v, non_blocking=True)
-            h2d += v.numel() * v.element_size()
-        self.run(i)
-        outs = [s["a_out"].to("cpu", non_blocking=True), s["g_out"].to("cpu", non_blocking=True),
-                self.lp.to("cpu", non_blocking=True)]
-        d2h = sum(o.numel() * o.element_size() for o in outs)
+        D2H of the outputs (attention rows + log-probs, GDN rows), one copy per
+        group.  Copies run on their own streams, one per direction: the GDN
+        inputs load while attention computes, the attention results return
+        while GDN computes, and the next steps' inputs (the other input sets)
+        load while this step computes and its results return."""
+        torch = self.torch
+        k_set = i % len(self.sets)
+        bufs, ho, cs, ds = self.set_bufs[k_set], self.host_out[k_set], self.copy_stream, self.d2h_stream
+        ev = self.e2e_events[k_set]
+        with torch.cuda.stream(cs):
+            if self.set_free[k_set] is not None:       # the set's previous step is done with it
+                cs.wait_event(self.set_free[k_set])
+        # (run() queues the metadata upload on the copy stream here, ahead of this step's inputs)
+        self.run(i, ev_a_in=ev[0], ev_g_in=ev[1], ev_a_done=ev[2], up=cs,
+                 inputs=lambda: self._inputs_h2d(bufs, ev))
+        ev[3].record(self.stream)
+        with torch.cuda.stream(ds):
+            ds.wait_event(ev[2])
+            ho["a_res"].copy_(bufs["a_res"], non_blocking=True)
+            ds.wait_event(ev[3])
+            ho["g_res"].copy_(bufs["g_res"], non_blocking=True)
+            ev[4].record(ds)
+        self.set_free[k_set] = ev[4]
+        h2d = self.host_buf["a_in"].numel() + self.host_buf["g_in"].numel()
+        d2h = ho["a_res"].numel() + ho["g_res"].numel()
         return h2d, d2h
 
 
@@ -376,7 +467,7 @@ def main():
     torch.cuda.synchronize()
     api.check_status(step.status)
 
-    # ---- device-timed region: K steps, inputs resident, 2 rotating input sets ----
+    # ---- device-timed region: K steps, inputs resident, 3 rotating input sets ----
     n0 = _lib.launch_count()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     step.ev_attn = []
@@ -408,9 +499,15 @@ def main():
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(step.stream)
+    step.copy_stream.wait_event(e0)          # no copy starts before the timed region
+    step.d2h_stream.wait_event(e0)
+    step.set_free = [None] * len(step.sets)
     h2d = d2h = 0
     for i in range(args.steps):
         h2d, d2h = step.run_e2e(i)
+    for f in step.set_free:                   # every result is back on the host before the region ends
+        if f is not None:
+            step.stream.wait_event(f)
     e1.record(step.stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(torch, e0.elapsed_time(e1), ws)
@@ -430,7 +527,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "tokens_per_step": tokens,
-                       "l2": "inputs > L2: 2 rotating input sets (~0.9 GB touched per step)",
+                       "l2": "inputs > L2: 3 rotating input sets (~0.9 GB touched per step)",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof,
             "kernels": {"fork_attn_ms": round(attn_ms, 4), "attn_bytes_per_step": attn_bytes(at),

@@ -110,9 +110,14 @@ class Round:
     def meta_bytes(self) -> int:
         return int(lib.hs_round_meta_bytes(C.byref(self.caps)))
 
-    def pack(self) -> "torch.Tensor":
+    def pack(self, out: "torch.Tensor" = None) -> "torch.Tensor":
+        """The metadata blob in host memory; `out` (int32, contiguous, e.g. a
+        pinned buffer for an asynchronous upload) receives it if given."""
         n = self.meta_bytes()
-        out = torch.empty(n // 4, dtype=torch.int32)
+        if out is None:
+            out = torch.empty(n // 4, dtype=torch.int32)
+        if out.device.type != "cpu" or not out.is_contiguous() or out.numel() * 4 < n:
+            raise ValueError("pack needs a contiguous host int32 tensor of at least meta_bytes()/4 words")
         check(lib.hs_round_pack(self._h, out.data_ptr(), n))
         return out
 
