@@ -199,14 +199,17 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         const int row0 = M.chunk(c_off + ci)[C_ROW0];
         const uint8_t* w = p.ws + ((size_t)(c_off + ci) * p.H + h) * gdnws::kBytes;
         uint8_t* sb = stage(ci);
-        tc::mbar_expect_tx(&bar_full[s], kStageTx);
+        // a group without outputs needs neither Q nor P; a transition (Ut = 0) not Ut either
+        tc::mbar_expect_tx(&bar_full[s], kStageTx - (outputs ? 0u : 16384u + 8192u) - (zero_ut ? 16384u : 0u));
         tc::bulk_load(sb + kStW, w + gdnws::kW, 16384, &bar_full[s]);
-        tc::bulk_load(sb + kStUt, w + gdnws::kU, 16384, &bar_full[s]);
+        if (!zero_ut) tc::bulk_load(sb + kStUt, w + gdnws::kU, 16384, &bar_full[s]);
         tc::bulk_load(sb + kStG, w + gdnws::kG, gdnws::kBytes - gdnws::kG, &bar_full[s]);
         tc::bulk_load(sb + kStK, w + gdnws::kK, 16384, &bar_full[s]);
-        for (int half = 0; half < 2; ++half)
-          tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
-        tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[s]);
+        if (outputs) {
+          for (int half = 0; half < 2; ++half)
+            tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
+          tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[s]);
+        }
         ++issued;
       }
       for (int ci = issued >= kStages ? issued - kStages : 0; ci < issued; ++ci)
