@@ -485,10 +485,15 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Two query heads per CTA (heads 2p and 2p + 1 of a KV-head group of even size
-// share every K and V page): the heads' online softmaxes run in two warp
-// groups while the MMA warp alternates between them, so one head's softmax
-// overlaps the other head's products and each K/V block is loaded once.
+// Two query heads per work item (heads 2p and 2p + 1 of a KV-head group of
+// even size share every K and V page): the heads' online softmaxes run in two
+// warp groups while the MMA warp alternates between them, so one head's
+// softmax overlaps the other head's products and each K/V block is loaded
+// once.  One persistent CTA per SM walks its items (tiles longest first,
+// dealt to the CTAs in snake order); block counters run across items, the
+// next item's Q loads once the current item's S products are done, and its
+// first P.V waits until the current item's O has been read out, so the next
+// item's first S products and copies overlap the current item's epilogue.
 //
 //   warp 8      TMA: Q of both heads once; per block K and V into a 2-stage
 //               ring (a K stage is refilled once both heads' S are computed,
@@ -520,23 +525,28 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                      const __grid_constant__ CUtensorMap tm_v128, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2], bar_sf[2], bar_pf[2], bar_pv[2], bar_done;
+  __shared__ uint64_t bar_q, bar_qe, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2];
+  __shared__ uint64_t bar_sf[2], bar_pf[2], bar_pv[2], bar_done;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   Meta M{p.meta};
   const int np = p.hq / 2;
-  const int tile = blockIdx.x / np;  // tile-major: both heads of the heaviest tiles first
-  if (tile >= M.h(H_N_TILE)) return;
-  const int32_t* tl = M.tile(tile);
-  const int h0 = 2 * (blockIdx.x % np);
-  const int kvh = h0 / (p.hq / p.hkv);
+  const int n_items = M.h(H_N_TILE) * np;  // (tile, head pair), heaviest tiles first
+  if ((int)blockIdx.x >= n_items) return;
+  // this CTA's k-th item: round k of the items, dealt to the CTAs in snake order
+  auto item_of = [&](int k) -> int {
+    const int G = gridDim.x;
+    const int w = k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    return w < n_items ? w : -1;
+  };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     tc::mbar_init(&bar_q, 1);
+    tc::mbar_init(&bar_qe, 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&bar_kf[s], 1);
       tc::mbar_init(&bar_vf[s], 1);
@@ -557,9 +567,6 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-
-  Cursor cur;
-  cur.init(M, tl);
   const int n_ref = M.h(H_N_PAGE_REF);
   const int32_t* refs = M.page_ref();
 
@@ -569,74 +576,93 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k16);
       tc::prefetch_tmap(&tm_v16);
-      tc::mbar_expect_tx(&bar_q, 2 * kTile);
-      for (int x = 0; x < 2; ++x) {
-        tc::tma_load_3d(smem + pair::kOffQ + x * kTile, &tm_q, 0, h0 + x, tl[TL_ROW0], &bar_q);
-        tc::tma_load_3d(smem + pair::kOffQ + x * kTile + kSlab, &tm_q, 64, h0 + x, tl[TL_ROW0], &bar_q);
-      }
       const int oob_y = p.hkv * p.n_pages * kPage;  // first row past the pool: zero fill
-      int j = 0;
-      while (cur.next()) {
-        const int s = j & 1, n = j >> 1;
-        const int npg = (cur.valid() + kPage - 1) / kPage;
-        int pg[8];
-        bool consecutive = npg == 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          pg[i] = -1;
-          if (i < npg) {
-            const int ref = cur.sp_off + cur.b0 / kPage + i;
-            const int page = ref < n_ref ? refs[ref] : -1;
-            if (page >= 0 && page < p.n_pages) {
-              pg[i] = page;
-            } else {
-              hsd::set_status(p.status, ref < n_ref ? HS_DEV_BAD_PAGE : HS_DEV_BAD_META);
-            }
-          }
-          if (i > 0 && (pg[i] < 0 || pg[i] != pg[i - 1] + 1)) consecutive = false;
-        }
-        if (pg[0] < 0) consecutive = false;
-        uint8_t* ks = smem + pair::kOffK + s * kTile;
-        uint8_t* vs = smem + pair::kOffV + s * kTile;
-        if (n > 0 && !tc::mbar_wait(&bar_ke[s], (n - 1) & 1, kWaitCycles)) {
+      int jg = 0, n_q = 0;                           // blocks and Q tiles (non-empty items) issued
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k);
+        if (w < 0) break;
+        const int32_t* tl = M.tile(w / np);
+        const int h0 = 2 * (w % np), kvh = h0 / (p.hq / p.hkv);
+        Cursor cur;
+        cur.init(M, tl);
+        if (!cur.next()) continue;  // an item without keys is skipped by every role
+        // Q of this item once every S product of the previous item is done
+        if (n_q >= 1 && !tc::mbar_wait(&bar_qe, (n_q - 1) & 1, kWaitCycles)) {
           record(p.status, &abort_flag, HS_DEV_TIMEOUT);
           break;
         }
         if (*(volatile int*)&abort_flag) break;
-        tc::mbar_expect_tx(&bar_kf[s], kTile);
-        if (consecutive) {
-          const int y = (kvh * p.n_pages + pg[0]) * kPage;
-          for (int half = 0; half < 2; ++half) tc::tma_load_2d(ks + half * kSlab, &tm_k128, half * 64, y, &bar_kf[s]);
-        } else {
-#pragma unroll
+        tc::mbar_expect_tx(&bar_q, 2 * kTile);
+        for (int x = 0; x < 2; ++x) {
+          tc::tma_load_3d(smem + pair::kOffQ + x * kTile, &tm_q, 0, h0 + x, tl[TL_ROW0], &bar_q);
+          tc::tma_load_3d(smem + pair::kOffQ + x * kTile + kSlab, &tm_q, 64, h0 + x, tl[TL_ROW0], &bar_q);
+        }
+        ++n_q;
+        do {
+          const int s = jg & 1, n = jg >> 1;
+          const int npg = (cur.valid() + kPage - 1) / kPage;
+          int pg[8];
+          bool consecutive = npg == 8;
           for (int i = 0; i < 8; ++i) {
-            const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
-            for (int half = 0; half < 2; ++half)
-              tc::tma_load_2d(ks + half * kSlab + i * 2048, &tm_k16, half * 64, y, &bar_kf[s]);
+            pg[i] = -1;
+            if (i < npg) {
+              const int ref = cur.sp_off + cur.b0 / kPage + i;
+              const int page = ref < n_ref ? refs[ref] : -1;
+              if (page >= 0 && page < p.n_pages) {
+                pg[i] = page;
+              } else {
+                hsd::set_status(p.status, ref < n_ref ? HS_DEV_BAD_PAGE : HS_DEV_BAD_META);
+              }
+            }
+            if (i > 0 && (pg[i] < 0 || pg[i] != pg[i - 1] + 1)) consecutive = false;
           }
-        }
-        if (n > 0 && !tc::mbar_wait(&bar_ve[s], (n - 1) & 1, kWaitCycles)) {
-          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
-          ++j;  // the K copy of this block is in flight: drain it below
-          break;
-        }
-        tc::mbar_expect_tx(&bar_vf[s], kTile);
-        if (consecutive) {
-          const int y = (kvh * p.n_pages + pg[0]) * kPage;
-          for (int half = 0; half < 2; ++half) tc::tma_load_2d(vs + half * kSlab, &tm_v128, half * 64, y, &bar_vf[s]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
-            for (int half = 0; half < 2; ++half)
-              tc::tma_load_2d(vs + half * kSlab + i * 2048, &tm_v16, half * 64, y, &bar_vf[s]);
+          if (pg[0] < 0) consecutive = false;
+          uint8_t* ks = smem + pair::kOffK + s * kTile;
+          uint8_t* vs = smem + pair::kOffV + s * kTile;
+          if (n > 0 && !tc::mbar_wait(&bar_ke[s], (n - 1) & 1, kWaitCycles)) {
+            record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+            ok = false;
+            break;
           }
-        }
-        ++j;
+          if (*(volatile int*)&abort_flag) {
+            ok = false;
+            break;
+          }
+          tc::mbar_expect_tx(&bar_kf[s], kTile);
+          if (consecutive) {
+            const int y = (kvh * p.n_pages + pg[0]) * kPage;
+            for (int half = 0; half < 2; ++half) tc::tma_load_2d(ks + half * kSlab, &tm_k128, half * 64, y, &bar_kf[s]);
+          } else {
+            for (int i = 0; i < 8; ++i) {
+              const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
+              for (int half = 0; half < 2; ++half)
+                tc::tma_load_2d(ks + half * kSlab + i * 2048, &tm_k16, half * 64, y, &bar_kf[s]);
+            }
+          }
+          if (n > 0 && !tc::mbar_wait(&bar_ve[s], (n - 1) & 1, kWaitCycles)) {
+            record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+            ++jg;  // the K copy of this block is in flight: drain it below
+            ok = false;
+            break;
+          }
+          tc::mbar_expect_tx(&bar_vf[s], kTile);
+          if (consecutive) {
+            const int y = (kvh * p.n_pages + pg[0]) * kPage;
+            for (int half = 0; half < 2; ++half) tc::tma_load_2d(vs + half * kSlab, &tm_v128, half * 64, y, &bar_vf[s]);
+          } else {
+            for (int i = 0; i < 8; ++i) {
+              const int y = pg[i] >= 0 ? (kvh * p.n_pages + pg[i]) * kPage : oob_y;
+              for (int half = 0; half < 2; ++half)
+                tc::tma_load_2d(vs + half * kSlab + i * 2048, &tm_v16, half * 64, y, &bar_vf[s]);
+            }
+          }
+          ++jg;
+        } while (cur.next());
       }
       // drain: every copy this thread issued has landed before the CTA leaves
-      tc::mbar_wait(&bar_q, 0, kWaitCycles);
-      for (int i = (j >= 2 ? j - 2 : 0); i < j; ++i) {
+      if (n_q > 0) tc::mbar_wait(&bar_q, (n_q - 1) & 1, kWaitCycles);
+      for (int i = (jg >= 2 ? jg - 2 : 0); i < jg; ++i) {
         tc::mbar_wait(&bar_kf[i & 1], (i >> 1) & 1, kWaitCycles);
         tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles);
       }
@@ -644,8 +670,8 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      bool ok = tc::mbar_wait(&bar_q, 0, kWaitCycles);
-      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      bool ok = true;
+      int jg = 0, kq = 0;  // blocks issued over all items, non-empty items
       auto s_mma = [&](int x, int jj) {  // S_X(jj) = Q_X K_jj^T
         const uint32_t sq = tc::smem_u32(smem + pair::kOffQ + x * kTile);
         const uint32_t sk = tc::smem_u32(smem + pair::kOffK + (jj & 1) * kTile);
@@ -657,7 +683,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         tc::mma_commit(&bar_sf[x]);
       };
-      auto pv_mma = [&](int x, int jj) {  // O_X += P_X(jj) V_jj, per 32 keys: high parts, then low parts
+      auto pv_mma = [&](int x, int jj, bool first) {  // O_X += P_X(jj) V_jj, per 32 keys: high, then low parts
         const uint32_t sv = tc::smem_u32(smem + pair::kOffV + (jj & 1) * kTile);
         const uint32_t pt = tmem + pair::kTmS + 128 * x;
 #pragma unroll
@@ -668,51 +694,64 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             for (int k = 0; k < 2; ++k) {  // keys 32 g4 + 16 k .. +15
               const uint64_t b = tc::sdesc_sw128(sv + g4 * 4096 + k * 2048, kSlab, 1024);
               tc::mma_bf16_ts(tmem + pair::kTmO + 128 * x, pt + 32 * g4 + 16 * part + 8 * k, b, kIdescPV,
-                              (jj > 0 || g4 > 0 || part > 0 || k > 0) ? 1u : 0u);
+                              (!first || g4 > 0 || part > 0 || k > 0) ? 1u : 0u);
             }
           }
         }
         tc::mma_commit(&bar_pv[x]);
       };
-      // the number of blocks of the tile, counted once (the loop then needs no cursor)
-      int n_blk = 0;
-      while (cur.next()) ++n_blk;
-      if (ok && n_blk > 0) {
-        if (!tc::mbar_wait(&bar_kf[0], 0, kWaitCycles)) {
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k);
+        if (w < 0) break;
+        Cursor cur;
+        cur.init(M, M.tile(w / np));
+        int n_blk = 0;
+        while (cur.next()) ++n_blk;  // counted once: the loop needs no cursor
+        if (n_blk == 0) continue;
+        if (!tc::mbar_wait(&bar_q, kq & 1, kWaitCycles) ||
+            !tc::mbar_wait_spin(&bar_kf[jg & 1], (jg >> 1) & 1, kWaitCycles)) {
           ok = false;
-        } else {
-          tc::fence_after_sync();
-          s_mma(0, 0);
-          s_mma(1, 0);
-          tc::mma_commit(&bar_ke[0]);
+          break;
         }
-      }
-      for (int j = 0; ok && j < n_blk; ++j) {
-        const bool more = j + 1 < n_blk;
-        for (int x = 0; x < 2 && ok; ++x) {
-          // (polling waits: a suspended MMA thread would notice the softmax late)
-          if (!tc::mbar_wait_spin(&bar_pf[x], j & 1, kWaitCycles) ||
-              (x == 0 && !tc::mbar_wait_spin(&bar_vf[j & 1], (j >> 1) & 1, kWaitCycles))) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          if (*(volatile int*)&abort_flag) {
-            ok = false;
-            break;
-          }
-          pv_mma(x, j);
-          if (x == 1) tc::mma_commit(&bar_ve[j & 1]);
-          if (more) {
-            if (x == 0 && !tc::mbar_wait_spin(&bar_kf[(j + 1) & 1], ((j + 1) >> 1) & 1, kWaitCycles)) {
+        tc::fence_after_sync();
+        // S of the item's first block: the S buffers hold the previous item's last P, whose P.V is issued
+        s_mma(0, jg);
+        s_mma(1, jg);
+        tc::mma_commit(&bar_ke[jg & 1]);
+        if (n_blk == 1) tc::mma_commit(&bar_qe);
+        for (int j = 0; ok && j < n_blk; ++j, ++jg) {
+          const bool more = j + 1 < n_blk;
+          for (int x = 0; x < 2 && ok; ++x) {
+            // (polling waits: a suspended MMA thread would notice the softmax late)
+            // (P_X of an item's first block is written after the previous item's O_X was read out, so
+            // the P.V that starts O_X afresh waits for nothing more)
+            if (!tc::mbar_wait_spin(&bar_pf[x], jg & 1, kWaitCycles) ||
+                (x == 0 && !tc::mbar_wait_spin(&bar_vf[jg & 1], (jg >> 1) & 1, kWaitCycles))) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
-            s_mma(x, j + 1);
-            if (x == 1) tc::mma_commit(&bar_ke[(j + 1) & 1]);
+            if (*(volatile int*)&abort_flag) {
+              ok = false;
+              break;
+            }
+            pv_mma(x, jg, j == 0);
+            if (x == 1) tc::mma_commit(&bar_ve[jg & 1]);
+            if (more) {
+              if (x == 0 && !tc::mbar_wait_spin(&bar_kf[(jg + 1) & 1], ((jg + 1) >> 1) & 1, kWaitCycles)) {
+                ok = false;
+                break;
+              }
+              tc::fence_after_sync();
+              s_mma(x, jg + 1);
+              if (x == 1) {
+                tc::mma_commit(&bar_ke[(jg + 1) & 1]);
+                if (j + 2 == n_blk) tc::mma_commit(&bar_qe);  // the item's last S products are issued
+              }
+            }
           }
         }
+        ++kq;
       }
       if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
       // every MMA issued by this thread completes before O is read and TMEM is freed
@@ -724,129 +763,140 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // ------------------------------------------------------------ softmax
     const int x = warp / 4;                      // head A or B
     const int t = (warp % 4) * 32 + lane;        // row of the tile == TMEM lane
-    const int row = tl[TL_ROW0] + t;
-    const bool active = t < tl[TL_N_ROWS];
-    int my_seg = -1, my_idx = 0;
-    if (active) {
-      my_seg = M.tok(row)[T_SEG];
-      my_idx = M.tok(row)[T_IDX];
-    }
     const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t sbuf = tmem + lane_base + pair::kTmS + 128 * x, obuf = tmem + lane_base + pair::kTmO + 128 * x;
-    float m_used = -INFINITY, l = 0.f;
     const float sl2 = p.scale_log2e;
-    int j = 0;
+    int jg = 0;  // blocks over all items
     bool ok = true;
-    while (cur.next()) {
-      // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[x], j & 1, kWaitCycles))) {
+    for (int k = 0; ok; ++k) {
+      const int w = item_of(k);
+      if (w < 0) break;
+      const int32_t* tl = M.tile(w / np);
+      const int h0 = 2 * (w % np);
+      Cursor cur;
+      cur.init(M, tl);
+      const int row = tl[TL_ROW0] + t;
+      const bool active = t < tl[TL_N_ROWS];
+      int my_seg = -1, my_idx = 0;
+      if (active) {
+        my_seg = M.tok(row)[T_SEG];
+        my_idx = M.tok(row)[T_IDX];
+      }
+      float m_used = -INFINITY, l = 0.f;
+      int j = 0;
+      while (cur.next()) {
+        // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[x], jg & 1, kWaitCycles))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const int lim = cur.full() ? kBlk
+                                   : (!active ? 0 : !cur.own ? cur.sp_n - cur.b0
+                                                             : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0));
+        // pass 1: the row max of the block, 32 scores at a time (scores past the row's visible keys read as -inf)
+        const bool masked = __any_sync(~0u, lim < kBlk);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(sbuf + 32 * c, r);
+          tc::tmem_wait_ld();
+          if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 32 * c + i < lim ? r[i] : 0xFF800000u;
+          }
+          float m2[2] = {mx, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < 16; ++i) m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          mx = fmaxf(m2[0], m2[1]);
+        }
+        const float m_new = fmaxf(m_used, mx * sl2);
+        float factor = 1.f;
+        const bool rescale = m_new > m_used + 8.f;
+        if (rescale) {
+          factor = exp2f(m_used - m_new);
+          m_used = m_new;
+        }
+        const float mref = m_used == -INFINITY ? 0.f : m_used;
+        // pass 2, 32 keys at a time: P = 2^(s log2e scale - m) over S in place; pairs of keys in fp32x2
+        const uint64_t sc2 = tc::f2_pack(sl2, sl2), mm2 = tc::f2_pack(-mref, -mref);
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {  // keys 32 g4 .. +31: P words in the same 32 columns (16 high, 16 low)
+          uint32_t r[32], hi[16], lo[16];
+          tc::tmem_ld32(sbuf + 32 * g4, r);
+          tc::tmem_wait_ld();
+          if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 32 * g4 + i < lim ? r[i] : 0xFF800000u;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float ya, yb;
+            tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
+            const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
+            const uint64_t ab = tc::f2_pack(a, b);
+            acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
+            hi[i] = tc::pack_bf16x2_trunc(a, b);
+            float da, db;
+            tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
+            lo[i] = tc::pack_bf16x2(da, db);
+          }
+          tc::tmem_st16(sbuf + 32 * g4, hi);
+          tc::tmem_st16(sbuf + 32 * g4 + 16, lo);
+        }
+        float rp[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) tc::f2_unpack(acc2[a], rp[2 * a], rp[2 * a + 1]);
+        const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+        l = l * factor + rs;
+        // O_X after P.V_X of the previous block (already complete: this S_X was issued after it), rescaled; rows
+        // of the warp that keep their max multiply by factor = 1, which is exact.  An item's first block never
+        // rescales (its P.V starts O_X afresh).
+        if (j >= 1 && __any_sync(~0u, rescale)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(obuf + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+            tc::tmem_st32(obuf + c * 32, o);
+          }
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&bar_pf[x]);
+        ++j;
+        ++jg;
+      }
+      if (!ok) break;
+      if (j == 0) continue;
+      // O_X / l once the item's last P.V_X is done; then O_X may be overwritten by the next item
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (jg - 1) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const int lim = cur.full() ? kBlk
-                                 : (!active ? 0 : !cur.own ? cur.sp_n - cur.b0
-                                                           : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0));
-      // pass 1: the row max of the block, 32 scores at a time (scores past the row's visible keys read as -inf)
-      const bool masked = __any_sync(~0u, lim < kBlk);
-      float mx = -INFINITY;
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst = p.out + ((size_t)row * p.hq + h0 + x) * kD;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(sbuf + 32 * c, r);
+        uint32_t o[32];
+        tc::tmem_ld32(obuf + c * 32, o);
         tc::tmem_wait_ld();
-        if (masked) {
+        if (active) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 32 * c + i < lim ? r[i] : 0xFF800000u;
-        }
-        float m2[2] = {mx, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        mx = fmaxf(m2[0], m2[1]);
-      }
-      const float m_new = fmaxf(m_used, mx * sl2);
-      float factor = 1.f;
-      const bool rescale = m_new > m_used + 8.f;
-      if (rescale) {
-        factor = exp2f(m_used - m_new);
-        m_used = m_new;
-      }
-      const float mref = m_used == -INFINITY ? 0.f : m_used;
-      // pass 2, 32 keys at a time: P = 2^(s log2e scale - m) over S in place; pairs of keys in fp32x2
-      const uint64_t sc2 = tc::f2_pack(sl2, sl2), mm2 = tc::f2_pack(-mref, -mref);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int g4 = 0; g4 < 4; ++g4) {  // keys 32 g4 .. +31: P words in the same 32 columns (16 high, 16 low)
-        uint32_t r[32], hi[16], lo[16];
-        tc::tmem_ld32(sbuf + 32 * g4, r);
-        tc::tmem_wait_ld();
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 32 * g4 + i < lim ? r[i] : 0xFF800000u;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float ya, yb;
-          tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
-          const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
-          const uint64_t ab = tc::f2_pack(a, b);
-          acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
-          hi[i] = tc::pack_bf16x2_trunc(a, b);
-          float da, db;
-          tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
-          lo[i] = tc::pack_bf16x2(da, db);
-        }
-        tc::tmem_st16(sbuf + 32 * g4, hi);
-        tc::tmem_st16(sbuf + 32 * g4 + 16, lo);
-      }
-      float rp[8];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) tc::f2_unpack(acc2[a], rp[2 * a], rp[2 * a + 1]);
-      const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
-      l = l * factor + rs;
-      // O_X after P.V_X(j-1) (already complete: S_X(j) was issued after it), rescaled to the new max; rows of
-      // the warp that keep their max multiply by factor = 1, which is exact
-      if (j >= 1 && __any_sync(~0u, rescale)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld32(obuf + c * 32, o);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-          tc::tmem_st32(obuf + c * 32, o);
-        }
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      tc::mbar_arrive(&bar_pf[x]);
-      ++j;
-    }
-    if (ok && j >= 1) {
-      // O_X / l once the last P.V_X is done
-      if (__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (j - 1) & 1, kWaitCycles))) {
-        tc::fence_after_sync();
-        const float inv = 1.f / l;
-        __nv_bfloat16* dst = p.out + ((size_t)row * p.hq + h0 + x) * kD;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld32(obuf + c * 32, o);
-          tc::tmem_wait_ld();
-          if (active) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
-              v.y = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
-              v.z = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
-              v.w = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
-            }
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
+            v.y = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
+            v.z = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
+            v.w = tc::pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
           }
         }
-      } else {
-        ok = false;
       }
     }
     if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
@@ -917,8 +967,16 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
     configured = true;
   }
   Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status};
-  if ((hq / hkv) % 2 == 0) {  // two query heads that share a KV head per CTA
-    fork_attn_tc2_kernel<<<dim3(caps->max_tiles * (hq / 2)), kThreads, pair::kSmemBytes + 1024, st>>>(
+  if ((hq / hkv) % 2 == 0) {  // two query heads that share a KV head per CTA, one persistent CTA per SM
+    static int n_sm = 0;
+    if (n_sm == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                    cudaSuccess || n_sm <= 0)
+        return hs::fail(HS_ECUDA, "fork_attn_tc: cannot read the SM count");
+    }
+    const int items = caps->max_tiles * (hq / 2);
+    fork_attn_tc2_kernel<<<dim3(items < n_sm ? items : n_sm), kThreads, pair::kSmemBytes + 1024, st>>>(
         m_q, m_k16, m_k128, m_v16, m_v128, prm);
   } else {
     fork_attn_tc_kernel<<<dim3(caps->max_tiles * hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
