@@ -70,7 +70,6 @@ constexpr int kSoftWarps = 8, kWarpProd = 8, kWarpMma = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmO = 256;               // O_0 at 256, O_1 at 384
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
-constexpr int HS_DEV_TIMEOUT = 4;
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, 128, 0, 0);  // A = Q (K-major), B = K (K-major)
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, 0, 1);  // A = P (K-major), B = V (N-major)
@@ -269,17 +268,23 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t sq = tc::smem_u32(smem + kOffQ);
-      bool ok = tc::mbar_wait(&bar_q, 0, kWaitCycles);
-      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+    // (the whole warp, converged: waits are voted, one elected lane issues)
+    {
+      // stage-base descriptors built once; a K or key step adds a constant to the start-address field
+      const uint32_t s0 = tc::smem_u32(smem);
+      const uint64_t dq = tc::sdesc_sw128(s0 + kOffQ, 16, 1024);
+      const uint64_t dk0 = tc::sdesc_sw128(s0 + kOffK, 16, 1024);
+      const uint64_t dv0 = tc::sdesc_sw128(s0 + kOffV, kSlab, 1024);
+      bool ok = __all_sync(~0u, tc::mbar_wait(&bar_q, 0, kWaitCycles));
+      if (!ok && lane == 0) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
       auto pv = [&](int i) -> bool {
         const int si = i % kStages;
-        if (!tc::mbar_wait(&bar_pf[i & 1], (i >> 1) & 1, kWaitCycles) ||
-            !tc::mbar_wait(&bar_vf[si], (i / kStages) & 1, kWaitCycles))
+        // (polling waits: a suspended MMA thread would notice the softmax late)
+        if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_pf[i & 1], (i >> 1) & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait_spin(&bar_vf[si], (i / kStages) & 1, kWaitCycles)))
           return false;
         tc::fence_after_sync();
-        const uint32_t sv = tc::smem_u32(smem + kOffV + si * kTile);
+        const uint64_t b0 = dv0 + (uint64_t)(si * (kTile >> 4));
         const uint32_t pt = tmem + (uint32_t)(i & 1) * 128;  // P_i sits where S_i was
 #pragma unroll
         for (int c = 0; c < 2; ++c) {        // key half c -> accumulator O_c
@@ -287,20 +292,20 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           for (int part = 0; part < 2; ++part) {  // P high part, then low part
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t b = tc::sdesc_sw128(sv + c * 8192 + k * 2048, kSlab, 1024);
-              tc::mma_bf16_ts(tmem + kTmO + 128 * c, pt + 64 * c + 32 * part + 8 * k, b, kIdescPV,
+              tc::mma_bf16_ts_w(tmem + kTmO + 128 * c, pt + 64 * c + 32 * part + 8 * k,
+                              b0 + (uint64_t)((c * 8192 + k * 2048) >> 4), kIdescPV,
                               (i > 0 || part > 0 || k > 0) ? 1u : 0u);
             }
           }
         }
-        tc::mma_commit(&bar_pv[i & 1]);
-        tc::mma_commit(&bar_ve[si]);
+        tc::mma_commit_w(&bar_pv[i & 1]);
+        tc::mma_commit_w(&bar_ve[si]);
         return true;
       };
       int j = 0;
       while (ok && cur.next()) {
         const int s = j % kStages;
-        if (!tc::mbar_wait(&bar_kf[s], (j / kStages) & 1, kWaitCycles)) {
+        if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_kf[s], (j / kStages) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
@@ -309,15 +314,14 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           ok = false;
           break;
         }
-        const uint32_t sk = tc::smem_u32(smem + kOffK + s * kTile);
+        const uint64_t b0 = dk0 + (uint64_t)(s * (kTile >> 4));
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = tc::sdesc_sw128(sq + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-          const uint64_t b = tc::sdesc_sw128(sk + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + (uint32_t)(j & 1) * 128, a, b, kIdescQK, k > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((k >> 2) * kSlab + (k & 3) * 32) >> 4);
+          tc::mma_bf16_ss_w(tmem + (uint32_t)(j & 1) * 128, dq + off, b0 + off, kIdescQK, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&bar_ke[s]);
-        tc::mma_commit(&bar_sf[j & 1]);
+        tc::mma_commit_w(&bar_ke[s]);
+        tc::mma_commit_w(&bar_sf[j & 1]);
         if (j >= 1 && !pv(j - 1)) {
           ok = false;
           break;
@@ -325,9 +329,9 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         ++j;
       }
       if (ok && j >= 1 && !pv(j - 1)) ok = false;
-      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      if (!ok && lane == 0) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
       // every MMA issued by this thread completes before O is read and TMEM is freed
-      tc::mma_commit(&bar_done);
+      tc::mma_commit_w(&bar_done);
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
     }
     __syncwarp();
@@ -517,16 +521,18 @@ constexpr int kOffQ = 0;                  // Q_A, Q_B: 32 KB each
 constexpr int kOffK = 2 * kTile;          // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
 constexpr int kSmemBytes = kOffV + 2 * kTile;  // 192 KB
-constexpr uint32_t kTmS = 0, kTmO = 256;  // S_X at 128 X, O_X at 256 + 128 X
+constexpr uint32_t kTmS = 0, kTmO = 256;  // S_X[h] at 128 X + 64 h, O_X at 256 + 128 X
+constexpr uint32_t kIdescQK = tc::idesc_bf16(128, 64, 0, 0);  // S of 64 keys: A = Q, B = K (K-major)
+constexpr int kWarpMmaB = 10, kThreads = 352;  // warp 9: MMAs of head A, warp 10: of head B
 }  // namespace pair
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(pair::kThreads, 1)
 fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
                      const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                      const __grid_constant__ CUtensorMap tm_v128, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qe, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2];
-  __shared__ uint64_t bar_sf[2], bar_pf[2], bar_pv[2], bar_done;
+  __shared__ uint64_t bar_sf[2][2], bar_pf[2][2], bar_pv[2], bar_done;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -546,17 +552,19 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   if (threadIdx.x == 0) {
     abort_flag = 0;
     tc::mbar_init(&bar_q, 1);
-    tc::mbar_init(&bar_qe, 1);
+    tc::mbar_init(&bar_qe, 2);  // both MMA warps
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&bar_kf[s], 1);
       tc::mbar_init(&bar_vf[s], 1);
-      tc::mbar_init(&bar_ke[s], 1);
-      tc::mbar_init(&bar_ve[s], 1);
-      tc::mbar_init(&bar_sf[s], 1);   // [X]: S_X done
-      tc::mbar_init(&bar_pf[s], 128); // [X]: P_X written
-      tc::mbar_init(&bar_pv[s], 1);   // [X]: P.V_X done
+      tc::mbar_init(&bar_ke[s], 2);  // both MMA warps
+      tc::mbar_init(&bar_ve[s], 2);
+      for (int h = 0; h < 2; ++h) {
+        tc::mbar_init(&bar_sf[s][h], 1);    // [X][h]: S_X of a block's key half h done
+        tc::mbar_init(&bar_pf[s][h], 128);  // [X][h]: P_X of key half h written
+      }
+      tc::mbar_init(&bar_pv[s], 1);   // [X]: P.V_X of a key half done
     }
-    tc::mbar_init(&bar_done, 1);
+    tc::mbar_init(&bar_done, 2);
     tc::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -667,38 +675,50 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         tc::mbar_wait(&bar_vf[i & 1], (i >> 1) & 1, kWaitCycles);
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || warp == pair::kWarpMmaB) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
+    // One warp per head (head A: warp 9, head B: warp 10, on different SM sub-partitions), each converged:
+    // waits are voted and one elected lane issues.  The two streams share the tensor pipe, so one warp's
+    // bookkeeping between MMA groups is covered by the other's products.
+    const int x = warp == kWarpMma ? 0 : 1;
+    // (the whole warp, converged: waits are voted, one elected lane issues)
+    {
       bool ok = true;
       int jg = 0, kq = 0;  // blocks issued over all items, non-empty items
-      auto s_mma = [&](int x, int jj) {  // S_X(jj) = Q_X K_jj^T
-        const uint32_t sq = tc::smem_u32(smem + pair::kOffQ + x * kTile);
-        const uint32_t sk = tc::smem_u32(smem + pair::kOffK + (jj & 1) * kTile);
+      // Descriptors of the stage bases, built once; a K step or a 16-key step adds a constant to the
+      // start-address field (addresses below 256 KB: no carry out of the field).  Every operand of an
+      // MMA is then one add away, so MMAs issue at the tensor pipe's rate.
+      const uint32_t s0 = tc::smem_u32(smem);
+      const uint64_t dq0 = tc::sdesc_sw128(s0 + pair::kOffQ, 16, 1024);
+      const uint64_t dk0 = tc::sdesc_sw128(s0 + pair::kOffK, 16, 1024);
+      const uint64_t dv0 = tc::sdesc_sw128(s0 + pair::kOffV, kSlab, 1024);
+      auto s_mma = [&](int x, int jj, int h) {  // S_X(jj, h) = Q_X K_jj[64h .. 64h+63]^T into S_X[h]
+        const uint64_t a0 = dq0 + (uint64_t)(x * (kTile >> 4));
+        const uint64_t b0 = dk0 + (uint64_t)(((jj & 1) * kTile + h * 8192) >> 4);
+        const uint32_t d = tmem + pair::kTmS + 128 * x + 64 * h;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = tc::sdesc_sw128(sq + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-          const uint64_t b = tc::sdesc_sw128(sk + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + pair::kTmS + 128 * x, a, b, kIdescQK, k > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((k >> 2) * kSlab + (k & 3) * 32) >> 4);
+          tc::mma_bf16_ss_w(d, a0 + off, b0 + off, pair::kIdescQK, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&bar_sf[x]);
+        tc::mma_commit_w(&bar_sf[x][h]);
       };
-      auto pv_mma = [&](int x, int jj, bool first) {  // O_X += P_X(jj) V_jj, per 32 keys: high, then low parts
-        const uint32_t sv = tc::smem_u32(smem + pair::kOffV + (jj & 1) * kTile);
-        const uint32_t pt = tmem + pair::kTmS + 128 * x;
+      // O_X += P_X(jj, h) V_jj[64h .. 64h+63], per 32 keys: high, then low parts
+      auto pv_mma = [&](int x, int jj, int h, bool first) {
+        const uint64_t b0 = dv0 + (uint64_t)(((jj & 1) * kTile + h * 8192) >> 4);
+        const uint32_t pt = tmem + pair::kTmS + 128 * x + 64 * h, d = tmem + pair::kTmO + 128 * x;
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
+        for (int g = 0; g < 2; ++g) {
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {  // keys 32 g4 + 16 k .. +15
-              const uint64_t b = tc::sdesc_sw128(sv + g4 * 4096 + k * 2048, kSlab, 1024);
-              tc::mma_bf16_ts(tmem + pair::kTmO + 128 * x, pt + 32 * g4 + 16 * part + 8 * k, b, kIdescPV,
-                              (!first || g4 > 0 || part > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 2; ++k) {  // keys 64 h + 32 g + 16 k .. +15
+              tc::mma_bf16_ts_w(d, pt + 32 * g + 16 * part + 8 * k, b0 + (uint64_t)((g * 4096 + k * 2048) >> 4),
+                              kIdescPV, (!first || g > 0 || part > 0 || k > 0) ? 1u : 0u);
             }
           }
         }
-        tc::mma_commit(&bar_pv[x]);
+        tc::mma_commit_w(&bar_pv[x]);
       };
       for (int k = 0; ok; ++k) {
         const int w = item_of(k);
@@ -708,54 +728,55 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         int n_blk = 0;
         while (cur.next()) ++n_blk;  // counted once: the loop needs no cursor
         if (n_blk == 0) continue;
-        if (!tc::mbar_wait(&bar_q, kq & 1, kWaitCycles) ||
-            !tc::mbar_wait_spin(&bar_kf[jg & 1], (jg >> 1) & 1, kWaitCycles)) {
+        const int nh = 2 * n_blk;  // key halves of the item
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_q, kq & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait_spin(&bar_kf[jg & 1], (jg >> 1) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        // S of the item's first block: the S buffers hold the previous item's last P, whose P.V is issued
-        s_mma(0, jg);
-        s_mma(1, jg);
-        tc::mma_commit(&bar_ke[jg & 1]);
-        if (n_blk == 1) tc::mma_commit(&bar_qe);
-        for (int j = 0; ok && j < n_blk; ++j, ++jg) {
-          const bool more = j + 1 < n_blk;
-          for (int x = 0; x < 2 && ok; ++x) {
+        // S of the item's first block, both halves: the buffers hold the previous item's last P, whose P.V is issued
+        s_mma(x, jg, 0);
+        s_mma(x, jg, 1);
+        tc::mma_commit_w(&bar_ke[jg & 1]);
+        if (n_blk == 1) tc::mma_commit_w(&bar_qe);
+        for (int v = 0; ok && v < nh; ++v) {
+          const int h = v & 1, jb = jg + (v >> 1);  // key half v: half h of block jb
+          const int v2 = v + 2, jb2 = jg + (v2 >> 1);  // the half whose S goes into buffer h next
+          {
             // (polling waits: a suspended MMA thread would notice the softmax late)
-            // (P_X of an item's first block is written after the previous item's O_X was read out, so
-            // the P.V that starts O_X afresh waits for nothing more)
-            if (!tc::mbar_wait_spin(&bar_pf[x], jg & 1, kWaitCycles) ||
-                (x == 0 && !tc::mbar_wait_spin(&bar_vf[jg & 1], (jg >> 1) & 1, kWaitCycles))) {
+            if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_pf[x][h], jb & 1, kWaitCycles)) ||
+                (h == 0 && !__all_sync(~0u, tc::mbar_wait_spin(&bar_vf[jb & 1], (jb >> 1) & 1, kWaitCycles)))) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
-            if (*(volatile int*)&abort_flag) {
-              ok = false;
-              break;
-            }
-            pv_mma(x, jg, j == 0);
-            if (x == 1) tc::mma_commit(&bar_ve[jg & 1]);
-            if (more) {
-              if (x == 0 && !tc::mbar_wait_spin(&bar_kf[(jg + 1) & 1], ((jg + 1) >> 1) & 1, kWaitCycles)) {
+            pv_mma(x, jb, h, v == 0);  // (the item's first P.V_X starts O_X afresh)
+            if (h == 1) tc::mma_commit_w(&bar_ve[jb & 1]);
+            if (v2 < nh) {
+              if (h == 0 && !__all_sync(~0u, tc::mbar_wait_spin(&bar_kf[jb2 & 1], (jb2 >> 1) & 1, kWaitCycles))) {
                 ok = false;
                 break;
               }
               tc::fence_after_sync();
-              s_mma(x, jg + 1);
-              if (x == 1) {
-                tc::mma_commit(&bar_ke[(jg + 1) & 1]);
-                if (j + 2 == n_blk) tc::mma_commit(&bar_qe);  // the item's last S products are issued
+              s_mma(x, jb2, h);  // S_X[h] is overwritten after the P.V_X that reads it (issue order)
+              if (h == 1) {
+                tc::mma_commit_w(&bar_ke[jb2 & 1]);
+                if (v2 == nh - 1) tc::mma_commit_w(&bar_qe);  // the item's last S products are issued
               }
+            }
+            if (*(volatile int*)&abort_flag) {  // (checked after the issue: off the P -> P.V path)
+              ok = false;
+              break;
             }
           }
         }
+        jg += n_blk;
         ++kq;
       }
-      if (!ok) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
-      // every MMA issued by this thread completes before O is read and TMEM is freed
-      tc::mma_commit(&bar_done);
+      if (!ok && lane == 0) record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+      // every MMA issued by the elected lane completes before O is read and TMEM is freed
+      tc::mma_commit_w(&bar_done);
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
     }
     __syncwarp();
@@ -783,98 +804,122 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         my_idx = M.tok(row)[T_IDX];
       }
       float m_used = -INFINITY, l = 0.f;
-      int j = 0;
-      while (cur.next()) {
-        // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[x], jg & 1, kWaitCycles))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
+      int j = 0, n_blk = 0;
+      {
+        Cursor c2 = cur;
+        while (c2.next()) ++n_blk;
+      }
+      while (ok && cur.next()) {
         const int lim = cur.full() ? kBlk
                                    : (!active ? 0 : !cur.own ? cur.sp_n - cur.b0
                                                              : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0));
-        // pass 1: the row max of the block, 32 scores at a time (scores past the row's visible keys read as -inf)
-        const bool masked = __any_sync(~0u, lim < kBlk);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(sbuf + 32 * c, r);
-          tc::tmem_wait_ld();
-          if (masked) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 32 * c + i < lim ? r[i] : 0xFF800000u;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {  // key half h of the block: S_X[h]
+          const int u = 2 * jg + h;    // key halves over all items (phases of bar_pv[x])
+          const uint32_t sb = sbuf + 64 * h;
+          const int lh = lim - 64 * h;  // this row's visible keys in the half
+          // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
+          if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[x][h], jg & 1, kWaitCycles))) {
+            ok = false;
+            break;
           }
-          float m2[2] = {mx, -INFINITY};
+          tc::fence_after_sync();
+          // pass 1: the row max of the half, 32 scores at a time (scores past the row's visible keys read as -inf)
+          const bool masked = __any_sync(~0u, lh < 64);
+          float mx = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          mx = fmaxf(m2[0], m2[1]);
-        }
-        const float m_new = fmaxf(m_used, mx * sl2);
-        float factor = 1.f;
-        const bool rescale = m_new > m_used + 8.f;
-        if (rescale) {
-          factor = exp2f(m_used - m_new);
-          m_used = m_new;
-        }
-        const float mref = m_used == -INFINITY ? 0.f : m_used;
-        // pass 2, 32 keys at a time: P = 2^(s log2e scale - m) over S in place; pairs of keys in fp32x2
-        const uint64_t sc2 = tc::f2_pack(sl2, sl2), mm2 = tc::f2_pack(-mref, -mref);
-        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {  // keys 32 g4 .. +31: P words in the same 32 columns (16 high, 16 low)
-          uint32_t r[32], hi[16], lo[16];
-          tc::tmem_ld32(sbuf + 32 * g4, r);
-          tc::tmem_wait_ld();
-          if (masked) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 32 * g4 + i < lim ? r[i] : 0xFF800000u;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float ya, yb;
-            tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
-            const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
-            const uint64_t ab = tc::f2_pack(a, b);
-            acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
-            hi[i] = tc::pack_bf16x2_trunc(a, b);
-            float da, db;
-            tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
-            lo[i] = tc::pack_bf16x2(da, db);
-          }
-          tc::tmem_st16(sbuf + 32 * g4, hi);
-          tc::tmem_st16(sbuf + 32 * g4 + 16, lo);
-        }
-        float rp[8];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) tc::f2_unpack(acc2[a], rp[2 * a], rp[2 * a + 1]);
-        const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
-        l = l * factor + rs;
-        // O_X after P.V_X of the previous block (already complete: this S_X was issued after it), rescaled; rows
-        // of the warp that keep their max multiply by factor = 1, which is exact.  An item's first block never
-        // rescales (its P.V starts O_X afresh).
-        if (j >= 1 && __any_sync(~0u, rescale)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(obuf + c * 32, o);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            tc::tmem_ld32(sb + 32 * c, r);
             tc::tmem_wait_ld();
+            if (masked) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-            tc::tmem_st32(obuf + c * 32, o);
+              for (int i = 0; i < 32; ++i) r[i] = 32 * c + i < lh ? r[i] : 0xFF800000u;
+            }
+            float m2[2] = {mx, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            mx = fmaxf(m2[0], m2[1]);
           }
+          const float m_new = fmaxf(m_used, mx * sl2);
+          float factor = 1.f;
+          const bool rescale = m_new > m_used + 8.f;
+          if (rescale) {
+            factor = exp2f(m_used - m_new);
+            m_used = m_new;
+          }
+          const float mref = m_used == -INFINITY ? 0.f : m_used;
+          // O_X rescaled before this half's P.V_X: it must first hold the previous half's P.V_X.  When this
+          // S_X was seen, every P.V_X up to half u - 2 was complete, so the parity of half u - 1 is unambiguous.
+          // Rows of the warp that keep their max multiply by factor = 1, which is exact.  The item's first half
+          // never rescales (its P.V starts O_X afresh).
+          if ((j > 0 || h > 0) && __any_sync(~0u, rescale)) {
+            if (!__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (u - 1) & 1, kWaitCycles))) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              tc::tmem_ld32(obuf + c * 32, o);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+              tc::tmem_st32(obuf + c * 32, o);
+            }
+          }
+          // pass 2, 32 keys at a time: P = 2^(s log2e scale - m) over S in place; pairs of keys in fp32x2
+          const uint64_t sc2 = tc::f2_pack(sl2, sl2), mm2 = tc::f2_pack(-mref, -mref);
+          uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {  // keys 64 h + 32 g .. +31: P words in the same 32 columns (16 high, 16 low)
+            uint32_t r[32], hi[16], lo[16];
+            tc::tmem_ld32(sb + 32 * g, r);
+            tc::tmem_wait_ld();
+            if (masked) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = 32 * g + i < lh ? r[i] : 0xFF800000u;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float ya, yb;
+              tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
+              const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
+              const uint64_t ab = tc::f2_pack(a, b);
+              acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
+              hi[i] = tc::pack_bf16x2_trunc(a, b);
+              float da, db;
+              tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
+              lo[i] = tc::pack_bf16x2(da, db);
+            }
+            tc::tmem_st16(sb + 32 * g, hi);
+            tc::tmem_st16(sb + 32 * g + 16, lo);
+          }
+          float rp[8];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) tc::f2_unpack(acc2[a], rp[2 * a], rp[2 * a + 1]);
+          const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+          l = l * factor + rs;
+          // Waits on bar_pv[x] are for half u - 1 and come before this half's P is released, so the barrier is
+          // never two phases past the one waited for.  The item's last half waits here for half u - 1, which
+          // leaves the epilogue one phase (its own) to wait for.
+          if (j == n_blk - 1 && h == 1 && !__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (u - 1) & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          tc::mbar_arrive(&bar_pf[x][h]);
         }
-        tc::tmem_wait_st();
-        tc::fence_before_sync();
-        tc::mbar_arrive(&bar_pf[x]);
         ++j;
         ++jg;
       }
       if (!ok) break;
       if (j == 0) continue;
-      // O_X / l once the item's last P.V_X is done; then O_X may be overwritten by the next item
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (jg - 1) & 1, kWaitCycles))) {
+      // O_X / l once the item's last P.V_X is done (the one before it was waited for); then O_X may be
+      // overwritten by the next item
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_pv[x], (2 * jg - 1) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
@@ -976,7 +1021,7 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
         return hs::fail(HS_ECUDA, "fork_attn_tc: cannot read the SM count");
     }
     const int items = caps->max_tiles * (hq / 2);
-    fork_attn_tc2_kernel<<<dim3(items < n_sm ? items : n_sm), kThreads, pair::kSmemBytes + 1024, st>>>(
+    fork_attn_tc2_kernel<<<dim3(items < n_sm ? items : n_sm), pair::kThreads, pair::kSmemBytes + 1024, st>>>(
         m_q, m_k16, m_k128, m_v16, m_v128, prm);
   } else {
     fork_attn_tc_kernel<<<dim3(caps->max_tiles * hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,

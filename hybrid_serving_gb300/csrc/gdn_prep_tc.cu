@@ -49,7 +49,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kThreads = 160;
 constexpr long long kWaitCycles = 4000000000LL;
-constexpr int HS_DEV_TIMEOUT = 4;
 // shared memory (from a 1024-aligned base).  Q, K, V: two [128][64] slabs each
 // (slab = 64 columns of d; rows 0..63 head a, 64..127 head b).
 constexpr int kOffQ = 0, kOffK = 32768, kOffV = 65536;

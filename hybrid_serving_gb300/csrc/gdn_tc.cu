@@ -52,7 +52,6 @@ constexpr int kD = 128;
 constexpr int kThreads = 352;
 constexpr int kWarpProd = 8, kWarpMma = 9, kWarpOmma = 10;
 constexpr long long kWaitCycles = 4000000000LL;
-constexpr int HS_DEV_TIMEOUT = 4;
 // one stage of chunk inputs (offsets from the stage base)
 constexpr int kStW = 0, kStQ = 16384, kStK = 32768, kStP = 49152, kStUt = 57344, kStG = 73728;
 constexpr int kStageBytes = 74752;  // 73728 + the 1 KB decay block

@@ -30,7 +30,6 @@ constexpr int kStageB = BN * BK * 2;  // 16 KB
 constexpr int kSmem = kStages * (kStageA + kStageB);
 constexpr int kThreads = 192;
 constexpr long long kWaitCycles = 4000000000LL;
-constexpr int HS_DEV_TIMEOUT = 4;
 constexpr uint32_t kIdesc = tc::idesc_bf16(BM, BN, 0, 0);
 
 struct GemmParams {

@@ -58,6 +58,7 @@ extern "C" hs_status hs_check_status(const int32_t* w) {
                   *w == HS_DEV_BAD_PAGE   ? "page id out of range"
                   : *w == HS_DEV_BAD_SLOT ? "state slot out of range"
                   : *w == HS_DEV_BAD_META ? "inconsistent metadata"
+                  : *w == HS_DEV_TIMEOUT  ? "a bounded wait in a kernel ran out"
                                           : "unknown");
 }
 

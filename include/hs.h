@@ -59,6 +59,7 @@ typedef enum { HS_F32 = 0, HS_BF16 = 1 } hs_dtype;
 #define HS_DEV_BAD_PAGE 1     /* a page id outside [0, n_pages) */
 #define HS_DEV_BAD_SLOT 2     /* a state slot outside [0, n_slots) */
 #define HS_DEV_BAD_META 3     /* counts above capacity or inconsistent records */
+#define HS_DEV_TIMEOUT 4      /* a bounded wait inside a kernel ran out (the call's outputs are invalid) */
 
 /* ------------------------------------------------------------------------ */
 /* Fixed capacities of a round.  They size the device metadata buffer and   */

@@ -311,3 +311,13 @@ def test_device_calls_fail_without_gpu():
     buf = (ctypes.c_float * 64)()
     st = _lib.lib.hs_gdn_state_checkpoint(ctypes.cast(buf, ctypes.c_void_p), 2, 0, 1, 1, 4, 4, None)
     assert st == _lib.HS_ECUDA
+
+
+def test_device_status_codes_map_to_edevice():
+    """Every nonzero status word is HS_EDEVICE with a message naming the
+    code; zero is HS_OK."""
+    import ctypes as C
+    assert _lib.lib.hs_check_status(C.byref(C.c_int32(0))) == _lib.HS_OK
+    for code, words in [(1, "page"), (2, "slot"), (3, "metadata"), (4, "wait"), (99, "unknown")]:
+        assert _lib.lib.hs_check_status(C.byref(C.c_int32(code))) == _lib.HS_EDEVICE
+        assert words in _lib.last_error(), (code, _lib.last_error())
