@@ -131,6 +131,8 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
 
   if (warp == 4) {
     // ------------------------------------------------------- copies and MMAs
+    // (copies from lane 0; the MMAs from the converged warp: voted waits, one elected lane issues, descriptors
+    // built once with a K step added to the start-address field)
     if (lane == 0) {
       tc::mbar_expect_tx(&bar_in, kInTx);
       for (int i = 0; i < 2; ++i) {
@@ -142,43 +144,43 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
           tc::tma_load_3d(smem + kOffV + o, &tm_v, half * 64, hh, row0, &bar_in);
         }
       }
-      bool ok = tc::mbar_wait(&bar_in, 0, kWaitCycles);
-      if (ok) {
-        tc::fence_after_sync();
-        const uint32_t sq = tc::smem_u32(smem + kOffQ), sk = tc::smem_u32(smem + kOffK);
+    }
+    __syncwarp();
+    bool ok = __all_sync(~0u, tc::mbar_wait(&bar_in, 0, kWaitCycles));
+    if (ok) {
+      tc::fence_after_sync();
+      const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(smem + kOffQ), 16, 1024);
+      const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(smem + kOffK), 16, 1024);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // K K^T, Q K^T over d (16 per step)
-          const uint64_t bk = tc::sdesc_sw128(sk + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          const uint64_t aq = tc::sdesc_sw128(sq + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + kTKK, bk, bk, kIdescSq, k > 0 ? 1u : 0u);
-          tc::mma_bf16_ss(tmem + kTQK, aq, bk, kIdescSq, k > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(&bar_d);
+      for (int k = 0; k < 8; ++k) {  // K K^T, Q K^T over d (16 per step)
+        const uint64_t off = (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+        tc::mma_bf16_ss_w(tmem + kTKK, dk + off, dk + off, kIdescSq, k > 0 ? 1u : 0u);
+        tc::mma_bf16_ss_w(tmem + kTQK, dq + off, dk + off, kIdescSq, k > 0 ? 1u : 0u);
       }
-      // W^T, then Ut^T, each from its T operand in the Q buffer
-      for (int pass = 0; pass < 2 && ok; ++pass) {
-        ok = tc::mbar_wait(pass == 0 ? &bar_b1 : &bar_b2, 0, kWaitCycles);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const int src = pass == 0 ? kOffK : kOffV;
+      tc::mma_commit_w(&bar_d);
+    }
+    // W^T, then Ut^T, each from its T operand in the Q buffer
+    for (int pass = 0; pass < 2 && ok; ++pass) {
+      ok = __all_sync(~0u, tc::mbar_wait(pass == 0 ? &bar_b1 : &bar_b2, 0, kWaitCycles));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const int src = pass == 0 ? kOffK : kOffV;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t a0 = tc::smem_u32(smem + src + i * 8192);
-          const uint32_t bb = tc::smem_u32(smem + kOffT + i * 16384);
+      for (int i = 0; i < 2; ++i) {
+        const uint64_t da = tc::sdesc_sw128(tc::smem_u32(smem + src + i * 8192), 16384, 1024);
+        const uint64_t db = tc::sdesc_sw128(tc::smem_u32(smem + kOffT + i * 16384), 8192, 1024);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
+        for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {  // over the chunk's tokens s, 16 per step
-              const uint64_t a = tc::sdesc_sw128(a0 + k * 2048, 16384, 1024);
-              const uint64_t b = tc::sdesc_sw128(bb + part * 8192 + k * 2048, 8192, 1024);
-              tc::mma_bf16_ss(tmem + (pass == 0 ? kTW : kTU) + 64 * i, a, b, kIdescWU, (part > 0 || k > 0) ? 1u : 0u);
-            }
+          for (int k = 0; k < 4; ++k) {  // over the chunk's tokens s, 16 per step
+            tc::mma_bf16_ss_w(tmem + (pass == 0 ? kTW : kTU) + 64 * i, da + (uint64_t)((k * 2048) >> 4),
+                              db + (uint64_t)((part * 8192 + k * 2048) >> 4), kIdescWU, (part > 0 || k > 0) ? 1u : 0u);
           }
         }
-        tc::mma_commit(pass == 0 ? &bar_w1 : &bar_w2);
       }
-      if (!ok) hsd::set_status(p.status, HS_DEV_TIMEOUT);
+      tc::mma_commit_w(pass == 0 ? &bar_w1 : &bar_w2);
     }
+    if (!ok && lane == 0) hsd::set_status(p.status, HS_DEV_TIMEOUT);
     __syncwarp();
   } else {
     // -------------------------------------------------------------- rows

@@ -216,101 +216,107 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA: the state chain
-    if (lane == 0) {
+    // (the whole warp, converged: waits are voted and one elected lane issues; descriptors are built once
+    // per stage and a K step adds a constant to the start-address field)
+    {
       bool ok = true;
       // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi into the fp32 state columns
       for (int q = 1; q <= n_comb && ok; ++q) {
-        if (!tc::mbar_wait(&bar_pm, (q - 1) & 1, kWaitCycles) || !tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles)) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_pm, (q - 1) & 1, kWaitCycles)) || !__all_sync(~0u, tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const uint32_t sm = tc::smem_u32(smem);
+        const uint64_t dm0 = tc::sdesc_sw128(sm, 16384, 1024), dm1 = tc::sdesc_sw128(sm + 32768, 16384, 1024);
 #pragma unroll
         for (int pr = 0; pr < 3; ++pr) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint64_t b = tc::sdesc_sw128(sm + (pr == 1 ? 32768 : 0) + k * 2048, 16384, 1024);
-            tc::mma_bf16_ts(tmem + kTS32, tmem + (pr == 2 ? kTSlo : kTS16) + 8 * k, b, kIdesc128mn,
-                            (pr > 0 || k > 0) ? 1u : 0u);
+            tc::mma_bf16_ts_w(tmem + kTS32, tmem + (pr == 2 ? kTSlo : kTS16) + 8 * k,
+                              (pr == 1 ? dm1 : dm0) + (uint64_t)((k * 2048) >> 4), kIdesc128mn,
+                              (pr > 0 || k > 0) ? 1u : 0u);
           }
         }
-        tc::mma_commit(&bar_pd);
+        tc::mma_commit_w(&bar_pd);
       }
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
-        if (!tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles) ||
-            !tc::mbar_wait_spin(&bar_s, ci & 1, kWaitCycles)) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait_spin(&bar_s, ci & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
+        const uint64_t dw = tc::sdesc_sw128(sb + kStW, 16384, 1024);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
-          const uint64_t bw = tc::sdesc_sw128(sb + kStW + k * 2048, 16384, 1024);
-          tc::mma_bf16_ts(tmem + kTD1, tmem + kTS16 + 8 * k, bw, kIdesc64mn, k > 0 ? 1u : 0u);
+          tc::mma_bf16_ts_w(tmem + kTD1, tmem + kTS16 + 8 * k, dw + (uint64_t)((k * 2048) >> 4), kIdesc64mn,
+                            k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&bar_d1);
-        if (!tc::mbar_wait_spin(&bar_u, ci & 1, kWaitCycles)) {
+        tc::mma_commit_w(&bar_d1);
+        if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_u, ci & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
+        const uint64_t dk = tc::sdesc_sw128(sb + kStK, 8192, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // S += U K'   (K = tokens; S already scaled by e^{gC})
-          const uint64_t bk = tc::sdesc_sw128(sb + kStK + k * 2048, 8192, 1024);
-          tc::mma_bf16_ts(tmem + kTS32, tmem + kTU + 8 * k, bk, kIdesc128mn, 1u);
+          tc::mma_bf16_ts_w(tmem + kTS32, tmem + kTU + 8 * k, dk + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
         }
-        tc::mma_commit(&bar_d4);
-        tc::mma_commit(&bar_empty[s]);
+        tc::mma_commit_w(&bar_d4);
+        tc::mma_commit_w(&bar_empty[s]);
         if (*(volatile int*)&abort_flag) ok = false;
       }
-      if (!ok) fail();
-      tc::mma_commit(&bar_done);
+      if (!ok && lane == 0) fail();
+      tc::mma_commit_w(&bar_done);
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
     }
     __syncwarp();
   } else if (warp == kWarpOmma) {
     // -------------------------------------------------- MMA: the outputs
-    if (lane == 0) {
+    // (converged warp, voted waits, one elected lane issues)
+    {
       bool ok = true;
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
-        if (!tc::mbar_wait(&bar_s, ci & 1, kWaitCycles) ||
-            !tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles) ||
-            (ci >= 1 && !tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles))) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_s, ci & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
+            (ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles)))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         if (outputs) {
+          const uint64_t dq = tc::sdesc_sw128(sb + kStQ, 16, 1024);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {  // D2 = S Q^T
-            const uint64_t bq = tc::sdesc_sw128(sb + kStQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-            tc::mma_bf16_ts(tmem + kTD2, tmem + kTS16 + 8 * k, bq, kIdesc64, k > 0 ? 1u : 0u);
+            tc::mma_bf16_ts_w(tmem + kTD2, tmem + kTS16 + 8 * k, dq + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
+                              kIdesc64, k > 0 ? 1u : 0u);
           }
         }
-        tc::mma_commit(&bar_d2);
-        if (!tc::mbar_wait(&bar_u, ci & 1, kWaitCycles)) {
+        tc::mma_commit_w(&bar_d2);
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_u, ci & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         if (outputs) {
+          const uint64_t dp = tc::sdesc_sw128(sb + kStP, 16, 1024);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // D3 = U P^T
-            const uint64_t bp = tc::sdesc_sw128(sb + kStP + k * 32, 16, 1024);
-            tc::mma_bf16_ts(tmem + kTD3, tmem + kTU + 8 * k, bp, kIdesc64, k > 0 ? 1u : 0u);
+            tc::mma_bf16_ts_w(tmem + kTD3, tmem + kTU + 8 * k, dp + (uint64_t)((k * 32) >> 4), kIdesc64, k > 0 ? 1u : 0u);
           }
         }
-        tc::mma_commit(&bar_d23);
-        tc::mma_commit(&bar_empty[s]);
+        tc::mma_commit_w(&bar_d23);
+        tc::mma_commit_w(&bar_empty[s]);
         if (*(volatile int*)&abort_flag) ok = false;
       }
-      if (!ok) fail();
-      tc::mma_commit(&bar_done2);
+      if (!ok && lane == 0) fail();
+      tc::mma_commit_w(&bar_done2);
       tc::mbar_wait(&bar_done2, 0, kWaitCycles);
     }
     __syncwarp();

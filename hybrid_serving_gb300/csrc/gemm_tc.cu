@@ -92,27 +92,27 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         tc::mbar_wait(&bar_full[kb % kStages], (kb / kStages) & 1, kWaitCycles);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // converged warp: voted waits, one elected lane issues; a K step adds a constant to the descriptors
+    {
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % kStages;
-        if (!tc::mbar_wait(&bar_full[s], (kb / kStages) & 1, kWaitCycles)) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (kb / kStages) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const uint32_t sa = tc::smem_u32(smem + s * (kStageA + kStageB));
-        const uint32_t sb = sa + kStageA;
+        const uint64_t da = tc::sdesc_sw128(sa, 16, 1024), db = tc::sdesc_sw128(sa + kStageA, 16, 1024);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t a = tc::sdesc_sw128(sa + k * 32, 16, 1024);
-          const uint64_t b = tc::sdesc_sw128(sb + k * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem, a, b, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+          const uint64_t off = (uint64_t)((k * 32) >> 4);
+          tc::mma_bf16_ss_w(tmem, da + off, db + off, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&bar_empty[s]);
+        tc::mma_commit_w(&bar_empty[s]);
       }
-      if (!ok) hsd::set_status(p.status, HS_DEV_TIMEOUT);
-      tc::mma_commit(&bar_acc);  // also drains every MMA before TMEM is freed
+      if (!ok && lane == 0) hsd::set_status(p.status, HS_DEV_TIMEOUT);
+      tc::mma_commit_w(&bar_acc);  // also drains every MMA before TMEM is freed
     }
     __syncwarp();
   } else {
