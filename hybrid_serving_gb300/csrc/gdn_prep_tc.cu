@@ -53,7 +53,7 @@ constexpr long long kWaitCycles = 4000000000LL;
 // (slab = 64 columns of d; rows 0..63 head a, 64..127 head b).
 constexpr int kOffQ = 0, kOffK = 32768, kOffV = 65536;
 constexpr int kSmem = 98304;
-constexpr int kOffA = kOffQ;  // A, fp32 [2][64][64], 16-byte chunks swizzled by row (after Q K^T)
+constexpr int kOffA = kOffQ;  // A^T, fp32 [2][64][64], 16-byte chunks swizzled by row (after Q K^T)
 constexpr int kOffT = kOffQ;  // per head: T hi, T lo, each [64 s][64 t] bf16 MN-major (after the solve)
 constexpr uint32_t kInTx = 3 * 32768;
 // tensor-memory columns (256): K K^T and Q K^T, then W^T and Ut^T over them
@@ -72,8 +72,10 @@ struct Prm {
   int32_t* status;
 };
 
-__device__ __forceinline__ int a_off(int t, int s) {  // byte offset of A[t][s] in one head's block
-  return t * 256 + ((((s >> 2) ^ (t & 15))) << 4) + (s & 3) * 4;
+// byte offset of A[u][s] in one head's block, stored transposed (row s holds column s of A: the
+// entries A[u][s], u = 0..63), its 16-byte chunks swizzled by s
+__device__ __forceinline__ int at_off(int s, int u) {
+  return s * 256 + ((((u >> 2) ^ (s & 15))) << 4) + (u & 3) * 4;
 }
 
 // Row j of T diag(scale) as the MN-major B operand of one head: high part at
@@ -231,11 +233,12 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
           for (int e = 0; e < 4; ++e) {
             const int s = half * 32 + c4 * 4 + e;
             const bool low = s <= t && t < len;
-            const float dec = low ? expf(gt - gsh[i][s]) : 0.f;
+            // e^{g_t - g_s} = 2^{(g_t - g_s) log2 e}, g_t <= g_s (hardware 2^x: relative error ~2^-22)
+            const float dec = low ? tc::ex2_approx((gt - gsh[i][s]) * 1.4426950408889634f) : 0.f;
             av[e] = (low && s < t) ? bt * dec * __uint_as_float(kk[c4 * 4 + e]) : 0.f;
             pv[e] = low ? dec * __uint_as_float(qk[c4 * 4 + e]) : 0.f;
+            *reinterpret_cast<float*>(Ai + at_off(s, t)) = av[e];  // A[t][s] into row s of A^T
           }
-          *reinterpret_cast<float4*>(Ai + a_off(t, half * 32 + c4 * 4)) = make_float4(av[0], av[1], av[2], av[3]);
           if (valid)  // four consecutive s: one half of a 16-byte chunk of P's swizzled row
             *reinterpret_cast<uint2*>(Pi + gdnws::sw128_off(t, half * 32 + c4 * 4, 64)) =
                 make_uint2(tc::pack_bf16x2(pv[0], pv[1]), tc::pack_bf16x2(pv[2], pv[3]));
@@ -243,24 +246,45 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       }
     }
     tc::named_sync(1, 128);
-    // column j = t of T = (I + A)^{-1} by forward substitution: x_u = [u == j] - sum_{s<u} A_us x_s
+    // column j = t of T = (I + A)^{-1} by forward substitution, x_u = [u == j] - sum_{s<u} A_us x_s, in the
+    // right-looking order: when x_s is final it is added into every later row at once (pairs of rows in
+    // fp32x2), so the updates of a step are independent and only x_{s+1} waits on x_s.  The sums run over s
+    // in increasing order, as in the plain recurrence.  A warp whose columns all lie at or past 32 starts
+    // at s = 32 (its x_s is zero before: T is lower triangular).
     float x[64];
     {
       const uint8_t* Ai = smem + kOffA + i * 16384;
+      uint64_t xp[32];  // x as pairs (x_{2k}, x_{2k+1}): partial sums until final
 #pragma unroll
-      for (int u = 0; u < 64; ++u) {
-        // four partial sums (s mod 4) so the products do not wait on one another, combined in a fixed order
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k = 0; k < 32; ++k) xp[k] = 0ull;
+      const int s_lo = (t & 32) ? 32 : 0;  // warp-uniform: columns 32..63 are one warp of the head
 #pragma unroll
-        for (int s = 0; s < u; s += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(Ai + a_off(u, s));
-          acc[0] = fmaf(a4.x, x[s], acc[0]);
-          if (s + 1 < u) acc[1] = fmaf(a4.y, x[s + 1], acc[1]);
-          if (s + 2 < u) acc[2] = fmaf(a4.z, x[s + 2], acc[2]);
-          if (s + 3 < u) acc[3] = fmaf(a4.w, x[s + 3], acc[3]);
+      for (int s = 0; s < 64; ++s) {
+        if (s < s_lo) continue;
+        float lo, hi;
+        tc::f2_unpack(xp[s >> 1], lo, hi);
+        float xs;
+        if ((s & 1) == 0) {
+          lo = (s == t ? 1.f : 0.f) - lo;
+          xs = lo;
+          hi = fmaf(*reinterpret_cast<const float*>(Ai + at_off(s, s + 1)), xs, hi);  // row s + 1
+        } else {
+          hi = (s == t ? 1.f : 0.f) - hi;
+          xs = hi;
         }
-        x[u] = (u == t ? 1.f : 0.f) - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        xp[s >> 1] = tc::f2_pack(lo, hi);
+        const uint64_t xs2 = tc::f2_pack(xs, xs);
+        // rows 2k, 2k+1 for k >= k0, read four at a time from row s of A^T
+        const int k0 = (s + 2) >> 1;
+#pragma unroll
+        for (int m = k0 >> 1; m < 16; ++m) {
+          const float4 a4 = *reinterpret_cast<const float4*>(Ai + at_off(s, 4 * m));
+          if (2 * m >= k0) xp[2 * m] = tc::f2_fma(tc::f2_pack(a4.x, a4.y), xs2, xp[2 * m]);
+          xp[2 * m + 1] = tc::f2_fma(tc::f2_pack(a4.z, a4.w), xs2, xp[2 * m + 1]);
+        }
       }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) tc::f2_unpack(xp[k], x[2 * k], x[2 * k + 1]);
     }
     tc::named_sync(1, 128);  // A is read by every thread before the T operands overwrite it
     // row j of T diag(beta e^g) for W, then (once the W products are done) of T diag(beta) for Ut
@@ -338,7 +362,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
           tc::bulk_store(dst + gdnws::kK, smem + kOffV + i2 * 16384, 16384);
         }
         tc::bulk_commit();
-        tc::bulk_wait_all();
+        tc::bulk_wait_read_all();  // the images may be overwritten once read; the writes finish on their own
       }
     } else {
       hsd::set_status(p.status, HS_DEV_TIMEOUT);
