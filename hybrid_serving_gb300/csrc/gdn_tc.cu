@@ -49,22 +49,49 @@ using hsd::Meta;
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 352;
-constexpr int kWarpProd = 8, kWarpMma = 9, kWarpOmma = 10;
 constexpr long long kWaitCycles = 4000000000LL;
-// one stage of chunk inputs (offsets from the stage base)
-constexpr int kStW = 0, kStQ = 16384, kStK = 32768, kStP = 49152, kStUt = 57344, kStG = 73728;
-constexpr int kStageBytes = 74752;  // 73728 + the 1 KB decay block
-constexpr int kStages = 3;
-constexpr int kSmem = kStages * kStageBytes;
-constexpr uint32_t kStageTx = 16384 * 4 + 8192 + 1024;
-static_assert(kStG + (gdnws::kBytes - gdnws::kG) == kStageBytes, "stage layout");
-// tensor-memory columns
-constexpr uint32_t kTS32 = 0;    // S fp32 [128][128]
-constexpr uint32_t kTS16 = 128;  // S bf16, two per column (64)
-constexpr uint32_t kTU = 192;    // U bf16 (32)
-constexpr uint32_t kTSlo = 192;  // S bf16 low part (64), only while a later group forms its start state
-constexpr uint32_t kTD1 = 256, kTD2 = 320, kTD3 = 384;  // fp32 [128][64] each
+
+// Two variants of the state pass.  With outputs (O = true): rows, outputs, producer, chain MMA and
+// output MMA warps, 3 stages of {W^T, Q, K', P, Ut^T, decay block}, all 512 TMEM columns.  Without
+// (O = false; the scan's first pass): rows, producer and chain MMA warps, 2 stages of {W^T, K', Ut^T,
+// decay block} and 256 TMEM columns (U written over the columns of D1 once D1 is read), so two CTAs
+// share an SM.
+template <bool O>
+struct Cfg;
+template <>
+struct Cfg<true> {
+  static constexpr int kThreads = 352, kMinBlocks = 1;
+  static constexpr int kWarpProd = 8, kWarpMma = 9, kWarpOmma = 10;
+  // one stage of chunk inputs (offsets from the stage base)
+  static constexpr int kStW = 0, kStQ = 16384, kStK = 32768, kStP = 49152, kStUt = 57344, kStG = 73728;
+  static constexpr int kStageBytes = 74752;  // 73728 + the 1 KB decay block
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kStageTx = 16384 * 4 + 8192 + 1024;
+  // tensor-memory columns
+  static constexpr uint32_t kTS32 = 0;    // S fp32 [128][128]
+  static constexpr uint32_t kTS16 = 128;  // S bf16, two per column (64)
+  static constexpr uint32_t kTU = 192;    // U bf16 (32)
+  static constexpr uint32_t kTSlo = 192;  // S bf16 low part (64), only while a later group forms its start state
+  static constexpr uint32_t kTD1 = 256, kTD2 = 320, kTD3 = 384;  // fp32 [128][64] each
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kEmptyCount = 2 + 8;  // two MMA commits + one arrival per row and output warp
+};
+template <>
+struct Cfg<false> {
+  static constexpr int kThreads = 192, kMinBlocks = 2;
+  static constexpr int kWarpProd = 4, kWarpMma = 5, kWarpOmma = -1;
+  static constexpr int kStW = 0, kStK = 16384, kStUt = 32768, kStG = 49152, kStQ = 0, kStP = 0;
+  static constexpr int kStageBytes = 50176;
+  static constexpr int kStages = 2;
+  static constexpr uint32_t kStageTx = 16384 * 3 + 1024;
+  static constexpr uint32_t kTS32 = 0, kTS16 = 128, kTD1 = 192, kTU = 192, kTSlo = 192, kTD2 = 0, kTD3 = 0;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr int kEmptyCount = 1 + 4;  // the chain's MMA commit + one arrival per row warp
+};
+static_assert(Cfg<true>::kStG + (gdnws::kBytes - gdnws::kG) == Cfg<true>::kStageBytes, "stage layout");
+static_assert(Cfg<false>::kStG + (gdnws::kBytes - gdnws::kG) == Cfg<false>::kStageBytes, "stage layout");
+template <bool O>
+constexpr int smem_bytes() { return Cfg<O>::kStages * Cfg<O>::kStageBytes; }
 
 constexpr uint32_t kIdesc64 = tc::idesc_bf16(128, 64, 0, 0);      // D[128x64], B K-major
 constexpr uint32_t kIdesc64mn = tc::idesc_bf16(128, 64, 0, 1);    // D[128x64], B N-major
@@ -73,7 +100,6 @@ constexpr uint32_t kIdesc128mn = tc::idesc_bf16(128, 128, 0, 1);  // D[128x128],
 struct Prm {
   const int32_t* meta;
   int level, H, n_slots;
-  int pass;  // 0: group 0 of every node, and N, M of the later groups; 1: the later groups
   const uint8_t* ws;
   uint8_t* scan;  // per (extra scan group, head) buffers (gdn_ws.h)
   float* state;
@@ -85,31 +111,47 @@ struct Prm {
 enum InitKind { kInitSlot, kInitZero, kInitIdentity, kInitScan };
 enum EndKind { kEndNone, kEndSlot, kEndScanS, kEndScanN, kEndScanM };
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool O>
+__global__ void __launch_bounds__(Cfg<O>::kThreads, Cfg<O>::kMinBlocks)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
+  using C = Cfg<O>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_s, bar_u, bar_of;
-  __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2, bar_pm, bar_ps, bar_pd;
+  __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_s, bar_u, bar_of;
+  __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2, bar_cb[3], bar_ps, bar_pd;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
   Meta M{p.meta};
   if (p.level >= M.h(H_N_LEVEL)) return;
-  // the task: (node, group g, part) -- part 1 = the group's transition M (pass 0 only)
+  // The task.  O = false (first pass of the two-level scan): for scan entry e (node, group g >= 1), part 0 =
+  // N_g (zero start), part 1 = M_g (identity start, Ut = 0), part 2 (g = 1 only) = the end state of group
+  // 0 (the node's own start).  O = true: blockIdx.x < cap_seg = the node's group 0 (a node without a
+  // scan: all of it); past it, scan entry e = group g >= 1 from its start state S_g (formed from the end
+  // of group 0 and the (M, N) of groups 1 .. g-1).  Every task with outputs writes the node's end state
+  // if it holds the node's last chunk.
   const int n_lev_seg = M.level_off()[p.level + 1] - M.level_off()[p.level];
   const int scan_lo = M.scan_level_off()[p.level];
   const int n_lev_scan = M.scan_level_off()[p.level + 1] - scan_lo;
   const int cap_seg = M.h(H_CAP_SEG), cap_scan = scan_cap(M.h(H_CAP_CHUNK));
   int seg, g = 0, part = 0, e = -1;
-  if (p.pass == 0 && (int)blockIdx.x < cap_seg) {
+  if (!O) {
+    part = (int)blockIdx.x / cap_scan;
+    const int t = (int)blockIdx.x % cap_scan;
+    if (part > 2 || t >= n_lev_scan) return;
+    e = scan_lo + t;
+    seg = M.scan()[2 * e];
+    g = M.scan()[2 * e + 1];
+    if (part == 2) {
+      if (g != 1) return;
+      g = 0;
+    }
+  } else if ((int)blockIdx.x < cap_seg) {
     if ((int)blockIdx.x >= n_lev_seg) return;
     seg = M.level_seg()[M.level_off()[p.level] + blockIdx.x];
   } else {
-    const int y = p.pass == 0 ? (int)blockIdx.x - cap_seg : (int)blockIdx.x;
-    part = y / cap_scan;
-    const int t = y % cap_scan;
-    if (part > (p.pass == 0 ? 1 : 0) || t >= n_lev_scan) return;
+    const int t = (int)blockIdx.x - cap_seg;
+    if (t >= n_lev_scan) return;
     e = scan_lo + t;
     seg = M.scan()[2 * e];
     g = M.scan()[2 * e + 1];
@@ -124,22 +166,22 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   const int n_all = sg[S_N_CHUNK], G = scan_groups(n_all), e1 = sg[S_SCAN1];
   const int c_off = sg[S_CHUNK_OFF] + (int)((long long)g * n_all / G);
   const int n_c = sg[S_CHUNK_OFF] + (int)((long long)(g + 1) * n_all / G) - c_off;
-  const bool outputs = p.pass == 1 || g == 0;
-  const bool zero_ut = part == 1;
-  const InitKind ik = p.pass == 1 ? kInitScan : g == 0 ? (init >= 0 ? kInitSlot : kInitZero)
-                                              : part == 0 ? kInitZero : kInitIdentity;
-  const EndKind ek = p.pass == 1 ? (g == G - 1 && endslot >= 0 ? kEndSlot : kEndNone)
-                     : g == 0    ? (G > 1 ? kEndScanS : endslot >= 0 ? kEndSlot : kEndNone)
-                                 : (part == 0 ? kEndScanN : kEndScanM);
-  const int n_comb = p.pass == 1 ? g - 1 : 0;  // products S <- S M_q + N_q before the chain (groups 1 .. g-1)
+  const bool outputs = O;
+  const bool zero_ut = !O && part == 1;
+  const InitKind ik = g == 0 ? (init >= 0 ? kInitSlot : kInitZero)
+                      : O    ? kInitScan
+                             : (part == 0 ? kInitZero : kInitIdentity);
+  const EndKind ek = O ? (g == G - 1 && endslot >= 0 ? kEndSlot : kEndNone)
+                       : (part == 2 ? kEndScanS : part == 0 ? kEndScanN : kEndScanM);
+  const int n_comb = O && g >= 1 ? g - 1 : 0;  // products S <- S M_q + N_q before the chain (groups 1 .. g-1)
   auto scanbuf = [&](int entry) { return p.scan + ((size_t)entry * p.H + h) * gdnws::kScanBytes; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       tc::mbar_init(&bar_full[s], 1);
-      tc::mbar_init(&bar_empty[s], 2 + 8);  // two MMA commits + one arrival per row and output warp
+      tc::mbar_init(&bar_empty[s], C::kEmptyCount);
     }
     tc::mbar_init(&bar_s, 128);
     tc::mbar_init(&bar_u, 128);
@@ -150,13 +192,13 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     tc::mbar_init(&bar_d23, 1);
     tc::mbar_init(&bar_done, 1);
     tc::mbar_init(&bar_done2, 1);
-    tc::mbar_init(&bar_pm, 1);
+    for (int b = 0; b < 3; ++b) tc::mbar_init(&bar_cb[b], 1);  // combine buffers (M or N images) filled
     tc::mbar_init(&bar_ps, 128);
     tc::mbar_init(&bar_pd, 1);
     tc::fence_mbar_init();
   }
-  if (warp == kWarpMma) {
-    tc::tmem_alloc(&tmem_slot, 512);
+  if (warp == C::kWarpMma) {
+    tc::tmem_alloc(&tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -167,29 +209,32 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     hsd::set_status(p.status, HS_DEV_TIMEOUT);
     atomicExch(&abort_flag, 1);
   };
-  auto stage = [&](int ci) { return smem + (ci % kStages) * kStageBytes; };
+  auto stage = [&](int ci) { return smem + (ci % C::kStages) * C::kStageBytes; };
 
-  if (warp == kWarpProd) {
+  if (warp == C::kWarpProd) {
     // ----------------------------------------------------------- producer
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
-      // the start state of a later group: the images of M_1 .. M_{g-1}, one at a time, in stage 0
+      // the start state of a later group: the images of M_q and N_q, q = 1 .. g-1, as items 2q-2 and 2q-1
+      // of a rotation through three 64 KB buffers (the stage regions), up to three items ahead; buffer b is
+      // refilled once the combine that read its previous item is done (bar_pd: never two phases ahead,
+      // since a later combine needs an item not yet issued)
       bool pro_ok = true;
-      for (int q = 1; q <= n_comb && pro_ok; ++q) {
-        if (q >= 2 && !tc::mbar_wait(&bar_pd, (q - 2) & 1, kWaitCycles)) {
+      for (int i = 0; i < 2 * n_comb && pro_ok; ++i) {
+        const int b = i % 3;
+        if (i >= 3 && !tc::mbar_wait(&bar_pd, ((i - 3) / 2) & 1, kWaitCycles)) {
           pro_ok = false;
           break;
         }
-        const uint8_t* sbq = scanbuf(e1 + q - 1);
-        tc::mbar_expect_tx(&bar_pm, 65536);
-        tc::bulk_load(smem, sbq + gdnws::kScanMhi, 32768, &bar_pm);
-        tc::bulk_load(smem + 32768, sbq + gdnws::kScanMlo, 32768, &bar_pm);
+        const uint8_t* src = scanbuf(e1 + i / 2) + ((i & 1) ? gdnws::kScanN : gdnws::kScanMhi);
+        tc::mbar_expect_tx(&bar_cb[b], 65536);
+        tc::bulk_load(smem + b * C::kStageBytes, src, 65536, &bar_cb[b]);
       }
       if (pro_ok && n_comb > 0 && !tc::mbar_wait(&bar_pd, (n_comb - 1) & 1, kWaitCycles)) pro_ok = false;
       if (!pro_ok) fail();
       int issued = 0;
       for (int ci = 0; ci < n_c && pro_ok; ++ci) {
-        const int s = ci % kStages, n = ci / kStages;
+        const int s = ci % C::kStages, n = ci / C::kStages;
         if (n >= 1 && !tc::mbar_wait(&bar_empty[s], (n - 1) & 1, kWaitCycles)) {
           fail();
           break;
@@ -198,61 +243,68 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         const int row0 = M.chunk(c_off + ci)[C_ROW0];
         const uint8_t* w = p.ws + ((size_t)(c_off + ci) * p.H + h) * gdnws::kBytes;
         uint8_t* sb = stage(ci);
-        // a group without outputs needs neither Q nor P; a transition (Ut = 0) not Ut either
-        tc::mbar_expect_tx(&bar_full[s], kStageTx - (outputs ? 0u : 16384u + 8192u) - (zero_ut ? 16384u : 0u));
-        tc::bulk_load(sb + kStW, w + gdnws::kW, 16384, &bar_full[s]);
-        if (!zero_ut) tc::bulk_load(sb + kStUt, w + gdnws::kU, 16384, &bar_full[s]);
-        tc::bulk_load(sb + kStG, w + gdnws::kG, gdnws::kBytes - gdnws::kG, &bar_full[s]);
-        tc::bulk_load(sb + kStK, w + gdnws::kK, 16384, &bar_full[s]);
+        // a transition (Ut = 0) needs no Ut
+        tc::mbar_expect_tx(&bar_full[s], C::kStageTx - (zero_ut ? 16384u : 0u));
+        tc::bulk_load(sb + C::kStW, w + gdnws::kW, 16384, &bar_full[s]);
+        if (!zero_ut) tc::bulk_load(sb + C::kStUt, w + gdnws::kU, 16384, &bar_full[s]);
+        tc::bulk_load(sb + C::kStG, w + gdnws::kG, gdnws::kBytes - gdnws::kG, &bar_full[s]);
+        tc::bulk_load(sb + C::kStK, w + gdnws::kK, 16384, &bar_full[s]);
         if (outputs) {
           for (int half = 0; half < 2; ++half)
-            tc::tma_load_3d(sb + kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
-          tc::bulk_load(sb + kStP, w + gdnws::kP, 8192, &bar_full[s]);
+            tc::tma_load_3d(sb + C::kStQ + half * 8192, &tm_q, half * 64, h, row0, &bar_full[s]);
+          tc::bulk_load(sb + C::kStP, w + gdnws::kP, 8192, &bar_full[s]);
         }
         ++issued;
       }
-      for (int ci = issued >= kStages ? issued - kStages : 0; ci < issued; ++ci)
-        tc::mbar_wait(&bar_full[ci % kStages], (ci / kStages) & 1, kWaitCycles);
+      for (int ci = issued >= C::kStages ? issued - C::kStages : 0; ci < issued; ++ci)
+        tc::mbar_wait(&bar_full[ci % C::kStages], (ci / C::kStages) & 1, kWaitCycles);
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == C::kWarpMma) {
     // ------------------------------------------------ MMA: the state chain
     // (the whole warp, converged: waits are voted and one elected lane issues; descriptors are built once
     // per stage and a K step adds a constant to the start-address field)
     {
       bool ok = true;
-      // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi into the fp32 state columns
+      // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi + I N_hi + I N_lo into the fp32
+      // state columns (I: a bf16 identity the rows place in the D1 columns, idle until the chunks)
       for (int q = 1; q <= n_comb && ok; ++q) {
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_pm, (q - 1) & 1, kWaitCycles)) || !__all_sync(~0u, tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles))) {
+        const int im = 2 * q - 2, in = 2 * q - 1;  // the items of M_q and N_q
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_cb[im % 3], (im / 3) & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait(&bar_cb[in % 3], (in / 3) & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const uint32_t sm = tc::smem_u32(smem);
-        const uint64_t dm0 = tc::sdesc_sw128(sm, 16384, 1024), dm1 = tc::sdesc_sw128(sm + 32768, 16384, 1024);
+        const uint64_t dm0 = tc::sdesc_sw128(sm + (im % 3) * C::kStageBytes, 16384, 1024);
+        const uint64_t dn0 = tc::sdesc_sw128(sm + (in % 3) * C::kStageBytes, 16384, 1024);
+        const uint64_t dm1 = dm0 + (uint64_t)(32768 >> 4), dn1 = dn0 + (uint64_t)(32768 >> 4);
 #pragma unroll
-        for (int pr = 0; pr < 3; ++pr) {
+        for (int pr = 0; pr < 5; ++pr) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            tc::mma_bf16_ts_w(tmem + kTS32, tmem + (pr == 2 ? kTSlo : kTS16) + 8 * k,
-                              (pr == 1 ? dm1 : dm0) + (uint64_t)((k * 2048) >> 4), kIdesc128mn,
+            const uint32_t a = pr == 2 ? C::kTSlo : pr >= 3 ? C::kTD1 : C::kTS16;
+            const uint64_t b = pr == 0 || pr == 2 ? dm0 : pr == 1 ? dm1 : pr == 3 ? dn0 : dn1;
+            tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + a + 8 * k, b + (uint64_t)((k * 2048) >> 4), kIdesc128mn,
                               (pr > 0 || k > 0) ? 1u : 0u);
           }
         }
         tc::mma_commit_w(&bar_pd);
       }
       for (int ci = 0; ci < n_c && ok; ++ci) {
-        const int s = ci % kStages;
+        const int s = ci % C::kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles)) ||
             !__all_sync(~0u, tc::mbar_wait_spin(&bar_s, ci & 1, kWaitCycles))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint64_t dw = tc::sdesc_sw128(sb + kStW, 16384, 1024);
+        const uint64_t dw = tc::sdesc_sw128(sb + C::kStW, 16384, 1024);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
-          tc::mma_bf16_ts_w(tmem + kTD1, tmem + kTS16 + 8 * k, dw + (uint64_t)((k * 2048) >> 4), kIdesc64mn,
+          tc::mma_bf16_ts_w(tmem + C::kTD1, tmem + C::kTS16 + 8 * k, dw + (uint64_t)((k * 2048) >> 4), kIdesc64mn,
                             k > 0 ? 1u : 0u);
         }
         tc::mma_commit_w(&bar_d1);
@@ -261,10 +313,10 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           break;
         }
         tc::fence_after_sync();
-        const uint64_t dk = tc::sdesc_sw128(sb + kStK, 8192, 1024);
+        const uint64_t dk = tc::sdesc_sw128(sb + C::kStK, 8192, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // S += U K'   (K = tokens; S already scaled by e^{gC})
-          tc::mma_bf16_ts_w(tmem + kTS32, tmem + kTU + 8 * k, dk + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
+          tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + C::kTU + 8 * k, dk + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
         }
         tc::mma_commit_w(&bar_d4);
         tc::mma_commit_w(&bar_empty[s]);
@@ -275,26 +327,26 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
     }
     __syncwarp();
-  } else if (warp == kWarpOmma) {
+  } else if (O && warp == C::kWarpOmma) {
     // -------------------------------------------------- MMA: the outputs
     // (converged warp, voted waits, one elected lane issues)
     {
       bool ok = true;
       for (int ci = 0; ci < n_c && ok; ++ci) {
-        const int s = ci % kStages;
+        const int s = ci % C::kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
         if (!__all_sync(~0u, tc::mbar_wait(&bar_s, ci & 1, kWaitCycles)) ||
-            !__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
+            !__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles)) ||
             (ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles)))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         if (outputs) {
-          const uint64_t dq = tc::sdesc_sw128(sb + kStQ, 16, 1024);
+          const uint64_t dq = tc::sdesc_sw128(sb + C::kStQ, 16, 1024);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {  // D2 = S Q^T
-            tc::mma_bf16_ts_w(tmem + kTD2, tmem + kTS16 + 8 * k, dq + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
+            tc::mma_bf16_ts_w(tmem + C::kTD2, tmem + C::kTS16 + 8 * k, dq + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
                               kIdesc64, k > 0 ? 1u : 0u);
           }
         }
@@ -305,10 +357,10 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         }
         tc::fence_after_sync();
         if (outputs) {
-          const uint64_t dp = tc::sdesc_sw128(sb + kStP, 16, 1024);
+          const uint64_t dp = tc::sdesc_sw128(sb + C::kStP, 16, 1024);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // D3 = U P^T
-            tc::mma_bf16_ts_w(tmem + kTD3, tmem + kTU + 8 * k, dp + (uint64_t)((k * 32) >> 4), kIdesc64, k > 0 ? 1u : 0u);
+            tc::mma_bf16_ts_w(tmem + C::kTD3, tmem + C::kTU + 8 * k, dp + (uint64_t)((k * 32) >> 4), kIdesc64, k > 0 ? 1u : 0u);
           }
         }
         tc::mma_commit_w(&bar_d23);
@@ -345,17 +397,30 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) f[i] = __float_as_uint(q * 32 + i == j ? 1.f : 0.f);
         }
-        tc::tmem_st32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_st32(tmem + lb + C::kTS32 + q * 32, f);
       }
       tc::tmem_wait_st();
     }
-    // a later group's start state: S <- S M_q + N_q for q = 1 .. g-1, on tensor cores with S and M split into
-    // bf16 high and low parts (S_hi M_hi + S_hi M_lo + S_lo M_hi), N_q added in fp32
+    // a later group's start state: S <- S M_q + N_q for q = 1 .. g-1, on tensor cores with S, M and N split
+    // into bf16 high and low parts (S_hi M_hi + S_hi M_lo + S_lo M_hi + I N_hi + I N_lo; I = the identity,
+    // written once into the D1 columns, which hold nothing until the chunks)
+    if (n_comb > 0) {
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t id[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = c4 * 32 + 2 * i;  // columns k0, k0 + 1 of row j
+          id[i] = (k0 == j ? 0x3F80u : 0u) | (k0 + 1 == j ? 0x3F800000u : 0u);
+        }
+        tc::tmem_st16(tmem + lb + C::kTD1 + c4 * 16, id);
+      }
+    }
     for (int q = 1; q <= n_comb && ok; ++q) {
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t f[32], bh[16], bl[16];
-        tc::tmem_ld32(tmem + lb + kTS32 + c4 * 32, f);
+        tc::tmem_ld32(tmem + lb + C::kTS32 + c4 * 32, f);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -363,8 +428,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           bh[i] = tc::pack_bf16x2(a, b);
           bl[i] = tc::pack_bf16x2(a - __uint_as_float(bh[i] << 16), b - __uint_as_float(bh[i] & 0xFFFF0000u));
         }
-        tc::tmem_st16(tmem + lb + kTS16 + c4 * 16, bh);
-        tc::tmem_st16(tmem + lb + kTSlo + c4 * 16, bl);
+        tc::tmem_st16(tmem + lb + C::kTS16 + c4 * 16, bh);
+        tc::tmem_st16(tmem + lb + C::kTSlo + c4 * 16, bl);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -374,69 +439,52 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         break;
       }
       tc::fence_after_sync();
-      const float4* nq = reinterpret_cast<const float4*>(scanbuf(e1 + q - 1) + gdnws::kScanN) + j * (kD / 4);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t f[32];
-        tc::tmem_ld32(tmem + lb + kTS32 + c4 * 32, f);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = nq[c4 * 8 + i];
-          f[4 * i] = __float_as_uint(__uint_as_float(f[4 * i]) + v.x);
-          f[4 * i + 1] = __float_as_uint(__uint_as_float(f[4 * i + 1]) + v.y);
-          f[4 * i + 2] = __float_as_uint(__uint_as_float(f[4 * i + 2]) + v.z);
-          f[4 * i + 3] = __float_as_uint(__uint_as_float(f[4 * i + 3]) + v.w);
-        }
-        tc::tmem_st32(tmem + lb + kTS32 + c4 * 32, f);
-      }
-      tc::tmem_wait_st();
     }
     // the bf16 operand of the start state
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint32_t f[32], b[16];
-      tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+      tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-      tc::tmem_st16(tmem + lb + kTS16 + q * 16, b);
+      tc::tmem_st16(tmem + lb + C::kTS16 + q * 16, b);
     }
     tc::tmem_wait_st();
     tc::fence_before_sync();
     tc::mbar_arrive(&bar_s);
     for (int ci = 0; ci < n_c; ++ci) {
-      const int s = ci % kStages;
+      const int s = ci % C::kStages;
       const uint8_t* sb = stage(ci);
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles))) {
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles))) {
         ok = false;
         break;
       }
-      const float* gblk = reinterpret_cast<const float*>(sb + kStG);  // e^g [64] | e^{gC-g} [64] | e^{gC}
+      const float* gblk = reinterpret_cast<const float*>(sb + C::kStG);  // e^g [64] | e^{gC-g} [64] | e^{gC}
       // S <- e^{gC} S in place (overlaps D1; D4 adds to it)
       const float ec = gblk[128];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t f[32];
-        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = __float_as_uint(ec * __uint_as_float(f[e]));
-        tc::tmem_st32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_st32(tmem + lb + C::kTS32 + q * 32, f);
       }
       // D1 done; D3 of the previous chunk (which reads U) done
       if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d1, ci & 1, kWaitCycles)) ||
-          (ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_d23, (ci - 1) & 1, kWaitCycles)))) {
+          (O && ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_d23, (ci - 1) & 1, kWaitCycles)))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
       // U = Ut^T - D1;  row j of Ut^T is one swizzled 128-byte row
-      const uint8_t* utj = sb + kStUt + j * 128;
+      const uint8_t* utj = sb + C::kStUt + j * 128;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t d1[32], u2[16];
-        tc::tmem_ld32(tmem + lb + kTD1 + half * 32, d1);
+        tc::tmem_ld32(tmem + lb + C::kTD1 + half * 32, d1);
         uint4 uv[4];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4)  // (a transition M runs with Ut = 0)
@@ -451,7 +499,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
             u2[c4 * 4 + e] = tc::pack_bf16x2(__uint_as_float(w4[e] << 16) - __uint_as_float(d1[c4 * 8 + 2 * e]),
                                              __uint_as_float(w4[e] & 0xFFFF0000u) - __uint_as_float(d1[c4 * 8 + 2 * e + 1]));
         }
-        tc::tmem_st16(tmem + lb + kTU + half * 16, u2);
+        tc::tmem_st16(tmem + lb + C::kTU + half * 16, u2);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -460,7 +508,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // Ut and the decay block are read
       // D4 done (new S), D2 done (the bf16 S may be overwritten)
       if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d4, ci & 1, kWaitCycles)) ||
-          !__all_sync(~0u, tc::mbar_wait(&bar_d2, ci & 1, kWaitCycles))) {
+          (O && !__all_sync(~0u, tc::mbar_wait(&bar_d2, ci & 1, kWaitCycles)))) {
         ok = false;
         break;
       }
@@ -469,11 +517,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t f[32], b[16];
-        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-        tc::tmem_st16(tmem + lb + kTS16 + q * 16, b);
+        tc::tmem_st16(tmem + lb + C::kTS16 + q * 16, b);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -481,30 +529,30 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     }
     if (!ok) {
       fail();
-    } else if (ek == kEndSlot || ek == kEndScanS || ek == kEndScanN) {
+    } else if (ek == kEndSlot || ek == kEndScanS) {
       float4* dst = reinterpret_cast<float4*>(
-          ek == kEndSlot    ? p.state + (((size_t)endslot * p.H + h) * kD + j) * kD
-          : ek == kEndScanS ? reinterpret_cast<float*>(scanbuf(e1) + gdnws::kScanS) + j * kD
-                            : reinterpret_cast<float*>(scanbuf(e) + gdnws::kScanN) + j * kD);
+          ek == kEndSlot ? p.state + (((size_t)endslot * p.H + h) * kD + j) * kD
+                         : reinterpret_cast<float*>(scanbuf(e1) + gdnws::kScanS) + j * kD);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t f[32];
-        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           dst[q * 8 + i] = make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]),
                                        __uint_as_float(f[4 * i + 2]), __uint_as_float(f[4 * i + 3]));
       }
-    } else if (ek == kEndScanM) {
-      // row j of the transition M as the bf16 high and low images of an MN-major B operand:
-      // element (j, n) in slab n / 64, 128-byte row j, 16-byte chunk (n % 64) / 8 swizzled by j % 8
-      uint8_t* mh = scanbuf(e) + gdnws::kScanMhi;
-      uint8_t* ml = scanbuf(e) + gdnws::kScanMlo;
+    } else if (ek == kEndScanM || ek == kEndScanN) {
+      // row j of the transition M (or of the zero-start end state N) as the bf16 high and low images of an
+      // MN-major B operand: element (j, n) in slab n / 64, 128-byte row j, 16-byte chunk (n % 64) / 8
+      // swizzled by j % 8
+      uint8_t* mh = scanbuf(e) + (ek == kEndScanM ? gdnws::kScanMhi : gdnws::kScanN);
+      uint8_t* ml = mh + 32768;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t f[32];
-        tc::tmem_ld32(tmem + lb + kTS32 + q * 32, f);
+        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -522,16 +570,16 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         }
       }
     }
-  } else {
+  } else if (O) {
     // ------------------------------------------------------------- outputs
     const int j = threadIdx.x - 128;  // TMEM lane j
     const uint32_t lb = (uint32_t)((warp - 4) * 32) << 16;
     bool ok = true;
     for (int ci = 0; ci < n_c; ++ci) {
-      const int s = ci % kStages;
+      const int s = ci % C::kStages;
       uint8_t* sb = stage(ci);
-      const float* egs = reinterpret_cast<const float*>(sb + kStG);
-      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / kStages) & 1, kWaitCycles)) ||
+      const float* egs = reinterpret_cast<const float*>(sb + C::kStG);
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles)) ||
           !__all_sync(~0u, tc::mbar_wait(&bar_d23, ci & 1, kWaitCycles))) {
         ok = false;
         break;
@@ -548,10 +596,10 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       // D2, D3 and e^g into registers first, so that D2, D3 are released at once and the
       // staging stores below do not wait on loads from the same buffer
       uint32_t d2[64], d3[64];
-      tc::tmem_ld32(tmem + lb + kTD2, *reinterpret_cast<uint32_t(*)[32]>(d2));
-      tc::tmem_ld32(tmem + lb + kTD2 + 32, *reinterpret_cast<uint32_t(*)[32]>(d2 + 32));
-      tc::tmem_ld32(tmem + lb + kTD3, *reinterpret_cast<uint32_t(*)[32]>(d3));
-      tc::tmem_ld32(tmem + lb + kTD3 + 32, *reinterpret_cast<uint32_t(*)[32]>(d3 + 32));
+      tc::tmem_ld32(tmem + lb + C::kTD2, *reinterpret_cast<uint32_t(*)[32]>(d2));
+      tc::tmem_ld32(tmem + lb + C::kTD2 + 32, *reinterpret_cast<uint32_t(*)[32]>(d2 + 32));
+      tc::tmem_ld32(tmem + lb + C::kTD3, *reinterpret_cast<uint32_t(*)[32]>(d3));
+      tc::tmem_ld32(tmem + lb + C::kTD3 + 32, *reinterpret_cast<uint32_t(*)[32]>(d3 + 32));
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       tc::mbar_arrive(&bar_of);  // D2, D3 may be overwritten
@@ -565,7 +613,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         o[4 * c4 + 3] = fmaf(e.w, __uint_as_float(d2[4 * c4 + 3]), __uint_as_float(d3[4 * c4 + 3]));
       }
       // O[t][j] into the chunk's Q buffer (D2 has read it), plain [64][128] bf16
-      __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sb + kStQ);
+      __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sb + C::kStQ);
 #pragma unroll
       for (int t = 0; t < 64; ++t) stg[t * kD + j] = __float2bfloat16_rn(o[t]);
       tc::named_sync(2, 128);
@@ -575,7 +623,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         const int e = j + 128 * i, t = e >> 4, c16 = e & 15;
         if (t < len)
           *reinterpret_cast<uint4*>(dst + (size_t)t * p.H * kD + c16 * 8) =
-              *reinterpret_cast<const uint4*>(sb + kStQ + t * 256 + c16 * 16);
+              *reinterpret_cast<const uint4*>(sb + C::kStQ + t * 256 + c16 * 16);
       }
       tc::fence_proxy_async_smem();  // the Q buffer is refilled by TMA after this
       __syncwarp();
@@ -586,7 +634,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == kWarpMma) tc::tmem_dealloc(tmem, 512);
+  if (warp == C::kWarpMma) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -626,21 +674,27 @@ hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta,
     return hs::fail(HS_ECUDA, "gdn: tensor map encoding failed");
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(gdn_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(gdn_chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<true>() + 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(gdn_chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<false>() + 1024) != cudaSuccess)
       return hs::fail(HS_ECUDA, "gdn_chain_tc: cannot raise the shared-memory limit");
     configured = true;
   }
-  // per level: group 0 of every node (and the later groups' N and M), then the later groups of the long nodes
+  // per level: the scan's first pass (group 0's end state and the later groups' N and M, no outputs), then
+  // every group of every node with outputs
   const int cap_scan = scan_cap(caps->max_chunks);
   const bool any_scan = caps->max_chunks >= 2 * kScanMinChunks;
   for (int lev = 0; lev < caps->max_levels && caps->max_segments > 0; ++lev) {
-    for (int pass = 0; pass < (any_scan ? 2 : 1); ++pass) {
-      Prm prm{meta, lev, H, n_slots, pass, ws, scan, state, (__nv_bfloat16*)out, status};
-      const int gx = pass == 0 ? caps->max_segments + (any_scan ? 2 * cap_scan : 0) : cap_scan;
-      gdn_chain_tc_kernel<<<dim3(gx, H), kThreads, kSmem + 1024, st>>>(mq, prm);
-      HS_LAUNCH_CHECK("gdn_chain_tc");
+    Prm prm{meta, lev, H, n_slots, ws, scan, state, (__nv_bfloat16*)out, status};
+    if (any_scan) {
+      gdn_chain_tc_kernel<false><<<dim3(3 * cap_scan, H), Cfg<false>::kThreads, smem_bytes<false>() + 1024, st>>>(
+          mq, prm);
+      HS_LAUNCH_CHECK("gdn_chain_tc (scan)");
     }
+    gdn_chain_tc_kernel<true><<<dim3(caps->max_segments + (any_scan ? cap_scan : 0), H), Cfg<true>::kThreads,
+                                  smem_bytes<true>() + 1024, st>>>(mq, prm);
+    HS_LAUNCH_CHECK("gdn_chain_tc");
   }
   return HS_OK;
 }

@@ -24,10 +24,11 @@ constexpr int kBytes = 58368;  // per (chunk, head); multiple of 1024
 constexpr int kFloats = kBytes / 4;
 
 // Per (extra scan group, head) buffers of the two-level state scan, after the
-// per-chunk blocks: the group's start state S (fp32 [128][128], rows d_v),
-// its zero-start end state N (fp32 [128][128]) and its transition M (d_k x
-// d_k) as the bf16 high and low images of the MN-major B operand of S M
-// (two [128][64] slabs each: row k holds M[k][n]).
+// per-chunk blocks: the end state of the node's first group S (fp32
+// [128][128], rows d_v; in the entry of group 1), the group's zero-start end
+// state N (d_v x d_k) and its transition M (d_k x d_k), each as the bf16 high
+// and low images of an MN-major B operand (two [128][64] slabs each: row k
+// holds X[k][n]; N enters the combine as I N).
 constexpr int kScanS = 0;
 constexpr int kScanN = 65536;
 constexpr int kScanMhi = 131072;

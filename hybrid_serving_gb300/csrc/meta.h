@@ -67,8 +67,8 @@ enum : int {
 // chunks that run side by side (a two-level scan of the affine chunk map
 // S -> S M_c + N_c): group g of a node with n chunks holds chunks
 // [g n / G, (g + 1) n / G).  G depends on the node's own length only.
-constexpr int kScanMinChunks = 24;
-constexpr int kScanMaxGroups = 5;
+constexpr int kScanMinChunks = 12;
+constexpr int kScanMaxGroups = 9;
 HSM_HD inline int32_t scan_groups(int32_t n_chunks) {
   if (n_chunks < 2 * kScanMinChunks) return 1;
   const int32_t g = n_chunks / kScanMinChunks;

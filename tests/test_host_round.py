@@ -205,11 +205,11 @@ def test_chunks_slots_readouts():
 
 
 def test_scan_group_table():
-    """The two-level scan of the GDN state chain: a node of n >= 48 chunks is
-    split into G = min(5, n // 24) groups (fixed examples below), listed per
+    """The two-level scan of the GDN state chain: a node of n >= 24 chunks is
+    split into G = min(9, n // 12) groups (fixed examples below), listed per
     level as (node, group) pairs for groups 1 .. G-1 in node order, with each
     long node pointing at its group-1 entry; short nodes have one group."""
-    expect_groups = {1: 1, 47: 1, 48: 2, 71: 2, 72: 3, 96: 4, 119: 4, 120: 5, 200: 5}
+    expect_groups = {1: 1, 23: 1, 24: 2, 35: 2, 36: 3, 47: 3, 48: 4, 72: 6, 107: 8, 108: 9, 200: 9}
     lens = [47 * 64, 48 * 64 - 10, 72 * 64, 200 * 64, 5]          # the second is 48 chunks (last one short)
     tree = synth.Tree([synth.fork_tree(lens[0], [lens[1], 60]), synth.fork_tree(lens[2], [lens[3]]),
                        synth.fork_tree(lens[4], [7])])
@@ -225,7 +225,7 @@ def test_scan_group_table():
             if int(segs[s][5]) != lev:
                 continue
             n_ch = int(segs[s][10])
-            G = expect_groups.get(n_ch, 1 if n_ch < 48 else min(5, n_ch // 24))
+            G = expect_groups.get(n_ch, 1 if n_ch < 24 else min(9, n_ch // 12))
             assert int(segs[s][14]) == (len(expected) if G > 1 else -1)
             expected += [(s, g) for g in range(1, G)]
     assert int(B.w[o_lev + levels]) == len(expected)
@@ -233,13 +233,13 @@ def test_scan_group_table():
     # the fixed examples are all present
     got = {int(segs[s][10]) for s in range(len(segs))}
     assert {47, 48, 72, 200} <= got
-    # group chunk ranges [g n / G, (g+1) n / G) tile each long node exactly, each >= 24 chunks
+    # group chunk ranges [g n / G, (g+1) n / G) tile each long node exactly, each >= 12 chunks
     for s in range(len(segs)):
         n_ch = int(segs[s][10])
-        G = expect_groups.get(n_ch, 1 if n_ch < 48 else min(5, n_ch // 24))
+        G = expect_groups.get(n_ch, 1 if n_ch < 24 else min(9, n_ch // 12))
         bounds = [g * n_ch // G for g in range(G + 1)]
         assert bounds[0] == 0 and bounds[-1] == n_ch
-        assert all(b - a >= (24 if G > 1 else 1) for a, b in zip(bounds, bounds[1:]))
+        assert all(b - a >= (12 if G > 1 else 1) for a, b in zip(bounds, bounds[1:]))
 
 
 def test_forkserve_pages_fork_and_commit():
