@@ -413,7 +413,10 @@ hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, 
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(gdn_chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
-        cudaSuccess)
+            cudaSuccess ||
+        // two CTAs per SM: every SM configured for all of its shared memory
+        cudaFuncSetAttribute(gdn_chunk_prep_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return hs::fail(HS_ECUDA, "gdn_chunk_prep_tc: cannot raise the shared-memory limit");
     configured = true;
   }

@@ -53,9 +53,10 @@ constexpr long long kWaitCycles = 4000000000LL;
 
 // Two variants of the state pass.  With outputs (O = true): rows, outputs, producer, chain MMA and
 // output MMA warps, 3 stages of {W^T, Q, K', P, Ut^T, decay block}, all 512 TMEM columns.  Without
-// (O = false; the scan's first pass): rows, producer and chain MMA warps, 2 stages of {W^T, K', Ut^T,
-// decay block} and 256 TMEM columns (U written over the columns of D1 once D1 is read), so two CTAs
-// share an SM.
+// (O = false; the scan's first pass): rows, producer and chain MMA warps, 3 stages of {W^T, K', Ut^T,
+// decay block}, and two chains over the same chunks -- the group's N (zero start) and M (identity
+// start, Ut = 0) -- in 256 TMEM columns each (U written over the columns of D1 once D1 is read); the
+// two chains' steps interleave, so one's products run while the rows work on the other.
 template <bool O>
 struct Cfg;
 template <>
@@ -78,14 +79,15 @@ struct Cfg<true> {
 };
 template <>
 struct Cfg<false> {
-  static constexpr int kThreads = 192, kMinBlocks = 2;
+  static constexpr int kThreads = 192, kMinBlocks = 1;
   static constexpr int kWarpProd = 4, kWarpMma = 5, kWarpOmma = -1;
   static constexpr int kStW = 0, kStK = 16384, kStUt = 32768, kStG = 49152, kStQ = 0, kStP = 0;
   static constexpr int kStageBytes = 50176;
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 3;
   static constexpr uint32_t kStageTx = 16384 * 3 + 1024;
-  static constexpr uint32_t kTS32 = 0, kTS16 = 128, kTD1 = 192, kTU = 192, kTSlo = 192, kTD2 = 0, kTD3 = 0;
-  static constexpr uint32_t kTmemCols = 256;
+  // per chain, from its base column (256 c)
+  static constexpr uint32_t kTS32 = 0, kTS16 = 128, kTD1 = 192, kTU = 192, kTD2 = 0, kTD3 = 0;
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr int kEmptyCount = 1 + 4;  // the chain's MMA commit + one arrival per row warp
 };
 static_assert(Cfg<true>::kStG + (gdnws::kBytes - gdnws::kG) == Cfg<true>::kStageBytes, "stage layout");
@@ -118,6 +120,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_s, bar_u, bar_of;
   __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2, bar_cb[3], bar_ps, bar_pd;
+  __shared__ uint64_t bar_sc[2], bar_uc[2], bar_d1c[2], bar_d4c[2];  // per chain (output-less variant)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -125,8 +128,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   Meta M{p.meta};
   if (p.level >= M.h(H_N_LEVEL)) return;
   // The task.  O = false (first pass of the two-level scan): for scan entry e (node, group g >= 1), part 0 =
-  // N_g (zero start), part 1 = M_g (identity start, Ut = 0), part 2 (g = 1 only) = the end state of group
-  // 0 (the node's own start).  O = true: blockIdx.x < cap_seg = the node's group 0 (a node without a
+  // N_g (zero start) and M_g (identity start, Ut = 0) as two chains, part 2 (g = 1 only) = the end state of
+  // group 0 (the node's own start).  O = true: task < cap_seg = the node's group 0 (a node without a
   // scan: all of it); past it, scan entry e = group g >= 1 from its start state S_g (formed from the end
   // of group 0 and the (M, N) of groups 1 .. g-1).  Every task with outputs writes the node's end state
   // if it holds the node's last chunk.
@@ -134,11 +137,17 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   const int scan_lo = M.scan_level_off()[p.level];
   const int n_lev_scan = M.scan_level_off()[p.level + 1] - scan_lo;
   const int cap_seg = M.h(H_CAP_SEG), cap_scan = scan_cap(M.h(H_CAP_CHUNK));
+  // blockIdx.x = head, blockIdx.y = task: blocks are dispatched x fastest, so every head's copy of a task
+  // is placed before the next task, and the tasks that exit at once come after the ones with work (measured:
+  // with the tasks of a head contiguous, a fifth of the first pass's CTAs waited for a second wave)
+  const int task = (int)blockIdx.y;
   int seg, g = 0, part = 0, e = -1;
   if (!O) {
-    part = (int)blockIdx.x / cap_scan;
-    const int t = (int)blockIdx.x % cap_scan;
-    if (part > 2 || t >= n_lev_scan) return;
+    // task t < cap_scan: N and M of entry t's group (part 0, two chains); task cap_scan + t: the end of
+    // group 0 (part 2, live for one entry per long node), so the tasks with work come first
+    part = task < cap_scan ? 0 : 2;
+    const int t = task < cap_scan ? task : task - cap_scan;
+    if (task >= 2 * cap_scan || t >= n_lev_scan) return;
     e = scan_lo + t;
     seg = M.scan()[2 * e];
     g = M.scan()[2 * e + 1];
@@ -146,18 +155,18 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       if (g != 1) return;
       g = 0;
     }
-  } else if ((int)blockIdx.x < cap_seg) {
-    if ((int)blockIdx.x >= n_lev_seg) return;
-    seg = M.level_seg()[M.level_off()[p.level] + blockIdx.x];
+  } else if (task < cap_seg) {
+    if (task >= n_lev_seg) return;
+    seg = M.level_seg()[M.level_off()[p.level] + task];
   } else {
-    const int t = (int)blockIdx.x - cap_seg;
+    const int t = task - cap_seg;
     if (t >= n_lev_scan) return;
     e = scan_lo + t;
     seg = M.scan()[2 * e];
     g = M.scan()[2 * e + 1];
   }
   const int32_t* sg = M.seg(seg);
-  const int h = blockIdx.y;
+  const int h = blockIdx.x;
   const int init = sg[S_INIT_SLOT], endslot = sg[S_END_SLOT];
   if (init >= p.n_slots || endslot >= p.n_slots) {
     if (threadIdx.x == 0) hsd::set_status(p.status, HS_DEV_BAD_SLOT);
@@ -187,6 +196,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     tc::mbar_init(&bar_u, 128);
     tc::mbar_init(&bar_of, 128);
     tc::mbar_init(&bar_d1, 1);
+    for (int c = 0; c < 2; ++c) {
+      tc::mbar_init(&bar_sc[c], 128);
+      tc::mbar_init(&bar_uc[c], 128);
+      tc::mbar_init(&bar_d1c[c], 1);
+      tc::mbar_init(&bar_d4c[c], 1);
+    }
     tc::mbar_init(&bar_d4, 1);
     tc::mbar_init(&bar_d2, 1);
     tc::mbar_init(&bar_d23, 1);
@@ -260,73 +275,120 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         tc::mbar_wait(&bar_full[ci % C::kStages], (ci / C::kStages) & 1, kWaitCycles);
     }
   } else if (warp == C::kWarpMma) {
-    // ------------------------------------------------ MMA: the state chain
-    // (the whole warp, converged: waits are voted and one elected lane issues; descriptors are built once
-    // per stage and a K step adds a constant to the start-address field)
-    {
+    if constexpr (!O) {
+      // ---------------------------------- MMA: the N and M chains of a group (or group 0's one chain)
+      // (converged warp, voted waits, one elected lane issues); per chunk D1 of each chain, then D4 of each
+      const int nch = part == 0 ? 2 : 1;
       bool ok = true;
-      // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi + I N_hi + I N_lo into the fp32
-      // state columns (I: a bf16 identity the rows place in the D1 columns, idle until the chunks)
-      for (int q = 1; q <= n_comb && ok; ++q) {
-        const int im = 2 * q - 2, in = 2 * q - 1;  // the items of M_q and N_q
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_cb[im % 3], (im / 3) & 1, kWaitCycles)) ||
-            !__all_sync(~0u, tc::mbar_wait(&bar_cb[in % 3], (in / 3) & 1, kWaitCycles)) ||
-            !__all_sync(~0u, tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        const uint32_t sm = tc::smem_u32(smem);
-        const uint64_t dm0 = tc::sdesc_sw128(sm + (im % 3) * C::kStageBytes, 16384, 1024);
-        const uint64_t dn0 = tc::sdesc_sw128(sm + (in % 3) * C::kStageBytes, 16384, 1024);
-        const uint64_t dm1 = dm0 + (uint64_t)(32768 >> 4), dn1 = dn0 + (uint64_t)(32768 >> 4);
-#pragma unroll
-        for (int pr = 0; pr < 5; ++pr) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t a = pr == 2 ? C::kTSlo : pr >= 3 ? C::kTD1 : C::kTS16;
-            const uint64_t b = pr == 0 || pr == 2 ? dm0 : pr == 1 ? dm1 : pr == 3 ? dn0 : dn1;
-            tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + a + 8 * k, b + (uint64_t)((k * 2048) >> 4), kIdesc128mn,
-                              (pr > 0 || k > 0) ? 1u : 0u);
-          }
-        }
-        tc::mma_commit_w(&bar_pd);
-      }
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % C::kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles)) ||
-            !__all_sync(~0u, tc::mbar_wait_spin(&bar_s, ci & 1, kWaitCycles))) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
-        tc::fence_after_sync();
         const uint64_t dw = tc::sdesc_sw128(sb + C::kStW, 16384, 1024);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
-          tc::mma_bf16_ts_w(tmem + C::kTD1, tmem + C::kTS16 + 8 * k, dw + (uint64_t)((k * 2048) >> 4), kIdesc64mn,
-                            k > 0 ? 1u : 0u);
-        }
-        tc::mma_commit_w(&bar_d1);
-        if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_u, ci & 1, kWaitCycles))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
         const uint64_t dk = tc::sdesc_sw128(sb + C::kStK, 8192, 1024);
+        for (int c = 0; c < nch && ok; ++c) {
+          if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_sc[c], ci & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t tb = tmem + 256 * c;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // S += U K'   (K = tokens; S already scaled by e^{gC})
-          tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + C::kTU + 8 * k, dk + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
+          for (int k = 0; k < 8; ++k)  // D1 = S W^T
+            tc::mma_bf16_ts_w(tb + C::kTD1, tb + C::kTS16 + 8 * k, dw + (uint64_t)((k * 2048) >> 4), kIdesc64mn,
+                              k > 0 ? 1u : 0u);
+          tc::mma_commit_w(&bar_d1c[c]);
         }
-        tc::mma_commit_w(&bar_d4);
+        for (int c = 0; c < nch && ok; ++c) {
+          if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_uc[c], ci & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t tb = tmem + 256 * c;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // S += U K'
+            tc::mma_bf16_ts_w(tb + C::kTS32, tb + C::kTU + 8 * k, dk + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
+          tc::mma_commit_w(&bar_d4c[c]);
+        }
         tc::mma_commit_w(&bar_empty[s]);
         if (*(volatile int*)&abort_flag) ok = false;
       }
       if (!ok && lane == 0) fail();
       tc::mma_commit_w(&bar_done);
       tc::mbar_wait(&bar_done, 0, kWaitCycles);
+    } else {
+    // ------------------------------------------------ MMA: the state chain
+      // (the whole warp, converged: waits are voted and one elected lane issues; descriptors are built once
+      // per stage and a K step adds a constant to the start-address field)
+      {
+        bool ok = true;
+        // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi + I N_hi + I N_lo into the fp32
+        // state columns (I: a bf16 identity the rows place in the D1 columns, idle until the chunks)
+        for (int q = 1; q <= n_comb && ok; ++q) {
+          const int im = 2 * q - 2, in = 2 * q - 1;  // the items of M_q and N_q
+          if (!__all_sync(~0u, tc::mbar_wait(&bar_cb[im % 3], (im / 3) & 1, kWaitCycles)) ||
+              !__all_sync(~0u, tc::mbar_wait(&bar_cb[in % 3], (in / 3) & 1, kWaitCycles)) ||
+              !__all_sync(~0u, tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t sm = tc::smem_u32(smem);
+          const uint64_t dm0 = tc::sdesc_sw128(sm + (im % 3) * C::kStageBytes, 16384, 1024);
+          const uint64_t dn0 = tc::sdesc_sw128(sm + (in % 3) * C::kStageBytes, 16384, 1024);
+          const uint64_t dm1 = dm0 + (uint64_t)(32768 >> 4), dn1 = dn0 + (uint64_t)(32768 >> 4);
+#pragma unroll
+          for (int pr = 0; pr < 5; ++pr) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t a = pr == 2 ? C::kTSlo : pr >= 3 ? C::kTD1 : C::kTS16;
+              const uint64_t b = pr == 0 || pr == 2 ? dm0 : pr == 1 ? dm1 : pr == 3 ? dn0 : dn1;
+              tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + a + 8 * k, b + (uint64_t)((k * 2048) >> 4), kIdesc128mn,
+                                (pr > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          tc::mma_commit_w(&bar_pd);
+        }
+        for (int ci = 0; ci < n_c && ok; ++ci) {
+          const int s = ci % C::kStages;
+          const uint32_t sb = tc::smem_u32(stage(ci));
+          if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles)) ||
+              !__all_sync(~0u, tc::mbar_wait_spin(&bar_s, ci & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t dw = tc::sdesc_sw128(sb + C::kStW, 16384, 1024);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // D1 = S W^T   (K = d_k, 16 per step; A = bf16 S in TMEM)
+            tc::mma_bf16_ts_w(tmem + C::kTD1, tmem + C::kTS16 + 8 * k, dw + (uint64_t)((k * 2048) >> 4), kIdesc64mn,
+                              k > 0 ? 1u : 0u);
+          }
+          tc::mma_commit_w(&bar_d1);
+          if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_u, ci & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t dk = tc::sdesc_sw128(sb + C::kStK, 8192, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // S += U K'   (K = tokens; S already scaled by e^{gC})
+            tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + C::kTU + 8 * k, dk + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
+          }
+          tc::mma_commit_w(&bar_d4);
+          tc::mma_commit_w(&bar_empty[s]);
+          if (*(volatile int*)&abort_flag) ok = false;
+        }
+        if (!ok && lane == 0) fail();
+        tc::mma_commit_w(&bar_done);
+        tc::mbar_wait(&bar_done, 0, kWaitCycles);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (O && warp == C::kWarpOmma) {
     // -------------------------------------------------- MMA: the outputs
     // (converged warp, voted waits, one elected lane issues)
@@ -373,6 +435,164 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     }
     __syncwarp();
   } else if (warp < 4) {
+    if constexpr (!O) {
+      // ------------------------------------- rows of the N and M chains (or of group 0's one chain)
+      const int j = threadIdx.x;  // row of S == TMEM lane
+      const uint32_t lb = (uint32_t)(warp * 32) << 16;
+      const int nch = part == 0 ? 2 : 1;
+      bool ok = true;
+      // start states: chain 0 from zero (N) or the node's start slot (group 0), chain 1 the identity (M)
+      for (int c = 0; c < nch; ++c) {
+        const float* src = c == 0 && ik == kInitSlot ? p.state + (((size_t)init * p.H + h) * kD + j) * kD : nullptr;
+        const uint32_t tb = tmem + lb + 256 * c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t f[32], b[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = src ? reinterpret_cast<const float4*>(src)[q * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            f[4 * i] = __float_as_uint(v.x);
+            f[4 * i + 1] = __float_as_uint(v.y);
+            f[4 * i + 2] = __float_as_uint(v.z);
+            f[4 * i + 3] = __float_as_uint(v.w);
+          }
+          if (c == 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __float_as_uint(q * 32 + i == j ? 1.f : 0.f);
+          }
+          tc::tmem_st32(tb + C::kTS32 + q * 32, f);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+          tc::tmem_st16(tb + C::kTS16 + q * 16, b);
+        }
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      for (int c = 0; c < nch; ++c) tc::mbar_arrive(&bar_sc[c]);
+      for (int ci = 0; ci < n_c && ok; ++ci) {
+        const int s = ci % C::kStages;
+        const uint8_t* sb = stage(ci);
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles))) {
+          ok = false;
+          break;
+        }
+        const float ec = reinterpret_cast<const float*>(sb + C::kStG)[128];  // e^{gC}
+        // S <- e^{gC} S in place, both chains (overlaps their D1; D4 adds to it)
+        for (int c = 0; c < nch; ++c) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t f[32];
+            tc::tmem_ld32(tmem + lb + 256 * c + C::kTS32 + q * 32, f);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e2 = 0; e2 < 32; ++e2) f[e2] = __float_as_uint(ec * __uint_as_float(f[e2]));
+            tc::tmem_st32(tmem + lb + 256 * c + C::kTS32 + q * 32, f);
+          }
+        }
+        // U = Ut^T - D1 (chain 0) and U = -D1 (chain 1, Ut = 0), over the D1 columns once read
+        const uint8_t* utj = sb + C::kStUt + j * 128;
+        for (int c = 0; c < nch && ok; ++c) {
+          if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d1c[c], ci & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t tb = tmem + lb + 256 * c;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t d1[32], u2[16];
+            tc::tmem_ld32(tb + C::kTD1 + half * 32, d1);
+            uint4 uv[4];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              uv[c4] = c == 1 ? make_uint4(0u, 0u, 0u, 0u)
+                              : *reinterpret_cast<const uint4*>(utj + (((half * 4 + c4) ^ (j & 7)) << 4));
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const uint32_t w4[4] = {uv[c4].x, uv[c4].y, uv[c4].z, uv[c4].w};
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2)
+                u2[c4 * 4 + e2] = tc::pack_bf16x2(__uint_as_float(w4[e2] << 16) - __uint_as_float(d1[c4 * 8 + 2 * e2]),
+                                                  __uint_as_float(w4[e2] & 0xFFFF0000u) - __uint_as_float(d1[c4 * 8 + 2 * e2 + 1]));
+            }
+            tc::tmem_st16(tb + C::kTU + half * 16, u2);
+          }
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          tc::mbar_arrive(&bar_uc[c]);
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // Ut and the decay block are read
+        // the bf16 operand of each new state
+        for (int c = 0; c < nch && ok; ++c) {
+          if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d4c[c], ci & 1, kWaitCycles))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t f[32], b[16];
+            tc::tmem_ld32(tmem + lb + 256 * c + C::kTS32 + q * 32, f);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
+            tc::tmem_st16(tmem + lb + 256 * c + C::kTS16 + q * 16, b);
+          }
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          tc::mbar_arrive(&bar_sc[c]);
+        }
+      }
+      if (!ok) {
+        fail();
+      } else {
+        for (int c = 0; c < nch; ++c) {
+          const EndKind ekc = c == 0 ? ek : kEndScanM;
+          const uint32_t tb = tmem + lb + 256 * c;
+          if (ekc == kEndScanS) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(scanbuf(e1) + gdnws::kScanS) + j * kD);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t f[32];
+              tc::tmem_ld32(tb + C::kTS32 + q * 32, f);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[q * 8 + i] = make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]),
+                                             __uint_as_float(f[4 * i + 2]), __uint_as_float(f[4 * i + 3]));
+            }
+          } else {
+            // row j of M (or N) as the bf16 high and low images of an MN-major B operand: element (j, n) in
+            // slab n / 64, 128-byte row j, 16-byte chunk (n % 64) / 8 swizzled by j % 8
+            uint8_t* mh = scanbuf(e) + (ekc == kEndScanM ? gdnws::kScanMhi : gdnws::kScanN);
+            uint8_t* ml = mh + 32768;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t f[32];
+              tc::tmem_ld32(tb + C::kTS32 + q * 32, f);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8) {
+                const int n0 = q * 32 + c8 * 8;
+                const int off = (n0 >> 6) * 16384 + (j >> 3) * 1024 + (j & 7) * 128 + ((((n0 & 63) >> 3) ^ (j & 7)) << 4);
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float a = __uint_as_float(f[c8 * 8 + 2 * i]), b = __uint_as_float(f[c8 * 8 + 2 * i + 1]);
+                  hw[i] = tc::pack_bf16x2(a, b);
+                  lw[i] = tc::pack_bf16x2(a - __uint_as_float(hw[i] << 16), b - __uint_as_float(hw[i] & 0xFFFF0000u));
+                }
+                *reinterpret_cast<uint4*>(mh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(ml + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+              }
+            }
+          }
+        }
+      }
+    } else {
     // ---------------------------------------------------- rows of the state
     const int j = threadIdx.x;  // row of S == TMEM lane
     const uint32_t lb = (uint32_t)(warp * 32) << 16;
@@ -570,6 +790,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         }
       }
     }
+    }
   } else if (O) {
     // ------------------------------------------------------------- outputs
     const int j = threadIdx.x - 128;  // TMEM lane j
@@ -688,11 +909,11 @@ hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta,
   for (int lev = 0; lev < caps->max_levels && caps->max_segments > 0; ++lev) {
     Prm prm{meta, lev, H, n_slots, ws, scan, state, (__nv_bfloat16*)out, status};
     if (any_scan) {
-      gdn_chain_tc_kernel<false><<<dim3(3 * cap_scan, H), Cfg<false>::kThreads, smem_bytes<false>() + 1024, st>>>(
+      gdn_chain_tc_kernel<false><<<dim3(H, 2 * cap_scan), Cfg<false>::kThreads, smem_bytes<false>() + 1024, st>>>(
           mq, prm);
       HS_LAUNCH_CHECK("gdn_chain_tc (scan)");
     }
-    gdn_chain_tc_kernel<true><<<dim3(caps->max_segments + (any_scan ? cap_scan : 0), H), Cfg<true>::kThreads,
+    gdn_chain_tc_kernel<true><<<dim3(H, caps->max_segments + (any_scan ? cap_scan : 0)), Cfg<true>::kThreads,
                                   smem_bytes<true>() + 1024, st>>>(mq, prm);
     HS_LAUNCH_CHECK("gdn_chain_tc");
   }
