@@ -40,7 +40,7 @@ WORKLOAD = ("fork_attn trunk4096+8br U[16,64] GQA32/8 d128 page16 bf16 + 4-optio
 N_OPT = 4
 # DRAM traffic per launch from one ncu capture (profiles/fork_attn_tc2_attention_tree.md),
 # valid only while the kernel source still has the hash it was captured with.
-NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "36ab6286050e07b6", 57.02e6)}
+NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "f0175bd36b7e7baa", 56.45e6)}
 
 
 def ncu_traffic(kernel: str):

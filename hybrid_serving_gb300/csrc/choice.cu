@@ -19,6 +19,21 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxOpt = 32;
 
+// eight consecutive elements as floats (16-byte aligned source)
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&h)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[2 * i] = __uint_as_float(w[i] << 16);
+    h[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&h)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  h[0] = a.x; h[1] = a.y; h[2] = a.z; h[3] = a.w; h[4] = b.x; h[5] = b.y; h[6] = b.z; h[7] = b.w;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 choice_kernel(const int32_t* __restrict__ meta, const T* __restrict__ hidden, long long stride, int dim,
@@ -35,11 +50,40 @@ choice_kernel(const int32_t* __restrict__ meta, const T* __restrict__ hidden, lo
   }
   const T* hr = hidden + (size_t)row * stride;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int o = 0; o < n_opt; ++o) {
-    float acc = 0.f;
-    for (int e = threadIdx.x; e < dim; e += kThreads) acc = fmaf(hsd::to_f(hr[e]), W[(size_t)o * dim + e], acc);
-    acc = hsd::warp_sum(acc);
-    if (lane == 0) part[warp][o] = acc;
+  // eight elements at a time in 16-byte loads when the row and the option rows allow it, four options per
+  // pass over the row (the loads of a pass are independent, so they are in flight together)
+  const bool vec = dim % 8 == 0 && ((uintptr_t)hr & 15) == 0 && ((uintptr_t)W & 15) == 0;
+  for (int o0 = 0; o0 < n_opt; o0 += 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (vec) {
+      for (int e8 = threadIdx.x; e8 < dim / 8; e8 += kThreads) {
+        float h[8];
+        load8(hr + (size_t)e8 * 8, h);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (o0 + k < n_opt) {
+            const float4* w4 = reinterpret_cast<const float4*>(W + (size_t)(o0 + k) * dim + (size_t)e8 * 8);
+            const float4 a = w4[0], b = w4[1];
+            float s = acc[k];
+            s = fmaf(h[0], a.x, s); s = fmaf(h[1], a.y, s); s = fmaf(h[2], a.z, s); s = fmaf(h[3], a.w, s);
+            s = fmaf(h[4], b.x, s); s = fmaf(h[5], b.y, s); s = fmaf(h[6], b.z, s); s = fmaf(h[7], b.w, s);
+            acc[k] = s;
+          }
+        }
+      }
+    } else {
+      for (int e = threadIdx.x; e < dim; e += kThreads) {
+        const float he = hsd::to_f(hr[e]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (o0 + k < n_opt) acc[k] = fmaf(he, W[(size_t)(o0 + k) * dim + e], acc[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v = hsd::warp_sum(acc[k]);
+      if (lane == 0 && o0 + k < n_opt) part[warp][o0 + k] = v;
+    }
   }
   __syncthreads();
   if (threadIdx.x < n_opt) {

@@ -40,7 +40,9 @@ kv_page_write_kernel(const int32_t* __restrict__ meta, int hkv, int d, const T* 
   const int n_ref = M.h(H_N_PAGE_REF);
   constexpr int VEC = 16 / sizeof(T);
   const int vpt = hkv * d / VEC;  // 16-byte vectors per token, per tensor
-  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+  // one token per warp: the eight warps' metadata lookups (token -> node -> page) are in flight together
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int t = blockIdx.x * 8 + warp; t < n_tok; t += gridDim.x * 8) {
     const int32_t* tk = M.tok(t);
     const int seg = tk[T_SEG], idx = tk[T_IDX];
     if (seg < 0 || seg >= n_seg) { hsd::set_status(status, HS_DEV_BAD_META); continue; }
@@ -51,7 +53,7 @@ kv_page_write_kernel(const int32_t* __restrict__ meta, int hkv, int d, const T* 
     if (page < 0 || page >= n_pages) { hsd::set_status(status, HS_DEV_BAD_PAGE); continue; }
     const int row = idx % kPage;
     const bool last = idx == sg[S_LEN] - 1;
-    for (int j = threadIdx.x; j < 2 * vpt; j += blockDim.x) {
+    for (int j = lane; j < 2 * vpt; j += 32) {
       const int which = j >= vpt;
       const int jj = which ? j - vpt : j;
       const int e = jj * VEC;
@@ -211,7 +213,8 @@ hs_status launch_attn_simt(const hs_round_caps* caps, const void* meta, int hq, 
 template <typename T>
 hs_status launch_kv_write(const hs_round_caps* caps, const void* meta, int hkv, int d, const void* k_new,
                           const void* v_new, void* kp, void* vp, int n_pages, int32_t* status, cudaStream_t st) {
-  int grid = caps->max_tokens < 152 * 16 ? caps->max_tokens : 152 * 16;
+  const int want = (caps->max_tokens + 7) / 8;  // eight tokens per block
+  const int grid = want < 152 * 8 ? want : 152 * 8;
   if (grid <= 0) return HS_OK;
   kv_page_write_kernel<T><<<grid, 256, 0, st>>>((const int32_t*)meta, hkv, d, (const T*)k_new, (const T*)v_new,
                                                 (T*)kp, (T*)vp, n_pages, status);
