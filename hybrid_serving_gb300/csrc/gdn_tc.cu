@@ -24,8 +24,8 @@
 //               factors from the workspace, TMA boxes of Q, up to 3 chunks
 //               ahead;
 //   warp 9      issues the state chain's MMAs (D1, then D4 as soon as U is
-//               written) from one thread;
-//   warp 10     issues the output MMAs (D2, D3) from one thread, so that they
+//               written), converged, from one elected lane;
+//   warp 10     issues the output MMAs (D2, D3) the same way, so that they
 //               never queue in front of the chain's;
 //   warps 0..3  rows of the state (thread j = TMEM lane j = row j of S):
 //               U, the scaling of S, the bf16 copy of S;
@@ -35,6 +35,13 @@
 // Operands are bf16, accumulation fp32.  The four hand-offs of the state chain
 // (S -> D1 -> U -> D4 -> S) poll their barriers without suspending.  Every
 // wait is bounded (HS_DEV_TIMEOUT).
+//
+// A long node (24 chunks or more) is split into groups of consecutive chunks
+// for a two-level scan of the affine chunk map S -> S M_c + N_c: a first pass
+// without outputs (the output-less variant: per group its N from the zero
+// state and its M from the identity with Ut = 0, two chains in one CTA; and
+// the end of group 0), then every group with outputs from its start state
+// S_g = (...(S_1 M_1 + N_1)...) M_{g-1} + N_{g-1}, formed on tensor cores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
