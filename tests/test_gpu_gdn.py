@@ -134,3 +134,14 @@ def test_state_checkpoint_copy_and_bad_slot():
                          run.ws, run.status)
     torch.cuda.synchronize()
     assert int(run.status.item()) == 2  # HS_DEV_BAD_SLOT
+
+
+def test_scan_group_counts():
+    """Long nodes split into 2, 3, 4, 5, 7 and 8 scan groups (24 .. 100 chunks of 64; the last one
+    ragged) in one round: the first pass (group 0's end, each later group's N and M as two chains
+    in one CTA), the start states combined from them and the replay with outputs, against the
+    step-by-step recurrence; a branch after each trunk continues from the trunk's end state."""
+    lens = [24 * 64, 36 * 64 - 5, 48 * 64, 60 * 64 + 17, 84 * 64, 100 * 64 - 33]
+    tree = synth.Tree([synth.fork_tree(n, [37]) for n in lens])
+    inp = synth.gdn_inputs(tree, 2, 128, 128, seed=3100, bf16=True, law="softplus")
+    _check(tree, inp, torch.bfloat16, TOL_BF16)
