@@ -38,6 +38,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 choice_kernel(const int32_t* __restrict__ meta, const T* __restrict__ hidden, long long stride, int dim,
               const float* __restrict__ W, int n_opt, float* __restrict__ logprobs, int32_t* status) {
+  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
+  hsd::pdl_trigger();
   __shared__ float part[kThreads / 32][kMaxOpt];
   __shared__ float z[kMaxOpt];
   Meta M{meta};
@@ -117,13 +119,13 @@ extern "C" hs_status hs_choice_logprobs(const hs_round_caps* caps, const void* d
   if (caps->max_readouts <= 0) return HS_OK;
   cudaStream_t st = (cudaStream_t)stream;
   if (dt == HS_BF16)
-    choice_kernel<__nv_bfloat16><<<caps->max_readouts, kThreads, 0, st>>>(
-        (const int32_t*)dev_meta, (const __nv_bfloat16*)hidden, hidden_stride, hidden_dim, option_rows, n_opt,
-        logprobs, dev_status);
+    hsd::launch_pdl(choice_kernel<__nv_bfloat16>, dim3(caps->max_readouts), dim3(kThreads), 0, st,
+                    (const int32_t*)dev_meta, (const __nv_bfloat16*)hidden, (long long)hidden_stride, (int)hidden_dim,
+                    option_rows, (int)n_opt, logprobs, dev_status);
   else
-    choice_kernel<float><<<caps->max_readouts, kThreads, 0, st>>>((const int32_t*)dev_meta, (const float*)hidden,
-                                                                  hidden_stride, hidden_dim, option_rows, n_opt,
-                                                                  logprobs, dev_status);
+    hsd::launch_pdl(choice_kernel<float>, dim3(caps->max_readouts), dim3(kThreads), 0, st, (const int32_t*)dev_meta,
+                    (const float*)hidden, (long long)hidden_stride, (int)hidden_dim, option_rows, (int)n_opt, logprobs,
+                    dev_status);
   HS_LAUNCH_CHECK("choice_logprobs");
   return HS_OK;
 }

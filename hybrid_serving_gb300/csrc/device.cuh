@@ -9,6 +9,13 @@
 
 namespace hsd {
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may start while the kernel before it in
+// the stream drains.  Such a kernel calls pdl_wait() before it touches global memory (it returns once every
+// earlier kernel in the stream has completed and its writes are visible), then pdl_trigger(), which lets the
+// next kernel start launching once all of this kernel's blocks have begun.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // First error wins; kernels skip the offending work instead of trapping.
 __device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
   if (st) atomicCAS(st, 0, code);
@@ -68,6 +75,26 @@ struct Meta {
 }  // namespace hsd
 
 // Host: check a launch, record failures.
+namespace hsd {
+// Launch with programmatic stream serialization allowed (see pdl_wait); errors surface through
+// cudaGetLastError as for a <<<>>> launch.
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+}  // namespace hsd
+
 #define HS_LAUNCH_CHECK(what)                                                          \
   do {                                                                                 \
     cudaError_t e__ = cudaGetLastError();                                              \

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(256)
 kv_page_write_kernel(const int32_t* __restrict__ meta, int hkv, int d, const T* __restrict__ k_new,
                      const T* __restrict__ v_new, T* __restrict__ kp, T* __restrict__ vp, int n_pages,
                      int32_t* status) {
+  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
+  hsd::pdl_trigger();
   Meta M{meta};
   const int n_tok = M.h(H_N_TOK);
   const int n_seg = M.h(H_N_SEG);
@@ -216,8 +218,8 @@ hs_status launch_kv_write(const hs_round_caps* caps, const void* meta, int hkv, 
   const int want = (caps->max_tokens + 7) / 8;  // eight tokens per block
   const int grid = want < 152 * 8 ? want : 152 * 8;
   if (grid <= 0) return HS_OK;
-  kv_page_write_kernel<T><<<grid, 256, 0, st>>>((const int32_t*)meta, hkv, d, (const T*)k_new, (const T*)v_new,
-                                                (T*)kp, (T*)vp, n_pages, status);
+  hsd::launch_pdl(kv_page_write_kernel<T>, dim3(grid), dim3(256), 0, st, (const int32_t*)meta, hkv, d,
+                  (const T*)k_new, (const T*)v_new, (T*)kp, (T*)vp, n_pages, status);
   HS_LAUNCH_CHECK("kv_page_write");
   return HS_OK;
 }

@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
                     const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                     const __grid_constant__ CUtensorMap tm_v128, const Params p) {
+  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
+  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kf[kStages], bar_vf[kStages], bar_ke[kStages], bar_ve[kStages];
   __shared__ uint64_t bar_sf[2], bar_pf[2], bar_pv[2], bar_done, bar_x;
@@ -530,6 +532,8 @@ __global__ void __launch_bounds__(pair::kThreads, 1)
 fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
                      const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                      const __grid_constant__ CUtensorMap tm_v128, const Params p) {
+  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
+  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qe, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2];
   __shared__ uint64_t bar_sf[2][2], bar_pf[2][2], bar_pv[2], bar_done;
@@ -1021,11 +1025,11 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
         return hs::fail(HS_ECUDA, "fork_attn_tc: cannot read the SM count");
     }
     const int items = caps->max_tiles * (hq / 2);
-    fork_attn_tc2_kernel<<<dim3(items < n_sm ? items : n_sm), pair::kThreads, pair::kSmemBytes + 1024, st>>>(
-        m_q, m_k16, m_k128, m_v16, m_v128, prm);
+    hsd::launch_pdl(fork_attn_tc2_kernel, dim3(items < n_sm ? items : n_sm), dim3(pair::kThreads),
+                    pair::kSmemBytes + 1024, st, m_q, m_k16, m_k128, m_v16, m_v128, prm);
   } else {
-    fork_attn_tc_kernel<<<dim3(caps->max_tiles * hq), kThreads, kSmemBytes + 1024, st>>>(m_q, m_k16, m_k128, m_v16,
-                                                                                          m_v128, prm);
+    hsd::launch_pdl(fork_attn_tc_kernel, dim3(caps->max_tiles * hq), dim3(kThreads), kSmemBytes + 1024, st,
+                    m_q, m_k16, m_k128, m_v16, m_v128, prm);
   }
   HS_LAUNCH_CHECK("fork_attn_tc");
   return HS_OK;

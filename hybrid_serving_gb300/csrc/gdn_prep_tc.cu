@@ -100,6 +100,8 @@ __device__ __forceinline__ void write_t_operand(uint8_t* bt, int j, const float 
 __global__ void __launch_bounds__(kThreads, 2)
 gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const Prm p) {
+  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
+  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_in, bar_d, bar_b1, bar_w1, bar_b2, bar_w2;
   __shared__ uint32_t tmem_slot;
@@ -421,7 +423,8 @@ hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, 
     configured = true;
   }
   Prm prm{meta, H, alpha, beta, ws, status};
-  gdn_chunk_prep_tc_kernel<<<dim3(caps->max_chunks, (H + 1) / 2), kThreads, kSmem + 1024, st>>>(mq, mk, mv, prm);
+  hsd::launch_pdl(gdn_chunk_prep_tc_kernel, dim3(caps->max_chunks, (H + 1) / 2), dim3(kThreads), kSmem + 1024, st, mq,
+                  mk, mv, prm);
   HS_LAUNCH_CHECK("gdn_chunk_prep_tc");
   return HS_OK;
 }

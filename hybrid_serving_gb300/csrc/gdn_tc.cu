@@ -124,6 +124,8 @@ template <bool O>
 __global__ void __launch_bounds__(Cfg<O>::kThreads, Cfg<O>::kMinBlocks)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   using C = Cfg<O>;
+  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
+  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_s, bar_u, bar_of;
   __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2, bar_cb[3], bar_ps, bar_pd;
@@ -916,12 +918,12 @@ hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta,
   for (int lev = 0; lev < caps->max_levels && caps->max_segments > 0; ++lev) {
     Prm prm{meta, lev, H, n_slots, ws, scan, state, (__nv_bfloat16*)out, status};
     if (any_scan) {
-      gdn_chain_tc_kernel<false><<<dim3(H, 2 * cap_scan), Cfg<false>::kThreads, smem_bytes<false>() + 1024, st>>>(
-          mq, prm);
+      hsd::launch_pdl(gdn_chain_tc_kernel<false>, dim3(H, 2 * cap_scan), dim3(Cfg<false>::kThreads),
+                      smem_bytes<false>() + 1024, st, mq, prm);
       HS_LAUNCH_CHECK("gdn_chain_tc (scan)");
     }
-    gdn_chain_tc_kernel<true><<<dim3(H, caps->max_segments + (any_scan ? cap_scan : 0)), Cfg<true>::kThreads,
-                                  smem_bytes<true>() + 1024, st>>>(mq, prm);
+    hsd::launch_pdl(gdn_chain_tc_kernel<true>, dim3(H, caps->max_segments + (any_scan ? cap_scan : 0)),
+                    dim3(Cfg<true>::kThreads), smem_bytes<true>() + 1024, st, mq, prm);
     HS_LAUNCH_CHECK("gdn_chain_tc");
   }
   return HS_OK;
