@@ -140,8 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
                     const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                     const __grid_constant__ CUtensorMap tm_v128, const Params p) {
-  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
-  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kf[kStages], bar_vf[kStages], bar_ke[kStages], bar_ve[kStages];
   __shared__ uint64_t bar_sf[2], bar_pf[2], bar_pv[2], bar_done, bar_x;
@@ -184,6 +182,13 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // (launched with launch_pdl) Everything above reads only the round's metadata, which host copies write;
+  // pages, inputs, workspace and state written by the earlier kernels in the stream are touched only after
+  // the wait.  The next kernel may start launching only now, once every block of this one holds its tensor
+  // memory: a block of the next kernel that took the columns first, then waited here for this kernel, would
+  // block this kernel's allocation for good.
+  hsd::pdl_trigger();
+  hsd::pdl_wait();
 
   Cursor cur;
   cur.init(M, tl);
@@ -532,8 +537,6 @@ __global__ void __launch_bounds__(pair::kThreads, 1)
 fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
                      const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
                      const __grid_constant__ CUtensorMap tm_v128, const Params p) {
-  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
-  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qe, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2];
   __shared__ uint64_t bar_sf[2][2], bar_pf[2][2], bar_pv[2], bar_done;
@@ -579,6 +582,13 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // (launched with launch_pdl) Everything above reads only the round's metadata, which host copies write;
+  // pages, inputs, workspace and state written by the earlier kernels in the stream are touched only after
+  // the wait.  The next kernel may start launching only now, once every block of this one holds its tensor
+  // memory: a block of the next kernel that took the columns first, then waited here for this kernel, would
+  // block this kernel's allocation for good.
+  hsd::pdl_trigger();
+  hsd::pdl_wait();
   const int n_ref = M.h(H_N_PAGE_REF);
   const int32_t* refs = M.page_ref();
 

@@ -100,8 +100,6 @@ __device__ __forceinline__ void write_t_operand(uint8_t* bt, int j, const float 
 __global__ void __launch_bounds__(kThreads, 2)
 gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const Prm p) {
-  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
-  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_in, bar_d, bar_b1, bar_w1, bar_b2, bar_w2;
   __shared__ uint32_t tmem_slot;
@@ -132,6 +130,13 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // (launched with launch_pdl) Everything above reads only the round's metadata, which host copies write;
+  // pages, inputs, workspace and state written by the earlier kernels in the stream are touched only after
+  // the wait.  The next kernel may start launching only now, once every block of this one holds its tensor
+  // memory: a block of the next kernel that took the columns first, then waited here for this kernel, would
+  // block this kernel's allocation for good.
+  hsd::pdl_trigger();
+  hsd::pdl_wait();
 
   if (warp == 4) {
     // ------------------------------------------------------- copies and MMAs

@@ -124,8 +124,6 @@ template <bool O>
 __global__ void __launch_bounds__(Cfg<O>::kThreads, Cfg<O>::kMinBlocks)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   using C = Cfg<O>;
-  hsd::pdl_wait();  // (launched with launch_pdl: nothing global before this)
-  hsd::pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_s, bar_u, bar_of;
   __shared__ uint64_t bar_d1, bar_d4, bar_d2, bar_d23, bar_done, bar_done2, bar_cb[3], bar_ps, bar_pd;
@@ -229,6 +227,13 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // (launched with launch_pdl) Everything above reads only the round's metadata, which host copies write;
+  // pages, inputs, workspace and state written by the earlier kernels in the stream are touched only after
+  // the wait.  The next kernel may start launching only now, once every block of this one holds its tensor
+  // memory: a block of the next kernel that took the columns first, then waited here for this kernel, would
+  // block this kernel's allocation for good.
+  hsd::pdl_trigger();
+  hsd::pdl_wait();
   auto fail = [&]() {
     hsd::set_status(p.status, HS_DEV_TIMEOUT);
     atomicExch(&abort_flag, 1);
