@@ -149,8 +149,8 @@ class Round:
         check(lib.hs_round_readout_rows(self._h, buf, n.value, C.byref(n)))
         return list(buf[:n.value])
 
-    def release(self, pool: PagePool, keep: Sequence[int] = ()):
-        check(lib.hs_round_release(self._h, pool._h, _i32arr(keep), len(keep)))
+    def release(self, pool: Optional[PagePool], keep: Sequence[int] = ()):
+        check(lib.hs_round_release(self._h, pool._h if pool is not None else None, _i32arr(keep), len(keep)))
 
 
 # ---------------------------------------------------------------------------

@@ -117,10 +117,20 @@ extern "C" hs_status hs_page_pool_refcount(const hs_page_pool* p, int32_t page, 
 }
 
 extern "C" hs_status hs_page_pool_decref(hs_page_pool* p, const int32_t* pages, int32_t n) {
-  HS_CHECK_ARG(p && (pages || n == 0), "null argument");
+  HS_CHECK_ARG(p && n >= 0 && (pages || n == 0), "null argument");
   for (int32_t i = 0; i < n; ++i) {
     HS_CHECK_ARG(pages[i] >= 0 && pages[i] < p->n_pages && p->ref[pages[i]] > 0,
                  "page %d is not live", pages[i]);
+  }
+  // a page listed k times must hold at least k references (checked before any change)
+  std::vector<int32_t> sorted(pages, pages + n);
+  std::sort(sorted.begin(), sorted.end());
+  for (int32_t i = 0; i < n;) {
+    int32_t j = i;
+    while (j < n && sorted[j] == sorted[i]) ++j;
+    HS_CHECK_ARG(j - i <= p->ref[sorted[i]], "page %d listed %d times but holds %d references", sorted[i], j - i,
+                 p->ref[sorted[i]]);
+    i = j;
   }
   for (int32_t i = 0; i < n; ++i) p->decref(pages[i]);
   return HS_OK;
@@ -152,6 +162,7 @@ struct hs_round {
   int32_t n_requests = 0;
   bool finalized = false;
   bool released = false;
+  hs_page_pool* pool = nullptr;  // the pool finalize allocated from (NULL: none)
   std::vector<int32_t> blob;
   hs_round_info info{};
   std::vector<int32_t> readouts;
@@ -266,14 +277,13 @@ extern "C" hs_status hs_round_attach_history(hs_round* r, int32_t seg, int32_t n
   HS_CHECK_ARG(r->segs[seg].parent < 0, "only a root has history (node %d has a parent)", seg);
   HS_CHECK_ARG(n_spans >= 0 && (n_spans == 0 || (ntok && pages)), "bad history spans");
   Seg& s = r->segs[seg];
-  s.hist_ntok.clear();
-  s.hist_pages.clear();
-  int32_t np = 0;
+  int64_t np = 0;
   for (int32_t i = 0; i < n_spans; ++i) {
     HS_CHECK_ARG(ntok[i] >= 1, "history span %d is empty", i);
     np += (ntok[i] + kPage - 1) / kPage;
-    s.hist_ntok.push_back(ntok[i]);
   }
+  HS_CHECK_ARG(np < ((int64_t)1 << 30), "history of %lld pages is too long", (long long)np);
+  s.hist_ntok.assign(ntok, ntok + n_spans);
   s.hist_pages.assign(pages, pages + np);
   return HS_OK;
 }
@@ -284,6 +294,10 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
   std::vector<Seg>& S = r->segs;
   const int32_t n = (int32_t)S.size();
   HS_CHECK_ARG(n > 0, "empty round");
+  for (auto& s : S) {  // a finalize retried after an error starts again from the nodes as added
+    s.hist_spans.clear();
+    s.pages.clear();
+  }
 
   // levels (parents precede children by construction)
   int32_t n_levels = 0;
@@ -314,12 +328,15 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     if (s.parent >= 0) {
       s.pos0 = S[s.parent].pos0 + S[s.parent].n_tok;
     } else {
-      int32_t hist = 0;
+      int64_t hist = 0;
       for (int32_t t : s.hist_ntok) hist += t;
       if (!s.hist_ntok.empty() && s.resume_pos >= 0 && hist != s.resume_pos)
-        return hs::fail(HS_EINVAL, "node %d: history holds %d tokens but resumes at %d", i, hist, s.resume_pos);
-      s.pos0 = s.resume_pos >= 0 ? s.resume_pos : hist;
+        return hs::fail(HS_EINVAL, "node %d: history holds %lld tokens but resumes at %d", i, (long long)hist,
+                        s.resume_pos);
+      if (hist >= ((int64_t)1 << 31)) return hs::fail(HS_EINVAL, "node %d: history too long", i);
+      s.pos0 = s.resume_pos >= 0 ? s.resume_pos : (int32_t)hist;
     }
+    if ((int64_t)s.pos0 + s.n_tok >= ((int64_t)1 << 31)) return hs::fail(HS_EINVAL, "node %d: positions overflow", i);
   }
 
   // pages: history pages are referenced, own pages allocated
@@ -443,9 +460,6 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     std::vector<int32_t> idx(n_tiles);
     for (int32_t i = 0; i < n_tiles; ++i) idx[i] = i;
     std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
-      int32_t wa = tiles[a * kTileWords + TL_WORK] * tiles[a * kTileWords + TL_N_ROWS];
-      int32_t wb = tiles[b * kTileWords + TL_WORK] * tiles[b * kTileWords + TL_N_ROWS];
-      (void)wa; (void)wb;
       return tiles[a * kTileWords + TL_WORK] > tiles[b * kTileWords + TL_WORK];
     });
     std::vector<int32_t> sorted(tiles.size());
@@ -654,8 +668,8 @@ extern "C" hs_status hs_round_finalize(hs_round* r, hs_page_pool* pool, int32_t 
   std::vector<int32_t> allocated;
   hs_status st = build(r, pool, temp_slot0, n_temp_slots, allocated);
   if (st != HS_OK) {
-    if (pool)
-      for (int32_t p : allocated) pool->decref(p);
+    if (pool)  // in reverse, so that the free list is restored in its old order
+      for (auto it = allocated.rbegin(); it != allocated.rend(); ++it) pool->decref(*it);
     for (auto& s : r->segs) s.pages.clear();
     return st;
   }
@@ -666,6 +680,7 @@ extern "C" hs_status hs_round_finalize(hs_round* r, hs_page_pool* pool, int32_t 
         r->hist_refs.push_back(p);
       }
   }
+  r->pool = pool;
   r->finalized = true;
   return HS_OK;
 }
@@ -735,19 +750,22 @@ extern "C" hs_status hs_round_readout_rows(const hs_round* r, int32_t* rows, int
 }
 
 extern "C" hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep, int32_t n_keep) {
-  HS_CHECK_ARG(r && pool, "null argument");
+  HS_CHECK_ARG(r, "null round");
   HS_CHECK_ARG(r->finalized, "round not finalized");
   HS_CHECK_ARG(!r->released, "round already released");
+  HS_CHECK_ARG(pool == r->pool || (!r->pool && !pool), "not the pool the round was finalized with");
   HS_CHECK_ARG(n_keep >= 0 && (n_keep == 0 || keep), "bad keep list");
   std::vector<char> kept(r->segs.size(), 0);
   for (int32_t i = 0; i < n_keep; ++i) {
     HS_CHECK_ARG(keep[i] >= 0 && keep[i] < (int32_t)r->segs.size(), "unknown node %d", keep[i]);
     kept[keep[i]] = 1;
   }
-  for (size_t i = 0; i < r->segs.size(); ++i)
-    if (!kept[i])
-      for (int32_t p : r->segs[i].pages) pool->decref(p);
-  for (int32_t p : r->hist_refs) pool->decref(p);
+  if (pool) {
+    for (size_t i = 0; i < r->segs.size(); ++i)
+      if (!kept[i])
+        for (int32_t p : r->segs[i].pages) pool->decref(p);
+    for (int32_t p : r->hist_refs) pool->decref(p);
+  }
   r->hist_refs.clear();
   r->released = true;
   return HS_OK;

@@ -98,7 +98,9 @@ void hs_page_pool_destroy(hs_page_pool* pool);
 /* number of free pages and of pages with refcount > 0 */
 hs_status hs_page_pool_stats(const hs_page_pool* pool, int32_t* n_free, int32_t* n_live);
 hs_status hs_page_pool_refcount(const hs_page_pool* pool, int32_t page, int32_t* ref);
-/* drop one reference of each page (pages reaching 0 return to the free list) */
+/* Drop one reference per listed page (pages reaching 0 return to the free
+ * list).  A page may be listed k times if it holds >= k references; any
+ * invalid entry fails the whole call with HS_EINVAL before anything changes. */
 hs_status hs_page_pool_decref(hs_page_pool* pool, const int32_t* pages, int32_t n);
 
 /* ------------------------------------------------------------------------ */
@@ -110,6 +112,8 @@ typedef struct hs_round hs_round;
 #define HS_SEG_NO_READOUT 2    /* suppress the default readout of a leaf */
 
 hs_status hs_round_create(const hs_round_caps* caps, hs_round** out);
+/* Frees the host object only: page references a finalized round holds stay
+ * until hs_round_release drops them. */
 void hs_round_destroy(hs_round* r);
 
 /* Add a node.  parent_seg = -1 starts a new request (its trunk).  Nodes of
@@ -142,7 +146,8 @@ hs_status hs_round_set_conv_window(hs_round* r, int32_t seg, int32_t window_row0
 /* Lay out the stream, allocate each node's own KV pages from `pool` (may be
  * NULL for GDN-only rounds), assign temporary GDN state slots
  * [temp_slot0, temp_slot0 + n_temp_slots) to inner nodes, and build the
- * metadata.  Errors leave the pool unchanged. */
+ * metadata.  Errors leave the pool unchanged, and a finalize retried after an
+ * error (e.g. with more temporary slots) starts again from the nodes as added. */
 hs_status hs_round_finalize(hs_round* r, hs_page_pool* pool, int32_t temp_slot0, int32_t n_temp_slots);
 
 /* Bytes of the device metadata buffer for these caps (fixed per caps). */
@@ -171,7 +176,8 @@ hs_status hs_round_readout_rows(const hs_round* r, int32_t* rows, int32_t cap, i
 /* Commit/abort (ForkServe README: commit keeps one path, abort decrefs the
  * residuals).  Drops the round's page references for every node NOT listed
  * in keep_segs and for the history pages; kept nodes' own pages stay live
- * (one reference each, now owned by the caller). */
+ * (one reference each, now owned by the caller).  `pool` must be the pool the
+ * round was finalized with (NULL if it was finalized without one). */
 hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep_segs, int32_t n_keep);
 
 /* ------------------------------------------------------------------------ */

@@ -321,3 +321,56 @@ def test_device_status_codes_map_to_edevice():
     for code, words in [(1, "page"), (2, "slot"), (3, "metadata"), (4, "wait"), (99, "unknown")]:
         assert _lib.lib.hs_check_status(C.byref(C.c_int32(code))) == _lib.HS_EDEVICE
         assert words in _lib.last_error(), (code, _lib.last_error())
+
+
+
+def _held_pages(pool, n_tok):
+    """Pages of one committed node (n_tok tokens) that stay live in `pool`."""
+    R = api.Round(api.round_caps_for(n_tok, 1, 1))
+    root = R.add_segment(-1, n_tok)
+    R.finalize(pool)
+    pages = R.segment_pages(root)
+    R.release(pool, keep=[root])
+    return pages
+
+
+def test_finalize_retry_and_release_checks():
+    """A finalize that failed (too few temporary slots) and is retried builds
+    the same metadata as a first finalize; decref rejects a page listed more
+    often than it is referenced; release wants the round's own pool."""
+    def make(hist_pages):
+        R = api.Round(api.round_caps_for(200, 6, 3, n_hist_spans=2, n_hist_pages=4))
+        root = R.add_segment(-1, 40)
+        R.attach_history(root, [20, 12], hist_pages)
+        R.gdn_state_resume(root, 3, 32)
+        mid = R.add_segment(root, 30)
+        R.add_segment(mid, 9)
+        R.add_segment(mid, 17)
+        R.add_segment(root, 5)
+        return R
+    pool, other = api.PagePool(64), api.PagePool(64)
+    held = _held_pages(pool, 40)
+    assert held == _held_pages(other, 40) and pool.stats() == (61, 3)
+    R0 = make(held)
+    R0.finalize(other, 8, 4)
+    want = R0.pack().clone()
+    R = make(held)
+    with pytest.raises(_lib.HsError) as e:
+        R.finalize(pool, 8, 1)                       # two inner nodes, one temporary slot
+    assert e.value.code == _lib.HS_ECAPACITY
+    assert pool.stats() == (61, 3)
+    R.finalize(pool, 8, 4)
+    assert np.array_equal(R.pack().numpy(), want.numpy())
+    with pytest.raises(_lib.HsError):
+        R.release(other)                             # not the round's pool
+    with pytest.raises(_lib.HsError):
+        pool.decref([held[0], held[0], held[0]])     # two references, listed three times
+    assert [pool.refcount(p) for p in held] == [2, 2, 2]
+    R.release(pool)
+    assert [pool.refcount(p) for p in held] == [1, 1, 1] and pool.stats() == (61, 3)
+    pool.decref(held)
+    assert pool.stats() == (64, 0)
+    Rn = api.Round(api.round_caps_for(10, 1, 1))
+    Rn.add_segment(-1, 4)
+    Rn.finalize(None)
+    Rn.release(None)
