@@ -251,6 +251,7 @@ extern "C" hs_status hs_rope_apply(const hs_round_caps* caps, const void* dev_me
                                    int32_t* dev_status, void* stream) {
   HS_CHECK_ARG(caps && dev_meta && x && table, "null argument");
   HS_CHECK_ARG(n_heads > 0 && d > 0 && d % 2 == 0 && col0 >= 0 && ldx >= col0 + (int64_t)n_heads * d, "bad shape");
+  HS_CHECK_ARG(max_pos > 0 && ((uintptr_t)table & 7) == 0, "the cos/sin table must be 8-byte aligned");
   if (hs_status s = need_device()) return s;
   if (caps->max_tokens <= 0) return HS_OK;
   rope_kernel<<<caps->max_tokens, 128, 0, (cudaStream_t)stream>>>((const int32_t*)dev_meta, (__nv_bfloat16*)x, ldx,
@@ -290,6 +291,7 @@ extern "C" hs_status hs_swiglu(const void* gu, int64_t ldg, int32_t T, int32_t F
   HS_CHECK_ARG(gu && out, "null argument");
   HS_CHECK_ARG(T >= 0 && F > 0 && F % 8 == 0 && ldg >= 2 * (int64_t)F && ldo >= F && ldg % 8 == 0 && ldo % 8 == 0,
                "bad shape");
+  HS_CHECK_ARG(al16(gu) && al16(out), "16-byte alignment required");
   if (hs_status s = need_device()) return s;
   if (T == 0) return HS_OK;
   swiglu_kernel<<<T, 256, 0, (cudaStream_t)stream>>>((const __nv_bfloat16*)gu, ldg, T, F, (__nv_bfloat16*)out, ldo);
@@ -301,6 +303,7 @@ extern "C" hs_status hs_copy_rows(const void* src, int64_t lds, const int32_t* s
                                   const int32_t* dst_rows, int32_t n, int32_t width_bytes, void* stream) {
   HS_CHECK_ARG(src && dst && (n == 0 || (src_rows && dst_rows)), "null argument");
   HS_CHECK_ARG(n >= 0 && width_bytes > 0 && width_bytes % 16 == 0 && lds % 16 == 0 && ldd % 16 == 0, "bad shape");
+  HS_CHECK_ARG(al16(src) && al16(dst), "16-byte alignment required");
   if (hs_status s = need_device()) return s;
   if (n == 0) return HS_OK;
   copy_rows_kernel<<<n, 128, 0, (cudaStream_t)stream>>>((const uint8_t*)src, lds, src_rows, (uint8_t*)dst, ldd,

@@ -307,7 +307,8 @@ hs_status hs_rope_table(float* host_table, int32_t max_pos, int32_t d, double th
 /* In place: rotate-half rotary embedding of n_heads heads of width d at
  * column col0 of x [Tcap, ldx], each token at its standalone position
  * (node pos0 + index; Flide section 3.2).  table: device copy of
- * hs_rope_table. */
+ * hs_rope_table (8-byte aligned); a position outside [0, max_pos) sets
+ * HS_DEV_BAD_META and leaves the token unrotated. */
 hs_status hs_rope_apply(const hs_round_caps* caps, const void* dev_meta, void* x, int64_t ldx, int32_t col0,
                         int32_t n_heads, int32_t d, const float* table, int32_t max_pos, int32_t* dev_status,
                         void* stream);
@@ -322,11 +323,14 @@ hs_status hs_rope_apply(const hs_round_caps* caps, const void* dev_meta, void* x
 hs_status hs_gdn_prep(const hs_round_caps* caps, const void* dev_meta, const void* proj, int64_t ldp,
                       const void* window, int64_t ldw, int32_t n_window_rows, const void* conv_w, int32_t h, int32_t d,
                       void* q, void* k, void* v, float* alpha, float* beta, int32_t* dev_status, void* stream);
-/* out[t, i] = silu(gu[t, i]) * gu[t, F + i] */
+/* out[t, i] = silu(gu[t, i]) * gu[t, F + i]; bf16, F, ldg, ldo multiples
+ * of 8, gu and out 16-byte aligned. */
 hs_status hs_swiglu(const void* gu, int64_t ldg, int32_t T, int32_t F, void* out, int64_t ldo, void* stream);
 /* dst row dst_rows[i] = src row src_rows[i] (device int32 row lists; row
- * strides lds, ldd and width_bytes in BYTES, multiples of 16; a
- * checkpoint's convolution window, for instance). */
+ * strides lds, ldd and width_bytes in BYTES, multiples of 16; src and dst
+ * 16-byte aligned; a checkpoint's convolution window, for instance).  The
+ * row lists are device data the host cannot check: each entry must index a
+ * row inside its buffer. */
 hs_status hs_copy_rows(const void* src, int64_t lds, const int32_t* src_rows, void* dst, int64_t ldd,
                        const int32_t* dst_rows, int32_t n, int32_t width_bytes, void* stream);
 
