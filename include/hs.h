@@ -66,6 +66,10 @@ typedef enum { HS_F32 = 0, HS_BF16 = 1 } hs_dtype;
 /* every launch grid, so rounds with the same caps reuse the same launch    */
 /* shapes (Flide section 3.3.2: launches fixed by capacity, the tree lives  */
 /* in GPU-resident metadata).                                               */
+/* Every device call below takes the caps of the round whose metadata sits  */
+/* in dev_meta: grids and the GDN workspace are sized from them, and the    */
+/* kernels trust the metadata's counts up to them.  Passing other caps is   */
+/* a caller error the host cannot detect.                                   */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t max_tokens;      /* stream tokens T */
