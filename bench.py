@@ -38,6 +38,7 @@ GDN = dict(h=16, d=128, seed=3000)
 WORKLOAD = ("fork_attn trunk4096+8br U[16,64] GQA32/8 d128 page16 bf16 + 4-option readout; "
             "gdn_fork trunk8192+16br U[8,128] H16 d128 chunk64 fp32-state bf16")
 N_OPT = 4
+METRIC = "tree-prefill tokens/s on 1 GB300 (ForkAttn + GDN); % of tensor/HBM roofline"
 # DRAM traffic per launch from one ncu capture (profiles/fork_attn_tc2_attention_tree.md),
 # valid only while the kernel source still has the hash it was captured with.
 NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "f0175bd36b7e7baa", 56.45e6)}
@@ -422,7 +423,7 @@ def run_reference(args):
         if i >= args.warmup:
             vals.append(b)
     v = statistics.median(x["value"] for x in vals)
-    line = {"metric": "tree-prefill tokens/s (ForkAttn + GDN)", "value": v, "unit": "tokens/s", "n_gpus": ws,
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (at.useful_tokens() +
                                                                               gt.useful_tokens()) / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -522,7 +523,7 @@ def main():
             "frac": round(achieved / peak, 4), "traffic": tr,
             "kernel": "fork_attn", "peak_kind": f"{pk_kind} bf16 dense burst",
             "flops_per_launch": fl, "ms_per_launch": round(attn_ms, 4)}
-    line = {"metric": "tree-prefill tokens/s (ForkAttn + GDN)", "value": round(value, 1), "unit": "tokens/s",
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
