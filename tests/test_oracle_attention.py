@@ -169,3 +169,44 @@ def test_resumed_root_equals_fresh_pass():
     b = forward.attention_tree(res, inp_r, 0.5)
     np.testing.assert_array_equal(a[(0, 1)], b[(0, 1)])
     np.testing.assert_array_equal(a[(0, 0)][7:], b[(0, 0)])
+
+
+def test_stream_permutation_leaves_results_unchanged():
+    """Eq. 3 depends only on each token's (request, node, position), not on
+    where the token sits in the flat stream: the masked brute force over a
+    randomly permuted stream, un-permuted, equals it over the Eq. 2 order."""
+    req = synth.Request(parents=[-1, 0, 0, 2], n_tok=[5, 2, 3, 2])
+    tree = synth.Tree([req, synth.fork_tree(4, [3, 1])])
+    hq, hkv, d = 2, 1, 4
+    inp = synth.attn_inputs(tree, hq, hkv, d, seed=9, bf16=False)
+    lay = layout.stream_layout(tree)
+    T = layout.stream_length(tree)
+    j, c, t, _ = layout.token_metadata(tree)
+    Q = np.zeros((T, hq, d)); K = np.zeros((T, hkv, d)); V = np.zeros((T, hkv, d))
+    for (r, i), off in lay.items():
+        n = tree.requests[r].n_tok[i]
+        Q[off:off + n] = inp.nodes[(r, i)]["q"]
+        K[off:off + n] = inp.nodes[(r, i)]["k"]
+        V[off:off + n] = inp.nodes[(r, i)]["v"]
+    anc = {(r, i): set(layout.ancestors(tree.requests[r], i))
+           for r, R in enumerate(tree.requests) for i in range(R.n_nodes)}
+
+    def brute(order):
+        jj, cc, tt = (np.asarray(z)[order] for z in (j, c, t))
+        mask = np.array([[jj[x] == jj[y] and cc[y] in anc[(int(jj[x]), int(cc[x]))] and tt[y] <= tt[x]
+                          for y in range(T)] for x in range(T)])
+        out = np.zeros((T, hq, d))
+        for h in range(hq):
+            S = np.where(mask, Q[order, h] @ K[order, h * hkv // hq].T / math.sqrt(d), -np.inf)
+            P = np.exp(S - S.max(1, keepdims=True))
+            out[:, h] = (P / P.sum(1, keepdims=True)) @ V[order, h * hkv // hq]
+        return out
+
+    base = brute(np.arange(T))
+    perm = np.random.default_rng(10).permutation(T)
+    moved = np.zeros_like(base)
+    moved[perm] = brute(perm)
+    np.testing.assert_allclose(moved, base, atol=1e-13)
+    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(d))
+    for (r, i), off in lay.items():
+        np.testing.assert_allclose(base[off:off + tree.requests[r].n_tok[i]], ref[(r, i)], atol=1e-13)
