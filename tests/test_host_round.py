@@ -76,13 +76,28 @@ def make(tree, n_pages=4096, resume=None, pool=None):
     return R, seg_of, pool, Blob(R.pack().numpy())
 
 
+def _random_tree(seed):
+    """Seeded random forest: 1-3 requests of 1-7 nodes, each node's parent
+    drawn among the earlier nodes, lengths around the page (16), tile (128)
+    and chunk (64) edges."""
+    rng = np.random.default_rng(seed)
+    edge = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129]
+    reqs = []
+    for _ in range(int(rng.integers(1, 4))):
+        n = int(rng.integers(1, 8))
+        parents = [-1] + [int(rng.integers(0, i)) for i in range(1, n)]
+        n_tok = [int(rng.choice(edge)) if rng.random() < 0.6 else int(rng.integers(1, 200)) for _ in range(n)]
+        reqs.append(synth.Request(parents=parents, n_tok=n_tok))
+    return synth.Tree(reqs)
+
+
 TREES = [
     synth.Tree([synth.fork_tree(64, [8, 8, 8])]),
     synth.Tree([synth.fork_tree(300, [17, 1, 128, 129]), synth.fork_tree(5, [40, 3])]),
     synth.Tree([synth.fanout_tree(40, 7, 3, 3)]),
     synth.Tree([synth.Request(parents=[-1, 0, 1, 1, 0, 4], n_tok=[33, 20, 5, 100, 9, 2]),
                 synth.fork_tree(129, [64, 65, 1])]),
-]
+] + [_random_tree(7100 + i) for i in range(16)]
 
 
 def test_abi_exports_every_declared_symbol():
@@ -182,17 +197,27 @@ def test_history_spans_and_resume():
     assert all(pool.refcount(p) == 1 for p in pages)
 
 
-def test_chunks_slots_readouts():
-    tree = TREES[1]
+@pytest.mark.parametrize("ti", range(len(TREES)))
+def test_chunks_slots_readouts(ti):
+    """Each node's chunks start at its first token and tile it in 64-token
+    steps (Flide section 3.5); a child starts from its parent's end slot;
+    inner nodes get distinct temporary slots, leaves none; readout rows are
+    the last token of each leaf."""
+    tree = TREES[ti]
     R, seg_of, pool, B = make(tree)
     ch = B.chunks
+    inner_slots = []
     for (r, i), s in seg_of.items():
         info = R.segment(s)
         mine = [c for c in ch if c[0] == s]
         assert [int(c[3]) for c in mine] == list(range(len(mine)))
-        assert int(mine[0][1]) == info.stream_off                       # starts at the node
+        assert [int(c[1]) for c in mine] == [info.stream_off + 64 * k for k in range(len(mine))]
         assert sum(int(c[2]) for c in mine) == info.n_tokens
         assert all(1 <= int(c[2]) <= 64 for c in mine)
+        has_child = i in tree.requests[r].parents
+        assert (info.end_slot >= 0) == has_child
+        if has_child:
+            inner_slots.append(info.end_slot)
         p = tree.requests[r].parents[i]
         if p >= 0:
             assert info.init_slot == R.segment(seg_of[(r, p)]).end_slot >= 0
@@ -202,6 +227,8 @@ def test_chunks_slots_readouts():
             assert info.readout_row == info.stream_off + info.n_tokens - 1
     assert list(B.readouts) == [R.segment(s).readout_row for s in sorted(seg_of.values())
                                 if R.segment(s).readout_row >= 0]
+    assert len(set(inner_slots)) == len(inner_slots)
+    assert B.h("N_CHUNK") == sum(-(-n // 64) for req in tree.requests for n in req.n_tok)
 
 
 def test_scan_group_table():
