@@ -97,7 +97,10 @@ __device__ __forceinline__ void write_t_operand(uint8_t* bt, int j, const float 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// No minimum-blocks hint: with one, ptxas kept fewer registers and spilled in
+// the solve; without it the kernel takes 155 registers (25,600 per CTA) and two
+// CTAs still fit on an SM.
+__global__ void __launch_bounds__(kThreads)
 gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
