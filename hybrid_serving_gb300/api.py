@@ -37,6 +37,62 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise HsError(_lib.HS_EINVAL, msg)
+
+
+def _device_ok(name: str, t: torch.Tensor):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.device.index == torch.cuda.current_device(), f"{name} is on {t.device}, not the current device")
+
+
+def _on_device(name: str, t, dtype=None, dim: Optional[int] = None, contiguous: bool = True):
+    """The C ABI takes raw device pointers with the layouts hs.h documents, so a
+    host tensor, another dtype or a strided view would be misread: refuse them."""
+    _need(isinstance(t, torch.Tensor), f"{name} must be a tensor")
+    _device_ok(name, t)
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype} (got {t.dtype})")
+    if dim is not None:
+        _need(t.dim() == dim, f"{name} must have {dim} dimensions (got shape {tuple(t.shape)})")
+    if contiguous:
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _meta_status(caps: Caps, dev_meta, dev_status):
+    _on_device("dev_meta", dev_meta, torch.int32)
+    _need(dev_meta.numel() * 4 >= lib.hs_round_meta_bytes(C.byref(caps)), "dev_meta is smaller than the caps' metadata")
+    _on_device("dev_status", dev_status, torch.int32)
+    _need(dev_status.numel() >= 1, "dev_status needs one int32")
+
+
+def _rows(name: str, t, caps: Caps):
+    _need(t.shape[0] >= caps.max_tokens, f"{name} has {t.shape[0]} rows < caps.max_tokens = {caps.max_tokens}")
+
+
+def _check_pages(caps, dev_meta, dev_status, dt, k_new, v_new, k_pages, v_pages):
+    _meta_status(caps, dev_meta, dev_status)
+    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        _on_device(name, t, dt, 4)
+    _need(k_pages.shape == v_pages.shape and k_pages.shape[2] == PAGE,
+          f"k_pages {tuple(k_pages.shape)} and v_pages {tuple(v_pages.shape)} must both be [hkv, n_pages, 16, d]")
+    if k_new is not None:
+        for name, t in (("k_new", k_new), ("v_new", v_new)):
+            _on_device(name, t, dt, 3)
+            _rows(name, t, caps)
+        _need(k_new.shape == v_new.shape and k_new.shape[1:] == (k_pages.shape[0], k_pages.shape[3]),
+              f"k_new/v_new {tuple(k_new.shape)} do not match the pools' [hkv, ., ., d]")
+
+
+def _check_attn(caps, q, out, k_pages, dt):
+    _on_device("q", q, dt, 3)
+    _on_device("out", out, dt, 3)
+    _rows("q", q, caps)
+    _need(out.shape == q.shape, f"out {tuple(out.shape)} must match q {tuple(q.shape)}")
+    _need(q.shape[2] == k_pages.shape[3], "q and the pools differ in head size")
+
+
 def _i32arr(xs: Sequence[int]):
     return (C.c_int32 * max(1, len(xs)))(*xs)
 
@@ -159,16 +215,21 @@ class Round:
 def fork_attn_prefill(caps: Caps, dev_meta: torch.Tensor, q, k_new, v_new, k_pages, v_pages, out,
                       dev_status: torch.Tensor, scale: Optional[float] = None, stream=None):
     """q [T,hq,d], k_new/v_new [T,hkv,d], k_pages/v_pages [hkv,n_pages,16,d], out [T,hq,d]."""
+    dt = _dt(q)
+    _check_pages(caps, dev_meta, dev_status, q.dtype, k_new, v_new, k_pages, v_pages)
+    _check_attn(caps, q, out, k_pages, q.dtype)
     T, hq, d = q.shape
     hkv = k_new.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    check(lib.hs_fork_attn_prefill(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, q.data_ptr(),
+    check(lib.hs_fork_attn_prefill(C.byref(caps), dev_meta.data_ptr(), dt, hq, hkv, d, scale, q.data_ptr(),
                                    k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
                                    k_pages.shape[1], out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
 
 
 def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_pages, dev_status: torch.Tensor,
                   stream=None):
+    _dt(k_new)
+    _check_pages(caps, dev_meta, dev_status, k_new.dtype, k_new, v_new, k_pages, v_pages)
     T, hkv, d = k_new.shape
     check(lib.hs_kv_page_write(C.byref(caps), dev_meta.data_ptr(), _dt(k_new), hkv, d, k_new.data_ptr(),
                                v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[1],
@@ -177,6 +238,9 @@ def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_p
 
 def fork_attn(caps: Caps, dev_meta: torch.Tensor, q, k_pages, v_pages, out, dev_status: torch.Tensor,
               scale: Optional[float] = None, stream=None):
+    _dt(q)
+    _check_pages(caps, dev_meta, dev_status, q.dtype, None, None, k_pages, v_pages)
+    _check_attn(caps, q, out, k_pages, q.dtype)
     T, hq, d = q.shape
     hkv = k_pages.shape[0]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -189,9 +253,29 @@ def gdn_workspace_bytes(caps: Caps, h: int, dk: int, dv: int) -> int:
     return int(lib.hs_gdn_workspace_bytes(C.byref(caps), h, dk, dv))
 
 
+def _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out):
+    dt = q.dtype
+    _dt(q)
+    _meta_status(caps, dev_meta, dev_status)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _on_device(name, t, dt, 3)
+        _rows(name, t, caps)
+    _need(k.shape == q.shape, f"k {tuple(k.shape)} must match q {tuple(q.shape)}")
+    _need(v.shape[1] == q.shape[1] and out.shape[1:] == v.shape[1:], "v and out must be [Tcap, h, dv]")
+    for name, t in (("alpha", alpha), ("beta", beta)):
+        _on_device(name, t, torch.float32, 2)
+        _rows(name, t, caps)
+        _need(t.shape[1] == q.shape[1], f"{name} must be [Tcap, h]")
+    _on_device("state_pool", state_pool, torch.float32, 4)
+    _need(tuple(state_pool.shape[1:]) == (q.shape[1], v.shape[2], q.shape[2]),
+          f"state_pool {tuple(state_pool.shape)} must be [n_slots, h, dv, dk]")
+
+
 def gdn_fork_prefill(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha, beta, state_pool, out, ws,
                      dev_status: torch.Tensor, chunk: int = CHUNK, stream=None):
     """q,k [T,h,dk], v [T,h,dv], alpha,beta [T,h] fp32, state_pool [slots,h,dv,dk] fp32, out [T,h,dv]."""
+    _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out)
+    _on_device("ws", ws)
     T, h, dk = q.shape
     dv = v.shape[2]
     check(lib.hs_gdn_fork_prefill(C.byref(caps), dev_meta.data_ptr(), _dt(q), h, dk, dv, chunk, q.data_ptr(),
@@ -204,6 +288,7 @@ def gdn_fork_prefill_noalloc(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha,
                              dev_status: torch.Tensor, chunk: int = CHUNK, stream=None):
     """hs_gdn_fork_prefill without a workspace argument: for callers that
     cannot allocate device memory (the library's built-in scratch is used)."""
+    _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out)
     T, h, dk = q.shape
     dv = v.shape[2]
     check(lib.hs_gdn_fork_prefill_noalloc(C.byref(caps), dev_meta.data_ptr(), _dt(q), h, dk, dv, chunk,
@@ -213,6 +298,7 @@ def gdn_fork_prefill_noalloc(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha,
 
 
 def gdn_state_checkpoint(state_pool, src_slot: int, dst_slot: int, stream=None):
+    _on_device("state_pool", state_pool, torch.float32, 4)
     n, h, dv, dk = state_pool.shape
     check(lib.hs_gdn_state_checkpoint(state_pool.data_ptr(), n, src_slot, dst_slot, h, dk, dv, _stream(stream)))
 
@@ -220,6 +306,15 @@ def gdn_state_checkpoint(state_pool, src_slot: int, dst_slot: int, stream=None):
 def choice_logprobs(caps: Caps, dev_meta: torch.Tensor, hidden, option_rows, logprobs,
                     dev_status: torch.Tensor, stream=None):
     """hidden [T, dim] (a strided 2-D view is fine), option_rows [n_opt, dim] fp32, logprobs [n_ro, n_opt]."""
+    _dt(hidden)
+    _meta_status(caps, dev_meta, dev_status)
+    _on_device("hidden", hidden, hidden.dtype, 2, contiguous=False)
+    _need(hidden.stride(1) == 1, "hidden rows must be contiguous")
+    _rows("hidden", hidden, caps)
+    _on_device("option_rows", option_rows, torch.float32, 2)
+    _need(option_rows.shape[1] == hidden.shape[1], "option_rows must be [n_opt, hidden_dim]")
+    _on_device("logprobs", logprobs, torch.float32, 2)
+    _need(logprobs.shape[1] == option_rows.shape[0], "logprobs must be [n_readouts, n_opt]")
     dim = hidden.shape[1]
     check(lib.hs_choice_logprobs(C.byref(caps), dev_meta.data_ptr(), _dt(hidden), hidden.data_ptr(),
                                  hidden.stride(0), dim, option_rows.data_ptr(), option_rows.shape[0],

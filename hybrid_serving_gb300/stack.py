@@ -82,7 +82,11 @@ class HybridStack:
         self.q = torch.zeros((Tcap, sh.attn_hq, sh.head_d), dtype=bf, device=DEV)
         self.k = torch.zeros((Tcap, sh.attn_hkv, sh.head_d), dtype=bf, device=DEV)
         self.v = torch.zeros_like(self.k)
-        self.o = torch.zeros((Tcap, max(sh.attn_hq * sh.head_d, sh.gdn_h * sh.gdn_d)), dtype=bf, device=DEV)
+        # token-mixer outputs: one buffer, a contiguous [Tcap, heads * d] view per mixer kind
+        wa, wg = sh.attn_hq * sh.head_d, sh.gdn_h * sh.gdn_d
+        self.o = torch.zeros(Tcap * max(wa, wg), dtype=bf, device=DEV)
+        self.o_attn = self.o[:Tcap * wa].view(Tcap, wa)
+        self.o_gdn = self.o[:Tcap * wg].view(Tcap, wg)
         self.gq = torch.zeros((Tcap, sh.gdn_h, sh.gdn_d), dtype=bf, device=DEV)
         self.gk = torch.zeros_like(self.gq)
         self.gv = torch.zeros_like(self.gq)
@@ -133,10 +137,10 @@ class HybridStack:
                                         sh.head_d, self.rope.data_ptr(), self.max_pos, st.data_ptr(), s))
                 check(lib.hs_rope_apply(C.byref(caps), meta.data_ptr(), kv.data_ptr(), kv.stride(0), 0, sh.attn_hkv,
                                         sh.head_d, self.rope.data_ptr(), self.max_pos, st.data_ptr(), s))
-                ov = self.o[:, :sh.attn_hq * sh.head_d].view(self.Tcap, sh.attn_hq, sh.head_d)
+                ov = self.o_attn.view(self.Tcap, sh.attn_hq, sh.head_d)
                 api.fork_attn_prefill(caps, meta, self.q, self.k, self.v, self.kp[ai], self.vp[ai], ov, st,
                                       stream=stream)
-                gemm(self.o[:, :sh.attn_hq * sh.head_d], self.W[p + "wo"], self.h, T, R=self.h, status=st,
+                gemm(self.o_attn, self.W[p + "wo"], self.h, T, R=self.h, status=st,
                      stream=stream)
                 ai += 1
             else:
@@ -155,10 +159,10 @@ class HybridStack:
                                       self.W[p + "conv"].data_ptr(), sh.gdn_h, sh.gdn_d, self.gq.data_ptr(),
                                       self.gk.data_ptr(), self.gv.data_ptr(), self.ga.data_ptr(), self.gb.data_ptr(),
                                       st.data_ptr(), s))
-                ov = self.o[:, :sh.gdn_h * sh.gdn_d].view(self.Tcap, sh.gdn_h, sh.gdn_d)
+                ov = self.o_gdn.view(self.Tcap, sh.gdn_h, sh.gdn_d)
                 api.gdn_fork_prefill(caps, meta, self.gq, self.gk, self.gv, self.ga, self.gb, self.state[gi], ov,
                                      self._ws(caps), st, stream=stream)
-                gemm(self.o[:, :sh.gdn_h * sh.gdn_d], self.W[p + "wo"], self.h, T, R=self.h, status=st,
+                gemm(self.o_gdn, self.W[p + "wo"], self.h, T, R=self.h, status=st,
                      stream=stream)
                 gi += 1
             check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),

@@ -232,9 +232,10 @@ size_t hs_gdn_workspace_bytes(const hs_round_caps* caps, int32_t h, int32_t dk, 
  * token.  Level by level: a root starts from zero (or its resume slot), a
  * child from its parent's end state (read through the slot index), and
  * every node that has children or a save slot writes its end state.
- *   q, k   [T, h, dk] dt    v [T, h, dv] dt    alpha, beta [T, h] fp32
+ *   q, k   [Tcap, h, dk] dt    v [Tcap, h, dv] dt    alpha, beta [Tcap, h] fp32
+ *   (Tcap = caps->max_tokens rows, contiguous; rows past the stream are padding)
  *   state_pool [n_slots, h, dv, dk] fp32 (read: init slots; written: end slots)
- *   out    [T, h, dv] dt
+ *   out    [Tcap, h, dv] dt (only the stream's rows are written)
  *   ws     >= hs_gdn_workspace_bytes(), 256-byte aligned, contents scratch
  * Supported: dt in {HS_F32, HS_BF16}; dk == dv in {64, 128}; chunk == 64. */
 hs_status hs_gdn_fork_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t h,
@@ -276,7 +277,8 @@ hs_status hs_gdn_state_checkpoint(float* state_pool, int32_t n_slots, int32_t sr
 /* Option log-probabilities at the readout rows (Flide section 3.1, Eq. 1;
  * section 3.3.3, selective readout through an index buffer):
  *   logprobs[i, o] = log softmax_o( option_rows[o] . hidden[row_i] )
- *   hidden      [T, hidden_dim] dt with row stride hidden_stride elements
+ *   hidden      [Tcap, hidden_dim] dt with row stride hidden_stride elements
+ *               (only the readout rows are read)
  *   option_rows [n_opt, hidden_dim] fp32
  *   logprobs    [n_readouts, n_opt] fp32
  * Dot products accumulate in fp32 in a fixed order.  n_opt <= 32. */

@@ -42,10 +42,11 @@ class AttnRun:
         self.n_pages_kernel = n_pages_kernel
 
     def run(self, scale=None):
-        kp = self.k_pages
-        if self.n_pages_kernel is not None:
-            kp = self.k_pages[:, : self.n_pages_kernel]
-        api.fork_attn_prefill(self.R.caps, self.meta, self.q, self.k, self.v, kp, self.v_pages, self.out,
+        kp, vp = self.k_pages, self.v_pages
+        if self.n_pages_kernel is not None:  # a smaller pool than the pages the round allocated
+            kp = self.k_pages[:, : self.n_pages_kernel].contiguous()
+            vp = self.v_pages[:, : self.n_pages_kernel].contiguous()
+        api.fork_attn_prefill(self.R.caps, self.meta, self.q, self.k, self.v, kp, vp, self.out,
                               self.status, scale=scale)
         torch.cuda.synchronize()
         return self
