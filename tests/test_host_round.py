@@ -401,3 +401,58 @@ def test_finalize_retry_and_release_checks():
     Rn.add_segment(-1, 4)
     Rn.finalize(None)
     Rn.release(None)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_resumed_rounds_visible_keys_match_eq3(seed):
+    """Round A: a random forest; each request keeps one random root-to-leaf
+    path (commit).  Round B resumes every request from that path -- its
+    pages as history spans, one per kept node -- with a random subtree on
+    top.  Every row of round B reaches exactly the Eq. 3 key set of the
+    oracle, history included, and the history pages gain and lose the round's
+    reference."""
+    rng = np.random.default_rng(8000 + seed)
+    tree_a = _random_tree(8100 + seed)
+    pool = api.PagePool(4096)
+    Ra, seg_a, _, _ = make(tree_a, pool=pool)
+    keep, hist = [], {}
+    for r, req in enumerate(tree_a.requests):
+        path = [int(rng.integers(0, req.n_nodes))]
+        while req.parents[path[-1]] >= 0:
+            path.append(req.parents[path[-1]])
+        path.reverse()
+        keep += [seg_a[(r, n)] for n in path]
+        hist[r] = [(req.n_tok[n], Ra.segment_pages(seg_a[(r, n)])) for n in path]
+    Ra.release(pool, keep=keep)
+    live = pool.stats()[1]
+    reqs_b = []
+    for r in range(len(tree_a.requests)):
+        sub = _random_tree(8200 + 10 * seed + r).requests[0]
+        reqs_b.append(synth.Request(parents=sub.parents, n_tok=sub.n_tok, hist_len=sum(n for n, _ in hist[r])))
+    tree_b = synth.Tree(reqs_b)
+    Rb, seg_b, _, B = make(tree_b, pool=pool, resume={r: (None, hist[r]) for r in hist})
+    assert pool.stats()[1] == live + sum(-(-n // PAGE) for req in reqs_b for n in req.n_tok)
+    where = _phys_of_tokens(Rb, seg_b, B)
+    for r, spans in hist.items():  # history rows: position u of the kept path
+        u = 0
+        for n, pages in spans:
+            for k in range(n):
+                where[(pages[k // PAGE], k % PAGE)] = ((r, -1), u + k)
+            u += n
+    node_of = {s: rn for rn, s in seg_b.items()}
+    toks, sp, ts, pref = B.toks, B.spans, B.tile_spans, B.page_ref
+    for tl in B.tiles:
+        row0, n_rows, soff, n_sh, n_own = (int(x) for x in tl[:5])
+        for row in range(row0, row0 + n_rows):
+            seg, idx = int(toks[row, 0]), int(toks[row, 1])
+            got = []
+            for k in range(n_sh + n_own):
+                off, ntok, owner = (int(x) for x in sp[int(ts[soff + k])][:3])
+                nvis = ntok if k < n_sh else (idx + 1 if owner == seg else 0)
+                for key in range(nvis):
+                    (rn, u) = where[(int(pref[off + key // PAGE]), key % PAGE)]
+                    got.append((rn[1], u))
+            r, i = node_of[seg]
+            assert sorted(got) == layout.visible_keys(tree_b, r, i, idx), (seed, row)
+    Rb.release(pool)
+    assert pool.stats()[1] == live
