@@ -48,3 +48,22 @@ def test_two_rank_max_and_aggregate():
     import bench
     # whole-job throughput: all ranks' units over the slowest rank's time
     assert bench.aggregate([0.12, 0.15], [100, 100]) == pytest.approx(200 / 0.15)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """bench.py --impl reference launched with two ranks: rank 0 alone times
+    the oracle and prints one JSON line; the other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
