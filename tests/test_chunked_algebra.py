@@ -129,3 +129,48 @@ def test_two_level_scan_matches_recurrence(G):
                 S_end[h] = Sg[0]
     np.testing.assert_allclose(o, o_ref, atol=1e-12)
     np.testing.assert_allclose(S_end, S_ref, atol=1e-12)
+
+
+def test_log_depth_combine_of_group_maps():
+    """The groups' affine maps (M_g, N_g) compose associatively:
+    (M_a, N_a) then (M_b, N_b) = (M_a M_b, N_a M_b + N_b).  An inclusive
+    prefix scan in ceil(log2 G) rounds (every entry combines with the one
+    2^r before it) gives the same start states as the sequential chain
+    S_{g+1} = S_g M_g + N_g, and both equal the recurrence's state at the
+    group boundaries."""
+    rng = np.random.default_rng(4100)
+    C, n_ch, dk, dv, G = 4, 40, 8, 6, 9
+    n = n_ch * C
+    q = rng.standard_normal((n, 1, dk)) / 8
+    k = rng.standard_normal((n, 1, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((n, 1, dv)) / 8
+    a = np.exp(-0.1 * np.log1p(np.exp(rng.standard_normal((n, 1)))))
+    b = 1 / (1 + np.exp(-rng.standard_normal((n, 1))))
+    S0 = rng.standard_normal((1, dv, dk)) * 0.1
+    bounds = [g * n_ch // G for g in range(G + 1)]
+    maps = []
+    for g in range(G):
+        Mg, Ng = np.eye(dk), np.zeros((dv, dk))
+        for c in range(bounds[g], bounds[g + 1]):
+            Mc, Nc = chunk_map(k, v, a, b, C, 0, c * C)
+            Mg, Ng = Mg @ Mc, Ng @ Mc + Nc
+        maps.append((Mg, Ng))
+    # sequential: S_{g+1} = S_g M_g + N_g from the node's start state
+    seq = [S0[0]]
+    for Mg, Ng in maps:
+        seq.append(seq[-1] @ Mg + Ng)
+    # log depth: after round r, entry g holds the composition of groups max(0, g - 2^(r+1) + 1) .. g
+    pre = list(maps)
+    r = 1
+    while r < G:
+        pre = [pre[g] if g < r else (pre[g - r][0] @ pre[g][0], pre[g - r][1] @ pre[g][0] + pre[g][1])
+               for g in range(G)]
+        r *= 2
+    for g in range(G):
+        np.testing.assert_allclose(S0[0] @ pre[g][0] + pre[g][1], seq[g + 1], atol=1e-12)
+    # both equal the step-by-step recurrence at the group boundaries
+    for g in range(1, G + 1):
+        t1 = bounds[g] * C
+        _, S_ref = gdn.gated_delta_rule(q[:t1], k[:t1], v[:t1], a[:t1], b[:t1], S0=S0)
+        np.testing.assert_allclose(seq[g], S_ref[0], atol=1e-12)
