@@ -37,59 +37,74 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _need(cond: bool, msg: str):
+def _need(cond: bool, msg: str, *args):
+    # the message is formatted only on failure: these checks run on every call of the hot path
     if not cond:
-        raise HsError(_lib.HS_EINVAL, msg)
+        raise HsError(_lib.HS_EINVAL, msg.format(*args))
 
 
-def _device_ok(name: str, t: torch.Tensor):
-    _need(t.is_cuda, f"{name} must be a CUDA tensor")
-    _need(t.device.index == torch.cuda.current_device(), f"{name} is on {t.device}, not the current device")
+def _cur_dev() -> int:
+    try:
+        return torch.cuda.current_device()
+    except (RuntimeError, AssertionError):  # no usable CUDA: every device tensor check then fails
+        return -1
 
 
-def _on_device(name: str, t, dtype=None, dim: Optional[int] = None, contiguous: bool = True):
+def _device_ok(name: str, t: torch.Tensor, dev: int):
+    if not t.is_cuda:
+        _need(False, "{} must be a CUDA tensor", name)
+    if t.get_device() != dev:
+        _need(False, "{} is on {}, not the current device cuda:{}", name, t.device, dev)
+
+
+def _on_device(name: str, t, dev: int, dtype=None, dim: Optional[int] = None, contiguous: bool = True):
     """The C ABI takes raw device pointers with the layouts hs.h documents, so a
     host tensor, another dtype or a strided view would be misread: refuse them."""
-    _need(isinstance(t, torch.Tensor), f"{name} must be a tensor")
-    _device_ok(name, t)
-    if dtype is not None:
-        _need(t.dtype == dtype, f"{name} must be {dtype} (got {t.dtype})")
-    if dim is not None:
-        _need(t.dim() == dim, f"{name} must have {dim} dimensions (got shape {tuple(t.shape)})")
-    if contiguous:
-        _need(t.is_contiguous(), f"{name} must be contiguous")
+    if not isinstance(t, torch.Tensor):
+        _need(False, "{} must be a tensor", name)
+    _device_ok(name, t, dev)
+    if dtype is not None and t.dtype != dtype:
+        _need(False, "{} must be {} (got {})", name, dtype, t.dtype)
+    if dim is not None and t.dim() != dim:
+        _need(False, "{} must have {} dimensions (got shape {})", name, dim, tuple(t.shape))
+    if contiguous and not t.is_contiguous():
+        _need(False, "{} must be contiguous", name)
 
 
-def _meta_status(caps: Caps, dev_meta, dev_status):
-    _on_device("dev_meta", dev_meta, torch.int32)
+def _meta_status(caps: Caps, dev_meta, dev_status, dev: int):
+    _on_device("dev_meta", dev_meta, dev, torch.int32)
     _need(dev_meta.numel() * 4 >= lib.hs_round_meta_bytes(C.byref(caps)), "dev_meta is smaller than the caps' metadata")
-    _on_device("dev_status", dev_status, torch.int32)
+    _on_device("dev_status", dev_status, dev, torch.int32)
     _need(dev_status.numel() >= 1, "dev_status needs one int32")
 
 
 def _rows(name: str, t, caps: Caps):
-    _need(t.shape[0] >= caps.max_tokens, f"{name} has {t.shape[0]} rows < caps.max_tokens = {caps.max_tokens}")
+    if t.shape[0] < caps.max_tokens:
+        _need(False, "{} has {} rows < caps.max_tokens = {}", name, t.shape[0], caps.max_tokens)
 
 
-def _check_pages(caps, dev_meta, dev_status, dt, k_new, v_new, k_pages, v_pages):
-    _meta_status(caps, dev_meta, dev_status)
-    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
-        _on_device(name, t, dt, 4)
-    _need(k_pages.shape == v_pages.shape and k_pages.shape[2] == PAGE,
-          f"k_pages {tuple(k_pages.shape)} and v_pages {tuple(v_pages.shape)} must both be [hkv, n_pages, 16, d]")
+def _check_pages(caps, dev_meta, dev_status, dt, k_new, v_new, k_pages, v_pages, dev):
+    _meta_status(caps, dev_meta, dev_status, dev)
+    _on_device("k_pages", k_pages, dev, dt, 4)
+    _on_device("v_pages", v_pages, dev, dt, 4)
+    if k_pages.shape != v_pages.shape or k_pages.shape[2] != PAGE:
+        _need(False, "k_pages {} and v_pages {} must both be [hkv, n_pages, 16, d]", tuple(k_pages.shape),
+              tuple(v_pages.shape))
     if k_new is not None:
-        for name, t in (("k_new", k_new), ("v_new", v_new)):
-            _on_device(name, t, dt, 3)
-            _rows(name, t, caps)
-        _need(k_new.shape == v_new.shape and k_new.shape[1:] == (k_pages.shape[0], k_pages.shape[3]),
-              f"k_new/v_new {tuple(k_new.shape)} do not match the pools' [hkv, ., ., d]")
+        _on_device("k_new", k_new, dev, dt, 3)
+        _on_device("v_new", v_new, dev, dt, 3)
+        _rows("k_new", k_new, caps)
+        ks = k_new.shape
+        if ks != v_new.shape or ks[1] != k_pages.shape[0] or ks[2] != k_pages.shape[3]:
+            _need(False, "k_new/v_new {} do not match the pools' [hkv, ., ., d]", tuple(ks))
 
 
-def _check_attn(caps, q, out, k_pages, dt):
-    _on_device("q", q, dt, 3)
-    _on_device("out", out, dt, 3)
+def _check_attn(caps, q, out, k_pages, dt, dev):
+    _on_device("q", q, dev, dt, 3)
+    _on_device("out", out, dev, dt, 3)
     _rows("q", q, caps)
-    _need(out.shape == q.shape, f"out {tuple(out.shape)} must match q {tuple(q.shape)}")
+    if out.shape != q.shape:
+        _need(False, "out {} must match q {}", tuple(out.shape), tuple(q.shape))
     _need(q.shape[2] == k_pages.shape[3], "q and the pools differ in head size")
 
 
@@ -216,8 +231,9 @@ def fork_attn_prefill(caps: Caps, dev_meta: torch.Tensor, q, k_new, v_new, k_pag
                       dev_status: torch.Tensor, scale: Optional[float] = None, stream=None):
     """q [T,hq,d], k_new/v_new [T,hkv,d], k_pages/v_pages [hkv,n_pages,16,d], out [T,hq,d]."""
     dt = _dt(q)
-    _check_pages(caps, dev_meta, dev_status, q.dtype, k_new, v_new, k_pages, v_pages)
-    _check_attn(caps, q, out, k_pages, q.dtype)
+    dev = _cur_dev()
+    _check_pages(caps, dev_meta, dev_status, q.dtype, k_new, v_new, k_pages, v_pages, dev)
+    _check_attn(caps, q, out, k_pages, q.dtype, dev)
     T, hq, d = q.shape
     hkv = k_new.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -229,7 +245,8 @@ def fork_attn_prefill(caps: Caps, dev_meta: torch.Tensor, q, k_new, v_new, k_pag
 def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_pages, dev_status: torch.Tensor,
                   stream=None):
     _dt(k_new)
-    _check_pages(caps, dev_meta, dev_status, k_new.dtype, k_new, v_new, k_pages, v_pages)
+    _check_pages(caps, dev_meta, dev_status, k_new.dtype, k_new, v_new, k_pages, v_pages,
+                 _cur_dev())
     T, hkv, d = k_new.shape
     check(lib.hs_kv_page_write(C.byref(caps), dev_meta.data_ptr(), _dt(k_new), hkv, d, k_new.data_ptr(),
                                v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[1],
@@ -239,8 +256,9 @@ def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_p
 def fork_attn(caps: Caps, dev_meta: torch.Tensor, q, k_pages, v_pages, out, dev_status: torch.Tensor,
               scale: Optional[float] = None, stream=None):
     _dt(q)
-    _check_pages(caps, dev_meta, dev_status, q.dtype, None, None, k_pages, v_pages)
-    _check_attn(caps, q, out, k_pages, q.dtype)
+    dev = _cur_dev()
+    _check_pages(caps, dev_meta, dev_status, q.dtype, None, None, k_pages, v_pages, dev)
+    _check_attn(caps, q, out, k_pages, q.dtype, dev)
     T, hq, d = q.shape
     hkv = k_pages.shape[0]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -253,29 +271,32 @@ def gdn_workspace_bytes(caps: Caps, h: int, dk: int, dv: int) -> int:
     return int(lib.hs_gdn_workspace_bytes(C.byref(caps), h, dk, dv))
 
 
-def _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out):
+def _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out, dev):
     dt = q.dtype
     _dt(q)
-    _meta_status(caps, dev_meta, dev_status)
+    _meta_status(caps, dev_meta, dev_status, dev)
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
-        _on_device(name, t, dt, 3)
+        _on_device(name, t, dev, dt, 3)
         _rows(name, t, caps)
-    _need(k.shape == q.shape, f"k {tuple(k.shape)} must match q {tuple(q.shape)}")
+    if k.shape != q.shape:
+        _need(False, "k {} must match q {}", tuple(k.shape), tuple(q.shape))
     _need(v.shape[1] == q.shape[1] and out.shape[1:] == v.shape[1:], "v and out must be [Tcap, h, dv]")
     for name, t in (("alpha", alpha), ("beta", beta)):
-        _on_device(name, t, torch.float32, 2)
+        _on_device(name, t, dev, torch.float32, 2)
         _rows(name, t, caps)
-        _need(t.shape[1] == q.shape[1], f"{name} must be [Tcap, h]")
-    _on_device("state_pool", state_pool, torch.float32, 4)
-    _need(tuple(state_pool.shape[1:]) == (q.shape[1], v.shape[2], q.shape[2]),
-          f"state_pool {tuple(state_pool.shape)} must be [n_slots, h, dv, dk]")
+        _need(t.shape[1] == q.shape[1], "{} must be [Tcap, h]", name)
+    _on_device("state_pool", state_pool, dev, torch.float32, 4)
+    ss = state_pool.shape
+    if ss[1] != q.shape[1] or ss[2] != v.shape[2] or ss[3] != q.shape[2]:
+        _need(False, "state_pool {} must be [n_slots, h, dv, dk]", tuple(ss))
 
 
 def gdn_fork_prefill(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha, beta, state_pool, out, ws,
                      dev_status: torch.Tensor, chunk: int = CHUNK, stream=None):
     """q,k [T,h,dk], v [T,h,dv], alpha,beta [T,h] fp32, state_pool [slots,h,dv,dk] fp32, out [T,h,dv]."""
-    _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out)
-    _on_device("ws", ws)
+    dev = _cur_dev()
+    _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out, dev)
+    _on_device("ws", ws, dev)
     T, h, dk = q.shape
     dv = v.shape[2]
     check(lib.hs_gdn_fork_prefill(C.byref(caps), dev_meta.data_ptr(), _dt(q), h, dk, dv, chunk, q.data_ptr(),
@@ -288,7 +309,7 @@ def gdn_fork_prefill_noalloc(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha,
                              dev_status: torch.Tensor, chunk: int = CHUNK, stream=None):
     """hs_gdn_fork_prefill without a workspace argument: for callers that
     cannot allocate device memory (the library's built-in scratch is used)."""
-    _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out)
+    _check_gdn(caps, dev_meta, dev_status, q, k, v, alpha, beta, state_pool, out, _cur_dev())
     T, h, dk = q.shape
     dv = v.shape[2]
     check(lib.hs_gdn_fork_prefill_noalloc(C.byref(caps), dev_meta.data_ptr(), _dt(q), h, dk, dv, chunk,
@@ -298,7 +319,7 @@ def gdn_fork_prefill_noalloc(caps: Caps, dev_meta: torch.Tensor, q, k, v, alpha,
 
 
 def gdn_state_checkpoint(state_pool, src_slot: int, dst_slot: int, stream=None):
-    _on_device("state_pool", state_pool, torch.float32, 4)
+    _on_device("state_pool", state_pool, _cur_dev(), torch.float32, 4)
     n, h, dv, dk = state_pool.shape
     check(lib.hs_gdn_state_checkpoint(state_pool.data_ptr(), n, src_slot, dst_slot, h, dk, dv, _stream(stream)))
 
@@ -307,13 +328,14 @@ def choice_logprobs(caps: Caps, dev_meta: torch.Tensor, hidden, option_rows, log
                     dev_status: torch.Tensor, stream=None):
     """hidden [T, dim] (a strided 2-D view is fine), option_rows [n_opt, dim] fp32, logprobs [n_ro, n_opt]."""
     _dt(hidden)
-    _meta_status(caps, dev_meta, dev_status)
-    _on_device("hidden", hidden, hidden.dtype, 2, contiguous=False)
+    dev = _cur_dev()
+    _meta_status(caps, dev_meta, dev_status, dev)
+    _on_device("hidden", hidden, dev, hidden.dtype, 2, contiguous=False)
     _need(hidden.stride(1) == 1, "hidden rows must be contiguous")
     _rows("hidden", hidden, caps)
-    _on_device("option_rows", option_rows, torch.float32, 2)
+    _on_device("option_rows", option_rows, dev, torch.float32, 2)
     _need(option_rows.shape[1] == hidden.shape[1], "option_rows must be [n_opt, hidden_dim]")
-    _on_device("logprobs", logprobs, torch.float32, 2)
+    _on_device("logprobs", logprobs, dev, torch.float32, 2)
     _need(logprobs.shape[1] == option_rows.shape[0], "logprobs must be [n_readouts, n_opt]")
     dim = hidden.shape[1]
     check(lib.hs_choice_logprobs(C.byref(caps), dev_meta.data_ptr(), _dt(hidden), hidden.data_ptr(),

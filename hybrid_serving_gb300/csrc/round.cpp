@@ -598,11 +598,16 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
   memcpy(h + L.off_readout, r->readouts.data(), r->readouts.size() * 4);
   memcpy(h + L.off_page_ref, page_ref.data(), page_ref.size() * 4);
   h[H_OFF_PRED] = L.off_pred;
-  // conv predecessors: walk back through the node, then its ancestors' last tokens
+  // conv predecessors: a node's first kPredWords tokens walk back through the node, then its ancestors'
+  // last tokens; every later token's predecessors are simply the stream rows before it
   for (int32_t i = 0; i < n; ++i) {
     const Seg& s = S[i];
-    for (int32_t u = 0; u < s.n_tok; ++u) {
-      int32_t* pr = h + L.off_pred + (s.stream_off + u) * kPredWords;
+    const int32_t head = std::min(s.n_tok, (int32_t)kPredWords);
+    int32_t* pn = h + L.off_pred + s.stream_off * kPredWords;
+    for (int32_t u = head; u < s.n_tok; ++u)
+      for (int32_t k = 1; k <= kPredWords; ++k) pn[u * kPredWords + k - 1] = s.stream_off + u - k;
+    for (int32_t u = 0; u < head; ++u) {
+      int32_t* pr = pn + u * kPredWords;
       for (int32_t k = 1; k <= kPredWords; ++k) {
         int32_t node = i, idx = u - k, val = -1;
         while (idx < 0 && S[node].parent >= 0) {

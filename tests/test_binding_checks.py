@@ -51,7 +51,8 @@ def host_run(monkeypatch):
     rec = Recorder(_lib.lib)
     monkeypatch.setattr(api, "lib", rec)
     monkeypatch.setattr(hstack, "lib", rec)
-    monkeypatch.setattr(api, "_device_ok", lambda name, t: None)
+    monkeypatch.setattr(api, "_device_ok", lambda *a: None)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
     monkeypatch.setattr(api, "_stream", lambda stream=None: 0)
     monkeypatch.setattr(hstack, "_s", lambda stream=None: 0)
     monkeypatch.setattr(torch.cuda, "synchronize", lambda *a, **k: None)

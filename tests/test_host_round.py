@@ -456,3 +456,40 @@ def test_resumed_rounds_visible_keys_match_eq3(seed):
             assert sorted(got) == layout.visible_keys(tree_b, r, i, idx), (seed, row)
     Rb.release(pool)
     assert pool.stats()[1] == live
+
+
+OFF_PRED, KPRED = 31, 3
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+def test_conv_predecessor_rows(ti):
+    """Per token, the stream rows of the kConvTaps - 1 = 3 tokens before it in
+    its standalone sequence (Flide section 3.2.2: a node's first tokens read
+    their ancestors' last ones); before the sequence start -1, or, for a root
+    resumed with a saved conv window w0 (section 3.4), the window row encoded
+    as -2 - (w0 + 3 + offset) for the offsets -3..-1 before the root."""
+    tree = TREES[ti]
+    windows = {}
+    if ti % 2:  # resumed roots with a conv window on every other tree
+        tree = synth.Tree([synth.Request(parents=q.parents, n_tok=q.n_tok, hist_len=5 + 3 * r)
+                           for r, q in enumerate(tree.requests)])
+        windows = {r: 7 * r for r in range(len(tree.requests))}
+    pool = api.PagePool(4096)
+    R, seg_of = rounds.build_round(tree, pool, resume={r: (None, [], w) for r, w in windows.items()})
+    words = R.pack().numpy().astype(np.int64)
+    pred = words[int(words[OFF_PRED]):][:R.info().n_tokens * KPRED].reshape(-1, KPRED)
+    for (r, i), s in seg_of.items():
+        req = tree.requests[r]
+        pos = layout.positions(req)
+        chain = layout.ancestors(req, i) + [i]
+        info = R.segment(s)
+        for u in range(req.n_tok[i]):
+            for k in range(1, KPRED + 1):
+                p = pos[i] + u - k
+                want = -1
+                if p >= req.hist_len:
+                    a = [c for c in chain if pos[c] <= p < pos[c] + req.n_tok[c]][0]
+                    want = R.segment(seg_of[(r, a)]).stream_off + p - pos[a]
+                elif r in windows and p >= req.hist_len - KPRED:
+                    want = -2 - (windows[r] + KPRED + (p - req.hist_len))
+                assert pred[info.stream_off + u, k - 1] == want, (ti, r, i, u, k)
