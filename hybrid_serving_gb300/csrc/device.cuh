@@ -1,6 +1,7 @@
 // device.cuh -- small device helpers shared by the kernels.
 #pragma once
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -8,6 +9,14 @@
 #include "meta.h"
 
 namespace hsd {
+
+// One-time launch setup (function attributes such as the dynamic shared-memory limit) is per device: a
+// launcher keeps a flag per device ordinal and fills the current device's slot on its first call there.
+constexpr int kMaxDevices = 64;
+inline int device_slot() {
+  int d = -1;
+  return (cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices) ? d : -1;
+}
 
 // Programmatic dependent launch: a kernel launched with launch_pdl may start while the kernel before it in
 // the stream drains.  Such a kernel calls pdl_wait() before it touches global memory (it returns once every

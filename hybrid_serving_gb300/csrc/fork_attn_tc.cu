@@ -1016,23 +1016,25 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
         !make_map(&m_v16, vp, 2, dims, strides, b16) || !make_map(&m_v128, vp, 2, dims, strides, b128))
       return hs::fail(HS_ECUDA, "tensor map for the page pools");
   }
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
+  const int slot = hsd::device_slot();
+  if (slot < 0) return hs::fail(HS_ECUDA, "fork_attn_tc: no usable CUDA device");
+  if (!configured[slot].load()) {
     if (cudaFuncSetAttribute(fork_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024) !=
             cudaSuccess ||
         cudaFuncSetAttribute(fork_attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair::kSmemBytes + 1024) != cudaSuccess)
       return hs::fail(HS_ECUDA, "fork_attn_tc: cannot raise the shared-memory limit");
-    configured = true;
+    configured[slot].store(true);
   }
   Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status};
   if ((hq / hkv) % 2 == 0) {  // two query heads that share a KV head per CTA, one persistent CTA per SM
-    static int n_sm = 0;
-    if (n_sm == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
-                                                    cudaSuccess || n_sm <= 0)
+    static std::atomic<int> sm_count[hsd::kMaxDevices];  // per device, 0 until read
+    int n_sm = sm_count[slot].load();
+    if (n_sm <= 0) {
+      if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, slot) != cudaSuccess || n_sm <= 0)
         return hs::fail(HS_ECUDA, "fork_attn_tc: cannot read the SM count");
+      sm_count[slot].store(n_sm);
     }
     const int items = caps->max_tiles * (hq / 2);
     hsd::launch_pdl(fork_attn_tc2_kernel, dim3(items < n_sm ? items : n_sm), dim3(pair::kThreads),

@@ -650,11 +650,13 @@ hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const v
   }
   // bf16 inputs take the pipelined state pass; fp32 rows do not fit its double buffer at d=128
   constexpr bool kPipelined = sizeof(T) == 2;
-  static bool configured = false;  // per template instance
+  static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
+  const int slot = hsd::device_slot();
+  if (slot < 0) return hs::fail(HS_ECUDA, "gdn: no usable CUDA device");
   auto ka = gdn_chunk_local_v2<T, D>;
   auto kb1 = gdn_state_pass_kernel<T, D, D>;
   auto kb2 = gdn_state_pass_v2<T, D>;
-  if (!configured) {
+  if (!configured[slot].load()) {
     bool ok = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemA2<D>()) == cudaSuccess;
     if (kPipelined)
       ok = ok && cudaFuncSetAttribute(kb2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemB2<T, D>()) ==
@@ -663,7 +665,7 @@ hs_status run_gdn(const hs_round_caps* caps, const int32_t* meta, int H, const v
       ok = ok && cudaFuncSetAttribute(kb1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemB<D, D>()) ==
                      cudaSuccess;
     if (!ok) return hs::fail(HS_ECUDA, "gdn: cannot raise the shared-memory limit");
-    configured = true;
+    configured[slot].store(true);
   }
   if (caps->max_chunks > 0) {
     ka<<<dim3(caps->max_chunks, H), kThreads, smemA2<D>(), st>>>(meta, H, (const T*)q, (const T*)k, (const T*)v,

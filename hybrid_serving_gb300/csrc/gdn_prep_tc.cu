@@ -420,15 +420,17 @@ hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, 
   if (!map_rows(&mq, q, H, caps->max_tokens) || !map_rows(&mk, k, H, caps->max_tokens) ||
       !map_rows(&mv, v, H, caps->max_tokens))
     return hs::fail(HS_ECUDA, "gdn: tensor map encoding failed");
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
+  const int slot = hsd::device_slot();
+  if (slot < 0) return hs::fail(HS_ECUDA, "gdn_chunk_prep_tc: no usable CUDA device");
+  if (!configured[slot].load()) {
     if (cudaFuncSetAttribute(gdn_chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
             cudaSuccess ||
         // two CTAs per SM: every SM configured for all of its shared memory
         cudaFuncSetAttribute(gdn_chunk_prep_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return hs::fail(HS_ECUDA, "gdn_chunk_prep_tc: cannot raise the shared-memory limit");
-    configured = true;
+    configured[slot].store(true);
   }
   Prm prm{meta, H, alpha, beta, ws, status};
   hsd::launch_pdl(gdn_chunk_prep_tc_kernel, dim3(caps->max_chunks, (H + 1) / 2), dim3(kThreads), kSmem + 1024, st, mq,

@@ -907,14 +907,16 @@ hs_status hs_gdn_chain_tc_launch(const hs_round_caps* caps, const int32_t* meta,
   CUtensorMap mq;
   if (!map_rows(&mq, q, H, caps->max_tokens))
     return hs::fail(HS_ECUDA, "gdn: tensor map encoding failed");
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
+  const int slot = hsd::device_slot();
+  if (slot < 0) return hs::fail(HS_ECUDA, "gdn_chain_tc: no usable CUDA device");
+  if (!configured[slot].load()) {
     if (cudaFuncSetAttribute(gdn_chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<true>() + 1024) != cudaSuccess ||
         cudaFuncSetAttribute(gdn_chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<false>() + 1024) != cudaSuccess)
       return hs::fail(HS_ECUDA, "gdn_chain_tc: cannot raise the shared-memory limit");
-    configured = true;
+    configured[slot].store(true);
   }
   // per level: the scan's first pass (group 0's end state and the later groups' N and M, no outputs), then
   // every group of every node with outputs

@@ -205,12 +205,14 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   CUtensorMap ma, mb;
   if (!map_2d(&ma, A, M, K, lda, BM) || !map_2d(&mb, B, N, K, ldb, BN))
     return hs::fail(HS_ECUDA, "gemm: tensor map encoding failed");
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
+  const int slot = hsd::device_slot();
+  if (slot < 0) return hs::fail(HS_ECUDA, "gemm: no usable CUDA device");
+  if (!configured[slot].load()) {
     if (cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
         cudaSuccess)
       return hs::fail(HS_ECUDA, "gemm: cannot raise the shared-memory limit");
-    configured = true;
+    configured[slot].store(true);
   }
   GemmParams prm{M, N, K, (__nv_bfloat16*)C, ldc, (const __nv_bfloat16*)R, ldr, dev_status};
   dim3 grid(N / BN, (M + BM - 1) / BM);

@@ -271,11 +271,13 @@ extern "C" hs_status hs_gdn_prep(const hs_round_caps* caps, const void* dev_meta
   if (hs_status s = need_device()) return s;
   if (caps->max_tokens <= 0) return HS_OK;
   const size_t smem = sizeof(float) * 3 * (size_t)h * d;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
+  const int slot = hsd::device_slot();
+  if (slot < 0) return hs::fail(HS_ECUDA, "gdn_prep: no usable CUDA device");
+  if (!configured[slot].load()) {
     if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
       return hs::fail(HS_ECUDA, "gdn_prep: cannot raise the shared-memory limit");
-    configured = true;
+    configured[slot].store(true);
   }
   HS_CHECK_ARG(smem <= 200 * 1024, "3*h*d too large");
   gdn_prep_kernel<<<caps->max_tokens, kPrepThreads, smem, (cudaStream_t)stream>>>(
