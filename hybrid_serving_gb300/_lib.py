@@ -59,6 +59,7 @@ _SIGS = {
     "hs_round_create": (I32, [CAPSP, C.POINTER(P)]),
     "hs_round_destroy": (None, [P]),
     "hs_round_add_segment": (I32, [P, I32, I32, I32, I32, I32P]),
+    "hs_round_add_segments": (I32, [P, I32, I32P, I32P, I32P, I32P, I32P]),
     "hs_gdn_state_resume": (I32, [P, I32, I32, I32]),
     "hs_round_attach_history": (I32, [P, I32, I32, I32P, I32P]),
     "hs_round_finalize": (I32, [P, P, I32, I32]),

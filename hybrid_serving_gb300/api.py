@@ -166,6 +166,15 @@ class Round:
         check(lib.hs_round_add_segment(self._h, parent, n_tokens, flags, save_slot, C.byref(s)))
         return s.value
 
+    def add_segments(self, parents: Sequence[int], n_tokens: Sequence[int], flags: Sequence[int],
+                     save_slots: Sequence[int]) -> int:
+        """Adds len(parents) nodes in one call; returns the first new node id."""
+        first = C.c_int32()
+        n = len(parents)
+        check(lib.hs_round_add_segments(self._h, n, _i32arr(parents), _i32arr(n_tokens), _i32arr(flags),
+                                        _i32arr(save_slots), C.byref(first)))
+        return first.value
+
     def gdn_state_resume(self, seg: int, ckpt_slot: int, ckpt_pos: int):
         check(lib.hs_gdn_state_resume(self._h, seg, ckpt_slot, ckpt_pos))
 

@@ -247,6 +247,41 @@ extern "C" hs_status hs_round_add_segment(hs_round* r, int32_t parent, int32_t n
   return HS_OK;
 }
 
+extern "C" hs_status hs_round_add_segments(hs_round* r, int32_t n, const int32_t* parent, const int32_t* n_tokens,
+                                           const int32_t* flags, const int32_t* save_slot, int32_t* first_id) {
+  HS_CHECK_ARG(r, "null round");
+  HS_CHECK_ARG(!r->finalized, "round already finalized");
+  HS_CHECK_ARG(n >= 0 && (n == 0 || (parent && n_tokens)), "bad node arrays");
+  const int32_t base = (int32_t)r->segs.size();
+  if ((int64_t)base + n > r->caps.max_segments)
+    return hs::fail(HS_ECAPACITY, "more than max_segments=%d nodes", r->caps.max_segments);
+  // every entry is checked before any node is added
+  for (int32_t j = 0; j < n; ++j) {
+    HS_CHECK_ARG(n_tokens[j] >= 1, "node %d needs at least one token (got %d)", base + j, n_tokens[j]);
+    HS_CHECK_ARG(parent[j] >= -1 && parent[j] < base + j, "node %d: unknown parent %d", base + j, parent[j]);
+    const int32_t f = flags ? flags[j] : 0, sv = save_slot ? save_slot[j] : -1;
+    HS_CHECK_ARG((f & ~(HS_SEG_READOUT | HS_SEG_NO_READOUT)) == 0, "node %d: unknown flags %d", base + j, f);
+    HS_CHECK_ARG(sv >= -1, "node %d: bad save slot %d", base + j, sv);
+  }
+  r->segs.reserve(base + n);
+  for (int32_t j = 0; j < n; ++j) {
+    Seg s;
+    s.parent = parent[j];
+    s.n_tok = n_tokens[j];
+    s.flags = flags ? flags[j] : 0;
+    s.save_slot = save_slot ? save_slot[j] : -1;
+    if (s.parent < 0) {
+      s.request = r->n_requests++;
+    } else {
+      s.request = r->segs[s.parent].request;
+      r->segs[s.parent].children.push_back(base + j);
+    }
+    r->segs.push_back(std::move(s));
+  }
+  if (first_id) *first_id = base;
+  return HS_OK;
+}
+
 extern "C" hs_status hs_gdn_state_resume(hs_round* r, int32_t seg, int32_t ckpt_slot, int32_t ckpt_pos) {
   HS_CHECK_ARG(r, "null round");
   HS_CHECK_ARG(!r->finalized, "round already finalized");

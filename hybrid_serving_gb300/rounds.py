@@ -39,11 +39,16 @@ def build_round(tree, pool: Optional[PagePool] = None, caps=None, temp_slot0: in
         caps = round_caps_for(T, n_seg, depth, n_hs, n_hp)
     R = Round(caps)
     seg_of = {}
-    for r, req in enumerate(tree.requests):
+    parents, n_tok, flags, saves = [], [], [], []
+    for r, req in enumerate(tree.requests):  # node ids in add order: requests in turn, nodes in order
         for i in range(req.n_nodes):
-            parent = -1 if i == 0 else seg_of[(r, req.parents[i])]
-            flags = _lib.HS_SEG_READOUT if req.readout[i] else _lib.HS_SEG_NO_READOUT
-            seg_of[(r, i)] = R.add_segment(parent, req.n_tok[i], flags, req.save.get(i, -1))
+            seg_of[(r, i)] = len(parents)
+            parents.append(-1 if i == 0 else seg_of[(r, req.parents[i])])
+            n_tok.append(req.n_tok[i])
+            flags.append(_lib.HS_SEG_READOUT if req.readout[i] else _lib.HS_SEG_NO_READOUT)
+            saves.append(req.save.get(i, -1))
+    R.add_segments(parents, n_tok, flags, saves)
+    for r, req in enumerate(tree.requests):
         if req.hist_len:
             res = resume.get(r, (None, []))
             slot, spans = res[0], res[1]

@@ -128,6 +128,14 @@ void hs_round_destroy(hs_round* r);
 hs_status hs_round_add_segment(hs_round* r, int32_t parent_seg, int32_t n_tokens, int32_t flags,
                                int32_t save_slot, int32_t* seg_out);
 
+/* Add n nodes in one call, as n calls of hs_round_add_segment would: node j
+ * gets id first + j, where first (written to *first_id) is the number of
+ * nodes added before; parent[j] is -1 or an id below first + j.  flags and
+ * save_slot may be NULL (0 and -1 for every node).  Every entry is checked
+ * first: on an error nothing is added. */
+hs_status hs_round_add_segments(hs_round* r, int32_t n, const int32_t* parent, const int32_t* n_tokens,
+                                const int32_t* flags, const int32_t* save_slot, int32_t* first_id);
+
 /* Resume a ROOT node from a checkpoint (Flide section 3.4): its first stream
  * token sits at position ckpt_pos and its GDN state starts from ckpt_slot. */
 hs_status hs_gdn_state_resume(hs_round* r, int32_t seg, int32_t ckpt_slot, int32_t ckpt_pos);

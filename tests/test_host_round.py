@@ -493,3 +493,38 @@ def test_conv_predecessor_rows(ti):
                 elif r in windows and p >= req.hist_len - KPRED:
                     want = -2 - (windows[r] + KPRED + (p - req.hist_len))
                 assert pred[info.stream_off + u, k - 1] == want, (ti, r, i, u, k)
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+def test_bulk_add_equals_one_by_one(ti):
+    """hs_round_add_segments builds, bit for bit, the round that one
+    hs_round_add_segment call per node builds."""
+    tree = TREES[ti]
+    _, _, _, bulk = make(tree)
+    n_seg = sum(r.n_nodes for r in tree.requests)
+    depth = max(max(layout.depth(r)) for r in tree.requests) + 1
+    R = api.Round(api.round_caps_for(sum(sum(r.n_tok) for r in tree.requests), n_seg, depth))
+    for req in tree.requests:
+        ids = []
+        for i in range(req.n_nodes):
+            flags = _lib.HS_SEG_READOUT if req.readout[i] else _lib.HS_SEG_NO_READOUT
+            ids.append(R.add_segment(-1 if i == 0 else ids[req.parents[i]], req.n_tok[i], flags))
+    R.finalize(api.PagePool(4096), 0, n_seg)
+    assert np.array_equal(R.pack().numpy(), bulk.w.astype(np.int32))
+
+
+def test_bulk_add_checks_everything_first():
+    R = api.Round(api.round_caps_for(100, 6, 3))
+    assert R.add_segments([-1, 0], [10, 5], [0, 0], [-1, -1]) == 0
+    for parents, n_tok, flags, saves, code in [
+            ([-1, 0, 4], [4, 4, 4], [0, 0, 0], [-1, -1, -1], _lib.HS_EINVAL),   # node 4 its own parent
+            ([5, 0], [4, 4], [0, 0], [-1, -1], _lib.HS_EINVAL),                # parent added after it
+            ([1, 0], [4, 0], [0, 0], [-1, -1], _lib.HS_EINVAL),                # empty node
+            ([0, 0], [4, 4], [0, 8], [-1, -1], _lib.HS_EINVAL),                # unknown flag
+            ([0, 0], [4, 4], [0, 0], [-1, -7], _lib.HS_EINVAL),                # bad save slot
+            ([-1, 0, 1, 2, 3], [1] * 5, [0] * 5, [-1] * 5, _lib.HS_ECAPACITY)]:  # 7 nodes > 6
+        with pytest.raises(_lib.HsError) as e:
+            R.add_segments(parents, n_tok, flags, saves)
+        assert e.value.code == code
+    # nothing of the refused calls was added: the next id is still 2
+    assert R.add_segments([1], [3], [0], [-1]) == 2
