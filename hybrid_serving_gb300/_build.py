@@ -1,13 +1,18 @@
 """Build libhsfork.so in-tree with nvcc for sm_103a (no cmake, no setuptools).
 
 Each translation unit compiles in parallel to ``_build/``; the shared
-library lands next to this file.  A unit is rebuilt only when it or a
-header is newer than its object.
+library lands next to this file.  A unit is rebuilt unless its object was
+made from exactly the current bytes of the unit, every header, this script
+and the nvcc command: a stamp file beside each object records the SHA-256
+of those inputs, so an object copied in from another checkout or machine
+(with whatever timestamps) is never linked against sources it was not
+built from.  The library carries a stamp over all its objects' stamps.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -34,35 +39,58 @@ def _sources():
 
 
 def _headers():
-    return glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        glob.glob(os.path.join(INCLUDE, "*.h"))
+    return sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
+                  glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def _mtime(p):
-    return os.path.getmtime(p) if os.path.exists(p) else -1.0
+def _digest(paths, extra: str) -> str:
+    h = hashlib.sha256(extra.encode())
+    for p in paths:
+        h.update(os.path.basename(p).encode() + b"\0")
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _stamp_ok(target: str, digest: str) -> bool:
+    try:
+        return os.path.exists(target) and open(target + ".sha").read().strip() == digest
+    except OSError:
+        return False
+
+
+def _write_stamp(target: str, digest: str) -> None:
+    with open(target + ".sha", "w") as f:
+        f.write(digest + "\n")
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    hdr_t = max([_mtime(h) for h in _headers()] + [_mtime(__file__)])
+    hdrs = _headers() + [os.path.abspath(__file__)]
     common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
     jobs = []
     objs = []
+    digests = []
     for src in _sources():
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        if src.endswith(".cu"):
+            cmd = [nvcc] + ARCH + common + ["-c", src, "-o", obj] + (["-Xptxas", "-v"] if verbose else [])
+        else:
+            cmd = [nvcc] + common + ["-x", "c++", "-c", src, "-o", obj]
+        dig = _digest([src] + hdrs, " ".join(c for c in cmd if c not in ("-Xptxas", "-v")))
         objs.append(obj)
-        if force or _mtime(obj) < max(_mtime(src), hdr_t):
-            cmd = [nvcc] + ARCH + common + ["-c", src, "-o", obj]
-            if src.endswith(".cu"):
-                cmd += ["-Xptxas", "-v"] if verbose else []
-            else:
-                cmd = [nvcc] + common + ["-x", "c++", "-c", src, "-o", obj]
-            jobs.append((src, cmd))
+        digests.append(dig)
+        if force or not _stamp_ok(obj, dig):
+            jobs.append((src, obj, dig, cmd))
 
     def run(job):
-        src, cmd = job
+        src, obj, dig, cmd = job
+        if os.path.exists(obj + ".sha"):
+            os.remove(obj + ".sha")
         r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode == 0:
+            _write_stamp(obj, dig)
         return src, r
 
     if jobs:
@@ -72,7 +100,8 @@ def build(verbose: bool = False, force: bool = False) -> str:
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
-    if force or jobs or _mtime(LIB) < max(_mtime(o) for o in objs):
+    lib_dig = hashlib.sha256("".join(digests).encode()).hexdigest()
+    if force or jobs or not _stamp_ok(LIB, lib_dig):
         tmp = LIB + ".tmp"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -80,6 +109,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("linking libhsfork.so failed")
         os.replace(tmp, LIB)
+        _write_stamp(LIB, lib_dig)
     return LIB
 
 
