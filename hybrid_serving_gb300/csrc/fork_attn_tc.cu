@@ -154,7 +154,9 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int h = blockIdx.x % p.hq;
   const int kvh = h / (p.hq / p.hkv);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
+  // a shared-memory access (an integer round trip would turn them into generic loads and stores)
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -554,7 +556,9 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     return w < n_items ? w : -1;
   };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
+  // a shared-memory access (an integer round trip would turn them into generic loads and stores)
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;

@@ -699,17 +699,26 @@ extern "C" size_t hs_gdn_workspace_bytes(const hs_round_caps* caps, int32_t h, i
   return n;
 }
 
+namespace {
+// The shapes and dtypes the GDN kernels are built for; both fork-prefill entry points check them first, so
+// they report the same error for the same bad arguments.
+hs_status gdn_shape_check(int32_t h, int32_t dk, int32_t dv, int32_t chunk, hs_dtype dt) {
+  HS_CHECK_ARG(h > 0, "h must be > 0");
+  if (chunk != kChunk) return hs::fail(HS_EUNSUPPORTED, "chunk %d (built: %d)", chunk, kChunk);
+  if (dk != dv || (dk != 64 && dk != 128)) return hs::fail(HS_EUNSUPPORTED, "dk=%d dv=%d (built: 64, 128)", dk, dv);
+  if (dt != HS_F32 && dt != HS_BF16) return hs::fail(HS_EUNSUPPORTED, "dtype %d", (int)dt);
+  return HS_OK;
+}
+}  // namespace
+
 extern "C" hs_status hs_gdn_fork_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t h,
                                          int32_t dk, int32_t dv, int32_t chunk, const void* q, const void* k,
                                          const void* v, const float* alpha, const float* beta, float* state_pool,
                                          int32_t n_slots, void* out, void* ws, size_t ws_bytes, int32_t* dev_status,
                                          void* stream) {
   HS_CHECK_ARG(caps && dev_meta && q && k && v && alpha && beta && out && ws, "null argument");
-  HS_CHECK_ARG(h > 0, "h must be > 0");
   HS_CHECK_ARG(n_slots >= 0 && (n_slots == 0 || state_pool), "bad state pool");
-  if (chunk != kChunk) return hs::fail(HS_EUNSUPPORTED, "chunk %d (built: %d)", chunk, kChunk);
-  if (dk != dv || (dk != 64 && dk != 128)) return hs::fail(HS_EUNSUPPORTED, "dk=%d dv=%d (built: 64, 128)", dk, dv);
-  if (dt != HS_F32 && dt != HS_BF16) return hs::fail(HS_EUNSUPPORTED, "dtype %d", (int)dt);
+  if (hs_status s = gdn_shape_check(h, dk, dv, chunk, dt)) return s;
   const size_t need = hs_gdn_workspace_bytes(caps, h, dk, dv);
   HS_CHECK_ARG(ws_bytes >= need, "workspace of %zu bytes < %zu", ws_bytes, need);
   HS_CHECK_ARG(((uintptr_t)ws & 255) == 0, "workspace must be 256-byte aligned");
@@ -773,6 +782,7 @@ extern "C" hs_status hs_gdn_fork_prefill_noalloc(const hs_round_caps* caps, cons
                                                  float* state_pool, int32_t n_slots, void* out, int32_t* dev_status,
                                                  void* stream) {
   HS_CHECK_ARG(caps, "null caps");
+  if (hs_status s = gdn_shape_check(h, dk, dv, chunk, dt)) return s;
   const size_t need = hs_gdn_workspace_bytes(caps, h, dk, dv);
   if (need > HS_GDN_NOALLOC_SCRATCH_BYTES)
     return hs::fail(HS_ECAPACITY, "round needs %zu bytes of GDN scratch; the built-in scratch holds %zu", need,

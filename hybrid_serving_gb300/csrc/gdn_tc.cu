@@ -130,7 +130,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
   __shared__ uint64_t bar_sc[2], bar_uc[2], bar_d1c[2], bar_d4c[2];  // per chain (output-less variant)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
+  // a shared-memory access (an integer round trip would turn them into generic loads and stores)
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
 
   Meta M{p.meta};
   if (p.level >= M.h(H_N_LEVEL)) return;

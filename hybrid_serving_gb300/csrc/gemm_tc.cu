@@ -47,7 +47,9 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc;
   __shared__ uint32_t tmem_slot;
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
+  // a shared-memory access (an integer round trip would turn them into generic loads and stores)
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
   const int nk = p.K / BK;
