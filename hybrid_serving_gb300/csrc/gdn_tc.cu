@@ -258,8 +258,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           break;
         }
         const uint8_t* src = scanbuf(e1 + i / 2) + ((i & 1) ? gdnws::kScanN : gdnws::kScanMhi);
-        tc::mbar_expect_tx(&bar_cb[b], 65536);
-        tc::bulk_load(smem + b * C::kStageBytes, src, 65536, &bar_cb[b]);
+        const uint32_t nb = (i & 1) ? 65536u : 32768u;  // N in fp32; the high part of M
+        tc::mbar_expect_tx(&bar_cb[b], nb);
+        tc::bulk_load(smem + b * C::kStageBytes, src, nb, &bar_cb[b]);
       }
       if (pro_ok && n_comb > 0 && !tc::mbar_wait(&bar_pd, (n_comb - 1) & 1, kWaitCycles)) pro_ok = false;
       if (!pro_ok) fail();
@@ -342,30 +343,23 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       // per stage and a K step adds a constant to the start-address field)
       {
         bool ok = true;
-        // start state of a later group: D = S_hi M_hi + S_hi M_lo + S_lo M_hi + I N_hi + I N_lo into the fp32
-        // state columns (I: a bf16 identity the rows place in the D1 columns, idle until the chunks)
+        // start state of a later group: S <- S M_q + N_q as D = N_q (placed in the fp32 state columns by the
+        // rows) + S_hi M_hi + S_lo M_hi, with S split into bf16 high and low parts and M in bf16
         for (int q = 1; q <= n_comb && ok; ++q) {
-          const int im = 2 * q - 2, in = 2 * q - 1;  // the items of M_q and N_q
+          const int im = 2 * q - 2;  // the item of M_q
           if (!__all_sync(~0u, tc::mbar_wait(&bar_cb[im % 3], (im / 3) & 1, kWaitCycles)) ||
-              !__all_sync(~0u, tc::mbar_wait(&bar_cb[in % 3], (in / 3) & 1, kWaitCycles)) ||
               !__all_sync(~0u, tc::mbar_wait_spin(&bar_ps, (q - 1) & 1, kWaitCycles))) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t sm = tc::smem_u32(smem);
-          const uint64_t dm0 = tc::sdesc_sw128(sm + (im % 3) * C::kStageBytes, 16384, 1024);
-          const uint64_t dn0 = tc::sdesc_sw128(sm + (in % 3) * C::kStageBytes, 16384, 1024);
-          const uint64_t dm1 = dm0 + (uint64_t)(32768 >> 4), dn1 = dn0 + (uint64_t)(32768 >> 4);
+          const uint64_t dm = tc::sdesc_sw128(tc::smem_u32(smem) + (im % 3) * C::kStageBytes, 16384, 1024);
 #pragma unroll
-          for (int pr = 0; pr < 5; ++pr) {
+          for (int pr = 0; pr < 2; ++pr) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t a = pr == 2 ? C::kTSlo : pr >= 3 ? C::kTD1 : C::kTS16;
-              const uint64_t b = pr == 0 || pr == 2 ? dm0 : pr == 1 ? dm1 : pr == 3 ? dn0 : dn1;
-              tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + a + 8 * k, b + (uint64_t)((k * 2048) >> 4), kIdesc128mn,
-                                (pr > 0 || k > 0) ? 1u : 0u);
-            }
+            for (int k = 0; k < 8; ++k)
+              tc::mma_bf16_ts_w(tmem + C::kTS32, tmem + (pr == 0 ? C::kTS16 : C::kTSlo) + 8 * k,
+                                dm + (uint64_t)((k * 2048) >> 4), kIdesc128mn, 1u);
           }
           tc::mma_commit_w(&bar_pd);
         }
@@ -580,11 +574,25 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
                 dst[q * 8 + i] = make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]),
                                              __uint_as_float(f[4 * i + 2]), __uint_as_float(f[4 * i + 3]));
             }
+          } else if (ekc == kEndScanN) {
+            // row j of N in fp32, its 16-byte pieces swizzled by j % 32 (read back row by row from shared
+            // memory by the rows of the combine, one row per lane)
+            uint8_t* dst = scanbuf(e) + gdnws::kScanN + j * 512;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t f[32];
+              tc::tmem_ld32(tb + C::kTS32 + q * 32, f);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4*>(dst + (((q * 8 + i) ^ (j & 31)) << 4)) =
+                    make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]), __uint_as_float(f[4 * i + 2]),
+                                __uint_as_float(f[4 * i + 3]));
+            }
           } else {
-            // row j of M (or N) as the bf16 high and low images of an MN-major B operand: element (j, n) in
-            // slab n / 64, 128-byte row j, 16-byte chunk (n % 64) / 8 swizzled by j % 8
-            uint8_t* mh = scanbuf(e) + (ekc == kEndScanM ? gdnws::kScanMhi : gdnws::kScanN);
-            uint8_t* ml = mh + 32768;
+            // row j of M as the bf16 image of an MN-major B operand: element (j, n) in slab n / 64, 128-byte
+            // row j, 16-byte chunk (n % 64) / 8 swizzled by j % 8
+            uint8_t* mh = scanbuf(e) + gdnws::kScanMhi;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint32_t f[32];
@@ -594,15 +602,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
               for (int c8 = 0; c8 < 4; ++c8) {
                 const int n0 = q * 32 + c8 * 8;
                 const int off = (n0 >> 6) * 16384 + (j >> 3) * 1024 + (j & 7) * 128 + ((((n0 & 63) >> 3) ^ (j & 7)) << 4);
-                uint32_t hw[4], lw[4];
+                uint32_t hw[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float a = __uint_as_float(f[c8 * 8 + 2 * i]), b = __uint_as_float(f[c8 * 8 + 2 * i + 1]);
-                  hw[i] = tc::pack_bf16x2(a, b);
-                  lw[i] = tc::pack_bf16x2(a - __uint_as_float(hw[i] << 16), b - __uint_as_float(hw[i] & 0xFFFF0000u));
-                }
+                for (int i = 0; i < 4; ++i)
+                  hw[i] = tc::pack_bf16x2(__uint_as_float(f[c8 * 8 + 2 * i]), __uint_as_float(f[c8 * 8 + 2 * i + 1]));
                 *reinterpret_cast<uint4*>(mh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(ml + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
               }
             }
           }
@@ -637,21 +641,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       tc::tmem_wait_st();
     }
-    // a later group's start state: S <- S M_q + N_q for q = 1 .. g-1, on tensor cores with S, M and N split
-    // into bf16 high and low parts (S_hi M_hi + S_hi M_lo + S_lo M_hi + I N_hi + I N_lo; I = the identity,
-    // written once into the D1 columns, which hold nothing until the chunks)
-    if (n_comb > 0) {
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t id[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k0 = c4 * 32 + 2 * i;  // columns k0, k0 + 1 of row j
-          id[i] = (k0 == j ? 0x3F80u : 0u) | (k0 + 1 == j ? 0x3F800000u : 0u);
-        }
-        tc::tmem_st16(tmem + lb + C::kTD1 + c4 * 16, id);
-      }
-    }
+    // a later group's start state: S <- S M_q + N_q for q = 1 .. g-1 on tensor cores: the rows split S into
+    // bf16 high and low parts, then write row j of N_q (fp32, from its combine buffer) over the fp32 state,
+    // and the MMAs add S_hi M_q + S_lo M_q to it
     for (int q = 1; q <= n_comb && ok; ++q) {
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
@@ -666,6 +658,27 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         }
         tc::tmem_st16(tmem + lb + C::kTS16 + c4 * 16, bh);
         tc::tmem_st16(tmem + lb + C::kTSlo + c4 * 16, bl);
+      }
+      const int in = 2 * q - 1;  // the item of N_q
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_cb[in % 3], (in / 3) & 1, kWaitCycles))) {
+        ok = false;
+        break;
+      }
+      {
+        const uint8_t* nrow = smem + (in % 3) * C::kStageBytes + j * 512;  // pieces swizzled by j % 32
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t f[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(nrow + (((c4 * 8 + i) ^ (j & 31)) << 4));
+            f[4 * i] = __float_as_uint(v.x);
+            f[4 * i + 1] = __float_as_uint(v.y);
+            f[4 * i + 2] = __float_as_uint(v.z);
+            f[4 * i + 3] = __float_as_uint(v.w);
+          }
+          tc::tmem_st32(tmem + lb + C::kTS32 + c4 * 32, f);
+        }
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -778,32 +791,6 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         for (int i = 0; i < 8; ++i)
           dst[q * 8 + i] = make_float4(__uint_as_float(f[4 * i]), __uint_as_float(f[4 * i + 1]),
                                        __uint_as_float(f[4 * i + 2]), __uint_as_float(f[4 * i + 3]));
-      }
-    } else if (ek == kEndScanM || ek == kEndScanN) {
-      // row j of the transition M (or of the zero-start end state N) as the bf16 high and low images of an
-      // MN-major B operand: element (j, n) in slab n / 64, 128-byte row j, 16-byte chunk (n % 64) / 8
-      // swizzled by j % 8
-      uint8_t* mh = scanbuf(e) + (ek == kEndScanM ? gdnws::kScanMhi : gdnws::kScanN);
-      uint8_t* ml = mh + 32768;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t f[32];
-        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int n0 = q * 32 + c * 8;
-          const int off = (n0 >> 6) * 16384 + (j >> 3) * 1024 + (j & 7) * 128 + ((((n0 & 63) >> 3) ^ (j & 7)) << 4);
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float a = __uint_as_float(f[c * 8 + 2 * i]), b = __uint_as_float(f[c * 8 + 2 * i + 1]);
-            hw[i] = tc::pack_bf16x2(a, b);
-            lw[i] = tc::pack_bf16x2(a - __uint_as_float(hw[i] << 16), b - __uint_as_float(hw[i] & 0xFFFF0000u));
-          }
-          *reinterpret_cast<uint4*>(mh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(ml + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
       }
     }
     }

@@ -26,14 +26,13 @@ constexpr int kFloats = kBytes / 4;
 // Per (extra scan group, head) buffers of the two-level state scan, after the
 // per-chunk blocks: the end state of the node's first group S (fp32
 // [128][128], rows d_v; in the entry of group 1), the group's zero-start end
-// state N (d_v x d_k) and its transition M (d_k x d_k), each as the bf16 high
-// and low images of an MN-major B operand (two [128][64] slabs each: row k
-// holds X[k][n]; N enters the combine as I N).
+// state N (fp32 [128][128], row j's 16-byte pieces swizzled by j % 32) and
+// its transition M (d_k x d_k) as the bf16 image of an MN-major B operand
+// (two [128][64] slabs: row k holds M[k][n]).
 constexpr int kScanS = 0;
 constexpr int kScanN = 65536;
 constexpr int kScanMhi = 131072;
-constexpr int kScanMlo = 163840;
-constexpr int kScanBytes = 196608;
+constexpr int kScanBytes = 163840;
 
 // Byte offset of bf16 element (row, col) in a 128-byte-swizzled K-major image
 // made of [rows][64]-element slabs (one slab per 64 columns): 16-byte chunk c
