@@ -520,7 +520,13 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 //               over the scores for the row max, a second for the
 //               exponentials, 32 keys at a time); P overwrites S in place:
 //               the 32 score columns of keys 32g .. 32g+31 become 16 columns
-//               of bf16 high parts (top 16 bits) and 16 of rounded low parts.
+//               of P in bf16.  A tile holding a readout row keeps ~16
+//               significant bits of P -- the 16 columns hold its high parts
+//               (top 16 bits), the next 16 its rounded low parts, and both
+//               enter P.V -- because the option distribution at a readout
+//               row is sensitive to single-ulp changes of the bf16 output;
+//               every other tile rounds P to bf16 (nearest) and issues half
+//               the P.V products.
 //               Since S_X(j) is computed after P.V_X(j-1) is issued, O_X is
 //               final for block j-1 when S_X(j) is seen, so a lazy rescale
 //               (running max grown by more than 2^8) never waits.
@@ -721,14 +727,16 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         tc::mma_commit_w(&bar_sf[x][h]);
       };
-      // O_X += P_X(jj, h) V_jj[64h .. 64h+63], per 32 keys: high, then low parts
-      auto pv_mma = [&](int x, int jj, int h, bool first) {
+      // O_X += P_X(jj, h) V_jj[64h .. 64h+63], per 32 keys: the high (or only) part, then (readout tiles)
+      // the low part
+      auto pv_mma = [&](int x, int jj, int h, bool first, bool precise) {
         const uint64_t b0 = dv0 + (uint64_t)(((jj & 1) * kTile + h * 8192) >> 4);
         const uint32_t pt = tmem + pair::kTmS + 128 * x + 64 * h, d = tmem + pair::kTmO + 128 * x;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
+            if (part == 1 && !precise) continue;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {  // keys 64 h + 32 g + 16 k .. +15
               tc::mma_bf16_ts_w(d, pt + 32 * g + 16 * part + 8 * k, b0 + (uint64_t)((g * 4096 + k * 2048) >> 4),
@@ -743,6 +751,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (w < 0) break;
         Cursor cur;
         cur.init(M, M.tile(w / np));
+        const bool precise = M.tile(w / np)[TL_READOUT] != 0;
         int n_blk = 0;
         while (cur.next()) ++n_blk;  // counted once: the loop needs no cursor
         if (n_blk == 0) continue;
@@ -769,7 +778,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
               break;
             }
             tc::fence_after_sync();
-            pv_mma(x, jb, h, v == 0);  // (the item's first P.V_X starts O_X afresh)
+            pv_mma(x, jb, h, v == 0, precise);  // (the item's first P.V_X starts O_X afresh)
             if (h == 1) tc::mma_commit_w(&bar_ve[jb & 1]);
             if (v2 < nh) {
               if (h == 0 && !__all_sync(~0u, tc::mbar_wait_spin(&bar_kf[jb2 & 1], (jb2 >> 1) & 1, kWaitCycles))) {
@@ -816,6 +825,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       cur.init(M, tl);
       const int row = tl[TL_ROW0] + t;
       const bool active = t < tl[TL_N_ROWS];
+      const bool precise = tl[TL_READOUT] != 0;
       int my_seg = -1, my_idx = 0;
       if (active) {
         my_seg = M.tok(row)[T_SEG];
@@ -899,20 +909,33 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = 32 * g + i < lh ? r[i] : 0xFF800000u;
             }
+            if (precise) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float ya, yb;
-              tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
-              const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
-              const uint64_t ab = tc::f2_pack(a, b);
-              acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
-              hi[i] = tc::pack_bf16x2_trunc(a, b);
-              float da, db;
-              tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
-              lo[i] = tc::pack_bf16x2(da, db);
+              for (int i = 0; i < 16; ++i) {
+                float ya, yb;
+                tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
+                const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
+                const uint64_t ab = tc::f2_pack(a, b);
+                acc2[i & 3] = tc::f2_add(acc2[i & 3], ab);
+                hi[i] = tc::pack_bf16x2_trunc(a, b);
+                float da, db;
+                tc::f2_unpack(tc::f2_sub(ab, tc::f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xFFFF0000u))), da, db);
+                lo[i] = tc::pack_bf16x2(da, db);
+              }
+              tc::tmem_st16(sb + 32 * g, hi);
+              tc::tmem_st16(sb + 32 * g + 16, lo);
+            } else {
+              // P rounded to bf16
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float ya, yb;
+                tc::f2_unpack(tc::f2_fma(tc::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, mm2), ya, yb);
+                const float a = tc::ex2_approx(ya), b = tc::ex2_approx(yb);
+                acc2[i & 3] = tc::f2_add(acc2[i & 3], tc::f2_pack(a, b));
+                hi[i] = tc::pack_bf16x2(a, b);
+              }
+              tc::tmem_st16(sb + 32 * g, hi);
             }
-            tc::tmem_st16(sb + 32 * g, hi);
-            tc::tmem_st16(sb + 32 * g + 16, lo);
           }
           float rp[8];
 #pragma unroll

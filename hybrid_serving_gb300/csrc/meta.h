@@ -117,8 +117,9 @@ enum : int { SP_PAGE_REF_OFF = 0, SP_N_TOK, SP_OWNER, SP_PAD };
 // attention tile: n_rows consecutive stream rows (all children of one parent,
 // or one segment), whose keys are the n_shared spans visible to every row
 // followed by n_own own spans (each visible causally to its owner's rows only).
+// READOUT = 1 when one of its rows is a readout row (the option head reads it).
 constexpr int kTileWords = 8;
-enum : int { TL_ROW0 = 0, TL_N_ROWS, TL_SPAN_OFF, TL_N_SHARED, TL_N_OWN, TL_WORK, TL_SEG0, TL_PAD };
+enum : int { TL_ROW0 = 0, TL_N_ROWS, TL_SPAN_OFF, TL_N_SHARED, TL_N_OWN, TL_WORK, TL_SEG0, TL_READOUT };
 
 // GDN chunk: len <= 64 rows starting at stream row ROW0, inside segment SEG
 constexpr int kChunkWords = 4;

@@ -444,6 +444,17 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     }
   }
 
+  // readouts (section 3.3.3): the last token of each readout node, in node order
+  r->readouts.clear();
+  for (int32_t i = 0; i < n; ++i) {
+    Seg& s = S[i];
+    bool ro = (s.flags & HS_SEG_READOUT) || (s.children.empty() && !(s.flags & HS_SEG_NO_READOUT));
+    s.readout_row = ro ? s.stream_off + s.n_tok - 1 : -1;
+    if (ro) r->readouts.push_back(s.readout_row);
+  }
+  if ((int32_t)r->readouts.size() > C.max_readouts)
+    return hs::fail(HS_ECAPACITY, "%d readouts > max_readouts %d", (int)r->readouts.size(), C.max_readouts);
+
   // attention tiles (section 3.3.1 tile table; section 3.5: tiles start at the node)
   std::vector<int32_t> tiles, tile_spans;
   auto blocks = [](int32_t keys) { return (keys + kTileRows - 1) / kTileRows; };
@@ -459,7 +470,8 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
         int32_t off = (int32_t)tile_spans.size();
         tile_spans.insert(tile_spans.end(), anc[id].begin(), anc[id].end());
         tile_spans.push_back(s.own_span);
-        int32_t rec[kTileWords] = {s.stream_off + r0, nr, off, (int32_t)anc[id].size(), 1, work, id, 0};
+        const int32_t ro = s.readout_row >= s.stream_off + r0 && s.readout_row < s.stream_off + r0 + nr;
+        int32_t rec[kTileWords] = {s.stream_off + r0, nr, off, (int32_t)anc[id].size(), 1, work, id, ro};
         tiles.insert(tiles.end(), rec, rec + kTileWords);
       }
       ++oi;
@@ -482,7 +494,9 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     int32_t off = (int32_t)tile_spans.size();
     tile_spans.insert(tile_spans.end(), anc[id].begin(), anc[id].end());
     for (int32_t m : members) tile_spans.push_back(S[m].own_span);
-    int32_t rec[kTileWords] = {s.stream_off, rows, off, (int32_t)anc[id].size(), (int32_t)members.size(), work, id, 0};
+    int32_t ro = 0;
+    for (int32_t m : members) ro |= S[m].readout_row >= 0;
+    int32_t rec[kTileWords] = {s.stream_off, rows, off, (int32_t)anc[id].size(), (int32_t)members.size(), work, id, ro};
     tiles.insert(tiles.end(), rec, rec + kTileWords);
     oi = oj;
   }
@@ -553,17 +567,6 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     }
     s.init_slot = s.parent >= 0 ? S[s.parent].end_slot : s.resume_slot;
   }
-
-  // readouts (section 3.3.3): the last token of each readout node, in node order
-  r->readouts.clear();
-  for (int32_t i = 0; i < n; ++i) {
-    Seg& s = S[i];
-    bool ro = (s.flags & HS_SEG_READOUT) || (s.children.empty() && !(s.flags & HS_SEG_NO_READOUT));
-    s.readout_row = ro ? s.stream_off + s.n_tok - 1 : -1;
-    if (ro) r->readouts.push_back(s.readout_row);
-  }
-  if ((int32_t)r->readouts.size() > C.max_readouts)
-    return hs::fail(HS_ECAPACITY, "%d readouts > max_readouts %d", (int)r->readouts.size(), C.max_readouts);
 
   // ---- pack ----
   const Layout& L = r->L;

@@ -48,3 +48,31 @@ def causal_attention(q, k, v, scale: float, rows=None, window: int | None = None
         o = np.einsum("hgu,uhd->hgd", p, vv) / l
         out[o_i] = o.reshape(hq, d)
     return out
+
+
+def causal_attention_rows(q, k, v, scale: float, rows=None, window: int | None = None):
+    """The same quantity as causal_attention, evaluated one query head at a
+    time as a matrix: the scores of the requested rows against every key,
+    the keys after a row (and, with ``window``, those W or more positions
+    before it) set to -inf, then the row-max-subtracted softmax and its
+    product with V, all in float64.  Same arguments and result layout.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    assert hq % hkv == 0
+    g = hq // hkv
+    rows = np.arange(n) if rows is None else np.asarray(list(rows), dtype=np.int64)
+    u = np.arange(n)
+    visible = u[None, :] <= rows[:, None]
+    if window is not None:
+        visible &= u[None, :] > rows[:, None] - window
+    out = np.empty((len(rows), hq, d), dtype=np.float64)
+    for h in range(hq):
+        kv = h // g
+        s = np.where(visible, (q[rows, h] @ k[:, kv].T) * scale, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        out[:, h] = (p @ v[:, kv]) / p.sum(axis=1, keepdims=True)
+    return out

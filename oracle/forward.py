@@ -29,11 +29,13 @@ def _path_seq(inp, r: int, req, node: int, key: str):
 
 def attention_tree(tree, inp, scale: float, nodes: Optional[Iterable[Tuple[int, int]]] = None,
                    rows: Optional[Dict[Tuple[int, int], Iterable[int]]] = None,
-                   window: Optional[int] = None):
+                   window: Optional[int] = None, matrix: bool = False):
     """Returns {(r, node): o [n_rows, Hq, d]} for the requested nodes.
 
     ``rows`` optionally restricts a node to some of its row indices (a
     sampled check); each row is still its isolated-sequence output.
+    ``matrix`` evaluates each isolated sequence with the matrix form of the
+    same definition (attention.causal_attention_rows) -- for thousands of rows.
     """
     out = {}
     if nodes is None:
@@ -46,8 +48,8 @@ def attention_tree(tree, inp, scale: float, nodes: Optional[Iterable[Tuple[int, 
         sel = list(range(req.n_tok[i])) if rows is None or (r, i) not in rows else list(rows[(r, i)])
         q = np.zeros((k.shape[0], inp.hq, inp.d))
         q[n_before:] = inp.nodes[(r, i)]["q"]
-        out[(r, i)] = _attn.causal_attention(q, k, v, scale, rows=[n_before + u for u in sel],
-                                             window=window)
+        f = _attn.causal_attention_rows if matrix else _attn.causal_attention
+        out[(r, i)] = f(q, k, v, scale, rows=[n_before + u for u in sel], window=window)
     return out
 
 

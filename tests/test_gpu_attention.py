@@ -30,6 +30,7 @@ def _check(tree, inp, dtype, tol, **kw):
     got = run.outputs()
     ref = forward.attention_tree(tree, inp, 1 / math.sqrt(inp.d))
     err = max_abs(got, ref)
+    print(f"[margin] attention {dtype} max-abs {err:.3e} (bar {tol:.0e})")
     assert err <= tol, f"max abs err {err}"
     return run, got, ref
 
@@ -78,22 +79,22 @@ def test_resumed_history_bf16():
     assert max_abs(got, ref) <= TOL_BF16
 
 
-def test_full_size_sampled_and_choices():
+def test_full_size_all_rows_and_choices():
     """The attention workload at full size (trunk 4096, 8 branches of
-    U[16,64], GQA 32/8, d=128, bf16): sampled trunk rows, every row of two
-    branches, and the 4-option distribution of every branch."""
+    U[16,64], GQA 32/8, d=128, bf16): every trunk row and every row of every
+    branch against its isolated pass -- so every work item of the persistent
+    kernel is checked -- and the 4-option distribution of every branch."""
     tree = synth.attn_tree()
     inp = synth.attn_inputs(tree, 32, 8, 128, seed=2000, bf16=True)
     run = AttnRun(tree, inp, torch.bfloat16).run()
     api.check_status(run.status)
     got = run.outputs()
     req = tree.requests[0]
-    rows = {(0, 0): [0, 1, 15, 16, 127, 128, 129, 1000, 2047, 2048, 4094, 4095]}
-    nodes = [(0, 0), (0, 1), (0, req.n_nodes - 1)]
-    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(128), nodes=nodes, rows=rows)
-    err = max(float(np.abs(got[(0, 0)][rows[(0, 0)]] - ref[(0, 0)]).max()),
-              max_abs(got, ref, keys=nodes[1:]))
-    assert err <= TOL_BF16, err
+    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(128), matrix=True)
+    e_tr = float(np.abs(got[(0, 0)] - ref[(0, 0)]).max())
+    e_br = max_abs(got, ref, keys=[(0, b) for b in range(1, req.n_nodes)])
+    print(f"[margin] attention full size: trunk rows max-abs {e_tr:.3e}, branch rows {e_br:.3e} (bar 2e-2)")
+    assert e_tr <= TOL_BF16 and e_br <= TOL_BF16
     # choices: logits over the concatenated head outputs of each branch's last token
     W = synth.option_rows(4, 32 * 128, seed=2001)
     Wd = torch.from_numpy(W).cuda()
@@ -107,6 +108,7 @@ def test_full_size_sampled_and_choices():
     p_ref = np.exp(ochoice.option_logprobs(h, W))
     p_gpu = np.exp(lp.cpu().numpy().astype(np.float64))
     tv = ochoice.total_variation(p_gpu, p_ref)
+    print(f"[margin] attention full size: option TV max {tv.max():.3e} (bar 1e-3)")
     assert tv.max() <= TOL_TV, tv
     assert (ochoice.top1(p_gpu) == ochoice.top1(p_ref)).all()
     # the kernel alone, on the GPU's own hidden rows

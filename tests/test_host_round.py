@@ -528,3 +528,19 @@ def test_bulk_add_checks_everything_first():
         assert e.value.code == code
     # nothing of the refused calls was added: the next id is still 2
     assert R.add_segments([1], [3], [0], [-1]) == 2
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+def test_tile_readout_flag(ti):
+    """Word 7 of a tile record is 1 exactly when one of the tile's rows is a
+    readout row (the attention kernel keeps ~16 bits of P there), and every
+    row of the stream lies in exactly one tile."""
+    tree = TREES[ti]
+    R, seg_of, pool, B = make(tree)
+    ro = set(int(x) for x in B.readouts)
+    covered = []
+    for tl in B.tiles:
+        rows = range(int(tl[0]), int(tl[0]) + int(tl[1]))
+        covered.extend(rows)
+        assert int(tl[7]) == int(any(r in ro for r in rows)), tl
+    assert sorted(covered) == list(range(B.h("N_TOK")))

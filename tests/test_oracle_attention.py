@@ -210,3 +210,26 @@ def test_stream_permutation_leaves_results_unchanged():
     ref = forward.attention_tree(tree, inp, 1 / math.sqrt(d))
     for (r, i), off in lay.items():
         np.testing.assert_allclose(base[off:off + tree.requests[r].n_tok[i]], ref[(r, i)], atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [None, 5])
+def test_matrix_form_equals_row_loop(window):
+    """causal_attention_rows (a masked score matrix per head) reproduces the
+    per-row definition on a ragged GQA case, all rows and a subset, with and
+    without a sliding window."""
+    rng = np.random.default_rng(41)
+    n, hq, hkv, d = 37, 6, 2, 16
+    q, k, v = (rng.standard_normal((n, h, d)) for h in (hq, hkv, hkv))
+    for rows in (None, [0, 1, 17, 36]):
+        a = attention.causal_attention(q, k, v, 0.3, rows=rows, window=window)
+        b = attention.causal_attention_rows(q, k, v, 0.3, rows=rows, window=window)
+        np.testing.assert_allclose(b, a, rtol=0, atol=1e-13)
+
+
+def test_matrix_form_tree_equals_row_loop():
+    tree = synth.Tree([synth.fork_tree(50, [7, 1, 12]), synth.fanout_tree(20, 5, 2, 2)])
+    inp = synth.attn_inputs(tree, 4, 2, 32, seed=42, bf16=False)
+    a = forward.attention_tree(tree, inp, 0.2)
+    b = forward.attention_tree(tree, inp, 0.2, matrix=True)
+    for key in a:
+        np.testing.assert_allclose(b[key], a[key], rtol=0, atol=1e-13)
