@@ -502,8 +502,9 @@ fork_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 // even size share every K and V page): the heads' online softmaxes run in two
 // warp groups while the MMA warp alternates between them, so one head's
 // softmax overlaps the other head's products and each K/V block is loaded
-// once.  One persistent CTA per SM walks its items (tiles longest first,
-// dealt to the CTAs in snake order); block counters run across items, the
+// once.  One persistent CTA per SM takes items one at a time from a counter
+// in the round's metadata (tiles longest first, so this is longest-first
+// list scheduling); block counters run across items, the
 // next item's Q loads once the current item's S products are done, and its
 // first P.V waits until the current item's O has been read out, so the next
 // item's first S products and copies overlap the current item's epilogue.
@@ -539,6 +540,7 @@ constexpr int kSmemBytes = kOffV + 2 * kTile;  // 192 KB
 constexpr uint32_t kTmS = 0, kTmO = 256;  // S_X[h] at 128 X + 64 h, O_X at 256 + 128 X
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, 64, 0, 0);  // S of 64 keys: A = Q, B = K (K-major)
 constexpr int kWarpMmaB = 10, kThreads = 352;  // warp 9: MMAs of head A, warp 10: of head B
+constexpr int kRing = 4;                       // items published ahead by the producer
 }  // namespace pair
 
 __global__ void __launch_bounds__(pair::kThreads, 1)
@@ -548,18 +550,27 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qe, bar_kf[2], bar_vf[2], bar_ke[2], bar_ve[2];
   __shared__ uint64_t bar_sf[2][2], bar_pf[2][2], bar_pv[2], bar_done;
+  __shared__ uint64_t bar_rf[pair::kRing], bar_re[pair::kRing];  // item ring: index written / read by all
+  __shared__ int ring[pair::kRing];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   Meta M{p.meta};
   const int np = p.hq / 2;
   const int n_items = M.h(H_N_TILE) * np;  // (tile, head pair), heaviest tiles first
+  const int n_cta = min((int)gridDim.x, n_items);
   if ((int)blockIdx.x >= n_items) return;
-  // this CTA's k-th item: round k of the items, dealt to the CTAs in snake order
-  auto item_of = [&](int k) -> int {
-    const int G = gridDim.x;
-    const int w = k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
-    return w < n_items ? w : -1;
+  // Items are handed out in order to whichever CTA asks next (a counter in the round's metadata, longest-
+  // first list scheduling): the producer lane takes the CTA's k-th item and publishes it in ring slot
+  // k % kRing; the MMA and softmax warps read the same sequence.  -1 ends it.
+  int32_t* ctr = const_cast<int32_t*>(p.meta);
+  auto item_of = [&](int k) -> int {  // every consumer warp, converged; false from a wait means a timeout
+    const int s = k % pair::kRing;
+    if (!__all_sync(~0u, tc::mbar_wait(&bar_rf[s], (k / pair::kRing) & 1, kWaitCycles))) return -2;
+    const int w = *(volatile int*)&ring[s];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&bar_re[s]);
+    return w;
   };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
@@ -582,6 +593,10 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tc::mbar_init(&bar_pv[s], 1);   // [X]: P.V_X of a key half done
     }
     tc::mbar_init(&bar_done, 2);
+    for (int r = 0; r < pair::kRing; ++r) {
+      tc::mbar_init(&bar_rf[r], 1);
+      tc::mbar_init(&bar_re[r], 2 + kSoftWarps);  // both MMA warps and the softmax warps
+    }
     tc::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -612,7 +627,19 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       int jg = 0, n_q = 0;                           // blocks and Q tiles (non-empty items) issued
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int w = item_of(k);
+        // take the next item and publish it (ring slot k % kRing once its previous item is read by all)
+        const int rs = k % pair::kRing;
+        if (k >= pair::kRing && !tc::mbar_wait(&bar_re[rs], (k / pair::kRing - 1) & 1, kWaitCycles)) {
+          record(p.status, &abort_flag, HS_DEV_TIMEOUT);
+          ok = false;
+        }
+        int w = -1;
+        if (ok && !*(volatile int*)&abort_flag) {
+          w = atomicAdd(ctr + H_ATTN_NEXT, 1);
+          if (w >= n_items) w = -1;
+        }
+        *(volatile int*)&ring[rs] = w;
+        tc::mbar_arrive(&bar_rf[rs]);
         if (w < 0) break;
         const int32_t* tl = M.tile(w / np);
         const int h0 = 2 * (w % np), kvh = h0 / (p.hq / p.hkv);
@@ -748,6 +775,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       };
       for (int k = 0; ok; ++k) {
         const int w = item_of(k);
+        if (w == -2) ok = false;
         if (w < 0) break;
         Cursor cur;
         cur.init(M, M.tile(w / np));
@@ -818,6 +846,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int w = item_of(k);
+      if (w == -2) ok = false;
       if (w < 0) break;
       const int32_t* tl = M.tile(w / np);
       const int h0 = 2 * (w % np);
@@ -852,21 +881,24 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             break;
           }
           tc::fence_after_sync();
-          // pass 1: the row max of the half, 32 scores at a time (scores past the row's visible keys read as -inf)
+          // the half's 64 scores in registers (one load, one wait; scores past the row's visible keys read as
+          // -inf), then pass 1: the row max
           const bool masked = __any_sync(~0u, lh < 64);
+          uint32_t sr[2][32];
+          tc::tmem_ld32(sb, sr[0]);
+          tc::tmem_ld32(sb + 32, sr[1]);
+          tc::tmem_wait_ld();
           float mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t r[32];
-            tc::tmem_ld32(sb + 32 * c, r);
-            tc::tmem_wait_ld();
             if (masked) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 32 * c + i < lh ? r[i] : 0xFF800000u;
+              for (int i = 0; i < 32; ++i) sr[c][i] = 32 * c + i < lh ? sr[c][i] : 0xFF800000u;
             }
             float m2[2] = {mx, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            for (int i = 0; i < 16; ++i)
+              m2[i & 1] = tc::max3(m2[i & 1], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
             mx = fmaxf(m2[0], m2[1]);
           }
           const float m_new = fmaxf(m_used, mx * sl2);
@@ -902,13 +934,8 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int g = 0; g < 2; ++g) {  // keys 64 h + 32 g .. +31: P words in the same 32 columns (16 high, 16 low)
-            uint32_t r[32], hi[16], lo[16];
-            tc::tmem_ld32(sb + 32 * g, r);
-            tc::tmem_wait_ld();
-            if (masked) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 32 * g + i < lh ? r[i] : 0xFF800000u;
-            }
+            const uint32_t* r = sr[g];
+            uint32_t hi[16], lo[16];
             if (precise) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -991,6 +1018,16 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   __syncthreads();
   tc::fence_after_sync();
   if (warp == kWarpMma) tc::tmem_dealloc(tmem, 512);
+  // the last CTA to finish sets the counters back to zero for the next launch on this metadata (every CTA's
+  // last take from H_ATTN_NEXT precedes its increment of H_ATTN_DONE)
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ctr + H_ATTN_DONE, 1) == n_cta - 1) {
+      atomicExch(ctr + H_ATTN_NEXT, 0);
+      atomicExch(ctr + H_ATTN_DONE, 0);
+      __threadfence();
+    }
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -61,6 +61,10 @@ enum : int {
   H_N_SCAN,          // extra scan groups (group 1 and up of the long nodes), all levels
   H_OFF_SCAN,        // [segment, group] per extra scan group, grouped by level
   H_OFF_SCAN_LEVEL,  // [max_levels + 1] prefix offsets into SCAN
+  // the paired-head attention kernel's work counters: the next (tile, head pair) item to hand out and the
+  // CTAs done; zero as uploaded, and set back to zero by the kernel's last CTA
+  H_ATTN_NEXT,
+  H_ATTN_DONE,
 };
 
 // The GDN state chain of a long node is split into groups of consecutive

@@ -504,13 +504,14 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
   if (n_tiles > C.max_tiles) return hs::fail(HS_ECAPACITY, "%d tiles > max_tiles %d", n_tiles, C.max_tiles);
   if ((int32_t)tile_spans.size() > C.max_tile_spans)
     return hs::fail(HS_ECAPACITY, "%d tile spans > max_tile_spans %d", (int)tile_spans.size(), C.max_tile_spans);
-  // heaviest tiles first (a static strided schedule then balances like LPT)
+  // heaviest tiles first: the paired-head attention kernel hands its (tile, head pair) items out in this
+  // order to whichever CTA asks next, i.e. longest-first list scheduling
   {
     std::vector<int32_t> idx(n_tiles);
     for (int32_t i = 0; i < n_tiles; ++i) idx[i] = i;
-    std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
-      return tiles[a * kTileWords + TL_WORK] > tiles[b * kTileWords + TL_WORK];
-    });
+    // (a tile with a readout row costs ~1.4x per key block: its P.V products carry P's low part too)
+    auto cost = [&](int32_t i) { return (int64_t)tiles[i * kTileWords + TL_WORK] * (tiles[i * kTileWords + TL_READOUT] ? 7 : 5); };
+    std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return cost(a) > cost(b); });
     std::vector<int32_t> sorted(tiles.size());
     for (int32_t i = 0; i < n_tiles; ++i)
       memcpy(&sorted[i * kTileWords], &tiles[idx[i] * kTileWords], kTileWords * 4);
