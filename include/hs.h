@@ -212,7 +212,16 @@ hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep_
  *   out    [Tcap, hq, d]  dt        (bf16 outputs are round-to-nearest-even)
  * Supported: dt in {HS_F32, HS_BF16}; d in {64, 128}; hq % hkv == 0;
  * page_size 16.  Inputs must be 16-byte aligned.  Accumulation is fp32;
- * the result of a row does not depend on what else is in the round. */
+ * the result of a row does not depend on what else is in the round.
+ * Precision (bf16, d = 128): P = softmax weights enter P.V rounded to bf16,
+ * except on attention tiles holding a readout row, where P keeps ~16
+ * significant bits (a bf16 high part and low part) because the option
+ * distribution read there is sensitive to single-ulp output changes.
+ * dev_meta is read, except for two header words (the bf16 d = 128 kernel's
+ * work counter: items are handed to CTAs in order, longest first): they are
+ * zero as the round uploads them and the kernel sets them back to zero
+ * before it completes, so launches on one metadata buffer must run one at a
+ * time (stream order or graph order), never concurrently. */
 hs_status hs_fork_attn_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt,
                                int32_t hq, int32_t hkv, int32_t d, float scale, const void* q,
                                const void* k_new, const void* v_new, void* k_pages, void* v_pages,
