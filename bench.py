@@ -107,25 +107,87 @@ def gdn_bytes(tree) -> float:
 # clock sampling during the timed region
 # ---------------------------------------------------------------------------
 class Clocks:
+    """SM clock and clock-event reasons sampled during the timed region.
+
+    Read-only NVML queries through ctypes (libnvidia-ml), polled every
+    ~0.2 ms from a thread, so a region of a few milliseconds still gets
+    samples; nvidia-smi (20 ms period) is the fallback.  The device is found
+    by the CUDA device's UUID, then its PCI bus id.
+    """
+    # clock-event reason bits (NVML's nvmlClocksEventReason* values)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, torch, index: int):
+        self.torch, self.index = torch, index
         self.p = None
+        self.nv = None
+        self.samples = []   # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.lines = []
+        self.source = "none"
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        props = self.torch.cuda.get_device_properties(self.index)
+        uuid = getattr(props, "uuid", None)
+        ok = False
+        if uuid is not None:
+            u = str(uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            ok = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        if not ok and hasattr(props, "pci_bus_id"):
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                        getattr(props, "pci_device_id", 0))
+            ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = nv.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) == 0
+        return (nv, h) if ok else (None, None)
 
     def __enter__(self):
+        import threading
+        try:
+            self.nv, self.h = self._nvml_handle()
+        except OSError:
+            self.nv = None
+        if self.nv is not None:
+            import ctypes
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+                self.max_mhz = float(mx.value)
+            self.stop = threading.Event()
+
+            def poll():
+                clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self.stop.is_set():
+                    if (self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0 and
+                            self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0):
+                        self.samples.append((float(clk.value), int(rs.value)))
+                    time.sleep(0.0002)
+            self.th = threading.Thread(target=poll, daemon=True)
+            self.th.start()
+            self.source = "nvml"
+            return self
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                                        "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except OSError:
             self.p = None
         return self
 
     def __exit__(self, *a):
-        self.lines = []
+        if self.nv is not None:
+            self.stop.set()
+            self.th.join(timeout=2)
         if self.p is not None:
             self.p.terminate()
             try:
@@ -137,6 +199,13 @@ class Clocks:
 
     def summary(self):
         sm, mx, reasons = [], [], set()
+        for mhz, bits in self.samples:
+            sm.append(mhz)
+            for b, n in self.REASONS.items():
+                if bits & b:
+                    reasons.add(n)
+        if self.max_mhz:
+            mx.append(self.max_mhz)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
@@ -149,9 +218,10 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm), "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -346,6 +416,108 @@ class Step:
         return h2d, d2h
 
 
+# ---------------------------------------------------------------------------
+# the other configurations: resume at full size, hybrid stack, agent tree
+# ---------------------------------------------------------------------------
+STACK = dict(hidden=2048, pattern="GGGAGGGA", attn_hq=16, attn_hkv=4, head_d=128, gdn_h=16, gdn_d=128, ffn=4096,
+             vocab=32768)
+
+
+def _timed(torch, fn, reps: int, warm: int = 1) -> float:
+    """Mean device ms of fn() over reps, CUDA events on the current stream, after warm-up."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        fn()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def gdn_resume_config(torch, api, rounds, pk, reps: int = 20):
+    """Resume from the checkpoint at 8192 after appending 1024 trunk tokens (16 branches): round A
+    saves the trunk's state at 8192 once; round B -- trunk tokens [8192, 9216) from that slot, then
+    the branches from the new end state -- is timed.  Tokens = the new tokens only."""
+    a_tree, b_tree, full = synth.gdn_checkpoint_trees(8192)
+    inp = synth.gdn_inputs(full, GDN["h"], GDN["d"], GDN["d"], seed=GDN["seed"], bf16=True, law="softplus")
+    state = torch.zeros((24, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def prep(tree, resume=None):
+        sub = synth.remap_inputs(full, inp, tree)
+        R, seg = rounds.build_round(tree, None, temp_slot0=4, n_temp_slots=20, resume=resume)
+        meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+        R.upload(meta)
+        x = [torch.from_numpy(rounds.to_stream(R, seg, sub.nodes, k)).cuda().to(dt)
+             for k, dt in (("q", torch.bfloat16), ("k", torch.bfloat16), ("v", torch.bfloat16),
+                           ("alpha", torch.float32), ("beta", torch.float32))]
+        out = torch.empty((x[0].shape[0], GDN["h"], GDN["d"]), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(api.gdn_workspace_bytes(R.caps, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.uint8,
+                         device="cuda")
+        return lambda: api.gdn_fork_prefill(R.caps, meta, *x, state, out, ws, status)
+
+    prep(a_tree)()
+    ms = _timed(torch, prep(b_tree, resume={0: (0, [])}), reps)
+    api.check_status(status)
+    T = b_tree.useful_tokens()
+    n_br = b_tree.requests[0].n_nodes - 1
+    h, d = GDN["h"], GDN["d"]
+    nbytes = T * h * (4 * d * 2 + 8) + (n_br + 2) * h * d * d * 4  # q,k,v,o + alpha,beta; checkpoint + branch reads, end write
+    return {"workload": "gdn resume: checkpoint at 8192, +1024 trunk tokens, 16 branches U[8,128], H16 d128",
+            "tokens": T, "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "bound": "hbm",
+            "bytes": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "peak_gbs": pk["hbm_gbs"],
+            "frac": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+
+
+def _linear_flops_per_token(W) -> float:
+    """2 x the weights every token multiplies by (the projections, output projections and MLPs of all
+    layers; the embedding is a lookup and the option rows are read at the readout rows only)."""
+    return 2.0 * sum(w.size for k, w in W.items() if k != "embed" and not k.endswith(".conv"))
+
+
+def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int = 3):
+    """The 8-layer hybrid stack (hidden 2048, G,G,G,A x2, random-init bf16 weights N(0, 0.02)) on the
+    64-request mixed batch and on the deep agent tree (10 sessions, trunk 256, depth 3 x fan-out 4
+    of 32-token residuals), one forward per timed repetition.  Tensor-core fraction: the linear
+    layers' flops (which dominate) over the forward's time, against the measured bf16 peak."""
+    from oracle import layout
+    from hybrid_serving_gb300.stack import HybridStack, StackShape
+    W = synth.stack_weights(STACK["hidden"], STACK["pattern"], STACK["attn_hq"], STACK["attn_hkv"], STACK["head_d"],
+                            STACK["gdn_h"], STACK["gdn_d"], STACK["ffn"], STACK["vocab"], seed=4100)
+    fpt = _linear_flops_per_token(W)
+    out = {}
+    for name, tree, reps in (("hybrid_stack", synth.mixed_tree(seed=4000), reps_mixed),
+                             ("agent_tree", synth.agent_tree(10, 256, 32, 4, 3, spine_slot=0), reps_agent)):
+        ids, _ = synth.token_ids(tree, STACK["vocab"], seed=4500)
+        T = tree.useful_tokens()
+        n_pages = layout.live_pages(tree, 16) + 64
+        n_seg = sum(r.n_nodes for r in tree.requests)
+        stk = HybridStack(StackShape(**STACK), W, max_pos=20000)
+        stk.alloc(Tcap=T, n_pages=n_pages, n_slots=n_seg + 40)
+        R, seg_of = rounds.build_round(tree, api.PagePool(n_pages), temp_slot0=32, n_temp_slots=n_seg + 8)
+        meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+        R.upload(meta)
+        idd = torch.from_numpy(rounds.to_stream(R, seg_of, ids)).cuda()
+        n_ro = R.info().n_readouts
+        ms = _timed(torch, lambda: stk.forward(R, meta, idd, n_ro), reps)
+        api.check_status(stk.status)
+        tf = fpt * T / (ms / 1e3) / 1e12
+        out[name] = {"tokens": T, "ms": round(ms, 3), "tokens_per_s": round(T / (ms / 1e3), 1), "bound": "tensor",
+                     "linear_tflops": round(tf, 1), "peak_tflops": pk["bf16_tflops_sustained"],
+                     "frac": round(tf / pk["bf16_tflops_sustained"], 4),
+                     "peak_kind": "measured bf16 dense sustained (a forward of tens to hundreds of ms)"}
+        del stk
+        torch.cuda.empty_cache()
+    out["hybrid_stack"]["workload"] = ("64 requests, trunks log-uniform [512,16384], 2-12 branches U[8,128]; "
+                                       "8 layers GGGA x2, hidden 2048")
+    out["agent_tree"]["workload"] = "10 sessions, trunk 256, depth 3 x fan-out 4, residual 32; 8 layers, hidden 2048"
+    return out
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
@@ -371,14 +543,10 @@ def aggregate(values_per_rank, units_per_rank):
     return sum(units_per_rank) / max(values_per_rank)
 
 
-def cpu_baseline(at, gt, a_inp, g_inp, budget_s: float = 12.0):
-    """The fp64 oracle timed on a bounded sample of the same workload and
-    extrapolated to the whole step: sampled trunk rows + one branch of the
-    attention tree, and a run of GDN recurrence steps (16 heads); the oracle
-    recomputes the trunk for every branch (isolated passes)."""
-    from oracle import attention as oattn
+def _oracle_sample(at, gt, a_inp, g_inp):
+    """Per-unit times of the fp64 oracle on a bounded sample: sampled trunk rows and every row of one
+    branch of the attention tree, and a run of GDN recurrence steps (16 heads)."""
     from oracle import forward, gdn as ogdn
-    t_cpu0, t0 = time.process_time(), time.perf_counter()
     scale = 1 / math.sqrt(ATTN["d"])
     req = at.requests[0]
     P = req.n_tok[0]
@@ -389,25 +557,88 @@ def cpu_baseline(at, gt, a_inp, g_inp, budget_s: float = 12.0):
     tb = time.perf_counter()
     forward.attention_tree(at, a_inp, scale, nodes=[(0, 1)])
     t_br = (time.perf_counter() - tb) / req.n_tok[1]       # per branch row (each sees ~P keys)
-    attn_est = t_rows * P + t_br * sum(req.n_tok[1:])
-    g = gt.requests[0]
     tr = g_inp.nodes[(0, 0)]
     n_steps = 1024
     tg = time.perf_counter()
     ogdn.gated_delta_rule(tr["q"][:n_steps], tr["k"][:n_steps], tr["v"][:n_steps], tr["alpha"][:n_steps],
                           tr["beta"][:n_steps])
     t_step = (time.perf_counter() - tg) / n_steps
-    gdn_steps = g.n_tok[0] + sum(g.n_tok[0] + l for l in g.n_tok[1:])   # trunk alone + each isolated branch
-    gdn_est = t_step * gdn_steps
-    wall = time.perf_counter() - t0
-    cores = max(1, round((time.process_time() - t_cpu0) / max(wall, 1e-9)))
-    tokens = at.useful_tokens() + gt.useful_tokens()
-    del oattn
-    return {"value": tokens / (attn_est + gdn_est), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": (f"fp64 oracle, {len(rows)} trunk rows + all {req.n_tok[1]} rows of one branch of the "
-                       f"attention tree, {n_steps} GDN recurrence steps (16 heads); extrapolated to the step "
-                       f"({attn_est:.1f} s attention + {gdn_est:.1f} s GDN, isolated passes); "
-                       f"sampling took {wall:.1f} s")}
+    return {"t_row": t_rows, "t_br": t_br, "t_step": t_step, "n_rows": len(rows), "n_br": req.n_tok[1],
+            "n_steps": n_steps}
+
+
+_WORKER_INPUTS = []
+
+
+def _oracle_worker(_):
+    """One pool worker (spawned, one BLAS thread): the same sample on its own copy of the inputs
+    (drawn once per worker)."""
+    if not _WORKER_INPUTS:
+        at, gt = trees()
+        _WORKER_INPUTS.extend([at, gt,
+                               synth.attn_inputs(at, ATTN["hq"], ATTN["hkv"], ATTN["d"], seed=ATTN["seed"], bf16=True),
+                               synth.gdn_inputs(gt, GDN["h"], GDN["d"], GDN["d"], seed=GDN["seed"], bf16=True,
+                                                law="softplus")])
+    return _oracle_sample(*_WORKER_INPUTS)
+
+
+def _oracle_step_s(at, gt, t):
+    """The whole step's oracle time from per-unit times: every trunk row, every branch row (each an
+    isolated pass over trunk + branch), the GDN trunk alone and each branch's isolated pass."""
+    req, g = at.requests[0], gt.requests[0]
+    attn = t["t_row"] * req.n_tok[0] + t["t_br"] * sum(req.n_tok[1:])
+    gdn = t["t_step"] * (g.n_tok[0] + sum(g.n_tok[0] + l for l in g.n_tok[1:]))
+    return attn, gdn
+
+
+class OracleBaseline:
+    """The fp64 oracle as it stands, timed on the host cores on a bounded sample of the step and
+    extrapolated to the whole step.  Two legs: one core, and every host core as a process pool
+    (spawn start, one BLAS thread each) running the sample concurrently, the step's independent
+    isolated passes then split evenly over the cores (the sample's own per-unit times under that
+    contention)."""
+
+    def __init__(self, all_cores: bool = True):
+        self.cores = os.cpu_count() or 1
+        self.pool = None
+        if all_cores and self.cores > 1:
+            import multiprocessing as mp
+            for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+                os.environ[v] = "1"
+            self.pool = mp.get_context("spawn").Pool(self.cores)
+            self.pool.map(abs, range(self.cores), chunksize=1)   # workers started before anything is timed
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+
+    def measure(self, at, gt, a_inp, g_inp):
+        tokens = at.useful_tokens() + gt.useful_tokens()
+        t0, c0 = time.perf_counter(), time.process_time()
+        t1 = _oracle_sample(at, gt, a_inp, g_inp)
+        wall1 = time.perf_counter() - t0
+        used1 = max(1, round((time.process_time() - c0) / max(wall1, 1e-9)))
+        a1, g1 = _oracle_step_s(at, gt, t1)
+        one = {"value": tokens / (a1 + g1), "unit": "tokens/s", "cores": used1, "kind": "oracle",
+               "sample_s": round(wall1, 2),
+               "sample": (f"fp64 oracle, {t1['n_rows']} trunk rows + all {t1['n_br']} rows of one branch of the "
+                          f"attention tree, {t1['n_steps']} GDN recurrence steps (16 heads), on one core; "
+                          f"extrapolated to the step ({a1:.1f} s attention + {g1:.1f} s GDN, isolated passes)")}
+        if self.pool is None:
+            return one
+        t0 = time.perf_counter()
+        res = self.pool.map(_oracle_worker, range(self.cores), chunksize=1)
+        wallc = time.perf_counter() - t0
+        tm = {k: statistics.mean(r[k] for r in res) for k in ("t_row", "t_br", "t_step")}
+        ac, gc = _oracle_step_s(at, gt, tm)
+        step_s = (ac + gc) / self.cores
+        return {"value": tokens / step_s, "unit": "tokens/s", "cores": self.cores, "kind": "oracle",
+                "sample_s": round(wallc, 2),
+                "sample": (f"fp64 oracle, the one-core sample run by {self.cores} spawned processes at once (one "
+                           f"BLAS thread each); the step's isolated passes split over {self.cores} cores at the "
+                           f"per-unit times measured under that load: {step_s:.1f} s per step, extrapolated"),
+                "one_core": one}
 
 
 def run_reference(args):
@@ -417,15 +648,21 @@ def run_reference(args):
     at, gt = trees()
     a_inp = synth.attn_inputs(at, ATTN["hq"], ATTN["hkv"], ATTN["d"], seed=ATTN["seed"], bf16=True)
     g_inp = synth.gdn_inputs(gt, GDN["h"], GDN["d"], GDN["d"], seed=GDN["seed"], bf16=True, law="softplus")
+    ob = OracleBaseline()
     vals = []
+    t_run = time.perf_counter()
     for i in range(args.warmup + args.steps):
-        b = cpu_baseline(at, gt, a_inp, g_inp)
+        b = ob.measure(at, gt, a_inp, g_inp)
         if i >= args.warmup:
             vals.append(b)
+    ob.close()
     v = statistics.median(x["value"] for x in vals)
+    tokens = at.useful_tokens() + gt.useful_tokens()
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (at.useful_tokens() +
-                                                                              gt.useful_tokens()) / v,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tokens / v,
+            "ms_per_step_kind": "extrapolated from the timed sample of each step (not a timing of a whole step)",
+            "sample_ms_per_step": round(1e3 * statistics.median(x["sample_s"] for x in vals), 1),
+            "wall_s": round(time.perf_counter() - t_run, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
@@ -443,13 +680,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the resume / stack / agent-tree lines")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
-    import torch
     ws, rank, local = dist_env()
+    # the oracle's process pool starts before the first GPU call (a pool forked after it can hang)
+    ob = OracleBaseline() if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    import torch
     if ws > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -475,7 +715,7 @@ def main():
     step.ev_gdn = []
     barrier(ws)
     torch.cuda.synchronize()
-    with Clocks(torch.cuda.current_device()) as clk:
+    with Clocks(torch, torch.cuda.current_device()) as clk:
         t0 = time.perf_counter()
         for i in range(args.steps):
             ev[i][0].record(step.stream)
@@ -541,8 +781,21 @@ def main():
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clk.summary(), "wall_s": round(wall, 4)}
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(at, gt, a_inp, g_inp)
+    # the two trees of the step on their own
+    a_tok, g_tok = at.useful_tokens(), gt.useful_tokens()
+    line["configs"] = {
+        "fork_attn": {"workload": "trunk 4096 + 8 branches U[16,64], GQA 32/8, d128, page 16, bf16",
+                      "tokens": a_tok, "ms": round(attn_ms, 4), "tokens_per_s": round(a_tok / (attn_ms / 1e3), 1),
+                      "bound": "tensor", "frac": roof["frac"], "peak_kind": roof["peak_kind"]},
+        "gdn_fork": {"workload": "trunk 8192 + 16 branches U[8,128], H16 d128, chunk 64, fp32 state, bf16",
+                     "tokens": g_tok, "ms": round(gdn_ms, 4), "tokens_per_s": round(g_tok / (gdn_ms / 1e3), 1),
+                     "bound": "hbm", "frac": line["kernels"]["gdn_fork_prefill"]["frac"]}}
+    if not args.no_extra:
+        line["configs"]["gdn_resume"] = gdn_resume_config(torch, api, rounds, pk)
+        line["configs"].update(stack_configs(torch, api, rounds, pk))
+    if ob is not None:
+        line["cpu_baseline"] = ob.measure(at, gt, a_inp, g_inp)
+        ob.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
