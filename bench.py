@@ -335,19 +335,16 @@ class Step:
             bufs["g_in"].copy_(self.host_buf["g_in"], non_blocking=True)
             ev[1].record(cs)
 
-    def run(self, i: int, time_attn: bool = False, ev_a_in=None, ev_g_in=None, ev_a_done=None, up=None,
-            inputs=None):
-        """One step on the compute stream.  `up` (a stream) carries the metadata
-        upload instead of the compute stream; the caller's ev_a_in then orders it."""
-        api, s = self.api, self.sets[i % len(self.sets)]
-        k_set = i % len(self.sets)
+    def prepare(self, k_set: int, us=None):
+        """Host half of a step: build both rounds, pack their metadata into this input set's pinned
+        buffers and upload it (on stream `us`, default the compute stream)."""
         R_a, R_g = self.build()
         ha, hg = self.meta_host[k_set]
         if self.meta_sent[k_set] is not None:
             self.meta_sent[k_set].synchronize()   # this pinned buffer's previous upload is done
         R_a.pack(ha)
         R_g.pack(hg)
-        us = up if up is not None else self.stream
+        us = us if us is not None else self.stream
         a_meta, g_meta = self.metas[k_set]
         with self.torch.cuda.stream(us):
             a_meta.copy_(ha, non_blocking=True)
@@ -355,6 +352,27 @@ class Step:
             if self.meta_sent[k_set] is None:
                 self.meta_sent[k_set] = self.torch.cuda.Event()
             self.meta_sent[k_set].record(us)
+        return R_a, R_g
+
+    def device_calls(self, k_set: int):
+        """Device half of a step (what a graph captures): page write, attention, option head, GDN."""
+        api, s = self.api, self.sets[k_set]
+        a_meta, g_meta = self.metas[k_set]
+        api.kv_page_write(self.a_caps, a_meta, s["a_k"], s["a_v"], self.k_pages, self.v_pages, self.status)
+        api.fork_attn(self.a_caps, a_meta, s["a_q"], self.k_pages, self.v_pages, s["a_out"], self.status)
+        api.choice_logprobs(self.a_caps, a_meta, s["a_out"].view(s["a_out"].shape[0], -1), self.W, s["lp"],
+                            self.status)
+        api.gdn_fork_prefill(self.g_caps, g_meta, s["g_q"], s["g_k"], s["g_v"], s["g_alpha"], s["g_beta"],
+                             self.state, s["g_out"], self.ws, self.status)
+
+    def run(self, i: int, time_attn: bool = False, ev_a_in=None, ev_g_in=None, ev_a_done=None, up=None,
+            inputs=None):
+        """One step on the compute stream.  `up` (a stream) carries the metadata
+        upload instead of the compute stream; the caller's ev_a_in then orders it."""
+        api, s = self.api, self.sets[i % len(self.sets)]
+        k_set = i % len(self.sets)
+        R_a, R_g = self.prepare(k_set, up)
+        a_meta, g_meta = self.metas[k_set]
         if inputs is not None:
             inputs()
         if ev_a_in is not None:
@@ -754,6 +772,32 @@ def main():
     e2e_ms = reduce_max(torch, e0.elapsed_time(e1), ws)
     e2e_value = ws * tokens * args.steps / (e2e_ms / 1e3)
 
+    # ---- the same steps through flat CUDA graphs (one capture per input set; per step the host builds
+    # and uploads the round's metadata, then replays) ----
+    from hybrid_serving_gb300.graphs import StepGraph
+    torch.cuda.synchronize()
+    graphs = [StepGraph(lambda k=k: step.device_calls(k)) for k in range(len(step.sets))]
+    for i in range(3):
+        R_a, _ = step.prepare(i % len(step.sets))
+        graphs[i % len(step.sets)].replay()
+        R_a.release(step.pool)
+    torch.cuda.synchronize()
+    barrier(ws)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host_s = 0.0
+    g0.record(step.stream)
+    for i in range(args.steps):
+        h0 = time.perf_counter()
+        R_a, _ = step.prepare(i % len(step.sets))
+        graphs[i % len(step.sets)].replay()
+        R_a.release(step.pool)
+        host_s += time.perf_counter() - h0
+    g1.record(step.stream)
+    torch.cuda.synchronize()
+    api.check_status(step.status)
+    graph_ms = reduce_max(torch, g0.elapsed_time(g1), ws) / args.steps
+    del graphs
+
     pk, pk_kind = peaks()
     fl = attn_flops(at)
     achieved = fl / (attn_ms / 1e3) / 1e12
@@ -780,7 +824,11 @@ def main():
                             "launches": "chunk-local pass + one state pass per tree level"}},
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": int(launches), "clocks": clk.summary(), "wall_s": round(wall, 4)}
+            "gpu_launches": int(launches), "clocks": clk.summary(), "wall_s": round(wall, 4),
+            "graph": {"ms_per_step": round(graph_ms, 4), "value": round(ws * tokens / (graph_ms / 1e3), 1),
+                      "unit": "tokens/s", "host_us_per_step": round(1e6 * host_s / args.steps, 1),
+                      "what": ("the step's device work captured once per input set (flat graphs over the "
+                               "capacities); per step: host round build + metadata pack and upload, replay")}}
     # the two trees of the step on their own
     a_tok, g_tok = at.useful_tokens(), gt.useful_tokens()
     line["configs"] = {

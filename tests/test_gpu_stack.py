@@ -62,20 +62,29 @@ def _oracle_node(oc, W, tree, ids_nodes, hist, r, node, both=False):
 
 def _assert_tv(lp_gpu, oc, W, h64, h32, what):
     """Option distributions within the stated 1e-3 plus twice the fp32
-    forward's TV over the same rows (Flide App. G's rounding-level bar)."""
+    forward's TV over the same rows (Flide App. G's rounding-level bar), and
+    within 1e-3 itself whenever the fp32 forward is (printed either way)."""
     p64 = np.exp(ostack.option_logprobs(oc, W, h64))
     p32 = np.exp(ostack.option_logprobs(oc, W, h32))
     tv_ref = float(ochoice.total_variation(p32, p64).max())
     tv = float(ochoice.total_variation(np.exp(lp_gpu), p64).max())
+    print(f"[margin] stack {what}: option TV {tv:.3e}, fp32-forward TV {tv_ref:.3e} (bar 1e-3)")
     assert tv <= TV + 2 * tv_ref, (what, tv, tv_ref)
+    if tv_ref <= TV:
+        assert tv <= TV, (what, tv, tv_ref)
 
 
 def _assert_rounding_level(got, ref, ref32, what):
-    """GPU error within twice the fp32-vs-fp64 oracle distance (Flide App. G)."""
+    """GPU error within twice the fp32-vs-fp64 oracle distance (Flide App.
+    G), and within the stated 2e-2 itself whenever the fp32 forward is
+    (printed either way)."""
     e_ref = float(np.abs(ref32 - ref).max())
     e_gpu = float(np.abs(got - ref).max())
+    print(f"[margin] stack {what}: max-abs {e_gpu:.3e}, fp32-forward distance {e_ref:.3e} (bar 2e-2)")
     assert e_gpu <= 2 * e_ref + 2e-3, (what, e_gpu, e_ref)
     assert e_ref <= 0.25, (what, e_ref)
+    if e_ref <= TOL:
+        assert e_gpu <= TOL, (what, e_gpu, e_ref)
 
 
 def test_small_stack_fork_parity_and_choices():
@@ -230,8 +239,18 @@ def test_mixed_batch_full_width_invariance_and_sampled_parity():
             a0, n = rows[(r, i)]
             b0 = R1.segment(s1[(0, i)]).stream_off
             assert torch.equal(h1[b0:b0 + n], mixed[a0:a0 + n]), ("request", r, "node", i)
+    # the shortest request, every node, and the option distributions at its readouts (the fp64 stack
+    # oracle takes ~25 ms per token per isolated pass, so a 16k-token request is out of a test's reach)
     r = order[0]
-    for i in (0, 1, tree.requests[r].n_nodes - 1):
+    ro_index = {s: k for k, s in enumerate(sorted(s for s in seg_of.values() if R.segment(s).readout_row >= 0))}
+    l64, l32, lpg = [], [], []
+    lp_h = lp.cpu().numpy()
+    for i in range(tree.requests[r].n_nodes):
         a0, n = rows[(r, i)]
         ref, ref32 = _oracle_node(oc, W, tree, ids, hist, r, i, both=True)
         _assert_rounding_level(mixed[a0:a0 + n].float().cpu().numpy(), ref, ref32, ("mixed", r, i))
+        if tree.requests[r].readout[i]:
+            l64.append(ref[-1])
+            l32.append(ref32[-1])
+            lpg.append(lp_h[ro_index[seg_of[(r, i)]]])
+    _assert_tv(np.stack(lpg), oc, W, np.stack(l64), np.stack(l32), ("mixed", r))
