@@ -522,12 +522,15 @@ def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int =
         idd = torch.from_numpy(rounds.to_stream(R, seg_of, ids)).cuda()
         n_ro = R.info().n_readouts
         ms = _timed(torch, lambda: stk.forward(R, meta, idd, n_ro), reps)
+        ms_sel = _timed(torch, lambda: stk.forward(R, meta, idd, n_ro, selective=True), reps)
         api.check_status(stk.status)
         tf = fpt * T / (ms / 1e3) / 1e12
         out[name] = {"tokens": T, "ms": round(ms, 3), "tokens_per_s": round(T / (ms / 1e3), 1), "bound": "tensor",
                      "linear_tflops": round(tf, 1), "peak_tflops": pk["bf16_tflops_sustained"],
                      "frac": round(tf / pk["bf16_tflops_sustained"], 4),
-                     "peak_kind": "measured bf16 dense sustained (a forward of tens to hundreds of ms)"}
+                     "peak_kind": "measured bf16 dense sustained (a forward of tens to hundreds of ms)",
+                     "selective_readout": {"ms": round(ms_sel, 3), "tokens_per_s": round(T / (ms_sel / 1e3), 1),
+                                           "what": "last layer's MLP, final norm and head at the readout rows only"}}
         del stk
         torch.cuda.empty_cache()
     out["hybrid_stack"]["workload"] = ("64 requests, trunks log-uniform [512,16384], 2-12 branches U[8,128]; "

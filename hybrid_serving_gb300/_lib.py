@@ -71,6 +71,7 @@ _SIGS = {
     "hs_round_segment_pages": (I32, [P, I32, I32P, I32, I32P]),
     "hs_round_readout_rows": (I32, [P, I32P, I32, I32P]),
     "hs_round_release": (I32, [P, P, I32P, I32]),
+    "hs_round_build_chunks": (I32, [CAPSP, P, P, P]),
     "hs_fork_attn_prefill": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, P, P, P, P, P, I32, P, P, P]),
     "hs_kv_page_write": (I32, [CAPSP, P, I32, I32, I32, P, P, P, P, I32, P, P]),
     "hs_fork_attn": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, P, P, P, I32, P, P, P]),

@@ -251,6 +251,13 @@ def fork_attn_prefill(caps: Caps, dev_meta: torch.Tensor, q, k_new, v_new, k_pag
                                    k_pages.shape[1], out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
 
 
+def round_build_chunks(caps: Caps, dev_meta: torch.Tensor, dev_status: torch.Tensor, stream=None):
+    """Rebuild the GDN chunk list of the round in dev_meta on the GPU (hs_round_build_chunks)."""
+    dev = _cur_dev()
+    _meta_status(caps, dev_meta, dev_status, dev)
+    check(lib.hs_round_build_chunks(C.byref(caps), dev_meta.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+
+
 def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_pages, dev_status: torch.Tensor,
                   stream=None):
     _dt(k_new)

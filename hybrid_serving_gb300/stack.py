@@ -109,16 +109,31 @@ class HybridStack:
 
     # ---------------------------------------------------------------- forward
     def forward(self, R: api.Round, meta: torch.Tensor, ids: torch.Tensor, n_readout: int,
-                save_windows: Optional[List[tuple]] = None, stream=None):
+                save_windows: Optional[List[tuple]] = None, stream=None, selective: bool = False):
         """One forked prefill round.  ``ids`` device int32 [Tcap] in stream
         order.  ``save_windows``: [(device src rows int32, device dst rows
         int32, n)] -- after each GDN layer's projection, copy those stream rows
         into the layer's conv-window buffer (a checkpoint's window).
+        ``selective`` (Flide section 3.3.3, selective readout): after the last
+        layer's token mixer only the readout rows go on -- its MLP, the final
+        norm and the option head run on those rows alone (row for row the same
+        bits: every step after the mixer works on each row by itself and the
+        GEMM's rows do not depend on M); the returned hidden rows are then
+        final at the readout rows only.
         Returns (final hidden [T, hidden] view, option logprobs [n_readout, n_opt])."""
         sh, st = self.sh, self.status
         caps = R.caps
         T = R.info().n_tokens
         s = _s(stream)
+        if selective and n_readout > 0:
+            ro_rows = torch.tensor(R.readout_rows(), dtype=torch.int32).to(DEV, non_blocking=True)
+            ro_idx = torch.arange(n_readout, dtype=torch.int32, device=DEV)
+            hr = torch.empty((n_readout, sh.hidden), dtype=torch.bfloat16, device=DEV)
+            ar = torch.empty_like(hr)
+            gur = torch.empty((n_readout, 2 * sh.ffn), dtype=torch.bfloat16, device=DEV)
+            mr = torch.empty((n_readout, sh.ffn), dtype=torch.bfloat16, device=DEV)
+        last = len(sh.pattern) - 1
+        row_bytes = sh.hidden * 2
         check(lib.hs_embed(ids.data_ptr(), T, self.W["embed"].data_ptr(), sh.vocab, sh.hidden, self.h.data_ptr(),
                            st.data_ptr(), s))
         ai = gi = 0
@@ -165,14 +180,29 @@ class HybridStack:
                 gemm(self.o_gdn, self.W[p + "wo"], self.h, T, R=self.h, status=st,
                      stream=stream)
                 gi += 1
+            if selective and li == last and n_readout > 0:
+                # the readout rows alone from here on: gather, MLP + final norm, scatter back for the head
+                check(lib.hs_copy_rows(self.h.data_ptr(), row_bytes, ro_rows.data_ptr(), hr.data_ptr(), row_bytes,
+                                       ro_idx.data_ptr(), n_readout, row_bytes, s))
+                check(lib.hs_rmsnorm(hr.data_ptr(), sh.hidden, n_readout, sh.hidden, None, sh.eps, ar.data_ptr(),
+                                     sh.hidden, s))
+                gemm(ar, self.W[p + "wgu"], gur, n_readout, status=st, stream=stream)
+                check(lib.hs_swiglu(gur.data_ptr(), gur.stride(0), n_readout, sh.ffn, mr.data_ptr(), sh.ffn, s))
+                gemm(mr, self.W[p + "wd"], hr, n_readout, R=hr, status=st, stream=stream)
+                check(lib.hs_rmsnorm(hr.data_ptr(), sh.hidden, n_readout, sh.hidden, None, sh.eps, ar.data_ptr(),
+                                     sh.hidden, s))
+                check(lib.hs_copy_rows(ar.data_ptr(), row_bytes, ro_idx.data_ptr(), self.a.data_ptr(), row_bytes,
+                                       ro_rows.data_ptr(), n_readout, row_bytes, s))
+                break
             check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
                                  sh.hidden, s))
             gu = self.proj[:, :2 * sh.ffn]
             gemm(self.a, self.W[p + "wgu"], gu, T, status=st, stream=stream)
             check(lib.hs_swiglu(gu.data_ptr(), gu.stride(0), T, sh.ffn, self.m.data_ptr(), sh.ffn, s))
             gemm(self.m, self.W[p + "wd"], self.h, T, R=self.h, status=st, stream=stream)
-        check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(), sh.hidden,
-                             s))
+        else:
+            check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
+                                 sh.hidden, s))
         lp = torch.empty((max(n_readout, 1), len(sh.option_ids)), dtype=torch.float32, device=DEV)
         api.choice_logprobs(caps, meta, self.a, self.opt, lp, st, stream=stream)
         return self.a[:T], lp[:n_readout]

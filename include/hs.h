@@ -192,6 +192,18 @@ hs_status hs_round_readout_rows(const hs_round* r, int32_t* rows, int32_t cap, i
  * round was finalized with (NULL if it was finalized without one). */
 hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep_segs, int32_t n_keep);
 
+/* The GDN chunk list built on the GPU (Flide section 3.3.1: GPU-resident
+ * metadata for the fixed-shape launches; section 3.5: every node starts a
+ * chunk): from the segment table already in dev_meta (each node's stream
+ * offset and length), rewrites in place the chunk list -- the nodes in
+ * stream order, each cut into 64-token chunks from its first token, record
+ * {node, first row, length, index} -- each node's first-chunk and
+ * chunk-count fields, and the header's chunk count and largest per-node
+ * count: word for word what the host round build writes.  One small launch
+ * on `stream`; a chunk list beyond caps->max_chunks sets HS_DEV_BAD_META.
+ * Supports caps->max_segments <= 4096 (HS_EINVAL above). */
+hs_status hs_round_build_chunks(const hs_round_caps* caps, void* dev_meta, int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Hot path                                                                  */
 /* ------------------------------------------------------------------------ */

@@ -122,6 +122,32 @@ def test_small_stack_batch_invariance_bitwise():
         assert np.array_equal(alone[(0, 0)], mixed[(1, 0)])
 
 
+def test_selective_readout_bitwise():
+    """Selective readout (Flide section 3.3.3): the last layer's MLP, the final norm and the option head
+    on the readout rows alone give the same bits at those rows, and the same option log-probs, as the
+    full forward."""
+    sh, oc, W = _cfgs(SMALL)
+    tree = synth.Tree([synth.fork_tree(150, [17, 1, 40]), synth.fork_tree(70, [9, 33]),
+                       synth.fanout_tree(30, 6, 3, 2)])
+    ids, _ = synth.token_ids(tree, SMALL["vocab"], seed=4250)
+    stk = HybridStack(sh, W, max_pos=1024)
+    stk.alloc(Tcap=tree.useful_tokens(), n_pages=96, n_slots=64)
+    R, seg_of = rounds.build_round(tree, api.PagePool(96), temp_slot0=32, n_temp_slots=32)
+    meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+    R.upload(meta)
+    idd = torch.from_numpy(rounds.to_stream(R, seg_of, ids)).cuda()
+    n_ro = R.info().n_readouts
+    h_full, lp_full = stk.forward(R, meta, idd, n_ro)
+    h_full, lp_full = h_full.clone(), lp_full.clone()
+    h_sel, lp_sel = stk.forward(R, meta, idd, n_ro, selective=True)
+    torch.cuda.synchronize()
+    api.check_status(stk.status)
+    rows = torch.tensor(R.readout_rows(), dtype=torch.long, device="cuda")
+    assert n_ro == len(rows) > 0
+    assert torch.equal(h_sel[rows], h_full[rows])
+    assert torch.equal(lp_sel, lp_full)
+
+
 def _agent_round_trip(dims, n_sessions, trunk, residual, depth, extra, check_leaves, seed):
     """Round A: depth-level fan-out of 4 per session, spine leaf saves its GDN
     state and conv window; commit keeps the spine pages.  Round B: each
