@@ -491,6 +491,53 @@ def gdn_resume_config(torch, api, rounds, pk, reps: int = 20):
             "frac": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
 
 
+# Shapes of the pages' workloads (Flide section 4, Table 2: mean state tokens, questions per request,
+# tokens per question; section 4.4, Fig. 5a: 1..64 questions on one ~2k-token state).  Synthetic
+# stand-ins with those statistics; no dataset item is used.
+SWEEP_SHAPES = ([(f"questions x{k} on a 2048-token state", 2048, k, 64) for k in (1, 2, 4, 8, 16, 32, 64)] +
+                [("RACE-all shape", 255, 4, 73), ("DI shape", 323, 5, 190), ("MultiRC shape", 327, 48, 49),
+                 ("QuALITY-all shape", 5835, 18, 89)])
+
+
+def sweep_configs(torch, api, rounds, reps: int = 10):
+    """Each shape as one request (state + k questions) through ForkAttention (GQA 32/8, d128, bf16) and
+    GDN fork prefill (16 heads, d128): device ms per round, tokens/s over the stream's P + sum |q|
+    tokens, and the stream's size against one sequence per question (n P + sum |q|, Table 2)."""
+    out = []
+    for name, P, k, ql in SWEEP_SHAPES:
+        tree = synth.Tree([synth.fork_tree(P, [ql] * k)])
+        T = tree.useful_tokens()
+        ai = synth.attn_inputs(tree, ATTN["hq"], ATTN["hkv"], ATTN["d"], seed=6000 + k, bf16=True)
+        gi = synth.gdn_inputs(tree, GDN["h"], GDN["d"], GDN["d"], seed=6100 + k, bf16=True, law="softplus")
+        n_pages = T // 16 + k + 16
+        Ra, sa = rounds.build_round(tree, api.PagePool(n_pages))
+        Rg, sg = rounds.build_round(tree, None, temp_slot0=1, n_temp_slots=4)
+        am = torch.empty(Ra.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+        gm = torch.empty(Rg.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+        Ra.upload(am)
+        Rg.upload(gm)
+        dev = lambda R, sg_, inp, key, dt: torch.from_numpy(rounds.to_stream(R, sg_, inp.nodes, key)).cuda().to(dt)
+        q, kk, v = (dev(Ra, sa, ai, x, torch.bfloat16) for x in "qkv")
+        kp = torch.zeros((ATTN["hkv"], n_pages, 16, ATTN["d"]), dtype=torch.bfloat16, device="cuda")
+        vp = torch.zeros_like(kp)
+        o = torch.empty_like(q)
+        gx = [dev(Rg, sg, gi, x, torch.bfloat16) for x in "qkv"] + [dev(Rg, sg, gi, x, torch.float32)
+                                                                    for x in ("alpha", "beta")]
+        state = torch.zeros((8, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.float32, device="cuda")
+        go = torch.empty_like(gx[2])
+        ws = torch.empty(api.gdn_workspace_bytes(Rg.caps, GDN["h"], GDN["d"], GDN["d"]), dtype=torch.uint8,
+                         device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ms_a = _timed(torch, lambda: api.fork_attn_prefill(Ra.caps, am, q, kk, v, kp, vp, o, st), reps)
+        ms_g = _timed(torch, lambda: api.gdn_fork_prefill(Rg.caps, gm, *gx, state, go, ws, st), reps)
+        api.check_status(st)
+        out.append({"shape": name, "state": P, "questions": k, "tokens_per_question": ql, "stream_tokens": T,
+                    "isolated_tokens": k * P + k * ql, "stream_vs_isolated": round((k * P + k * ql) / T, 3),
+                    "attn_ms": round(ms_a, 4), "gdn_ms": round(ms_g, 4),
+                    "tokens_per_s": round(T / ((ms_a + ms_g) / 1e3), 1)})
+    return out
+
+
 def _linear_flops_per_token(W) -> float:
     """2 x the weights every token multiplies by (the projections, output projections and MLPs of all
     layers; the embedding is a lookup and the option rows are read at the readout rows only)."""
@@ -844,6 +891,7 @@ def main():
     if not args.no_extra:
         line["configs"]["gdn_resume"] = gdn_resume_config(torch, api, rounds, pk)
         line["configs"].update(stack_configs(torch, api, rounds, pk))
+        line["configs"]["sweep"] = sweep_configs(torch, api, rounds)
     if ob is not None:
         line["cpu_baseline"] = ob.measure(at, gt, a_inp, g_inp)
         ob.close()

@@ -44,6 +44,10 @@ class SegmentInfo(C.Structure):
                                           "init_slot", "end_slot", "readout_row", "n_pages")]
 
 
+class AttnMask(C.Structure):
+    _fields_ = [("window", C.c_int32), ("bidirectional_root", C.c_int32)]
+
+
 P = C.c_void_p
 I32 = C.c_int32
 I32P = C.POINTER(C.c_int32)
@@ -72,6 +76,8 @@ _SIGS = {
     "hs_round_readout_rows": (I32, [P, I32P, I32, I32P]),
     "hs_round_release": (I32, [P, P, I32P, I32]),
     "hs_round_build_chunks": (I32, [CAPSP, P, P, P]),
+    "hs_fork_attn_masked": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, C.POINTER(AttnMask), P, P, P, I32, P,
+                                  P, P]),
     "hs_fork_attn_prefill": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, P, P, P, P, P, I32, P, P, P]),
     "hs_kv_page_write": (I32, [CAPSP, P, I32, I32, I32, P, P, P, P, I32, P, P]),
     "hs_fork_attn": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, P, P, P, I32, P, P, P]),

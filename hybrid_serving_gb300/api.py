@@ -270,7 +270,8 @@ def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_p
 
 
 def fork_attn(caps: Caps, dev_meta: torch.Tensor, q, k_pages, v_pages, out, dev_status: torch.Tensor,
-              scale: Optional[float] = None, stream=None):
+              scale: Optional[float] = None, stream=None, window: int = 0, bidirectional_root: bool = False):
+    """hs_fork_attn; a sliding ``window`` or ``bidirectional_root`` goes through hs_fork_attn_masked."""
     _dt(q)
     dev = _cur_dev()
     _check_pages(caps, dev_meta, dev_status, q.dtype, None, None, k_pages, v_pages, dev)
@@ -278,6 +279,12 @@ def fork_attn(caps: Caps, dev_meta: torch.Tensor, q, k_pages, v_pages, out, dev_
     T, hq, d = q.shape
     hkv = k_pages.shape[0]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if window or bidirectional_root:
+        mask = _lib.AttnMask(int(window), int(bool(bidirectional_root)))
+        check(lib.hs_fork_attn_masked(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, C.byref(mask),
+                                      q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[1],
+                                      out.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+        return
     check(lib.hs_fork_attn(C.byref(caps), dev_meta.data_ptr(), _dt(q), hq, hkv, d, scale, q.data_ptr(),
                            k_pages.data_ptr(), v_pages.data_ptr(), k_pages.shape[1], out.data_ptr(),
                            dev_status.data_ptr(), _stream(stream)))

@@ -84,7 +84,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kSimtRows * 32)
 fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float scale_log2e,
                       const T* __restrict__ q, const T* __restrict__ kp, const T* __restrict__ vp, int n_pages,
-                      T* __restrict__ out, int32_t* status) {
+                      T* __restrict__ out, int32_t* status, int window, int bidir_root) {
   constexpr int DP = D + 1;
   constexpr int CPL = D / 32;  // output columns per lane
   __shared__ float q_s[kSimtRows][D];
@@ -108,10 +108,12 @@ fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float s
   const int n_ref = M.h(H_N_PAGE_REF);
   const int32_t* refs = M.page_ref();
 
-  int my_seg = -1, my_idx = 0;
+  int my_seg = -1, my_idx = 0, my_pos = 0, my_whole = 0;
   if (active) {
     my_seg = M.tok(row)[T_SEG];
     my_idx = M.tok(row)[T_IDX];
+    my_pos = M.seg(my_seg)[S_POS0] + my_idx;
+    my_whole = bidir_root && M.seg(my_seg)[S_LEVEL] == 0;  // a bidirectional root: its rows see all of it
   }
   // stage this warp's query row, pre-scaled so that exp2 gives e^(scale s)
   for (int c = lane; c < D; c += 32)
@@ -124,19 +126,27 @@ fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float s
 
   const int n_shared = tl[TL_N_SHARED], n_spans = n_shared + tl[TL_N_OWN];
   const int32_t* tspans = M.tile_spans() + tl[TL_SPAN_OFF];
+  int p_shared = 0;  // position of the next shared span's first key (shared spans follow the path in order)
   for (int si = 0; si < n_spans; ++si) {
     const int32_t* sp = M.span(tspans[si]);
     const int sp_off = sp[SP_PAGE_REF_OFF], sp_n = sp[SP_N_TOK], owner = sp[SP_OWNER];
     const bool own = si >= n_shared;
     int kmax = sp_n;  // keys this thread block needs from the span
+    int p0 = p_shared;  // position of the span's first key
     if (own) {
       const int32_t* og = M.seg(owner);
       const int lo = max(sub_lo, og[S_STREAM_OFF]);
       const int hi = min(sub_hi, og[S_STREAM_OFF] + og[S_LEN]);
-      kmax = hi > lo ? hi - og[S_STREAM_OFF] : 0;
+      const bool whole = bidir_root && og[S_LEVEL] == 0;
+      kmax = hi > lo ? (whole ? og[S_LEN] : hi - og[S_STREAM_OFF]) : 0;
+      p0 = og[S_POS0];
+    } else {
+      p_shared += sp_n;
     }
-    // keys of this span the row sees: all (shared), up to itself (own), none (sibling)
-    const int my_n = !active ? 0 : !own ? sp_n : (owner == my_seg ? my_idx + 1 : 0);
+    // keys of this span the row sees: [my_lo, my_n) -- all (shared), up to itself (own; all of a
+    // bidirectional root), none (sibling); a window starts them at position my_pos - W + 1
+    const int my_n = !active ? 0 : !own ? sp_n : (owner == my_seg ? (my_whole ? sp_n : my_idx + 1) : 0);
+    const int my_lo = (window > 0 && active) ? max(0, my_pos - window + 1 - p0) : 0;
     for (int b0 = 0; b0 < kmax; b0 += kSimtKeys) {
       __syncthreads();
       const int nb = min(kSimtKeys, kmax - b0);
@@ -165,10 +175,10 @@ fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float s
         }
       }
       __syncthreads();
-      const int nvis = min(kSimtKeys, my_n - b0);
-      if (nvis <= 0) continue;  // this row sees nothing in the block
+      const int nvis = min(kSimtKeys, my_n - b0), nlo = max(0, my_lo - b0);
+      if (nvis <= nlo) continue;  // this row sees nothing in the block
       float s = -INFINITY;
-      if (lane < nvis) {
+      if (lane < nvis && lane >= nlo) {
         float acc = 0.f;
 #pragma unroll 8
         for (int c = 0; c < D; ++c) acc = fmaf(q_s[warp][c], k_s[lane][c], acc);
@@ -176,7 +186,7 @@ fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float s
       }
       const float m_new = fmaxf(m, hsd::warp_max(s));
       const float corr = exp2f(m - m_new);
-      const float p = lane < nvis ? exp2f(s - m_new) : 0.f;
+      const float p = (lane < nvis && lane >= nlo) ? exp2f(s - m_new) : 0.f;
       l = l * corr + hsd::warp_sum(p);
 #pragma unroll
       for (int i = 0; i < CPL; ++i) o[i] *= corr;
@@ -198,16 +208,18 @@ fork_attn_simt_kernel(const int32_t* __restrict__ meta, int hq, int hkv, float s
 template <typename T>
 hs_status launch_attn_simt(const hs_round_caps* caps, const void* meta, int hq, int hkv, int d, float scale,
                            const void* q, const void* kp, const void* vp, int n_pages, void* out, int32_t* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, int window, int bidir_root) {
   dim3 grid(caps->max_tiles * (kTileRows / kSimtRows), hq);
   const float sl2 = scale * 1.4426950408889634f;
   if (grid.x == 0) return HS_OK;
   if (d == 128)
     fork_attn_simt_kernel<T, 128><<<grid, kSimtRows * 32, 0, st>>>(
-        (const int32_t*)meta, hq, hkv, sl2, (const T*)q, (const T*)kp, (const T*)vp, n_pages, (T*)out, status);
+        (const int32_t*)meta, hq, hkv, sl2, (const T*)q, (const T*)kp, (const T*)vp, n_pages, (T*)out, status,
+        window, bidir_root);
   else
     fork_attn_simt_kernel<T, 64><<<grid, kSimtRows * 32, 0, st>>>(
-        (const int32_t*)meta, hq, hkv, sl2, (const T*)q, (const T*)kp, (const T*)vp, n_pages, (T*)out, status);
+        (const int32_t*)meta, hq, hkv, sl2, (const T*)q, (const T*)kp, (const T*)vp, n_pages, (T*)out, status,
+        window, bidir_root);
   HS_LAUNCH_CHECK("fork_attn_simt");
   return HS_OK;
 }
@@ -229,7 +241,7 @@ hs_status launch_kv_write(const hs_round_caps* caps, const void* meta, int hkv, 
 // tensor-core path (fork_attn_tc.cu); returns HS_EUNSUPPORTED when it does not apply
 hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, int hq, int hkv, int d, float scale,
                                  const void* q, const void* kp, const void* vp, int n_pages, void* out,
-                                 int32_t* status, cudaStream_t st);
+                                 int32_t* status, cudaStream_t st, int window, int bidir_root);
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
@@ -260,24 +272,37 @@ extern "C" hs_status hs_kv_page_write(const hs_round_caps* caps, const void* dev
   return launch_kv_write<float>(caps, dev_meta, hkv, d, k_new, v_new, k_pages, v_pages, n_pages, dev_status, st);
 }
 
-extern "C" hs_status hs_fork_attn(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hq,
-                                  int32_t hkv, int32_t d, float scale, const void* q, const void* k_pages,
-                                  const void* v_pages, int32_t n_pages, void* out, int32_t* dev_status, void* stream) {
+extern "C" hs_status hs_fork_attn_masked(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hq,
+                                         int32_t hkv, int32_t d, float scale, const hs_attn_mask* mask, const void* q,
+                                         const void* k_pages, const void* v_pages, int32_t n_pages, void* out,
+                                         int32_t* dev_status, void* stream) {
   HS_CHECK_ARG(q && k_pages && v_pages && out, "null argument");
   HS_CHECK_ARG(hq > 0 && hkv > 0 && hq % hkv == 0, "hq=%d must be a positive multiple of hkv=%d", hq, hkv);
   HS_CHECK_ARG(scale > 0.f && scale < 1e30f, "bad scale");
   HS_CHECK_ARG(aligned16(q) && aligned16(k_pages) && aligned16(v_pages) && aligned16(out),
                "tensors must be 16-byte aligned");
+  const int window = mask ? mask->window : 0, bidir = mask ? mask->bidirectional_root : 0;
+  HS_CHECK_ARG(window >= 0, "window %d must be >= 0 (0 = none)", window);
+  HS_CHECK_ARG(bidir == 0 || bidir == 1, "bidirectional_root must be 0 or 1");
   hs_status s = check_common(caps, dev_meta, dt, hkv, d, n_pages);
   if (s != HS_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
   if (dt == HS_BF16) {
-    s = hs_fork_attn_tc_launch(caps, dev_meta, hq, hkv, d, scale, q, k_pages, v_pages, n_pages, out, dev_status, st);
+    s = hs_fork_attn_tc_launch(caps, dev_meta, hq, hkv, d, scale, q, k_pages, v_pages, n_pages, out, dev_status, st,
+                               window, bidir);
     if (s != HS_EUNSUPPORTED) return s;
     return launch_attn_simt<__nv_bfloat16>(caps, dev_meta, hq, hkv, d, scale, q, k_pages, v_pages, n_pages, out,
-                                           dev_status, st);
+                                           dev_status, st, window, bidir);
   }
-  return launch_attn_simt<float>(caps, dev_meta, hq, hkv, d, scale, q, k_pages, v_pages, n_pages, out, dev_status, st);
+  return launch_attn_simt<float>(caps, dev_meta, hq, hkv, d, scale, q, k_pages, v_pages, n_pages, out, dev_status, st,
+                                 window, bidir);
+}
+
+extern "C" hs_status hs_fork_attn(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hq,
+                                  int32_t hkv, int32_t d, float scale, const void* q, const void* k_pages,
+                                  const void* v_pages, int32_t n_pages, void* out, int32_t* dev_status, void* stream) {
+  return hs_fork_attn_masked(caps, dev_meta, dt, hq, hkv, d, scale, nullptr, q, k_pages, v_pages, n_pages, out,
+                             dev_status, stream);
 }
 
 extern "C" hs_status hs_fork_attn_prefill(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hq,

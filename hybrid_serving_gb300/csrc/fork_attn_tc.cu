@@ -80,16 +80,25 @@ struct Params {
   float scale_log2e;
   __nv_bfloat16* out;
   int32_t* status;
+  int window;      // sliding width W (> 0: a row sees keys t_x - t_y < W), 0 = none
+  int bidir_root;  // 1: a root node's rows see the whole root
 };
 
-// The key blocks of a tile in the order every role walks them.
-struct Cursor {
+// The key blocks of a tile in the order every role walks them.  Mask variants: with a sliding window the
+// blocks that end before the tile's first window start are skipped by every role (they are hidden from every
+// row of the tile; each row still masks its own window start); with a bidirectional root the rows of a root
+// node see all of it.  A key's position: a shared span's keys follow the earlier shared spans along the path
+// (history first, then each ancestor), an own span's start at its node's first position.  kMask = false
+// compiles the mask tests out (plain causal attention).
+template <bool kMask>
+struct CursorT {
   Meta M;
   const int32_t* tspans;
   int n_shared, n_spans, n_own, tile_lo, tile_hi;
   int si, b0, kmax;
   int sp_off, sp_n, owner, own, first_idx;
-  __device__ void init(Meta m, const int32_t* tl) {
+  int p0, p_shared, lo_min, window, bidir, whole;
+  __device__ void init(Meta m, const int32_t* tl, int window_ = 0, int bidir_ = 0) {
     M = m;
     tspans = m.tile_spans() + tl[TL_SPAN_OFF];
     n_shared = tl[TL_N_SHARED];
@@ -100,36 +109,60 @@ struct Cursor {
     si = -1;
     b0 = 0;
     kmax = 0;
+    p0 = p_shared = 0;
+    window = kMask ? window_ : 0;
+    bidir = kMask ? bidir_ : 0;
+    whole = 0;
+    lo_min = -(1 << 30);
+    if (kMask && window > 0) {  // the tile's first row has its smallest position
+      const int32_t* tk = m.tok(tile_lo);
+      lo_min = m.seg(tk[T_SEG])[S_POS0] + tk[T_IDX] - window + 1;
+    }
   }
   // advance to the next block; false when the tile has no more
   __device__ bool next() {
     b0 += kBlk;
-    while (b0 >= kmax) {
-      if (++si >= n_spans) return false;
-      const int32_t* sp = M.span(tspans[si]);
-      sp_off = sp[SP_PAGE_REF_OFF];
-      sp_n = sp[SP_N_TOK];
-      owner = sp[SP_OWNER];
-      own = si >= n_shared;
-      kmax = sp_n;
-      first_idx = 0;
-      if (own) {
-        const int32_t* og = M.seg(owner);
-        const int lo = max(tile_lo, og[S_STREAM_OFF]);
-        const int hi = min(tile_hi, og[S_STREAM_OFF] + og[S_LEN]);
-        kmax = hi > lo ? hi - og[S_STREAM_OFF] : 0;
-        first_idx = lo - og[S_STREAM_OFF];
+    while (true) {
+      while (b0 >= kmax) {
+        if (++si >= n_spans) return false;
+        const int32_t* sp = M.span(tspans[si]);
+        sp_off = sp[SP_PAGE_REF_OFF];
+        sp_n = sp[SP_N_TOK];
+        owner = sp[SP_OWNER];
+        own = si >= n_shared;
+        kmax = sp_n;
+        first_idx = 0;
+        whole = 0;
+        if (own) {
+          const int32_t* og = M.seg(owner);
+          const int lo = max(tile_lo, og[S_STREAM_OFF]);
+          const int hi = min(tile_hi, og[S_STREAM_OFF] + og[S_LEN]);
+          whole = kMask && bidir && og[S_LEVEL] == 0;  // a bidirectional root: its rows see the whole node
+          kmax = hi > lo ? (whole ? og[S_LEN] : hi - og[S_STREAM_OFF]) : 0;
+          first_idx = lo - og[S_STREAM_OFF];
+          p0 = og[S_POS0];
+        } else {
+          p0 = p_shared;
+          p_shared += sp_n;
+        }
+        b0 = 0;
       }
-      b0 = 0;
+      if (kMask && p0 + b0 + kBlk <= lo_min) {  // wholly before every row's window
+        b0 += kBlk;
+        continue;
+      }
+      return true;
     }
-    return true;
   }
   __device__ int valid() const { return min(kBlk, sp_n - b0); }
   // every row of the tile sees every key of the block
   __device__ bool full() const {
-    return own ? (n_own == 1 && b0 + kBlk <= first_idx && b0 + kBlk <= sp_n) : (sp_n - b0 >= kBlk);
+    if (kMask && window > 0) return false;
+    if (!own) return sp_n - b0 >= kBlk;
+    return n_own == 1 && b0 + kBlk <= sp_n && ((kMask && whole) || b0 + kBlk <= first_idx);
   }
 };
+using Cursor = CursorT<false>;
 
 __device__ __forceinline__ void record(int32_t* status, int* abort_flag, int code) {
   hsd::set_status(status, code);
@@ -543,6 +576,7 @@ constexpr int kWarpMmaB = 10, kThreads = 352;  // warp 9: MMAs of head A, warp 1
 constexpr int kRing = 4;                       // items published ahead by the producer
 }  // namespace pair
 
+template <bool kMask>
 __global__ void __launch_bounds__(pair::kThreads, 1)
 fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
                      const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v16,
@@ -643,8 +677,8 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (w < 0) break;
         const int32_t* tl = M.tile(w / np);
         const int h0 = 2 * (w % np), kvh = h0 / (p.hq / p.hkv);
-        Cursor cur;
-        cur.init(M, tl);
+        CursorT<kMask> cur;
+        cur.init(M, tl, p.window, p.bidir_root);
         if (!cur.next()) continue;  // an item without keys is skipped by every role
         // Q of this item once every S product of the previous item is done
         if (n_q >= 1 && !tc::mbar_wait(&bar_qe, (n_q - 1) & 1, kWaitCycles)) {
@@ -777,8 +811,8 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int w = item_of(k);
         if (w == -2) ok = false;
         if (w < 0) break;
-        Cursor cur;
-        cur.init(M, M.tile(w / np));
+        CursorT<kMask> cur;
+        cur.init(M, M.tile(w / np), p.window, p.bidir_root);
         const bool precise = M.tile(w / np)[TL_READOUT] != 0;
         int n_blk = 0;
         while (cur.next()) ++n_blk;  // counted once: the loop needs no cursor
@@ -850,31 +884,37 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (w < 0) break;
       const int32_t* tl = M.tile(w / np);
       const int h0 = 2 * (w % np);
-      Cursor cur;
-      cur.init(M, tl);
+      CursorT<kMask> cur;
+      cur.init(M, tl, p.window, p.bidir_root);
       const int row = tl[TL_ROW0] + t;
       const bool active = t < tl[TL_N_ROWS];
       const bool precise = tl[TL_READOUT] != 0;
-      int my_seg = -1, my_idx = 0;
+      int my_seg = -1, my_idx = 0, my_pos = 0, my_whole = 0;
       if (active) {
         my_seg = M.tok(row)[T_SEG];
         my_idx = M.tok(row)[T_IDX];
+        my_pos = M.seg(my_seg)[S_POS0] + my_idx;
+        my_whole = kMask && p.bidir_root && M.seg(my_seg)[S_LEVEL] == 0;
       }
       float m_used = -INFINITY, l = 0.f;
       int j = 0, n_blk = 0;
       {
-        Cursor c2 = cur;
+        CursorT<kMask> c2 = cur;
         while (c2.next()) ++n_blk;
       }
       while (ok && cur.next()) {
         const int lim = cur.full() ? kBlk
                                    : (!active ? 0 : !cur.own ? cur.sp_n - cur.b0
-                                                             : (cur.owner == my_seg ? my_idx + 1 - cur.b0 : 0));
+                                                             : (cur.owner == my_seg ? (kMask && my_whole ? cur.sp_n : my_idx + 1) - cur.b0
+                                                                                    : 0));
+        // a window: this row's keys start at position my_pos - W + 1
+        const int lo_in = (kMask && p.window > 0 && active) ? my_pos - p.window + 1 - (cur.p0 + cur.b0) : -(1 << 30);
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {  // key half h of the block: S_X[h]
           const int u = 2 * jg + h;    // key halves over all items (phases of bar_pv[x])
           const uint32_t sb = sbuf + 64 * h;
-          const int lh = lim - 64 * h;  // this row's visible keys in the half
+          const int lh = lim - 64 * h;  // this row's visible keys in the half: [lo_h, lh)
+          const int lo_h = lo_in - 64 * h;
           // tcgen05.ld/st are warp-collective: every branch around them is decided warp-wide
           if (!__all_sync(~0u, tc::mbar_wait(&bar_sf[x][h], jg & 1, kWaitCycles))) {
             ok = false;
@@ -883,7 +923,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tc::fence_after_sync();
           // the half's 64 scores in registers (one load, one wait; scores past the row's visible keys read as
           // -inf), then pass 1: the row max
-          const bool masked = __any_sync(~0u, lh < 64);
+          const bool masked = __any_sync(~0u, lh < 64 || lo_h > 0);
           uint32_t sr[2][32];
           tc::tmem_ld32(sb, sr[0]);
           tc::tmem_ld32(sb + 32, sr[1]);
@@ -893,7 +933,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           for (int c = 0; c < 2; ++c) {
             if (masked) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) sr[c][i] = 32 * c + i < lh ? sr[c][i] : 0xFF800000u;
+              for (int i = 0; i < 32; ++i) sr[c][i] = (32 * c + i < lh && 32 * c + i >= lo_h) ? sr[c][i] : 0xFF800000u;
             }
             float m2[2] = {mx, -INFINITY};
 #pragma unroll
@@ -1059,7 +1099,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 // HS_EUNSUPPORTED otherwise so the caller takes the CUDA-core kernel.
 hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, int hq, int hkv, int d, float scale,
                                  const void* q, const void* kp, const void* vp, int n_pages, void* out,
-                                 int32_t* status, cudaStream_t st) {
+                                 int32_t* status, cudaStream_t st, int window, int bidir_root) {
   if (d != kD) return HS_EUNSUPPORTED;
   if (caps->max_tiles <= 0) return HS_OK;
   // the pool rows must be addressable by 32-bit TMA coordinates
@@ -1086,12 +1126,16 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
   if (!configured[slot].load()) {
     if (cudaFuncSetAttribute(fork_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(fork_attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(fork_attn_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair::kSmemBytes + 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(fork_attn_tc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair::kSmemBytes + 1024) != cudaSuccess)
       return hs::fail(HS_ECUDA, "fork_attn_tc: cannot raise the shared-memory limit");
     configured[slot].store(true);
   }
-  Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status};
+  Params prm{(const int32_t*)meta, hq, hkv, n_pages, scale * 1.4426950408889634f, (__nv_bfloat16*)out, status,
+             window, bidir_root};
+  if ((window > 0 || bidir_root) && (hq / hkv) % 2 != 0) return HS_EUNSUPPORTED;  // (masks: the paired kernel)
   if ((hq / hkv) % 2 == 0) {  // two query heads that share a KV head per CTA, one persistent CTA per SM
     static std::atomic<int> sm_count[hsd::kMaxDevices];  // per device, 0 until read
     int n_sm = sm_count[slot].load();
@@ -1101,8 +1145,13 @@ hs_status hs_fork_attn_tc_launch(const hs_round_caps* caps, const void* meta, in
       sm_count[slot].store(n_sm);
     }
     const int items = caps->max_tiles * (hq / 2);
-    hsd::launch_pdl(fork_attn_tc2_kernel, dim3(items < n_sm ? items : n_sm), dim3(pair::kThreads),
-                    pair::kSmemBytes + 1024, st, m_q, m_k16, m_k128, m_v16, m_v128, prm);
+    const dim3 grid(items < n_sm ? items : n_sm);
+    if (window > 0 || bidir_root)
+      hsd::launch_pdl(fork_attn_tc2_kernel<true>, grid, dim3(pair::kThreads), pair::kSmemBytes + 1024, st, m_q,
+                      m_k16, m_k128, m_v16, m_v128, prm);
+    else
+      hsd::launch_pdl(fork_attn_tc2_kernel<false>, grid, dim3(pair::kThreads), pair::kSmemBytes + 1024, st, m_q,
+                      m_k16, m_k128, m_v16, m_v128, prm);
   } else {
     hsd::launch_pdl(fork_attn_tc_kernel, dim3(caps->max_tiles * hq), dim3(kThreads), kSmemBytes + 1024, st,
                     m_q, m_k16, m_k128, m_v16, m_v128, prm);

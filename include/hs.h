@@ -252,6 +252,30 @@ hs_status hs_fork_attn(const hs_round_caps* caps, const void* dev_meta, hs_dtype
                        int32_t d, float scale, const void* q, const void* k_pages, const void* v_pages,
                        int32_t n_pages, void* out, int32_t* dev_status, void* stream);
 
+/* Mask variants of ForkAttention (Flide section 3.2.1: a sliding window adds
+ * t_x - t_y < W to Eq. 3; Appendix H: models that read their state both
+ * ways see it as a block).  Positions are along the row's own path (a
+ * resumed history, every ancestor, the node): the trunk's tokens count
+ * from 0 (or from the history's length), a child's from its parent's end.
+ *   window              > 0: a row sees only keys with t_x - t_y < window;
+ *                       0: no window
+ *   bidirectional_root  1: a root node's rows see every token of the root
+ *                       (and its history), later ones included; every
+ *                       other node stays causal; 0: plain Eq. 3 */
+typedef struct {
+  int32_t window;
+  int32_t bidirectional_root;
+} hs_attn_mask;
+
+/* hs_fork_attn with a mask (NULL = none, the same as hs_fork_attn).  The
+ * bf16 d = 128 tensor-core kernel takes masks when a KV head's query-head
+ * group has an even size; other shapes run the CUDA-core kernel.  Blocks a
+ * window hides from every row of a tile are skipped. */
+hs_status hs_fork_attn_masked(const hs_round_caps* caps, const void* dev_meta, hs_dtype dt, int32_t hq,
+                              int32_t hkv, int32_t d, float scale, const hs_attn_mask* mask, const void* q,
+                              const void* k_pages, const void* v_pages, int32_t n_pages, void* out,
+                              int32_t* dev_status, void* stream);
+
 /* Workspace bytes hs_gdn_fork_prefill needs for these caps and shapes. */
 size_t hs_gdn_workspace_bytes(const hs_round_caps* caps, int32_t h, int32_t dk, int32_t dv);
 

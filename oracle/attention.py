@@ -18,12 +18,25 @@ from __future__ import annotations
 import numpy as np
 
 
-def causal_attention(q, k, v, scale: float, rows=None, window: int | None = None):
+def visible_range(t: int, window: int | None = None, bidir: int = 0):
+    """Keys [lo, hi) row t sees: u <= t (causal), t - u < W with a window (Flide, section 3.2.1), and,
+    with a bidirectional block of the first ``bidir`` tokens (Flide, Appendix H: the state of a model
+    that reads it both ways), every token of that block for a row inside it."""
+    hi = t + 1
+    if t < bidir:
+        hi = bidir
+    lo = 0 if window is None else max(0, t - window + 1)
+    return lo, hi
+
+
+def causal_attention(q, k, v, scale: float, rows=None, window: int | None = None, bidir: int = 0):
     """q [n, Hq, d]; k, v [n, Hkv, d]; returns o [len(rows), Hq, d] float64.
 
     ``rows``: indices t of the query rows to produce (default: all).  A query
-    row t only reads q[t]; keys/values 0..t are read.  ``window``: optional
-    sliding width W (Flide, section 3.2.1: adds t_x - t_y < W).
+    row t only reads q[t]; keys/values in visible_range(t) are read.
+    ``window``: optional sliding width W (Flide, section 3.2.1: adds
+    t_x - t_y < W).  ``bidir``: the first ``bidir`` tokens form a block seen
+    both ways (their rows see the whole block; later rows are causal).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -37,9 +50,9 @@ def causal_attention(q, k, v, scale: float, rows=None, window: int | None = None
     rows = list(rows)
     out = np.empty((len(rows), hq, d), dtype=np.float64)
     for o_i, t in enumerate(rows):
-        lo = 0 if window is None else max(0, t - window + 1)
-        kk = k[lo:t + 1]                         # [u, Hkv, d]
-        vv = v[lo:t + 1]
+        lo, hi = visible_range(t, window, bidir)
+        kk = k[lo:hi]                            # [u, Hkv, d]
+        vv = v[lo:hi]
         qt = q[t].reshape(hkv, g, d)             # [Hkv, G, d]
         s = np.einsum("hgd,uhd->hgu", qt, kk) * scale
         m = s.max(axis=-1, keepdims=True)
@@ -50,7 +63,7 @@ def causal_attention(q, k, v, scale: float, rows=None, window: int | None = None
     return out
 
 
-def causal_attention_rows(q, k, v, scale: float, rows=None, window: int | None = None):
+def causal_attention_rows(q, k, v, scale: float, rows=None, window: int | None = None, bidir: int = 0):
     """The same quantity as causal_attention, evaluated one query head at a
     time as a matrix: the scores of the requested rows against every key,
     the keys after a row (and, with ``window``, those W or more positions
@@ -66,7 +79,8 @@ def causal_attention_rows(q, k, v, scale: float, rows=None, window: int | None =
     g = hq // hkv
     rows = np.arange(n) if rows is None else np.asarray(list(rows), dtype=np.int64)
     u = np.arange(n)
-    visible = u[None, :] <= rows[:, None]
+    hi = np.where(rows < bidir, bidir, rows + 1)
+    visible = u[None, :] < hi[:, None]
     if window is not None:
         visible &= u[None, :] > rows[:, None] - window
     out = np.empty((len(rows), hq, d), dtype=np.float64)

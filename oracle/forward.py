@@ -29,13 +29,15 @@ def _path_seq(inp, r: int, req, node: int, key: str):
 
 def attention_tree(tree, inp, scale: float, nodes: Optional[Iterable[Tuple[int, int]]] = None,
                    rows: Optional[Dict[Tuple[int, int], Iterable[int]]] = None,
-                   window: Optional[int] = None, matrix: bool = False):
+                   window: Optional[int] = None, matrix: bool = False, bidir_root: bool = False):
     """Returns {(r, node): o [n_rows, Hq, d]} for the requested nodes.
 
     ``rows`` optionally restricts a node to some of its row indices (a
     sampled check); each row is still its isolated-sequence output.
     ``matrix`` evaluates each isolated sequence with the matrix form of the
     same definition (attention.causal_attention_rows) -- for thousands of rows.
+    ``window``: sliding width; ``bidir_root``: the root's tokens (with any
+    resumed history) form a block seen both ways (attention.visible_range).
     """
     out = {}
     if nodes is None:
@@ -49,7 +51,8 @@ def attention_tree(tree, inp, scale: float, nodes: Optional[Iterable[Tuple[int, 
         q = np.zeros((k.shape[0], inp.hq, inp.d))
         q[n_before:] = inp.nodes[(r, i)]["q"]
         f = _attn.causal_attention_rows if matrix else _attn.causal_attention
-        out[(r, i)] = f(q, k, v, scale, rows=[n_before + u for u in sel], window=window)
+        bidir = inp.hist[r]["k"].shape[0] + req.n_tok[0] if bidir_root else 0
+        out[(r, i)] = f(q, k, v, scale, rows=[n_before + u for u in sel], window=window, bidir=bidir)
     return out
 
 

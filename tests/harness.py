@@ -51,6 +51,14 @@ class AttnRun:
         torch.cuda.synchronize()
         return self
 
+    def run_masked(self, window=0, bidirectional_root=False):
+        """Page write, then the attention with a mask (hs_fork_attn_masked)."""
+        api.kv_page_write(self.R.caps, self.meta, self.k, self.v, self.k_pages, self.v_pages, self.status)
+        api.fork_attn(self.R.caps, self.meta, self.q, self.k_pages, self.v_pages, self.out, self.status,
+                      window=window, bidirectional_root=bidirectional_root)
+        torch.cuda.synchronize()
+        return self
+
     def outputs(self):
         o = self.out.float().cpu().numpy().astype(np.float64)
         return rounds.from_stream(self.R, self.seg_of, o)

@@ -140,3 +140,40 @@ def test_bad_page_sets_status_without_fault():
     assert int(run.status.item()) == 1  # HS_DEV_BAD_PAGE
     with pytest.raises(_lib.HsError):
         api.check_status(run.status)
+
+
+MASK_PATHS = [("paired tensor-core", torch.bfloat16, 8, 2, 128), ("CUDA cores fp32", torch.float32, 4, 2, 64),
+              ("odd group (CUDA cores)", torch.bfloat16, 6, 2, 128)]
+MASKS = [(37, False), (300, False), (0, True), (50, True)]
+
+
+@pytest.mark.parametrize("path", range(len(MASK_PATHS)))
+@pytest.mark.parametrize("mask", range(len(MASKS)))
+def test_masks_match_oracle(path, mask):
+    """Mask variants (Flide section 3.2.1 sliding window t_x - t_y < W; Appendix H bidirectional state):
+    every row of a ragged multi-level round against the oracle's isolated pass with the same mask."""
+    name, dt, hq, hkv, d = MASK_PATHS[path]
+    W, bidir = MASKS[mask]
+    tree = synth.Tree([synth.fork_tree(333, [17, 1, 64, 130]), synth.fanout_tree(60, 20, 2, 2)])
+    inp = synth.attn_inputs(tree, hq, hkv, d, seed=1700 + path, bf16=dt == torch.bfloat16)
+    run = AttnRun(tree, inp, dt).run_masked(window=W, bidirectional_root=bidir)
+    api.check_status(run.status)
+    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(d), window=W or None, bidir_root=bidir, matrix=True)
+    err = max_abs(run.outputs(), ref)
+    tol = TOL_BF16 if dt == torch.bfloat16 else TOL_F32
+    print(f"[margin] attention mask W={W} bidir={bidir} {name}: max-abs {err:.3e} (bar {tol:.0e})")
+    assert err <= tol
+
+
+def test_window_batch_invariance_bitwise():
+    base = synth.fork_tree(777, [20, 50, 13, 100])
+    tree = synth.Tree([synth.fork_tree(300, [9, 9]), base])
+    inp = synth.attn_inputs(tree, 8, 2, 128, seed=1800, bf16=True)
+    mixed = AttnRun(tree, inp, torch.bfloat16).run_masked(window=200).raw_outputs()
+    for b in range(1, 5):
+        alone_tree = synth.Tree([synth.fork_tree(777, [base.n_tok[b]])])
+        alone_inp = synth.AttnInputs(8, 2, 128, True, {(0, 0): inp.nodes[(1, 0)], (0, 1): inp.nodes[(1, b)]},
+                                     {0: inp.hist[1]})
+        alone = AttnRun(alone_tree, alone_inp, torch.bfloat16).run_masked(window=200).raw_outputs()
+        assert torch.equal(alone[(0, 1)], mixed[(1, b)]), f"branch {b} differs"
+        assert torch.equal(alone[(0, 0)], mixed[(1, 0)])

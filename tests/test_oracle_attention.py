@@ -233,3 +233,69 @@ def test_matrix_form_tree_equals_row_loop():
     b = forward.attention_tree(tree, inp, 0.2, matrix=True)
     for key in a:
         np.testing.assert_allclose(b[key], a[key], rtol=0, atol=1e-13)
+
+
+def _positions(req):
+    """Position of each node's first token along its path (history first, then every ancestor)."""
+    pos0 = [req.hist_len] * req.n_nodes
+    for i in range(1, req.n_nodes):
+        pos0[i] = pos0[req.parents[i]] + req.n_tok[req.parents[i]]
+    return pos0
+
+
+def _zero_query_case(seed):
+    req = synth.Request(parents=[-1, 0, 0, 1, 1, 2], n_tok=[5, 3, 4, 2, 3, 1], hist_len=6)
+    tree = synth.Tree([req, synth.fork_tree(3, [2, 2])])
+    inp = synth.attn_inputs(tree, 4, 2, 3, seed=seed, bf16=False)
+    for key in inp.nodes:
+        inp.nodes[key]["q"] = np.zeros_like(inp.nodes[key]["q"])
+    return tree, inp
+
+
+def _value(inp, r, nd, x):
+    return inp.hist[r]["v"][x] if nd < 0 else inp.nodes[(r, nd)]["v"][x]
+
+
+@pytest.mark.parametrize("W", [1, 2, 5, 9])
+def test_zero_query_window_is_mean_over_window(W):
+    """Sliding window (Flide section 3.2.1, t_x - t_y < W): with q = 0 a row's output is the mean of v
+    over the keys Eq. 3 lets it see (enumerated by layout.visible_keys) whose position is within W."""
+    tree, inp = _zero_query_case(12)
+    out = forward.attention_tree(tree, inp, scale=0.5, window=W)
+    for (r, i), o in out.items():
+        req = tree.requests[r]
+        pos0 = _positions(req)
+        for u in range(req.n_tok[i]):
+            t = pos0[i] + u
+            keep = [(nd, x) for nd, x in layout.visible_keys(tree, r, i, u)
+                    if t - (x if nd < 0 else pos0[nd] + x) < W]
+            mean = np.mean(np.asarray([_value(inp, r, nd, x) for nd, x in keep], np.float64), axis=0)
+            for h in range(4):
+                np.testing.assert_allclose(o[u, h], mean[h // 2], atol=1e-14)
+
+
+def test_zero_query_bidirectional_root():
+    """Bidirectional state block (Flide Appendix H): a root row sees every token of the history and of
+    the root, later and earlier alike; every other row keeps Eq. 3's causal set."""
+    tree, inp = _zero_query_case(13)
+    out = forward.attention_tree(tree, inp, scale=0.5, bidir_root=True)
+    for (r, i), o in out.items():
+        req = tree.requests[r]
+        for u in range(req.n_tok[i]):
+            if i == 0:
+                keys = [(-1, x) for x in range(req.hist_len)] + [(0, x) for x in range(req.n_tok[0])]
+            else:
+                keys = layout.visible_keys(tree, r, i, u)
+            mean = np.mean(np.asarray([_value(inp, r, nd, x) for nd, x in keys], np.float64), axis=0)
+            for h in range(4):
+                np.testing.assert_allclose(o[u, h], mean[h // 2], atol=1e-14)
+
+
+def test_matrix_form_equals_row_loop_with_bidirectional_block():
+    rng = np.random.default_rng(43)
+    n, d = 29, 16
+    q, k, v = (rng.standard_normal((n, 2, d)) for _ in range(3))
+    for bidir, window in ((11, None), (11, 4), (0, 3)):
+        a = attention.causal_attention(q, k, v, 0.3, window=window, bidir=bidir)
+        b = attention.causal_attention_rows(q, k, v, 0.3, window=window, bidir=bidir)
+        np.testing.assert_allclose(b, a, rtol=0, atol=1e-13)
