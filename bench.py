@@ -39,19 +39,27 @@ WORKLOAD = ("fork_attn trunk4096+8br U[16,64] GQA32/8 d128 page16 bf16 + 4-optio
             "gdn_fork trunk8192+16br U[8,128] H16 d128 chunk64 fp32-state bf16")
 N_OPT = 4
 METRIC = "tree-prefill tokens/s on 1 GB300 (ForkAttn + GDN); % of tensor/HBM roofline"
-# DRAM traffic per launch from one ncu capture (profiles/fork_attn_tc2_attention_tree.md),
-# valid only while the kernel source still has the hash it was captured with.
-NCU_TRAFFIC = {"fork_attn": ("hybrid_serving_gb300/csrc/fork_attn_tc.cu", "f0175bd36b7e7baa", 56.45e6)}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of this
+# bench's workload, valid only while every listed kernel source still has the hash it was captured with.
+# gdn_fork: the sum over the launches of one call (chunk-local pass, two state passes per tree level).
+NCU_TRAFFIC = {
+    "fork_attn": ({"hybrid_serving_gb300/csrc/fork_attn_tc.cu": "fdc41de45030cdd0"}, 56.58e6),
+    "gdn_fork": ({"hybrid_serving_gb300/csrc/gdn_prep_tc.cu": "4490dfd481c219c1",
+                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "ef8bad51c6a7024b"}, 512.17e6),
+}
 
 
 def ncu_traffic(kernel: str):
     import hashlib
-    path, sha, nbytes = NCU_TRAFFIC[kernel]
-    try:
-        h = hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
-    return nbytes if h == sha else None
+    srcs, nbytes = NCU_TRAFFIC[kernel]
+    for path, sha in srcs.items():
+        try:
+            h = hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        if h != sha:
+            return None
+    return nbytes
 
 
 def peaks():
@@ -749,6 +757,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the resume / stack / agent-tree lines")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="one input set, the warm-up steps only, no timing and no JSON line: the case that ncu "
+                         "captures of single kernels run (a few hundred MB on the device)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -756,7 +767,7 @@ def main():
 
     ws, rank, local = dist_env()
     # the oracle's process pool starts before the first GPU call (a pool forked after it can hang)
-    ob = OracleBaseline() if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    ob = OracleBaseline() if (rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.profile_case) else None
     import torch
     if ws > 1:
         import torch.distributed as dist
@@ -768,8 +779,16 @@ def main():
     a_inp = synth.attn_inputs(at, ATTN["hq"], ATTN["hkv"], ATTN["d"], seed=ATTN["seed"], bf16=True)
     g_inp = synth.gdn_inputs(gt, GDN["h"], GDN["d"], GDN["d"], seed=GDN["seed"], bf16=True, law="softplus")
     W = synth.option_rows(N_OPT, ATTN["hq"] * ATTN["d"], seed=ATTN["seed"] + 1)
-    step = Step(torch, api, rounds, at, gt, a_inp, g_inp, W)
+    step = Step(torch, api, rounds, at, gt, a_inp, g_inp, W, n_sets=1 if args.profile_case else 3)
     tokens = at.useful_tokens() + gt.useful_tokens()
+    if args.profile_case:
+        for i in range(args.warmup):
+            step.run(i)
+        torch.cuda.synchronize()
+        api.check_status(step.status)
+        print(f"profile case: {args.warmup} steps, device memory held "
+              f"{torch.cuda.max_memory_allocated() / 2**20:.0f} MiB", flush=True)
+        return 0
 
     for i in range(args.warmup):
         step.run(i)
@@ -871,6 +890,7 @@ def main():
                             "achieved": round(gdn_bytes(gt) / (gdn_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                             "peak": pk["hbm_gbs"],
                             "frac": round(gdn_bytes(gt) / (gdn_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                            "traffic": ncu_traffic("gdn_fork"),
                             "launches": "chunk-local pass + one state pass per tree level"}},
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
