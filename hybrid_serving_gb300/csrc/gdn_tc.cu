@@ -25,8 +25,10 @@
 //               ahead;
 //   warp 9      issues the state chain's MMAs (D1, then D4 as soon as U is
 //               written), converged, from one elected lane;
-//   warp 10     issues the output MMAs (D2, D3) the same way, so that they
-//               never queue in front of the chain's;
+//   warp 10     issues the output MMAs the same way, each in a gap of the
+//               chain's: D2 once D1 is done (while the rows form U), D3 once
+//               D4 is done (while the rows form the bf16 state), so that
+//               they never share the tensor pipe with the chain's products;
 //   warps 0..3  rows of the state (thread j = TMEM lane j = row j of S):
 //               U, the scaling of S, the bf16 copy of S;
 //   warps 4..7  outputs: O for chunk c (staged in the chunk's Q buffer, then
@@ -105,6 +107,41 @@ constexpr int smem_bytes() { return Cfg<O>::kStages * Cfg<O>::kStageBytes; }
 constexpr uint32_t kIdesc64 = tc::idesc_bf16(128, 64, 0, 0);      // D[128x64], B K-major
 constexpr uint32_t kIdesc64mn = tc::idesc_bf16(128, 64, 0, 1);    // D[128x64], B N-major
 constexpr uint32_t kIdesc128mn = tc::idesc_bf16(128, 128, 0, 1);  // D[128x128], B N-major
+
+// The rows' tensor-memory round trips, two 32-column loads in flight per wait.
+// bf16 copy of this lane's 128 fp32 state columns (s32) into 64 packed columns (s16).
+__device__ __forceinline__ void state_to_bf16(uint32_t s32, uint32_t s16) {
+#pragma unroll
+  for (int q2 = 0; q2 < 2; ++q2) {
+    uint32_t f[2][32];
+    tc::tmem_ld32(s32 + q2 * 64, f[0]);
+    tc::tmem_ld32(s32 + q2 * 64 + 32, f[1]);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t b[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[h][2 * i]), __uint_as_float(f[h][2 * i + 1]));
+      tc::tmem_st16(s16 + q2 * 32 + h * 16, b);
+    }
+  }
+}
+// the 128 fp32 state columns scaled by ec in place
+__device__ __forceinline__ void state_scale(uint32_t s32, float ec) {
+#pragma unroll
+  for (int q2 = 0; q2 < 2; ++q2) {
+    uint32_t f[2][32];
+    tc::tmem_ld32(s32 + q2 * 64, f[0]);
+    tc::tmem_ld32(s32 + q2 * 64 + 32, f[1]);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[h][e] = __float_as_uint(ec * __uint_as_float(f[h][e]));
+      tc::tmem_st32(s32 + q2 * 64 + h * 32, f[h]);
+    }
+  }
+}
 
 struct Prm {
   const int32_t* meta;
@@ -407,9 +444,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % C::kStages;
         const uint32_t sb = tc::smem_u32(stage(ci));
+        // D2 once the chain's D1 is done and D3 once its D4 is done: the output products fill the tensor pipe
+        // while the rows form U and the bf16 state, instead of sharing it with the chain's products
         if (!__all_sync(~0u, tc::mbar_wait(&bar_s, ci & 1, kWaitCycles)) ||
             !__all_sync(~0u, tc::mbar_wait(&bar_full[s], (ci / C::kStages) & 1, kWaitCycles)) ||
-            (ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles)))) {
+            (ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_of, (ci - 1) & 1, kWaitCycles))) ||
+            !__all_sync(~0u, tc::mbar_wait(&bar_d1, ci & 1, kWaitCycles))) {
           ok = false;
           break;
         }
@@ -423,7 +463,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           }
         }
         tc::mma_commit_w(&bar_d2);
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_u, ci & 1, kWaitCycles))) {
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_d4, ci & 1, kWaitCycles))) {  // (D4 read U: U is written)
           ok = false;
           break;
         }
@@ -488,17 +528,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
         }
         const float ec = reinterpret_cast<const float*>(sb + C::kStG)[128];  // e^{gC}
         // S <- e^{gC} S in place, both chains (overlaps their D1; D4 adds to it)
-        for (int c = 0; c < nch; ++c) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t f[32];
-            tc::tmem_ld32(tmem + lb + 256 * c + C::kTS32 + q * 32, f);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e2 = 0; e2 < 32; ++e2) f[e2] = __float_as_uint(ec * __uint_as_float(f[e2]));
-            tc::tmem_st32(tmem + lb + 256 * c + C::kTS32 + q * 32, f);
-          }
-        }
+        for (int c = 0; c < nch; ++c) state_scale(tmem + lb + 256 * c + C::kTS32, ec);
         // U = Ut^T - D1 (chain 0) and U = -D1 (chain 1, Ut = 0), over the D1 columns once read
         const uint8_t* utj = sb + C::kStUt + j * 128;
         for (int c = 0; c < nch && ok; ++c) {
@@ -508,23 +538,26 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           }
           tc::fence_after_sync();
           const uint32_t tb = tmem + lb + 256 * c;
+          // both halves of D1 in registers before U is written over their columns
+          uint32_t d1[2][32];
+          tc::tmem_ld32(tb + C::kTD1, d1[0]);
+          tc::tmem_ld32(tb + C::kTD1 + 32, d1[1]);
+          uint4 uv[8];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            uv[c8] = c == 1 ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(utj + ((c8 ^ (j & 7)) << 4));
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            uint32_t d1[32], u2[16];
-            tc::tmem_ld32(tb + C::kTD1 + half * 32, d1);
-            uint4 uv[4];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-              uv[c4] = c == 1 ? make_uint4(0u, 0u, 0u, 0u)
-                              : *reinterpret_cast<const uint4*>(utj + (((half * 4 + c4) ^ (j & 7)) << 4));
-            tc::tmem_wait_ld();
+            uint32_t u2[16];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-              const uint32_t w4[4] = {uv[c4].x, uv[c4].y, uv[c4].z, uv[c4].w};
+              const uint4 w = uv[half * 4 + c4];
+              const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2)
-                u2[c4 * 4 + e2] = tc::pack_bf16x2(__uint_as_float(w4[e2] << 16) - __uint_as_float(d1[c4 * 8 + 2 * e2]),
-                                                  __uint_as_float(w4[e2] & 0xFFFF0000u) - __uint_as_float(d1[c4 * 8 + 2 * e2 + 1]));
+                u2[c4 * 4 + e2] = tc::pack_bf16x2(__uint_as_float(w4[e2] << 16) - __uint_as_float(d1[half][c4 * 8 + 2 * e2]),
+                                                  __uint_as_float(w4[e2] & 0xFFFF0000u) - __uint_as_float(d1[half][c4 * 8 + 2 * e2 + 1]));
             }
             tc::tmem_st16(tb + C::kTU + half * 16, u2);
           }
@@ -542,15 +575,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
             break;
           }
           tc::fence_after_sync();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t f[32], b[16];
-            tc::tmem_ld32(tmem + lb + 256 * c + C::kTS32 + q * 32, f);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-            tc::tmem_st16(tmem + lb + 256 * c + C::kTS16 + q * 16, b);
-          }
+          state_to_bf16(tmem + lb + 256 * c + C::kTS32, tmem + lb + 256 * c + C::kTS16);
           tc::tmem_wait_st();
           tc::fence_before_sync();
           tc::mbar_arrive(&bar_sc[c]);
@@ -623,21 +648,22 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
                          : ik == kInitScan ? reinterpret_cast<const float*>(scanbuf(e1) + gdnws::kScanS) + j * kD
                                            : nullptr;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t f[32];
+      for (int q2 = 0; q2 < 2; ++q2) {  // 16 loads in flight, then two stores
+        uint32_t f[2][32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = src ? reinterpret_cast<const float4*>(src)[q * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
-          f[4 * i] = __float_as_uint(v.x);
-          f[4 * i + 1] = __float_as_uint(v.y);
-          f[4 * i + 2] = __float_as_uint(v.z);
-          f[4 * i + 3] = __float_as_uint(v.w);
+        for (int i = 0; i < 16; ++i) {
+          const float4 v = src ? reinterpret_cast<const float4*>(src)[q2 * 16 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+          f[i >> 3][4 * (i & 7)] = __float_as_uint(v.x);
+          f[i >> 3][4 * (i & 7) + 1] = __float_as_uint(v.y);
+          f[i >> 3][4 * (i & 7) + 2] = __float_as_uint(v.z);
+          f[i >> 3][4 * (i & 7) + 3] = __float_as_uint(v.w);
         }
         if (ik == kInitIdentity) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __float_as_uint(q * 32 + i == j ? 1.f : 0.f);
+          for (int i = 0; i < 64; ++i) f[i >> 5][i & 31] = __float_as_uint(q2 * 64 + i == j ? 1.f : 0.f);
         }
-        tc::tmem_st32(tmem + lb + C::kTS32 + q * 32, f);
+        tc::tmem_st32(tmem + lb + C::kTS32 + q2 * 64, f[0]);
+        tc::tmem_st32(tmem + lb + C::kTS32 + q2 * 64 + 32, f[1]);
       }
       tc::tmem_wait_st();
     }
@@ -646,18 +672,23 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     // and the MMAs add S_hi M_q + S_lo M_q to it
     for (int q = 1; q <= n_comb && ok; ++q) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t f[32], bh[16], bl[16];
-        tc::tmem_ld32(tmem + lb + C::kTS32 + c4 * 32, f);
+      for (int q2 = 0; q2 < 2; ++q2) {
+        uint32_t f[2][32];
+        tc::tmem_ld32(tmem + lb + C::kTS32 + q2 * 64, f[0]);
+        tc::tmem_ld32(tmem + lb + C::kTS32 + q2 * 64 + 32, f[1]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = __uint_as_float(f[2 * i]), b = __uint_as_float(f[2 * i + 1]);
-          bh[i] = tc::pack_bf16x2(a, b);
-          bl[i] = tc::pack_bf16x2(a - __uint_as_float(bh[i] << 16), b - __uint_as_float(bh[i] & 0xFFFF0000u));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t bh[16], bl[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = __uint_as_float(f[hf][2 * i]), b = __uint_as_float(f[hf][2 * i + 1]);
+            bh[i] = tc::pack_bf16x2(a, b);
+            bl[i] = tc::pack_bf16x2(a - __uint_as_float(bh[i] << 16), b - __uint_as_float(bh[i] & 0xFFFF0000u));
+          }
+          tc::tmem_st16(tmem + lb + C::kTS16 + (2 * q2 + hf) * 16, bh);
+          tc::tmem_st16(tmem + lb + C::kTSlo + (2 * q2 + hf) * 16, bl);
         }
-        tc::tmem_st16(tmem + lb + C::kTS16 + c4 * 16, bh);
-        tc::tmem_st16(tmem + lb + C::kTSlo + c4 * 16, bl);
       }
       const int in = 2 * q - 1;  // the item of N_q
       if (!__all_sync(~0u, tc::mbar_wait(&bar_cb[in % 3], (in / 3) & 1, kWaitCycles))) {
@@ -667,17 +698,18 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       {
         const uint8_t* nrow = smem + (in % 3) * C::kStageBytes + j * 512;  // pieces swizzled by j % 32
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t f[32];
+        for (int q2 = 0; q2 < 2; ++q2) {
+          uint32_t f[2][32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = *reinterpret_cast<const float4*>(nrow + (((c4 * 8 + i) ^ (j & 31)) << 4));
-            f[4 * i] = __float_as_uint(v.x);
-            f[4 * i + 1] = __float_as_uint(v.y);
-            f[4 * i + 2] = __float_as_uint(v.z);
-            f[4 * i + 3] = __float_as_uint(v.w);
+          for (int i = 0; i < 16; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(nrow + (((q2 * 16 + i) ^ (j & 31)) << 4));
+            f[i >> 3][4 * (i & 7)] = __float_as_uint(v.x);
+            f[i >> 3][4 * (i & 7) + 1] = __float_as_uint(v.y);
+            f[i >> 3][4 * (i & 7) + 2] = __float_as_uint(v.z);
+            f[i >> 3][4 * (i & 7) + 3] = __float_as_uint(v.w);
           }
-          tc::tmem_st32(tmem + lb + C::kTS32 + c4 * 32, f);
+          tc::tmem_st32(tmem + lb + C::kTS32 + q2 * 64, f[0]);
+          tc::tmem_st32(tmem + lb + C::kTS32 + q2 * 64 + 32, f[1]);
         }
       }
       tc::tmem_wait_st();
@@ -690,15 +722,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       tc::fence_after_sync();
     }
     // the bf16 operand of the start state
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t f[32], b[16];
-      tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-      tc::tmem_st16(tmem + lb + C::kTS16 + q * 16, b);
-    }
+    state_to_bf16(tmem + lb + C::kTS32, tmem + lb + C::kTS16);
     tc::tmem_wait_st();
     tc::fence_before_sync();
     tc::mbar_arrive(&bar_s);
@@ -711,16 +735,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       const float* gblk = reinterpret_cast<const float*>(sb + C::kStG);  // e^g [64] | e^{gC-g} [64] | e^{gC}
       // S <- e^{gC} S in place (overlaps D1; D4 adds to it)
-      const float ec = gblk[128];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t f[32];
-        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) f[e] = __float_as_uint(ec * __uint_as_float(f[e]));
-        tc::tmem_st32(tmem + lb + C::kTS32 + q * 32, f);
-      }
+      state_scale(tmem + lb + C::kTS32, gblk[128]);
       // D1 done; D3 of the previous chunk (which reads U) done
       if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_d1, ci & 1, kWaitCycles)) ||
           (O && ci >= 1 && !__all_sync(~0u, tc::mbar_wait(&bar_d23, (ci - 1) & 1, kWaitCycles)))) {
@@ -730,25 +745,29 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       tc::fence_after_sync();
       // U = Ut^T - D1;  row j of Ut^T is one swizzled 128-byte row
       const uint8_t* utj = sb + C::kStUt + j * 128;
+      {
+        uint32_t d1[2][32];
+        tc::tmem_ld32(tmem + lb + C::kTD1, d1[0]);
+        tc::tmem_ld32(tmem + lb + C::kTD1 + 32, d1[1]);
+        uint4 uv[8];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t d1[32], u2[16];
-        tc::tmem_ld32(tmem + lb + C::kTD1 + half * 32, d1);
-        uint4 uv[4];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)  // (a transition M runs with Ut = 0)
-          uv[c4] = zero_ut ? make_uint4(0u, 0u, 0u, 0u)
-                           : *reinterpret_cast<const uint4*>(utj + (((half * 4 + c4) ^ (j & 7)) << 4));
+        for (int c8 = 0; c8 < 8; ++c8)  // (a transition M runs with Ut = 0)
+          uv[c8] = zero_ut ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(utj + ((c8 ^ (j & 7)) << 4));
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const uint32_t w4[4] = {uv[c4].x, uv[c4].y, uv[c4].z, uv[c4].w};
+        for (int half = 0; half < 2; ++half) {
+          uint32_t u2[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            u2[c4 * 4 + e] = tc::pack_bf16x2(__uint_as_float(w4[e] << 16) - __uint_as_float(d1[c4 * 8 + 2 * e]),
-                                             __uint_as_float(w4[e] & 0xFFFF0000u) - __uint_as_float(d1[c4 * 8 + 2 * e + 1]));
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const uint4 w = uv[half * 4 + c4];
+            const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              u2[c4 * 4 + e] = tc::pack_bf16x2(__uint_as_float(w4[e] << 16) - __uint_as_float(d1[half][c4 * 8 + 2 * e]),
+                                               __uint_as_float(w4[e] & 0xFFFF0000u) - __uint_as_float(d1[half][c4 * 8 + 2 * e + 1]));
+          }
+          tc::tmem_st16(tmem + lb + C::kTU + half * 16, u2);
         }
-        tc::tmem_st16(tmem + lb + C::kTU + half * 16, u2);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -763,15 +782,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       tc::fence_after_sync();
       // the bf16 operand of the new state
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t f[32], b[16];
-        tc::tmem_ld32(tmem + lb + C::kTS32 + q * 32, f);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) b[i] = tc::pack_bf16x2(__uint_as_float(f[2 * i]), __uint_as_float(f[2 * i + 1]));
-        tc::tmem_st16(tmem + lb + C::kTS16 + q * 16, b);
-      }
+      state_to_bf16(tmem + lb + C::kTS32, tmem + lb + C::kTS16);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bar_s);
