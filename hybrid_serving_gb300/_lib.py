@@ -12,6 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libhsfork.so")
 
 HS_OK, HS_EINVAL, HS_ECAPACITY, HS_EUNSUPPORTED, HS_ECUDA, HS_EDEVICE, HS_ENOPAGES = 0, -1, -2, -3, -4, -5, -6
+# device status codes (values of the int32 status word)
+HS_DEV_OK, HS_DEV_BAD_PAGE, HS_DEV_BAD_SLOT, HS_DEV_BAD_META, HS_DEV_TIMEOUT = 0, 1, 2, 3, 4
 HS_F32, HS_BF16 = 0, 1
 HS_SEG_READOUT, HS_SEG_NO_READOUT = 1, 2
 _NAMES = {HS_EINVAL: "HS_EINVAL", HS_ECAPACITY: "HS_ECAPACITY", HS_EUNSUPPORTED: "HS_EUNSUPPORTED",
@@ -97,6 +99,7 @@ _SIGS = {
     "hs_swiglu": (I32, [P, C.c_int64, I32, I32, P, C.c_int64, P]),
     "hs_copy_rows": (I32, [P, C.c_int64, P, P, C.c_int64, P, I32, I32, P]),
     "hs_check_status": (I32, [I32P]),
+    "hs_debug_wait_timeout": (I32, [C.c_int64, P, P, P]),
     "hs_last_error": (C.c_char_p, []),
     "hs_launch_count": (C.c_int64, []),
     "hs_version": (C.c_char_p, []),

@@ -369,3 +369,16 @@ def choice_logprobs(caps: Caps, dev_meta: torch.Tensor, hidden, option_rows, log
 def check_status(dev_status: torch.Tensor):
     w = C.c_int32(int(dev_status.item()))
     check(lib.hs_check_status(C.byref(w)))
+
+
+def debug_wait_timeout(wait_cycles: int, dev_status: torch.Tensor, dev_elapsed: Optional[torch.Tensor] = None,
+                       stream=None):
+    """Run the bounded-wait failure path on purpose (hs_debug_wait_timeout): the status word receives
+    HS_DEV_TIMEOUT and dev_elapsed (int64[2]) the clocks each of the two waits lasted."""
+    dev = _cur_dev()
+    _on_device("dev_status", dev_status, dev, torch.int32)
+    _need(dev_status.numel() >= 1, "dev_status needs one int32")
+    if dev_elapsed is not None:
+        _on_device("dev_elapsed", dev_elapsed, dev, torch.int64)
+        _need(dev_elapsed.numel() >= 2, "dev_elapsed needs two int64")
+    check(lib.hs_debug_wait_timeout(int(wait_cycles), dev_status.data_ptr(), _ptr(dev_elapsed), _stream(stream)))

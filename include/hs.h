@@ -396,6 +396,20 @@ hs_status hs_copy_rows(const void* src, int64_t lds, const int32_t* src_rows, vo
 /* ------------------------------------------------------------------------ */
 /* Status and diagnostics                                                    */
 /* ------------------------------------------------------------------------ */
+/* Failure detection of the bounded device waits.  Every wait of a tcgen05
+ * kernel on a shared-memory barrier gives up after a cycle limit: the kernel
+ * records HS_DEV_TIMEOUT in the status word, lets its own copies in flight
+ * land, frees its tensor memory and returns, so the context stays usable and
+ * the host learns of the failure from the status word.  This call takes that
+ * path on purpose on one CTA: holding 32 tensor-memory columns and a 1 KB
+ * bulk copy in flight, two warps wait on barriers that nothing ever completes
+ * -- one with the suspending try_wait poll, one with the spinning test_wait
+ * poll -- for wait_cycles SM clocks each (1 .. 2^31); then the copy is
+ * waited for and the columns freed.  *dev_status (device int32) receives
+ * HS_DEV_TIMEOUT; dev_elapsed (device int64[2], or NULL) the clocks each
+ * wait lasted.  Asynchronous on `stream`.  HS_EINVAL: a null status word or
+ * wait_cycles outside the range. */
+hs_status hs_debug_wait_timeout(int64_t wait_cycles, int32_t* dev_status, int64_t* dev_elapsed, void* stream);
 /* Map a host copy of the device status word to HS_OK / HS_EDEVICE. */
 hs_status hs_check_status(const int32_t* host_status_word);
 /* Thread-local message of the last failing call on this thread. */
