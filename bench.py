@@ -41,11 +41,12 @@ N_OPT = 4
 METRIC = "tree-prefill tokens/s on 1 GB300 (ForkAttn + GDN); % of tensor/HBM roofline"
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of this
 # bench's workload, valid only while every listed kernel source still has the hash it was captured with.
-# gdn_fork: the sum over the launches of one call (chunk-local pass, two state passes per tree level).
+# fork_attn: the mean of three captures of one launch; gdn_fork: the sum over the launches of one call
+# (chunk-local pass, two state passes per tree level).
 NCU_TRAFFIC = {
-    "fork_attn": ({"hybrid_serving_gb300/csrc/fork_attn_tc.cu": "fdc41de45030cdd0"}, 56.58e6),
+    "fork_attn": ({"hybrid_serving_gb300/csrc/fork_attn_tc.cu": "fdc41de45030cdd0"}, 56.45e6),
     "gdn_fork": ({"hybrid_serving_gb300/csrc/gdn_prep_tc.cu": "4490dfd481c219c1",
-                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "ef8bad51c6a7024b"}, 512.17e6),
+                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "6b88e2b513537d34"}, 512.67e6),
 }
 
 
