@@ -1,6 +1,6 @@
 // gemm_tc.cu -- batch-invariant bf16 GEMM on tcgen05 for sm_103a.
 //
-//   C[M, N] = A[M, K] . B[N, K]^T  (+ R[M, N])      bf16 in, fp32 accumulate, bf16 out
+//   C[M, N] = A[M, K] . B[N, K]^T  (+ R[M, N])      bf16 in, fp32 accumulate, C and R bf16 or fp32
 //
 // Flide, "Accelerating Decision Inference with Exact State Forking",
 // section 3.5: every matrix product sums each output element in a fixed
@@ -12,8 +12,9 @@
 // One CTA per output tile.  Warp 0 streams A and B tiles with TMA into a
 // 3-stage ring (128-byte swizzle); warp 1 owns 128 TMEM columns and issues
 // tcgen05.mma (M=128, N=128, K=16) from one thread; warps 2..5 read the
-// accumulator back (thread = row), add the optional residual and store
-// bf16.  Waits are bounded and report HS_DEV_TIMEOUT through the status word.
+// accumulator back (thread = row), add the optional residual and store C
+// (bf16 rounded to nearest, or fp32: a residual stream kept in fp32).  Waits
+// are bounded and report HS_DEV_TIMEOUT through the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -32,18 +33,44 @@ constexpr int kThreads = 192;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr uint32_t kIdesc = tc::idesc_bf16(BM, BN, 0, 0);
 
+template <typename CT>
 struct GemmParams {
   int M, N, K;
-  __nv_bfloat16* C;
+  CT* C;
   long long ldc;
-  const __nv_bfloat16* R;  // optional residual, same layout as C
+  const CT* R;  // optional residual, same layout and type as C
   long long ldr;
   int32_t* status;
 };
 
+// eight accumulator values (+ the residual's eight) into C
+__device__ __forceinline__ void epi8(float (&f)[8], const __nv_bfloat16* res, __nv_bfloat16* dst) {
+  if (res) {
+    float rr[8];
+    hsd::cvt16(*reinterpret_cast<const float4*>(res), rr, __nv_bfloat16());
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] += rr[i];
+  }
+  uint4 o;
+  o.x = tc::pack_bf16x2(f[0], f[1]);
+  o.y = tc::pack_bf16x2(f[2], f[3]);
+  o.z = tc::pack_bf16x2(f[4], f[5]);
+  o.w = tc::pack_bf16x2(f[6], f[7]);
+  *reinterpret_cast<uint4*>(dst) = o;
+}
+__device__ __forceinline__ void epi8(float (&f)[8], const float* res, float* dst) {
+  if (res) {
+    const float4 a = reinterpret_cast<const float4*>(res)[0], b = reinterpret_cast<const float4*>(res)[1];
+    f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w; f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+  }
+  reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+template <typename CT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                    const GemmParams p) {
+                    const GemmParams<CT> p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc;
   __shared__ uint32_t tmem_slot;
@@ -130,25 +157,14 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         tc::tmem_wait_ld();
         if (row < p.M) {
           const int col0 = n0 + c * 32;
-          __nv_bfloat16* dst = p.C + (size_t)row * p.ldc + col0;
-          const __nv_bfloat16* res = p.R ? p.R + (size_t)row * p.ldr + col0 : nullptr;
+          CT* dst = p.C + (size_t)row * p.ldc + col0;
+          const CT* res = p.R ? p.R + (size_t)row * p.ldr + col0 : nullptr;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float f[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[q * 8 + i]);
-            if (res) {
-              float rr[8];
-              hsd::cvt16(*reinterpret_cast<const float4*>(res + q * 8), rr, __nv_bfloat16());
-#pragma unroll
-              for (int i = 0; i < 8; ++i) f[i] += rr[i];
-            }
-            uint4 o;
-            o.x = tc::pack_bf16x2(f[0], f[1]);
-            o.y = tc::pack_bf16x2(f[2], f[3]);
-            o.z = tc::pack_bf16x2(f[4], f[5]);
-            o.w = tc::pack_bf16x2(f[6], f[7]);
-            *reinterpret_cast<uint4*>(dst + q * 8) = o;
+            epi8(f, res ? res + q * 8 : nullptr, dst + q * 8);
           }
         }
       }
@@ -190,9 +206,10 @@ bool map_2d(CUtensorMap* m, const void* base, long long rows, long long cols, lo
 }  // namespace
 
 extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B,
-                                  int64_t ldb, void* C, int64_t ldc, const void* R, int64_t ldr, int32_t* dev_status,
-                                  void* stream) {
+                                  int64_t ldb, void* C, int64_t ldc, const void* R, int64_t ldr, hs_dtype c_dtype,
+                                  int32_t* dev_status, void* stream) {
   HS_CHECK_ARG(A && B && C, "null argument");
+  if (c_dtype != HS_BF16 && c_dtype != HS_F32) return hs::fail(HS_EUNSUPPORTED, "gemm: C dtype %d", c_dtype);
   HS_CHECK_ARG(M >= 0 && N > 0 && K > 0, "bad shape %d x %d x %d", M, N, K);
   if (N % BN != 0 || K % BK != 0)
     return hs::fail(HS_EUNSUPPORTED, "N (%d) must be a multiple of %d and K (%d) of %d", N, BN, K, BK);
@@ -211,14 +228,21 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   const int slot = hsd::device_slot();
   if (slot < 0) return hs::fail(HS_ECUDA, "gemm: no usable CUDA device");
   if (!configured[slot].load()) {
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem + 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_bf16_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
+            cudaSuccess)
       return hs::fail(HS_ECUDA, "gemm: cannot raise the shared-memory limit");
     configured[slot].store(true);
   }
-  GemmParams prm{M, N, K, (__nv_bfloat16*)C, ldc, (const __nv_bfloat16*)R, ldr, dev_status};
   dim3 grid(N / BN, (M + BM - 1) / BM);
-  gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
+  if (c_dtype == HS_F32) {
+    GemmParams<float> prm{M, N, K, (float*)C, ldc, (const float*)R, ldr, dev_status};
+    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
+  } else {
+    GemmParams<__nv_bfloat16> prm{M, N, K, (__nv_bfloat16*)C, ldc, (const __nv_bfloat16*)R, ldr, dev_status};
+    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
+  }
   HS_LAUNCH_CHECK("gemm_bf16");
   return HS_OK;
 }

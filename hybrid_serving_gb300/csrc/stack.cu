@@ -26,53 +26,72 @@ namespace {
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 __device__ __forceinline__ float softplus(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 
+// eight consecutive elements as floats, and back (16-byte aligned; bf16 stores round to nearest even)
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
+  hsd::cvt16(*reinterpret_cast<const float4*>(p), f, __nv_bfloat16());
+}
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
+  __nv_bfloat162 o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  *reinterpret_cast<float4*>(p) = *reinterpret_cast<float4*>(o);
+}
+__device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
 // ---------------------------------------------------------------- embedding
+template <typename O>
 __global__ void embed_kernel(const int32_t* __restrict__ ids, int T, const __nv_bfloat16* __restrict__ table,
-                             int vocab, int dim, __nv_bfloat16* __restrict__ out, int32_t* status) {
+                             int vocab, int dim, O* __restrict__ out, int32_t* status) {
   const int t = blockIdx.x;
   if (t >= T) return;
   const int id = ids[t];
   const bool ok = id >= 0 && id < vocab;
   if (!ok && threadIdx.x == 0) hsd::set_status(status, HS_DEV_BAD_META);
   for (int c = threadIdx.x * 8; c < dim; c += blockDim.x * 8) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok) v = *reinterpret_cast<const float4*>(table + (size_t)id * dim + c);
-    *reinterpret_cast<float4*>(out + (size_t)t * dim + c) = v;
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (ok) load8(table + (size_t)id * dim + c, f);
+    store8(out + (size_t)t * dim + c, f);
   }
 }
 
 // ------------------------------------------------------------------ RMSNorm
 // one warp per row: lane-strided fp32 sums of squares, then a fixed butterfly
-__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, long long ldx, int T, int dim,
-                               const __nv_bfloat16* __restrict__ w, float eps, __nv_bfloat16* __restrict__ out,
-                               long long ldo) {
+template <typename X, typename O>
+__global__ void rmsnorm_kernel(const X* __restrict__ x, long long ldx, int T, int dim,
+                               const __nv_bfloat16* __restrict__ w, float eps, O* __restrict__ out, long long ldo) {
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= T) return;
-  const __nv_bfloat16* xr = x + (size_t)row * ldx;
+  const X* xr = x + (size_t)row * ldx;
   float ss = 0.f;
   for (int c = lane * 8; c < dim; c += 256) {
     float f[8];
-    hsd::cvt16(*reinterpret_cast<const float4*>(xr + c), f, __nv_bfloat16());
+    load8(xr + c, f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
   }
   ss = hsd::warp_sum(ss);
   const float inv = 1.f / sqrtf(ss / (float)dim + eps);
-  __nv_bfloat16* orow = out + (size_t)row * ldo;
+  O* orow = out + (size_t)row * ldo;
   for (int c = lane * 8; c < dim; c += 256) {
     float f[8], g[8];
-    hsd::cvt16(*reinterpret_cast<const float4*>(xr + c), f, __nv_bfloat16());
+    load8(xr + c, f);
     if (w) {
-      hsd::cvt16(*reinterpret_cast<const float4*>(w + c), g, __nv_bfloat16());
+      load8(w + c, g);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) g[i] = 1.f;
     }
-    __nv_bfloat162 o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = __floats2bfloat162_rn(f[2 * i] * inv * g[2 * i], f[2 * i + 1] * inv * g[2 * i + 1]);
-    *reinterpret_cast<float4*>(orow + c) = *reinterpret_cast<float4*>(o);
+    for (int i = 0; i < 8; ++i) f[i] = f[i] * inv * g[i];
+    store8(orow + c, f);
   }
 }
 
@@ -207,29 +226,43 @@ hs_status need_device() {
 }  // namespace
 
 extern "C" hs_status hs_embed(const int32_t* ids, int32_t T, const void* table, int32_t vocab, int32_t dim,
-                              void* out, int32_t* dev_status, void* stream) {
+                              void* out, hs_dtype out_dtype, int32_t* dev_status, void* stream) {
   HS_CHECK_ARG(ids && table && out, "null argument");
   HS_CHECK_ARG(T >= 0 && vocab > 0 && dim > 0 && dim % 8 == 0, "bad shape");
   HS_CHECK_ARG(al16(table) && al16(out), "16-byte alignment required");
+  if (out_dtype != HS_BF16 && out_dtype != HS_F32) return hs::fail(HS_EUNSUPPORTED, "embed: output dtype %d", out_dtype);
   if (hs_status s = need_device()) return s;
   if (T == 0) return HS_OK;
-  embed_kernel<<<T, 128, 0, (cudaStream_t)stream>>>(ids, T, (const __nv_bfloat16*)table, vocab, dim,
-                                                    (__nv_bfloat16*)out, dev_status);
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (out_dtype == HS_F32)
+    embed_kernel<<<T, 128, 0, st>>>(ids, T, (const __nv_bfloat16*)table, vocab, dim, (float*)out, dev_status);
+  else
+    embed_kernel<<<T, 128, 0, st>>>(ids, T, (const __nv_bfloat16*)table, vocab, dim, (__nv_bfloat16*)out, dev_status);
   HS_LAUNCH_CHECK("embed");
   return HS_OK;
 }
 
-extern "C" hs_status hs_rmsnorm(const void* x, int64_t ldx, int32_t T, int32_t dim, const void* w, float eps,
-                                void* out, int64_t ldo, void* stream) {
+extern "C" hs_status hs_rmsnorm(const void* x, int64_t ldx, hs_dtype x_dtype, int32_t T, int32_t dim, const void* w,
+                                float eps, void* out, int64_t ldo, hs_dtype out_dtype, void* stream) {
   HS_CHECK_ARG(x && out, "null argument");
   HS_CHECK_ARG(T >= 0 && dim > 0 && dim % 8 == 0 && ldx >= dim && ldo >= dim && ldx % 8 == 0 && ldo % 8 == 0,
                "bad shape");
   HS_CHECK_ARG(al16(x) && al16(out) && al16(w), "16-byte alignment required");
+  if ((x_dtype != HS_BF16 && x_dtype != HS_F32) || (out_dtype != HS_BF16 && out_dtype != HS_F32))
+    return hs::fail(HS_EUNSUPPORTED, "rmsnorm: dtypes %d -> %d", x_dtype, out_dtype);
   if (hs_status s = need_device()) return s;
   if (T == 0) return HS_OK;
-  rmsnorm_kernel<<<(T + 7) / 8, 256, 0, (cudaStream_t)stream>>>((const __nv_bfloat16*)x, ldx, T, dim,
-                                                                (const __nv_bfloat16*)w, eps,
-                                                                (__nv_bfloat16*)out, ldo);
+  const dim3 grid((T + 7) / 8), block(256);
+  const cudaStream_t st = (cudaStream_t)stream;
+  const __nv_bfloat16* wb = (const __nv_bfloat16*)w;
+  if (x_dtype == HS_F32 && out_dtype == HS_F32)
+    rmsnorm_kernel<<<grid, block, 0, st>>>((const float*)x, ldx, T, dim, wb, eps, (float*)out, ldo);
+  else if (x_dtype == HS_F32)
+    rmsnorm_kernel<<<grid, block, 0, st>>>((const float*)x, ldx, T, dim, wb, eps, (__nv_bfloat16*)out, ldo);
+  else if (out_dtype == HS_F32)
+    rmsnorm_kernel<<<grid, block, 0, st>>>((const __nv_bfloat16*)x, ldx, T, dim, wb, eps, (float*)out, ldo);
+  else
+    rmsnorm_kernel<<<grid, block, 0, st>>>((const __nv_bfloat16*)x, ldx, T, dim, wb, eps, (__nv_bfloat16*)out, ldo);
   HS_LAUNCH_CHECK("rmsnorm");
   return HS_OK;
 }

@@ -9,7 +9,8 @@ SwiGLU, option log-probs).  PyTorch only allocates device memory.
 Layer definition (the pages give none; see the oracle for the same text):
 pre-norm residual blocks of a token mixer ('A' attention, 'G' Gated
 DeltaNet) and a SwiGLU MLP; final RMSNorm; option logits against embedding
-rows of the option tokens (Flide section 3.1, Eq. 1).  Every tensor between
+rows of the option tokens (Flide section 3.1, Eq. 1).  The residual stream
+and the final norm's output are kept in fp32; every other tensor between
 operations is stored in bf16 (gates fp32).
 """
 from __future__ import annotations
@@ -21,7 +22,7 @@ from typing import Dict, List, Optional
 import numpy as np
 import torch
 
-from . import api
+from . import _lib, api
 from ._lib import check, lib
 
 DEV = "cuda"
@@ -47,12 +48,22 @@ def _s(stream=None) -> int:
     return (stream or torch.cuda.current_stream()).cuda_stream
 
 
+def _dt(t) -> int:
+    return _lib.HS_F32 if t.dtype == torch.float32 else _lib.HS_BF16
+
+
 def gemm(A, B, Cout, M: int, R=None, status=None, stream=None):
-    """Cout[:M] = A[:M] @ B^T (+ R[:M]) through hs_gemm_bf16."""
+    """Cout[:M] = A[:M] @ B^T (+ R[:M]) through hs_gemm_bf16 (Cout and R bf16 or fp32)."""
     N, K = B.shape
     check(lib.hs_gemm_bf16(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), Cout.data_ptr(),
                            Cout.stride(0), R.data_ptr() if R is not None else None,
-                           R.stride(0) if R is not None else 0, status.data_ptr(), _s(stream)))
+                           R.stride(0) if R is not None else 0, _dt(Cout), status.data_ptr(), _s(stream)))
+
+
+def rmsnorm(x, T: int, dim: int, eps: float, out, stream=None):
+    """out[:T] = RMSNorm(x[:T]) with unit weight (x and out bf16 or fp32)."""
+    check(lib.hs_rmsnorm(x.data_ptr(), x.stride(0), _dt(x), T, dim, None, eps, out.data_ptr(), out.stride(0),
+                         _dt(out), _s(stream)))
 
 
 class HybridStack:
@@ -75,8 +86,9 @@ class HybridStack:
         sh = self.sh
         bf = torch.bfloat16
         self.Tcap = Tcap
-        self.h = torch.zeros((Tcap, sh.hidden), dtype=bf, device=DEV)
-        self.a = torch.zeros_like(self.h)
+        self.h = torch.zeros((Tcap, sh.hidden), dtype=torch.float32, device=DEV)  # residual stream
+        self.a = torch.zeros((Tcap, sh.hidden), dtype=bf, device=DEV)             # normed GEMM input
+        self.hf = torch.zeros((Tcap, sh.hidden), dtype=torch.float32, device=DEV)  # final norm
         wp_n = max(v.shape[0] for k, v in self.W.items() if k.endswith("wp")) if self.n_gdn else 0
         self.proj = torch.zeros((Tcap, max(wp_n, 2 * sh.ffn)), dtype=bf, device=DEV)
         self.q = torch.zeros((Tcap, sh.attn_hq, sh.head_d), dtype=bf, device=DEV)
@@ -120,7 +132,7 @@ class HybridStack:
         bits: every step after the mixer works on each row by itself and the
         GEMM's rows do not depend on M); the returned hidden rows are then
         final at the readout rows only.
-        Returns (final hidden [T, hidden] view, option logprobs [n_readout, n_opt])."""
+        Returns (final hidden [T, hidden] fp32 view, option logprobs [n_readout, n_opt])."""
         sh, st = self.sh, self.status
         caps = R.caps
         T = R.info().n_tokens
@@ -128,19 +140,19 @@ class HybridStack:
         if selective and n_readout > 0:
             ro_rows = torch.tensor(R.readout_rows(), dtype=torch.int32).to(DEV, non_blocking=True)
             ro_idx = torch.arange(n_readout, dtype=torch.int32, device=DEV)
-            hr = torch.empty((n_readout, sh.hidden), dtype=torch.bfloat16, device=DEV)
-            ar = torch.empty_like(hr)
+            hr = torch.empty((n_readout, sh.hidden), dtype=torch.float32, device=DEV)
+            ar = torch.empty((n_readout, sh.hidden), dtype=torch.bfloat16, device=DEV)
+            fr = torch.empty_like(hr)
             gur = torch.empty((n_readout, 2 * sh.ffn), dtype=torch.bfloat16, device=DEV)
             mr = torch.empty((n_readout, sh.ffn), dtype=torch.bfloat16, device=DEV)
         last = len(sh.pattern) - 1
-        row_bytes = sh.hidden * 2
+        row_bytes = sh.hidden * 4  # (fp32 rows)
         check(lib.hs_embed(ids.data_ptr(), T, self.W["embed"].data_ptr(), sh.vocab, sh.hidden, self.h.data_ptr(),
-                           st.data_ptr(), s))
+                           _lib.HS_F32, st.data_ptr(), s))
         ai = gi = 0
         for li, kind in enumerate(sh.pattern):
             p = f"l{li}."
-            check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
-                                 sh.hidden, s))
+            rmsnorm(self.h, T, sh.hidden, sh.eps, self.a, stream)
             if kind == "A":
                 qv = self.q.view(self.Tcap, -1)
                 kv = self.k.view(self.Tcap, -1)
@@ -184,25 +196,21 @@ class HybridStack:
                 # the readout rows alone from here on: gather, MLP + final norm, scatter back for the head
                 check(lib.hs_copy_rows(self.h.data_ptr(), row_bytes, ro_rows.data_ptr(), hr.data_ptr(), row_bytes,
                                        ro_idx.data_ptr(), n_readout, row_bytes, s))
-                check(lib.hs_rmsnorm(hr.data_ptr(), sh.hidden, n_readout, sh.hidden, None, sh.eps, ar.data_ptr(),
-                                     sh.hidden, s))
+                rmsnorm(hr, n_readout, sh.hidden, sh.eps, ar, stream)
                 gemm(ar, self.W[p + "wgu"], gur, n_readout, status=st, stream=stream)
                 check(lib.hs_swiglu(gur.data_ptr(), gur.stride(0), n_readout, sh.ffn, mr.data_ptr(), sh.ffn, s))
                 gemm(mr, self.W[p + "wd"], hr, n_readout, R=hr, status=st, stream=stream)
-                check(lib.hs_rmsnorm(hr.data_ptr(), sh.hidden, n_readout, sh.hidden, None, sh.eps, ar.data_ptr(),
-                                     sh.hidden, s))
-                check(lib.hs_copy_rows(ar.data_ptr(), row_bytes, ro_idx.data_ptr(), self.a.data_ptr(), row_bytes,
+                rmsnorm(hr, n_readout, sh.hidden, sh.eps, fr, stream)
+                check(lib.hs_copy_rows(fr.data_ptr(), row_bytes, ro_idx.data_ptr(), self.hf.data_ptr(), row_bytes,
                                        ro_rows.data_ptr(), n_readout, row_bytes, s))
                 break
-            check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
-                                 sh.hidden, s))
+            rmsnorm(self.h, T, sh.hidden, sh.eps, self.a, stream)
             gu = self.proj[:, :2 * sh.ffn]
             gemm(self.a, self.W[p + "wgu"], gu, T, status=st, stream=stream)
             check(lib.hs_swiglu(gu.data_ptr(), gu.stride(0), T, sh.ffn, self.m.data_ptr(), sh.ffn, s))
             gemm(self.m, self.W[p + "wd"], self.h, T, R=self.h, status=st, stream=stream)
         else:
-            check(lib.hs_rmsnorm(self.h.data_ptr(), sh.hidden, T, sh.hidden, None, sh.eps, self.a.data_ptr(),
-                                 sh.hidden, s))
+            rmsnorm(self.h, T, sh.hidden, sh.eps, self.hf, stream)
         lp = torch.empty((max(n_readout, 1), len(sh.option_ids)), dtype=torch.float32, device=DEV)
-        api.choice_logprobs(caps, meta, self.a, self.opt, lp, st, stream=stream)
-        return self.a[:T], lp[:n_readout]
+        api.choice_logprobs(caps, meta, self.hf, self.opt, lp, st, stream=stream)
+        return self.hf[:T], lp[:n_readout]

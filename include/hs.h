@@ -347,19 +347,25 @@ hs_status hs_choice_logprobs(const hs_round_caps* caps, const void* dev_meta, hs
 /* (elements); every row is computed alone, in a fixed reduction order.     */
 /* ------------------------------------------------------------------------ */
 
-/* C[M,N] = A[M,K] . B[N,K]^T (+ R[M,N]), bf16 in/out, fp32 accumulation in a
- * fixed order for any M (one 128x128 tile per CTA, no split-K; Flide
- * section 3.5).  N % 128 == 0, K % 64 == 0, leading dimensions % 8 == 0,
- * 16-byte aligned pointers.  R may be NULL; R may alias C. */
+/* C[M,N] = A[M,K] . B[N,K]^T (+ R[M,N]), A and B bf16, fp32 accumulation in
+ * a fixed order for any M (one 128x128 tile per CTA, no split-K; Flide
+ * section 3.5); C and R in c_dtype (HS_BF16, rounded to nearest even, or
+ * HS_F32: a residual stream kept in fp32).  N % 128 == 0, K % 64 == 0,
+ * leading dimensions % 8 == 0, 16-byte aligned pointers.  R may be NULL; R
+ * may alias C.  HS_EUNSUPPORTED: another c_dtype or shape. */
 hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                       void* C, int64_t ldc, const void* R, int64_t ldr, int32_t* dev_status, void* stream);
-/* out[t] = table[ids[t]] (ids: device int32 [T]; an id outside [0,vocab)
+                       void* C, int64_t ldc, const void* R, int64_t ldr, hs_dtype c_dtype, int32_t* dev_status,
+                       void* stream);
+/* out[t] = table[ids[t]], table bf16 [vocab, dim], out in out_dtype (HS_BF16
+ * or HS_F32) [T, dim] (ids: device int32 [T]; an id outside [0,vocab)
  * gives a zero row and HS_DEV_BAD_META). */
 hs_status hs_embed(const int32_t* ids, int32_t T, const void* table, int32_t vocab, int32_t dim, void* out,
-                   int32_t* dev_status, void* stream);
-/* out = x / sqrt(mean(x^2) + eps) * w   (w bf16 [dim] or NULL for ones) */
-hs_status hs_rmsnorm(const void* x, int64_t ldx, int32_t T, int32_t dim, const void* w, float eps, void* out,
-                     int64_t ldo, void* stream);
+                   hs_dtype out_dtype, int32_t* dev_status, void* stream);
+/* out = x / sqrt(mean(x^2) + eps) * w   (w bf16 [dim] or NULL for ones);
+ * x in x_dtype and out in out_dtype, each HS_BF16 or HS_F32 (sums of
+ * squares in fp32, a fixed lane-strided order and butterfly per row). */
+hs_status hs_rmsnorm(const void* x, int64_t ldx, hs_dtype x_dtype, int32_t T, int32_t dim, const void* w, float eps,
+                     void* out, int64_t ldo, hs_dtype out_dtype, void* stream);
 /* Host: cos/sin table [max_pos][d/2][2] fp32 of angle p * theta^(-2i/d),
  * computed in double. */
 hs_status hs_rope_table(float* host_table, int32_t max_pos, int32_t d, double theta);

@@ -24,9 +24,10 @@ mixer followed by a SwiGLU MLP.
 * Readout: final RMSNorm; option log-probabilities against the embedding
   rows of the option tokens (Flide section 3.1, Eq. 1).
 
-A bf16 model stores every tensor between operations in bf16: the oracle
-computes each operation in fp64 and rounds its stored result to bf16 at the
-same points (gates in fp32), so that it defines the bf16 model itself.
+The model keeps its residual stream and the final norm's output in fp32 and
+stores every other tensor between operations in bf16 (the gates in fp32):
+the oracle computes each operation in fp64 and rounds its stored result to
+the same precision at the same points, so that it defines the model itself.
 
 ``forward(..., gemm_dtype=np.float32)`` runs the projections in fp32 instead:
 the "reference library in lower precision" of Flide's Appendix G forward
@@ -99,7 +100,7 @@ def causal_conv(x, w):
 def forward(cfg: StackConfig, W: Dict[str, np.ndarray], ids, rows=None, gemm_dtype=np.float64):
     """Run the stack over one isolated token sequence (positions 0..n-1).
 
-    Returns the final-norm hidden rows (bf16 values, fp64 dtype) for
+    Returns the final-norm hidden rows (fp32 values, fp64 dtype) for
     ``rows`` (default all).
     """
     def mm(a, w):
@@ -121,7 +122,7 @@ def forward(cfg: StackConfig, W: Dict[str, np.ndarray], ids, rows=None, gemm_dty
             q = round_bf16(rope(q, pos, cfg.rope_theta))
             k = round_bf16(rope(k, pos, cfg.rope_theta))
             o = round_bf16(_attn.causal_attention(q, k, v, 1.0 / np.sqrt(d)))
-            h = round_bf16(h + mm(o.reshape(n, hq * d), W[p + "wo"]))
+            h = round_f32(h + mm(o.reshape(n, hq * d), W[p + "wo"]))
         else:
             H, d = cfg.gdn_h, cfg.gdn_d
             C = 3 * H * d
@@ -136,13 +137,13 @@ def forward(cfg: StackConfig, W: Dict[str, np.ndarray], ids, rows=None, gemm_dty
             be = round_f32(1.0 / (1.0 + np.exp(-pr[:, C + H:C + 2 * H])))
             o, _ = _gdn.gated_delta_rule(q, kk, v, al, be)
             o = round_bf16(o)
-            h = round_bf16(h + mm(o.reshape(n, H * d), W[p + "wo"]))
+            h = round_f32(h + mm(o.reshape(n, H * d), W[p + "wo"]))
         b = round_bf16(rmsnorm(h, cfg.eps))
         gu = round_bf16(mm(b, W[p + "wgu"]))
         F = cfg.ffn
         m = round_bf16(silu(gu[:, :F]) * gu[:, F:])
-        h = round_bf16(h + mm(m, W[p + "wd"]))
-    out = round_bf16(rmsnorm(h, cfg.eps))
+        h = round_f32(h + mm(m, W[p + "wd"]))
+    out = round_f32(rmsnorm(h, cfg.eps))
     return out if rows is None else out[list(rows)]
 
 
