@@ -81,3 +81,43 @@ def from_stream(R: Round, seg_of: Dict[Tuple[int, int], int], arr) -> Dict[Tuple
         info = R.segment(s)
         out[node] = arr[info.stream_off:info.stream_off + info.n_tokens]
     return out
+
+
+def split_at_requests(tree, caps, resume: Optional[Dict[int, tuple]] = None):
+    """Split a batch of requests into rounds that each fit the capacity bucket ``caps``, at request
+    boundaries and in request order (Flide section 3.3.2: rounds are cut between requests, so every
+    request's result is the one it has alone -- section 3.5).  Requests are packed greedily: a run of
+    whole requests goes into one round while the capacities ``hs_round_caps_for`` derives from the
+    run's totals (tokens, nodes, depth, history spans and pages) are within ``caps`` in every field;
+    those capacities suffice for any round of those totals, so every group builds.  ``resume`` as for
+    build_round.  Returns a list of lists of request indices; a request that does not fit alone
+    raises HsError(HS_ECAPACITY)."""
+    resume = resume or {}
+    bucket = caps.as_dict()
+
+    def totals(r):
+        req = tree.requests[r]
+        d = [0] * len(req.parents)
+        for i in range(1, len(req.parents)):
+            d[i] = d[req.parents[i]] + 1
+        spans = resume.get(r, (None, []))[1]
+        return (sum(req.n_tok), len(req.parents), max(d) + 1, len(spans), sum(len(p) for _, p in spans))
+
+    def fits(t):
+        need = round_caps_for(t[0], t[1], t[2], t[3], t[4]).as_dict()
+        return all(need[k] <= bucket[k] for k in need)
+
+    groups, cur, acc = [], [], None
+    for r in range(len(tree.requests)):
+        t = totals(r)
+        if not fits(t):
+            raise _lib.HsError(_lib.HS_ECAPACITY, f"request {r} alone exceeds the bucket's capacities")
+        nxt = t if acc is None else (acc[0] + t[0], acc[1] + t[1], max(acc[2], t[2]), acc[3] + t[3], acc[4] + t[4])
+        if cur and not fits(nxt):
+            groups.append(cur)
+            cur, nxt = [], t
+        cur.append(r)
+        acc = nxt
+    if cur:
+        groups.append(cur)
+    return groups

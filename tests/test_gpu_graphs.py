@@ -118,3 +118,42 @@ def test_graph_replay_matches_eager_across_rounds():
     graph.replay()
     torch.cuda.synchronize()
     assert _same(b.results(*n), eager)
+
+
+def _subset(inp, group, reqs):
+    """The inputs of the requests in ``group``, renumbered 0, 1, ..."""
+    import dataclasses
+    nodes = {(j, i): inp.nodes[(r, i)] for j, r in enumerate(group) for i in range(reqs[r].n_nodes)}
+    hist = {j: inp.hist[r] for j, r in enumerate(group) if r in inp.hist}
+    return dataclasses.replace(inp, nodes=nodes, hist=hist)
+
+
+def test_rounds_split_at_request_boundaries_bitwise():
+    """A batch split into rounds of one capacity bucket at request boundaries gives every request the
+    same output bits as the batch in one round (attention and GDN): rounds cut between requests change
+    nothing a request computes (Flide sections 3.3.2 and 3.5)."""
+    from harness import AttnRun, GdnRun
+    reqs = [synth.fork_tree(n, br) for n, br in [(300, [20, 7]), (90, [40]), (700, [9, 9, 60]), (150, [3]),
+                                                  (1100, [17, 80]), (64, [64])]]
+    tree = synth.Tree(reqs)
+    ainp = synth.attn_inputs(tree, HQ, HKV, D, seed=71, bf16=True)
+    ginp = synth.gdn_inputs(tree, H, D, D, seed=72, bf16=True, law="softplus")
+    a_all = AttnRun(tree, ainp, torch.bfloat16).run()
+    g_all = GdnRun(tree, ginp, torch.bfloat16).run()
+    api.check_status(a_all.status)
+    api.check_status(g_all.status)
+    ra, rg = a_all.raw_outputs(), g_all.raw_outputs()
+    bucket = api.round_caps_for(1300, 8, 2)
+    groups = rounds.split_at_requests(tree, bucket)
+    assert len(groups) >= 3
+    for g in groups:
+        sub = synth.Tree([reqs[r] for r in g])
+        a = AttnRun(sub, _subset(ainp, g, reqs), torch.bfloat16).run()
+        gg = GdnRun(sub, _subset(ginp, g, reqs), torch.bfloat16).run()
+        api.check_status(a.status)
+        api.check_status(gg.status)
+        sa, sg = a.raw_outputs(), gg.raw_outputs()
+        for j, r in enumerate(g):
+            for i in range(reqs[r].n_nodes):
+                assert torch.equal(sa[(j, i)], ra[(r, i)]), ("attention", r, i)
+                assert torch.equal(sg[(j, i)], rg[(r, i)]), ("gdn", r, i)

@@ -544,3 +544,26 @@ def test_tile_readout_flag(ti):
         covered.extend(rows)
         assert int(tl[7]) == int(any(r in ro for r in rows)), tl
     assert sorted(covered) == list(range(B.h("N_TOK")))
+
+
+def test_split_at_requests():
+    """Rounds cut at request boundaries (Flide section 3.3.2): every group is a run of whole requests in
+    order, builds under the bucket's capacities, and the groups cover the batch; a request larger than
+    the bucket is refused."""
+    tree = synth.mixed_tree(seed=4000)                          # 64 requests, trunks 512 .. 16384
+    bucket = api.round_caps_for(40000, 120, 2)
+    groups = rounds.split_at_requests(tree, bucket)
+    assert [r for g in groups for r in g] == list(range(len(tree.requests)))
+    assert len(groups) > 1
+    for g in groups:
+        sub = synth.Tree([tree.requests[r] for r in g])
+        R, _ = rounds.build_round(sub, api.PagePool(sub.useful_tokens() // 16 + 64 * len(g)), caps=bucket)
+        assert R.info().n_tokens == sub.useful_tokens()
+    # greedy: the next request did not fit into the group before it
+    for a, b in zip(groups, groups[1:]):
+        sub = synth.Tree([tree.requests[r] for r in a + b[:1]])
+        need = api.round_caps_for(sub.useful_tokens(), sum(r.n_nodes for r in sub.requests), 2).as_dict()
+        assert any(need[k] > v for k, v in bucket.as_dict().items())
+    with pytest.raises(_lib.HsError) as e:
+        rounds.split_at_requests(tree, api.round_caps_for(1000, 120, 2))
+    assert e.value.code == _lib.HS_ECAPACITY
