@@ -78,6 +78,7 @@ _SIGS = {
     "hs_round_readout_rows": (I32, [P, I32P, I32, I32P]),
     "hs_round_release": (I32, [P, P, I32P, I32]),
     "hs_round_build_chunks": (I32, [CAPSP, P, P, P]),
+    "hs_round_build_tiles": (I32, [CAPSP, P, P, P]),
     "hs_fork_attn_masked": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, C.POINTER(AttnMask), P, P, P, I32, P,
                                   P, P]),
     "hs_fork_attn_prefill": (I32, [CAPSP, P, I32, I32, I32, I32, C.c_float, P, P, P, P, P, I32, P, P, P]),

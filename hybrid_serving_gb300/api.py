@@ -258,6 +258,13 @@ def round_build_chunks(caps: Caps, dev_meta: torch.Tensor, dev_status: torch.Ten
     check(lib.hs_round_build_chunks(C.byref(caps), dev_meta.data_ptr(), dev_status.data_ptr(), _stream(stream)))
 
 
+def round_build_tiles(caps: Caps, dev_meta: torch.Tensor, dev_status: torch.Tensor, stream=None):
+    """Rebuild the attention tile table of the round in dev_meta on the GPU (hs_round_build_tiles)."""
+    dev = _cur_dev()
+    _meta_status(caps, dev_meta, dev_status, dev)
+    check(lib.hs_round_build_tiles(C.byref(caps), dev_meta.data_ptr(), dev_status.data_ptr(), _stream(stream)))
+
+
 def kv_page_write(caps: Caps, dev_meta: torch.Tensor, k_new, v_new, k_pages, v_pages, dev_status: torch.Tensor,
                   stream=None):
     _dt(k_new)

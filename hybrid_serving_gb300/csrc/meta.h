@@ -99,7 +99,9 @@ enum : int {
   S_PAGE_REF_OFF,    // first own page in the page-ref array
   S_N_PAGES,
   S_SCAN1,           // scan-table entry of the node's group 1 (-1 = one group); groups 2.. follow it
+  S_HIST,            // a resumed root's history spans: first span | count << kHistShift (0: none)
 };
+constexpr int kHistShift = 20;  // history spans of one root: first < 2^20, count < 2^11
 
 // Causal-conv predecessors of a token (Flide section 3.2.2: the convolution
 // reads a token's predecessors through an index, so a question's first tokens

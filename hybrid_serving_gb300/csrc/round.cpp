@@ -382,6 +382,12 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
   }
   if (n_hist_spans > C.max_hist_spans)
     return hs::fail(HS_ECAPACITY, "%d history spans > max_hist_spans %d", n_hist_spans, C.max_hist_spans);
+  if (n_hist_spans >= (1 << kHistShift))
+    return hs::fail(HS_ECAPACITY, "%d history spans (at most %d)", n_hist_spans, (1 << kHistShift) - 1);
+  for (const auto& s : S)
+    if (s.hist_ntok.size() >= (size_t)1 << (31 - kHistShift))
+      return hs::fail(HS_ECAPACITY, "a root with %d history spans (at most %d)", (int)s.hist_ntok.size(),
+                      (1 << (31 - kHistShift)) - 1);
   int64_t n_own_pages = 0;
   if (pool)
     for (auto& s : S) n_own_pages += (s.n_tok + kPage - 1) / kPage;
@@ -624,6 +630,7 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     g[S_READOUT_ROW] = s.readout_row;
     g[S_PAGE_REF_OFF] = s.page_ref_off;
     g[S_N_PAGES] = s.n_pages;
+    g[S_HIST] = s.hist_spans.empty() ? 0 : s.hist_spans[0] | ((int32_t)s.hist_spans.size() << kHistShift);
     for (int32_t u = 0; u < s.n_tok; ++u) {
       int32_t* t = h + L.off_tok + (s.stream_off + u) * kTokWords;
       t[T_SEG] = i;

@@ -203,6 +203,21 @@ hs_status hs_round_release(hs_round* r, hs_page_pool* pool, const int32_t* keep_
  * on `stream`; a chunk list beyond caps->max_chunks sets HS_DEV_BAD_META.
  * Supports caps->max_segments <= 4096 (HS_EINVAL above). */
 hs_status hs_round_build_chunks(const hs_round_caps* caps, void* dev_meta, int32_t* dev_status, void* stream);
+/* The attention tile table built on the GPU (Flide section 3.3.1: a tile
+ * table in GPU-resident metadata; section 3.5: tiles start at the node):
+ * from the segment table (stream offsets, lengths, parents, own spans, each
+ * root's history spans, readout rows) and the span lengths already in
+ * dev_meta, rewrites in place the tile records, the tile span lists and the
+ * header's tile and tile-span counts -- word for word what the host round
+ * build writes: in stream order a root or a node of more than 128 tokens
+ * gets one tile per 128 rows, a run of consecutive siblings of at most 128
+ * rows each is packed into tiles of at most 128 rows; a tile's spans are the
+ * root's history, every ancestor's own span (root first) and its nodes' own
+ * spans; tiles ordered by work x (7 with a readout row, else 5), heaviest
+ * first, ties in that order.  One small launch on `stream`; a table beyond
+ * the caps (or inconsistent parents) sets HS_DEV_BAD_META.  Supports
+ * caps->max_segments <= 4096 and caps->max_tiles <= 4096 (HS_EINVAL above). */
+hs_status hs_round_build_tiles(const hs_round_caps* caps, void* dev_meta, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Hot path                                                                  */
