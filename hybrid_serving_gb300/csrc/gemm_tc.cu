@@ -4,17 +4,22 @@
 //
 // Flide, "Accelerating Decision Inference with Exact State Forking",
 // section 3.5: every matrix product sums each output element in a fixed
-// order whatever the number of rows.  Here every output tile is 128 x 128,
+// order whatever the number of rows.  Here every output tile is 128 x 256,
 // there is no split-K, and the K loop runs in the same 64-wide stages and
 // 16-wide MMA steps for any M, so a row's result does not depend on which
 // other rows share the launch.
 //
-// One CTA per output tile.  Warp 0 streams A and B tiles with TMA into a
-// 3-stage ring (128-byte swizzle); warp 1 owns 128 TMEM columns and issues
-// tcgen05.mma (M=128, N=128, K=16) from one thread; warps 2..5 read the
-// accumulator back (thread = row), add the optional residual and store C
-// (bf16 rounded to nearest, or fp32: a residual stream kept in fp32).  Waits
-// are bounded and report HS_DEV_TIMEOUT through the status word.
+// Persistent: one CTA per SM walks the output tiles t = blockIdx.x, + grid,
+// ... in row-block-major order (the CTAs working at one time share their A
+// rows, and B -- the weights -- stays in L2).  Warp 0 streams A and B tiles
+// with TMA into a 4-stage ring (128-byte swizzle; rows of B past N read as
+// zeros); warp 1 owns all 512 TMEM columns as two 256-column accumulators and
+// issues tcgen05.mma (M=128, N=256, K=16) from one elected lane of the
+// converged warp; warps 2..5 read an accumulator back (thread = row), add the
+// optional residual and store C (bf16 rounded to nearest, or fp32: a residual
+// stream kept in fp32), while the MMAs of the next tile fill the other
+// accumulator.  Waits are bounded and report HS_DEV_TIMEOUT through the
+// status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -24,11 +29,11 @@
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kStages = 3;
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
 constexpr int kStageA = BM * BK * 2;  // 16 KB
-constexpr int kStageB = BN * BK * 2;  // 16 KB
-constexpr int kSmem = kStages * (kStageA + kStageB);
+constexpr int kStageB = BN * BK * 2;  // 32 KB
+constexpr int kSmem = kStages * (kStageA + kStageB);  // 192 KB
 constexpr int kThreads = 192;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr uint32_t kIdesc = tc::idesc_bf16(BM, BN, 0, 0);
@@ -72,25 +77,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const GemmParams<CT> p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc;
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc[2], bar_free[2], bar_done;
   __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
   // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
   // a shared-memory access (an integer round trip would turn them into generic loads and stores)
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
   const int nk = p.K / BK;
+  const int n_tn = (p.N + BN - 1) / BN, n_tiles = ((p.M + BM - 1) / BM) * n_tn;
+  // this CTA's tiles: blockIdx.x, + gridDim.x, ... (row block t / n_tn, column block t % n_tn)
+  const int n_mine = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
   if (threadIdx.x == 0) {
+    abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&bar_full[s], 1);
       tc::mbar_init(&bar_empty[s], 1);
     }
-    tc::mbar_init(&bar_acc, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bar_acc[b], 1);     // accumulator b complete (MMA commit)
+      tc::mbar_init(&bar_free[b], 128);  // accumulator b read out (every epilogue thread)
+    }
+    tc::mbar_init(&bar_done, 1);
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&tmem_slot, 128);
+    tc::tmem_alloc(&tmem_slot, 512);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -102,31 +115,50 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     if (lane == 0) {
       tc::prefetch_tmap(&tm_a);
       tc::prefetch_tmap(&tm_b);
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !tc::mbar_wait(&bar_empty[s], ((kb / kStages) - 1) & 1, kWaitCycles)) {
-          hsd::set_status(p.status, HS_DEV_TIMEOUT);
-          break;
+      int issued = 0;  // stages over all tiles
+      bool ok = true;
+      for (int j = 0; j < n_mine && ok; ++j) {
+        const int t = (int)blockIdx.x + j * (int)gridDim.x;
+        const int m0 = (t / n_tn) * BM, n0 = (t % n_tn) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++issued) {
+          const int s = issued % kStages;
+          if (issued >= kStages && !tc::mbar_wait(&bar_empty[s], ((issued / kStages) - 1) & 1, kWaitCycles)) {
+            hsd::set_status(p.status, HS_DEV_TIMEOUT);
+            atomicExch(&abort_flag, 1);
+            ok = false;
+            break;
+          }
+          if (*(volatile int*)&abort_flag) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * (kStageA + kStageB);
+          uint8_t* sb = sa + kStageA;
+          tc::mbar_expect_tx(&bar_full[s], kStageA + kStageB);
+          tc::tma_load_2d(sa, &tm_a, kb * BK, m0, &bar_full[s]);
+          tc::tma_load_2d(sb, &tm_b, kb * BK, n0, &bar_full[s]);
         }
-        uint8_t* sa = smem + s * (kStageA + kStageB);
-        uint8_t* sb = sa + kStageA;
-        tc::mbar_expect_tx(&bar_full[s], kStageA + kStageB);
-        tc::tma_load_2d(sa, &tm_a, kb * BK, m0, &bar_full[s]);
-        tc::tma_load_2d(sb, &tm_b, kb * BK, n0, &bar_full[s]);
-        ++issued;
       }
       // drain: the last copies have landed before the CTA leaves
-      for (int kb = issued > kStages ? issued - kStages : 0; kb < issued; ++kb)
-        tc::mbar_wait(&bar_full[kb % kStages], (kb / kStages) & 1, kWaitCycles);
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        tc::mbar_wait(&bar_full[i % kStages], (i / kStages) & 1, kWaitCycles);
     }
   } else if (warp == 1) {
     // converged warp: voted waits, one elected lane issues; a K step adds a constant to the descriptors
-    {
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (kb / kStages) & 1, kWaitCycles))) {
+    bool ok = true;
+    int used = 0;  // stages consumed over all tiles
+    for (int j = 0; j < n_mine && ok; ++j) {
+      const int b = j & 1;
+      // accumulator b is free once the epilogue has read tile j - 2 out of it
+      if (j >= 2 && !__all_sync(~0u, tc::mbar_wait(&bar_free[b], ((j - 2) >> 1) & 1, kWaitCycles))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t acc = tmem + 256 * b;
+      for (int kb = 0; kb < nk; ++kb, ++used) {
+        const int s = used % kStages;
+        if (!__all_sync(~0u, tc::mbar_wait(&bar_full[s], (used / kStages) & 1, kWaitCycles))) {
           ok = false;
           break;
         }
@@ -136,27 +168,49 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint64_t off = (uint64_t)((k * 32) >> 4);
-          tc::mma_bf16_ss_w(tmem, da + off, db + off, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+          tc::mma_bf16_ss_w(acc, da + off, db + off, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
         }
         tc::mma_commit_w(&bar_empty[s]);
+        if (*(volatile int*)&abort_flag) {
+          ok = false;
+          break;
+        }
       }
-      if (!ok && lane == 0) hsd::set_status(p.status, HS_DEV_TIMEOUT);
-      tc::mma_commit_w(&bar_acc);  // also drains every MMA before TMEM is freed
+      if (!ok) break;
+      tc::mma_commit_w(&bar_acc[b]);
     }
-    __syncwarp();
+    if (!ok && lane == 0) {
+      hsd::set_status(p.status, HS_DEV_TIMEOUT);
+      atomicExch(&abort_flag, 1);
+    }
+    // every MMA issued has completed before the CTA leaves and TMEM is freed
+    tc::mma_commit_w(&bar_done);
+    __all_sync(~0u, tc::mbar_wait(&bar_done, 0, kWaitCycles));
   } else {
     const int quarter = warp % 4;  // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
-    const int row = m0 + r;
-    if (__all_sync(~0u, tc::mbar_wait(&bar_acc, 0, kWaitCycles))) {  // warp-wide: tcgen05.ld is collective
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int j = 0; j < n_mine && ok; ++j) {
+      const int b = j & 1;
+      const int t = (int)blockIdx.x + j * (int)gridDim.x;
+      const int row = (t / n_tn) * BM + r, n0 = (t % n_tn) * BN;
+      if (!__all_sync(~0u, tc::mbar_wait(&bar_acc[b], (j >> 1) & 1, kWaitCycles))) {  // warp-wide: ld is collective
+        ok = false;
+        break;
+      }
       tc::fence_after_sync();
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
+        tc::tmem_ld32(tmem + lanes + 256 * b + c * 32, v);
         tc::tmem_wait_ld();
-        if (row < p.M) {
-          const int col0 = n0 + c * 32;
+        if (c == BN / 32 - 1) {  // the accumulator is read out: the MMAs of tile j + 2 may start
+          tc::fence_before_sync();
+          tc::mbar_arrive(&bar_free[b]);
+        }
+        const int col0 = n0 + c * 32;
+        if (row < p.M && col0 < p.N) {
           CT* dst = p.C + (size_t)row * p.ldc + col0;
           const CT* res = p.R ? p.R + (size_t)row * p.ldr + col0 : nullptr;
 #pragma unroll
@@ -168,14 +222,16 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
           }
         }
       }
-    } else {
+    }
+    if (!ok) {
       hsd::set_status(p.status, HS_DEV_TIMEOUT);
+      atomicExch(&abort_flag, 1);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 1) tc::tmem_dealloc(tmem, 128);
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -211,8 +267,8 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   HS_CHECK_ARG(A && B && C, "null argument");
   if (c_dtype != HS_BF16 && c_dtype != HS_F32) return hs::fail(HS_EUNSUPPORTED, "gemm: C dtype %d", c_dtype);
   HS_CHECK_ARG(M >= 0 && N > 0 && K > 0, "bad shape %d x %d x %d", M, N, K);
-  if (N % BN != 0 || K % BK != 0)
-    return hs::fail(HS_EUNSUPPORTED, "N (%d) must be a multiple of %d and K (%d) of %d", N, BN, K, BK);
+  if (N % 128 != 0 || K % BK != 0)
+    return hs::fail(HS_EUNSUPPORTED, "N (%d) must be a multiple of 128 and K (%d) of %d", N, K, BK);
   HS_CHECK_ARG(lda >= K && ldb >= K && ldc >= N && (!R || ldr >= N), "leading dimensions too small");
   HS_CHECK_ARG(lda % 8 == 0 && ldb % 8 == 0 && ldc % 8 == 0 && (!R || ldr % 8 == 0),
                "leading dimensions must be multiples of 8 elements");
@@ -235,7 +291,15 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
       return hs::fail(HS_ECUDA, "gemm: cannot raise the shared-memory limit");
     configured[slot].store(true);
   }
-  dim3 grid(N / BN, (M + BM - 1) / BM);
+  static std::atomic<int> sm_count[hsd::kMaxDevices];  // per device, 0 until read
+  int n_sm = sm_count[slot].load();
+  if (n_sm <= 0) {
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, slot) != cudaSuccess || n_sm <= 0)
+      return hs::fail(HS_ECUDA, "gemm: cannot read the SM count");
+    sm_count[slot].store(n_sm);
+  }
+  const long long n_tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const dim3 grid((unsigned)(n_tiles < n_sm ? n_tiles : n_sm));  // persistent: one CTA per SM
   if (c_dtype == HS_F32) {
     GemmParams<float> prm{M, N, K, (float*)C, ldc, (const float*)R, ldr, dev_status};
     gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
