@@ -15,11 +15,14 @@
 // with TMA into a 4-stage ring (128-byte swizzle; rows of B past N read as
 // zeros); warp 1 owns all 512 TMEM columns as two 256-column accumulators and
 // issues tcgen05.mma (M=128, N=256, K=16) from one elected lane of the
-// converged warp; warps 2..5 read an accumulator back (thread = row), add the
-// optional residual and store C (bf16 rounded to nearest, or fp32: a residual
-// stream kept in fp32), while the MMAs of the next tile fill the other
-// accumulator.  Waits are bounded and report HS_DEV_TIMEOUT through the
-// status word.
+// converged warp; warps 2..5 read an accumulator back (thread = row) 64 bytes
+// of each row at a time, add the optional residual (TMA-loaded two pieces
+// ahead into a shared staging buffer), write the piece into a second staging
+// buffer and store it with one TMA store per 128 rows x 64 bytes (C in bf16
+// rounded to nearest, or fp32: a residual stream kept in fp32), while the
+// MMAs of the next tile fill the other accumulator.  Waits are bounded and
+// report HS_DEV_TIMEOUT through the status word; the epilogue warps take
+// every decision together, so a timeout never leaves one at a barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -33,7 +36,9 @@ constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kStages = 4;
 constexpr int kStageA = BM * BK * 2;  // 16 KB
 constexpr int kStageB = BN * BK * 2;  // 32 KB
-constexpr int kSmem = kStages * (kStageA + kStageB);  // 192 KB
+constexpr int kRing = kStages * (kStageA + kStageB);  // 192 KB
+constexpr int kStg = BM * 64;                          // a staging buffer: 128 rows x 64 bytes
+constexpr int kSmem = kRing + 4 * kStg;                // + C and R pieces, two each: 224 KB
 constexpr int kThreads = 192;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr uint32_t kIdesc = tc::idesc_bf16(BM, BN, 0, 0);
@@ -72,14 +77,61 @@ __device__ __forceinline__ void epi8(float (&f)[8], const float* res, float* dst
   reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// 64 bytes of a row: 16 fp32 or 32 bf16 values
+template <typename CT>
+struct Piece;
+template <>
+struct Piece<float> {
+  static constexpr int kCols = 16;
+  static __device__ __forceinline__ void load(uint32_t taddr, uint32_t (&v)[32]) {
+    tc::tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
+  }
+  // v + residual (from shared memory) into 64 bytes of shared memory
+  static __device__ __forceinline__ void put(const uint32_t (&v)[32], const uint8_t* res, uint8_t* dst) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 o = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                             __uint_as_float(v[4 * q + 3]));
+      if (res) {
+        const float4 r = tc::lds_f4(tc::smem_u32(res) + 16 * q);
+        o.x += r.x; o.y += r.y; o.z += r.z; o.w += r.w;
+      }
+      tc::sts_f4(tc::smem_u32(dst) + 16 * q, o);
+    }
+  }
+};
+template <>
+struct Piece<__nv_bfloat16> {
+  static constexpr int kCols = 32;
+  static __device__ __forceinline__ void load(uint32_t taddr, uint32_t (&v)[32]) { tc::tmem_ld32(taddr, v); }
+  static __device__ __forceinline__ void put(const uint32_t (&v)[32], const uint8_t* res, uint8_t* dst) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[8 * q + i]);
+      if (res) {
+        float rr[8];
+        const uint4 rw = tc::lds_u4(tc::smem_u32(res) + 16 * q);
+        hsd::cvt16(*reinterpret_cast<const float4*>(&rw), rr, __nv_bfloat16());
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] += rr[i];
+      }
+      tc::sts_u4(tc::smem_u32(dst) + 16 * q, make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
+                                                        tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7])));
+    }
+  }
+};
+
 template <typename CT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_r,
                     const GemmParams<CT> p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc[2], bar_free[2], bar_done;
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc[2], bar_free[2], bar_done, bar_r[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
+  __shared__ int abort_flag, epi_go;
   // aligned up to 1024 bytes by pointer arithmetic on the shared array, so every access through smem stays
   // a shared-memory access (an integer round trip would turn them into generic loads and stores)
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -100,6 +152,8 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       tc::mbar_init(&bar_free[b], 128);  // accumulator b read out (every epilogue thread)
     }
     tc::mbar_init(&bar_done, 1);
+    tc::mbar_init(&bar_r[0], 1);  // residual pieces landed
+    tc::mbar_init(&bar_r[1], 1);
     tc::fence_mbar_init();
   }
   if (warp == 1) {
@@ -187,45 +241,79 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     tc::mma_commit_w(&bar_done);
     __all_sync(~0u, tc::mbar_wait(&bar_done, 0, kWaitCycles));
   } else {
-    const int quarter = warp % 4;  // TMEM lanes this warp may read
+    // ------------------------------------------------------------ epilogue (warps 2..5, barrier 1)
+    using PC = Piece<CT>;
+    constexpr int kPieces = BN / PC::kCols;  // per tile (even)
+    const int quarter = warp % 4;            // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
+    const bool issuer = r == 0;
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-    bool ok = true;
-    for (int j = 0; j < n_mine && ok; ++j) {
+    uint8_t* cst = smem + kRing;            // C pieces: cst + b * kStg
+    uint8_t* rst = smem + kRing + 2 * kStg;  // R pieces
+    const bool has_r = p.R != nullptr;
+    // the residual piece g (over all tiles) of this CTA: TMA into rst[g & 1]
+    auto load_r = [&](int g) {
+      const int j = g / kPieces, c = g % kPieces;
+      if (!has_r || j >= n_mine) return;
+      const int t = (int)blockIdx.x + j * (int)gridDim.x;
+      tc::mbar_expect_tx(&bar_r[g & 1], kStg);
+      tc::tma_load_2d(rst + (g & 1) * kStg, &tm_r, (t % n_tn) * BN + c * PC::kCols, (t / n_tn) * BM, &bar_r[g & 1]);
+    };
+    if (issuer) {
+      tc::prefetch_tmap(&tm_c);
+      if (has_r) tc::prefetch_tmap(&tm_r);
+      load_r(0);
+      load_r(1);
+    }
+    int stored = 0;  // pieces over all tiles
+    for (int j = 0; j < n_mine; ++j) {
+      // one decision for the four warps: go on unless a role gave up
+      if (issuer) epi_go = !*(volatile int*)&abort_flag;
+      tc::named_sync(1, 128);
+      if (!epi_go) break;
       const int b = j & 1;
       const int t = (int)blockIdx.x + j * (int)gridDim.x;
-      const int row = (t / n_tn) * BM + r, n0 = (t % n_tn) * BN;
+      const int m0 = (t / n_tn) * BM, n0 = (t % n_tn) * BN;
       if (!__all_sync(~0u, tc::mbar_wait(&bar_acc[b], (j >> 1) & 1, kWaitCycles))) {  // warp-wide: ld is collective
-        ok = false;
-        break;
+        hsd::set_status(p.status, HS_DEV_TIMEOUT);
+        atomicExch(&abort_flag, 1);  // (this tile goes on with whatever it holds; the next one stops)
       }
       tc::fence_after_sync();
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < kPieces; ++c, ++stored) {
+        const int pb = stored & 1;
         uint32_t v[32];
-        tc::tmem_ld32(tmem + lanes + 256 * b + c * 32, v);
+        PC::load(tmem + lanes + 256 * b + c * PC::kCols, v);
         tc::tmem_wait_ld();
-        if (c == BN / 32 - 1) {  // the accumulator is read out: the MMAs of tile j + 2 may start
+        if (c == kPieces - 1) {  // the accumulator is read out: the MMAs of tile j + 2 may start
           tc::fence_before_sync();
           tc::mbar_arrive(&bar_free[b]);
         }
-        const int col0 = n0 + c * 32;
-        if (row < p.M && col0 < p.N) {
-          CT* dst = p.C + (size_t)row * p.ldc + col0;
-          const CT* res = p.R ? p.R + (size_t)row * p.ldr + col0 : nullptr;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[q * 8 + i]);
-            epi8(f, res ? res + q * 8 : nullptr, dst + q * 8);
+        if (has_r && !__all_sync(~0u, tc::mbar_wait(&bar_r[pb], (stored >> 1) & 1, kWaitCycles))) {
+          hsd::set_status(p.status, HS_DEV_TIMEOUT);
+          atomicExch(&abort_flag, 1);
+        }
+        if (issuer && stored >= 2) tc::bulk_wait_read_but1();  // the store of piece stored - 2 has read cst[pb]
+        tc::named_sync(1, 128);
+        PC::put(v, has_r ? rst + pb * kStg + r * 64 : nullptr, cst + pb * kStg + r * 64);
+        tc::fence_proxy_async_smem();
+        tc::named_sync(1, 128);
+        if (issuer) {
+          if (n0 + c * PC::kCols < p.N) {  // (a piece wholly past N is not stored)
+            tc::tma_store_2d(&tm_c, n0 + c * PC::kCols, m0, cst + pb * kStg);
+            tc::bulk_commit();
           }
+          load_r(stored + 2);  // rst[pb] is read by every row (barrier above)
         }
       }
     }
-    if (!ok) {
-      hsd::set_status(p.status, HS_DEV_TIMEOUT);
-      atomicExch(&abort_flag, 1);
+    if (issuer) {
+      tc::bulk_wait_all();  // the stores have completed
+      // residual pieces loaded ahead but not used (the loop stopped early) land before the CTA leaves
+      if (has_r) {
+        const int n_loaded = min(stored + 2, n_mine * kPieces);
+        for (int g = stored; g < n_loaded; ++g) tc::mbar_wait(&bar_r[g & 1], (g >> 1) & 1, kWaitCycles);
+      }
     }
   }
   tc::fence_before_sync();
@@ -258,6 +346,19 @@ bool map_2d(CUtensorMap* m, const void* base, long long rows, long long cols, lo
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// C or R [rows, cols] (leading dimension ld) in pieces of 128 rows x 64 bytes, unswizzled
+bool map_piece(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, bool f32) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int es_b = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * es_b};
+  cuuint32_t box[2] = {(cuuint32_t)(64 / es_b), (cuuint32_t)BM};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -278,7 +379,10 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return hs::fail(HS_ECUDA, "no CUDA device");
   CUtensorMap ma, mb;
-  if (!map_2d(&ma, A, M, K, lda, BM) || !map_2d(&mb, B, N, K, ldb, BN))
+  CUtensorMap mc, mr;
+  const bool f32 = c_dtype == HS_F32;
+  if (!map_2d(&ma, A, M, K, lda, BM) || !map_2d(&mb, B, N, K, ldb, BN) || !map_piece(&mc, C, M, N, ldc, f32) ||
+      !map_piece(&mr, R ? R : C, M, N, R ? ldr : ldc, f32))
     return hs::fail(HS_ECUDA, "gemm: tensor map encoding failed");
   static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
   const int slot = hsd::device_slot();
@@ -302,10 +406,10 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   const dim3 grid((unsigned)(n_tiles < n_sm ? n_tiles : n_sm));  // persistent: one CTA per SM
   if (c_dtype == HS_F32) {
     GemmParams<float> prm{M, N, K, (float*)C, ldc, (const float*)R, ldr, dev_status};
-    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
+    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, mc, mr, prm);
   } else {
     GemmParams<__nv_bfloat16> prm{M, N, K, (__nv_bfloat16*)C, ldc, (const __nv_bfloat16*)R, ldr, dev_status};
-    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, prm);
+    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, mc, mr, prm);
   }
   HS_LAUNCH_CHECK("gemm_bf16");
   return HS_OK;
