@@ -750,6 +750,28 @@ def run_reference(args):
     return 0
 
 
+def profile_gemm():
+    import torch
+    from hybrid_serving_gb300 import api
+    from hybrid_serving_gb300.stack import gemm
+    M = 65536
+    g = torch.Generator(device="cuda").manual_seed(7)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    A = torch.randn(M, 4096, device="cuda", generator=g).to(torch.bfloat16)
+    Wgu = (torch.randn(8192, 2048, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    Wd = (torch.randn(2048, 4096, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    gu = torch.empty(M, 8192, device="cuda", dtype=torch.bfloat16)
+    h = torch.zeros(M, 2048, device="cuda", dtype=torch.float32)
+    for _ in range(3):
+        gemm(A[:, :2048], Wgu, gu, M, status=st)
+    for _ in range(3):
+        gemm(A, Wd, h, M, R=h, status=st)
+    torch.cuda.synchronize()
+    api.check_status(st)
+    print(f"profile gemm: device memory held {torch.cuda.max_memory_allocated() / 2**20:.0f} MiB", flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -758,12 +780,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the resume / stack / agent-tree lines")
+    ap.add_argument("--profile-gemm", action="store_true",
+                    help="three launches of the hybrid stack's gate/up projection (M=65536, N=8192, K=2048, bf16 "
+                         "out) and three of its down projection with the fp32 residual (N=2048, K=4096): the "
+                         "case that ncu captures of the GEMM run (about 2 GB on the device)")
     ap.add_argument("--profile-case", action="store_true",
                     help="one input set, the warm-up steps only, no timing and no JSON line: the case that ncu "
                          "captures of single kernels run (a few hundred MB on the device)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_gemm:
+        return profile_gemm()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     ws, rank, local = dist_env()
