@@ -571,8 +571,11 @@ def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int =
         n_pages = layout.live_pages(tree, 16) + 64
         n_seg = sum(r.n_nodes for r in tree.requests)
         stk = HybridStack(StackShape(**STACK), W, max_pos=20000)
-        stk.alloc(Tcap=T, n_pages=n_pages, n_slots=n_seg + 40)
-        R, seg_of = rounds.build_round(tree, api.PagePool(n_pages), temp_slot0=32, n_temp_slots=n_seg + 8)
+        stk.alloc(Tcap=T, n_pages=n_pages + 10 * 32 + 16, n_slots=n_seg + 40,
+                  n_windows=3 * len(tree.requests) if name == "agent_tree" else 0)
+        pool = api.PagePool(n_pages + 10 * 32 + 16)
+        RA_POOL[0] = pool
+        R, seg_of = rounds.build_round(tree, pool, temp_slot0=32, n_temp_slots=n_seg + 8)
         meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
         R.upload(meta)
         idd = torch.from_numpy(rounds.to_stream(R, seg_of, ids)).cuda()
@@ -587,12 +590,60 @@ def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int =
                      "peak_kind": "measured bf16 dense sustained (a forward of tens to hundreds of ms)",
                      "selective_readout": {"ms": round(ms_sel, 3), "tokens_per_s": round(T / (ms_sel / 1e3), 1),
                                            "what": "last layer's MLP, final norm and head at the readout rows only"}}
+        if name == "agent_tree":
+            out["agent_tree_resume"] = _agent_resume(torch, api, rounds, stk, tree, ids, n_pages, R, seg_of, reps)
         del stk
         torch.cuda.empty_cache()
     out["hybrid_stack"]["workload"] = ("64 requests, trunks log-uniform [512,16384], 2-12 branches U[8,128]; "
                                        "8 layers GGGA x2, hidden 2048")
     out["agent_tree"]["workload"] = "10 sessions, trunk 256, depth 3 x fan-out 4, residual 32; 8 layers, hidden 2048"
     return out
+
+
+def _agent_resume(torch, api, rounds, stk, tree, ids, n_pages, RA, segA, reps, extra: int = 512):
+    """The agent tree's commit and resume: round A (just timed) saved each session's spine-leaf GDN state
+    (slot = session) and its last 3 conv rows; committing keeps the spine's pages; round B resumes every
+    spine with ``extra`` new tokens (the cached pages as its history, the saved state and window).  Times
+    round B's forward."""
+    n_ses = len(tree.requests)
+    src, dst, keep, spans = [], [], [], {}
+    for s, req in enumerate(tree.requests):
+        info = RA.segment(segA[(s, synth.spine_leaf(req))])
+        src += [info.stream_off + info.n_tokens - 3 + j for j in range(3)]
+        dst += [3 * s + j for j in range(3)]
+    # round A again with the windows saved (the timed runs did not save them)
+    R = RA
+    meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+    R.upload(meta)
+    idd = torch.from_numpy(rounds.to_stream(R, segA, ids)).cuda()
+    sw = [(torch.tensor(src, dtype=torch.int32, device="cuda"), torch.tensor(dst, dtype=torch.int32, device="cuda"),
+           len(src))]
+    stk.forward(R, meta, idd, R.info().n_readouts, save_windows=sw)
+    torch.cuda.synchronize()
+    for s, req in enumerate(tree.requests):
+        path = synth.spine_path(req)
+        keep += [segA[(s, n)] for n in path]
+        spans[s] = [(req.n_tok[n], RA.segment_pages(segA[(s, n)])) for n in path]
+    RA.release(RA_POOL[0], keep=keep)
+    spine = [sum(req.n_tok[n] for n in synth.spine_path(req)) for req in tree.requests]
+    treeB = synth.Tree([synth.Request(parents=[-1], n_tok=[extra], hist_len=spine[s]) for s in range(n_ses)])
+    rng = np.random.default_rng(5099)
+    idsB = {(s, 0): rng.integers(0, STACK["vocab"], size=extra).astype(np.int32) for s in range(n_ses)}
+    resume = {s: (s, spans[s], 3 * s) for s in range(n_ses)}
+    RB, segB = rounds.build_round(treeB, RA_POOL[0], temp_slot0=32, n_temp_slots=8, resume=resume)
+    metaB = torch.empty(RB.meta_bytes() // 4, dtype=torch.int32, device="cuda")
+    RB.upload(metaB)
+    iddB = torch.zeros(stk.Tcap, dtype=torch.int32, device="cuda")
+    iddB[:RB.info().n_tokens] = torch.from_numpy(rounds.to_stream(RB, segB, idsB)).cuda()
+    ms = _timed(torch, lambda: stk.forward(RB, metaB, iddB, RB.info().n_readouts), reps)
+    api.check_status(stk.status)
+    T = treeB.useful_tokens()
+    return {"workload": f"every committed agent spine resumed with {extra} new tokens ({n_ses} sessions; cached "
+                        "K/V pages, saved GDN states and conv windows)", "tokens": T, "ms": round(ms, 3),
+            "tokens_per_s": round(T / (ms / 1e3), 1)}
+
+
+RA_POOL = [None]  # the agent tree round's page pool (its spine pages outlive the round)
 
 
 def dist_env():
