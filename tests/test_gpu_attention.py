@@ -177,3 +177,28 @@ def test_window_batch_invariance_bitwise():
         alone = AttnRun(alone_tree, alone_inp, torch.bfloat16).run_masked(window=200).raw_outputs()
         assert torch.equal(alone[(0, 1)], mixed[(1, b)]), f"branch {b} differs"
         assert torch.equal(alone[(0, 0)], mixed[(1, 0)])
+
+
+@pytest.mark.parametrize("W, bidir", [(50, False), (0, True), (30, True), (260, False)])
+def test_masks_with_resumed_history(W, bidir):
+    """Mask variants on a resumed root: round B resumes a 200-token trunk from its cached pages with 37 new
+    trunk tokens and two branches, under a sliding window (positions continue through the history, so a
+    row's window reaches back into the cached pages) and/or a bidirectional root (the root's rows see the
+    whole root and its history); every row against the oracle's masked isolated pass from position 0."""
+    full = synth.Tree([synth.fork_tree(237, [11, 30])])
+    inp = synth.attn_inputs(full, 8, 2, 128, seed=1310, bf16=True)
+    a_tree = synth.Tree([synth.fork_tree(200, [4])])
+    a_inp = synth.remap_inputs(full, inp, synth.Tree([synth.fork_tree(200, [11, 30])]))
+    a_inp.nodes = {(0, 0): a_inp.nodes[(0, 0)], (0, 1): {k: v[:4] for k, v in a_inp.nodes[(0, 1)].items()}}
+    A = AttnRun(a_tree, a_inp, torch.bfloat16, n_pages=64).run()
+    pages = A.R.segment_pages(A.seg_of[(0, 0)])
+    A.R.release(A.pool, keep=[A.seg_of[(0, 0)]])
+    b_tree = synth.Tree([synth.fork_tree(37, [11, 30], hist_len=200)])
+    b_inp = synth.remap_inputs(full, inp, b_tree)
+    B = AttnRun(b_tree, b_inp, torch.bfloat16, pool=A.pool, k_pages=A.k_pages, v_pages=A.v_pages,
+                resume={0: (None, [(200, pages)])}).run_masked(window=W, bidirectional_root=bidir)
+    api.check_status(B.status)
+    ref = forward.attention_tree(b_tree, b_inp, 1 / math.sqrt(128), window=W or None, bidir_root=bidir, matrix=True)
+    err = max_abs(B.outputs(), ref)
+    print(f"[margin] attention mask W={W} bidir={bidir} resumed history: max-abs {err:.3e} (bar 2e-02)")
+    assert err <= TOL_BF16
