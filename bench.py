@@ -573,8 +573,7 @@ def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int =
         stk = HybridStack(StackShape(**STACK), W, max_pos=20000)
         stk.alloc(Tcap=T, n_pages=n_pages + 10 * 32 + 16, n_slots=n_seg + 40,
                   n_windows=3 * len(tree.requests) if name == "agent_tree" else 0)
-        pool = api.PagePool(n_pages + 10 * 32 + 16)
-        RA_POOL[0] = pool
+        pool = api.PagePool(n_pages + 10 * 32 + 16)  # (+ the resumed spines' pages)
         R, seg_of = rounds.build_round(tree, pool, temp_slot0=32, n_temp_slots=n_seg + 8)
         meta = torch.empty(R.meta_bytes() // 4, dtype=torch.int32, device="cuda")
         R.upload(meta)
@@ -591,7 +590,7 @@ def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int =
                      "selective_readout": {"ms": round(ms_sel, 3), "tokens_per_s": round(T / (ms_sel / 1e3), 1),
                                            "what": "last layer's MLP, final norm and head at the readout rows only"}}
         if name == "agent_tree":
-            out["agent_tree_resume"] = _agent_resume(torch, api, rounds, stk, tree, ids, n_pages, R, seg_of, reps)
+            out["agent_tree_resume"] = _agent_resume(torch, rounds, stk, tree, ids, pool, R, seg_of, reps)
         del stk
         torch.cuda.empty_cache()
     out["hybrid_stack"]["workload"] = ("64 requests, trunks log-uniform [512,16384], 2-12 branches U[8,128]; "
@@ -600,7 +599,7 @@ def stack_configs(torch, api, rounds, pk, reps_mixed: int = 2, reps_agent: int =
     return out
 
 
-def _agent_resume(torch, api, rounds, stk, tree, ids, n_pages, RA, segA, reps, extra: int = 512):
+def _agent_resume(torch, rounds, stk, tree, ids, pool, RA, segA, reps, extra: int = 512):
     """The agent tree's commit and resume: round A (just timed) saved each session's spine-leaf GDN state
     (slot = session) and its last 3 conv rows; committing keeps the spine's pages; round B resumes every
     spine with ``extra`` new tokens (the cached pages as its history, the saved state and window).  Times
@@ -624,26 +623,24 @@ def _agent_resume(torch, api, rounds, stk, tree, ids, n_pages, RA, segA, reps, e
         path = synth.spine_path(req)
         keep += [segA[(s, n)] for n in path]
         spans[s] = [(req.n_tok[n], RA.segment_pages(segA[(s, n)])) for n in path]
-    RA.release(RA_POOL[0], keep=keep)
+    RA.release(pool, keep=keep)
     spine = [sum(req.n_tok[n] for n in synth.spine_path(req)) for req in tree.requests]
     treeB = synth.Tree([synth.Request(parents=[-1], n_tok=[extra], hist_len=spine[s]) for s in range(n_ses)])
     rng = np.random.default_rng(5099)
     idsB = {(s, 0): rng.integers(0, STACK["vocab"], size=extra).astype(np.int32) for s in range(n_ses)}
     resume = {s: (s, spans[s], 3 * s) for s in range(n_ses)}
-    RB, segB = rounds.build_round(treeB, RA_POOL[0], temp_slot0=32, n_temp_slots=8, resume=resume)
+    RB, segB = rounds.build_round(treeB, pool, temp_slot0=32, n_temp_slots=8, resume=resume)
     metaB = torch.empty(RB.meta_bytes() // 4, dtype=torch.int32, device="cuda")
     RB.upload(metaB)
     iddB = torch.zeros(stk.Tcap, dtype=torch.int32, device="cuda")
     iddB[:RB.info().n_tokens] = torch.from_numpy(rounds.to_stream(RB, segB, idsB)).cuda()
     ms = _timed(torch, lambda: stk.forward(RB, metaB, iddB, RB.info().n_readouts), reps)
+    from hybrid_serving_gb300 import api
     api.check_status(stk.status)
     T = treeB.useful_tokens()
     return {"workload": f"every committed agent spine resumed with {extra} new tokens ({n_ses} sessions; cached "
                         "K/V pages, saved GDN states and conv windows)", "tokens": T, "ms": round(ms, 3),
             "tokens_per_s": round(T / (ms / 1e3), 1)}
-
-
-RA_POOL = [None]  # the agent tree round's page pool (its spine pages outlive the round)
 
 
 def dist_env():
