@@ -45,8 +45,8 @@ METRIC = "tree-prefill tokens/s on 1 GB300 (ForkAttn + GDN); % of tensor/HBM roo
 # (chunk-local pass, two state passes per tree level).
 NCU_TRAFFIC = {
     "fork_attn": ({"hybrid_serving_gb300/csrc/fork_attn_tc.cu": "fdc41de45030cdd0"}, 56.45e6),
-    "gdn_fork": ({"hybrid_serving_gb300/csrc/gdn_prep_tc.cu": "4490dfd481c219c1",
-                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "6b88e2b513537d34"}, 512.67e6),
+    "gdn_fork": ({"hybrid_serving_gb300/csrc/gdn_prep_tc.cu": "81dca39759adefd7",
+                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "6b88e2b513537d34"}, 509.09e6),
 }
 
 

@@ -14,8 +14,13 @@
 // (C = last token).  The results go to the compact workspace that the
 // tensor-core state pass reads (layout in gdn_ws.h).
 //
-// One CTA = one chunk x one head; two CTAs share an SM (96 KB of shared
-// memory and 256 tensor-memory columns each).
+// Persistent: two CTAs share an SM (96 KB of shared memory and 256
+// tensor-memory columns each), and each walks the (chunk, head) items
+// blockIdx.x, + gridDim.x, ... -- the barriers' phases follow the items it
+// has taken and the tensor memory is allocated once.  The next item's K, Q
+// and V are loaded as soon as the last MMA that reads this item's tiles has
+// completed (its K' stores have read the Q rows before the T operands are
+// released), so the load runs under this item's images.
 //   warp 8      TMA of K, Q, V, tensor-memory allocation, and the MMAs from
 //               the converged warp: [K; Q] K^T as one M = 128 product (rows
 //               0..63 give K K^T, rows 64..127 Q K^T), then
@@ -99,7 +104,7 @@ __device__ __forceinline__ float dot4(const float4& a, const float4& b, float ac
 }
 
 // No minimum-blocks hint: two CTAs per SM are set by the shared memory and the tensor-memory columns.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const Prm p) {
   extern __shared__ uint8_t smem_raw[];
@@ -111,10 +116,6 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
 
   Meta M{p.meta};
-  const int c = blockIdx.x, hh = blockIdx.y;
-  if (c >= M.h(H_N_CHUNK)) return;
-  const int32_t* ch = M.chunk(c);
-  const int row0 = ch[C_ROW0], len = ch[C_LEN];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -141,21 +142,34 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   // block this kernel's allocation for good.
   hsd::pdl_trigger();
   hsd::pdl_wait();
+  const int n_items = M.h(H_N_CHUNK) * p.H;
+  // K, Q, V of item wi into the tiles, completing the next phase of bar_kq / bar_v (lane 0 of the copy warp)
+  auto load_item = [&](int wi) {
+    const int hq = wi % p.H, r0 = M.chunk(wi / p.H)[C_ROW0];
+    tc::mbar_expect_tx(&bar_kq, kTxKQ);
+    for (int h = 0; h < 2; ++h) {
+      tc::tma_load_3d(smem + kOffKQ + h * 16384, &tm_k, h * 64, hq, r0, &bar_kq);
+      tc::tma_load_3d(smem + kOffKQ + h * 16384 + 8192, &tm_q, h * 64, hq, r0, &bar_kq);
+    }
+    tc::mbar_expect_tx(&bar_v, kTxV);
+    for (int h = 0; h < 2; ++h) tc::tma_load_3d(smem + kOffV + h * 8192, &tm_v, h * 64, hq, r0, &bar_v);
+  };
+  bool ahead = false;  // (copy warp) the next item's loads are in flight
+  int it = 0;          // items taken by this CTA: the phases of its barriers
+  for (int w = (int)blockIdx.x; w < n_items; w += (int)gridDim.x, ++it) {
+  const int c = w / p.H, hh = w % p.H;
+  const int32_t* ch = M.chunk(c);
+  const int row0 = ch[C_ROW0], len = ch[C_LEN];
+  const uint32_t ph = (uint32_t)it & 1u;
+  bool item_ok = true;
 
   if (warp == kWarpCtl) {
     // ------------------------------------------------------- copies and MMAs
-    // (copies from lane 0; the MMAs from the converged warp: voted waits, one elected lane issues)
-    if (lane == 0) {
-      tc::mbar_expect_tx(&bar_kq, kTxKQ);
-      for (int h = 0; h < 2; ++h) {
-        tc::tma_load_3d(smem + kOffKQ + h * 16384, &tm_k, h * 64, hh, row0, &bar_kq);
-        tc::tma_load_3d(smem + kOffKQ + h * 16384 + 8192, &tm_q, h * 64, hh, row0, &bar_kq);
-      }
-      tc::mbar_expect_tx(&bar_v, kTxV);
-      for (int h = 0; h < 2; ++h) tc::tma_load_3d(smem + kOffV + h * 8192, &tm_v, h * 64, hh, row0, &bar_v);
-    }
+    // (copies from lane 0; the MMAs from the converged warp: voted waits, one elected lane issues; the
+    // first item's tiles are loaded here, every later one's by the item before)
+    if (it == 0 && lane == 0) load_item(w);
     __syncwarp();
-    bool ok = __all_sync(~0u, tc::mbar_wait(&bar_kq, 0, kWaitCycles));
+    bool ok = __all_sync(~0u, tc::mbar_wait(&bar_kq, ph, kWaitCycles));
     int issued = 0;  // MMA groups committed: [K; Q] K^T, W^T, Ut^T
     if (ok) {
       tc::fence_after_sync();
@@ -169,8 +183,8 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       issued = 1;
     }
     // W^T from the K rows and Ut^T from V, back to back once both T operands are written
-    if (ok) ok = __all_sync(~0u, tc::mbar_wait(&bar_b1, 0, kWaitCycles)) &&
-                 __all_sync(~0u, tc::mbar_wait(&bar_v, 0, kWaitCycles));
+    if (ok) ok = __all_sync(~0u, tc::mbar_wait(&bar_b1, ph, kWaitCycles)) &&
+                 __all_sync(~0u, tc::mbar_wait(&bar_v, ph, kWaitCycles));
     for (int pass = 0; pass < 2 && ok; ++pass) {
       if (pass == 0) tc::fence_after_sync();
       const uint64_t da = pass == 0 ? tc::sdesc_sw128(tc::smem_u32(smem + kOffKQ), 16384, 1024)
@@ -191,12 +205,17 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
     // drain: every copy into this CTA's shared memory has landed and every MMA issued has completed
     // before the block may exit (bounded as every wait)
     if (lane == 0) {
-      tc::mbar_wait(&bar_kq, 0, kWaitCycles);
-      tc::mbar_wait(&bar_v, 0, kWaitCycles);
+      tc::mbar_wait(&bar_kq, ph, kWaitCycles);
+      tc::mbar_wait(&bar_v, ph, kWaitCycles);
     }
     uint64_t* last = issued == 3 ? &bar_w2 : issued == 2 ? &bar_w1 : issued == 1 ? &bar_d : nullptr;
-    if (last) __all_sync(~0u, tc::mbar_wait(last, 0, kWaitCycles));
+    if (last) ok = __all_sync(~0u, tc::mbar_wait(last, ph, kWaitCycles)) && ok;
+    // the MMAs that read K, V and the K rows are complete, both phases of the tiles' barriers are seen, and
+    // the K' stores have read the Q rows (before bar_b1): the next item's tiles may be loaded
+    ahead = ok && w + (int)gridDim.x < n_items;
+    if (ahead && lane == 0) load_item(w + (int)gridDim.x);
     __syncwarp();
+    item_ok = ok;
   } else {
     // -------------------------------------------------------------- rows
     // (shared memory through explicit ld/st.shared on 32-bit addresses: sb = the aligned base)
@@ -231,7 +250,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       gd[64 + r] = r < len ? expf(gC - gt) : 0.f;
       if (r == 0) gd[128] = expf(gC);
     }
-    bool ok = __all_sync(~0u, tc::mbar_wait(&bar_d, 0, kWaitCycles));
+    bool ok = __all_sync(~0u, tc::mbar_wait(&bar_d, ph, kWaitCycles));
     if (ok) {
       // half a row of A (lanes 0..63, fp32, swizzled, in shared memory) or of P (lanes 64..127, bf16, its
       // swizzled 128-byte row of the workspace image)
@@ -372,7 +391,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       // ================================ K' = diag(e^{g_C - g}) K over the Q rows (warps 4..7, barrier 3)
       // thread = (row t, slab h); the row's eight 16-byte pieces in an order rotated by the row, so the
       // lanes of a warp touch different banks
-      ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_kq, 0, kWaitCycles));  // (makes the TMA-written tile visible)
+      ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_kq, ph, kWaitCycles));  // (makes the TMA-written tile visible)
       if (ok) {
         const int t = (r - 128) & 63, h = (r - 128) >> 6;
         const float dk = t < len ? expf(gC - gsh[t]) : 0.f;
@@ -486,8 +505,9 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       }
       tc::fence_proxy_async_smem();
     };
+    if (r == 128) tc::bulk_wait_read_all();  // the K' stores have read the Q rows: they are the next item's
     tc::mbar_arrive(&bar_b1);
-    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w1, 0, kWaitCycles));
+    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w1, ph, kWaitCycles));
     if (ok) {
       tc::fence_after_sync();
       image_out(kTW, kOffB);  // W^T image over its (read) operand
@@ -497,7 +517,7 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       tc::bulk_store(wsi + gdnws::kW, smem + kOffB, 16384);
       tc::bulk_commit();
     }
-    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w2, 0, kWaitCycles));
+    ok = ok && __all_sync(~0u, tc::mbar_wait(&bar_w2, ph, kWaitCycles));
     if (ok) {
       tc::fence_after_sync();
       image_out(kTU, kOffT);  // Ut^T image over Tt
@@ -510,12 +530,22 @@ gdn_chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       }
       tc::bulk_wait_read_all();  // the images may be released once read; the writes finish on their own
     }
-    if (r == 128) tc::bulk_wait_read_all();  // the K' stores
     if (!ok && lane == 0) hsd::set_status(p.status, HS_DEV_TIMEOUT);
+    item_ok = ok;
   }
+  // every MMA of the item is complete and its bulk stores have read shared memory (a wait that ran out
+  // anywhere stops every thread here, once the copies already issued for the next item have landed)
   tc::fence_before_sync();
-  __syncthreads();
+  const bool stop = __syncthreads_or(!item_ok);
   tc::fence_after_sync();
+  if (stop) {
+    if (warp == kWarpCtl && lane == 0 && ahead) {
+      tc::mbar_wait(&bar_kq, ph ^ 1u, kWaitCycles);
+      tc::mbar_wait(&bar_v, ph ^ 1u, kWaitCycles);
+    }
+    break;
+  }
+  }
   if (warp == kWarpCtl) tc::tmem_dealloc(tmem, 256);
 }
 
@@ -568,8 +598,16 @@ hs_status hs_gdn_prep_tc_launch(const hs_round_caps* caps, const int32_t* meta, 
     configured[slot].store(true);
   }
   Prm prm{meta, H, alpha, beta, ws, status};
-  hsd::launch_pdl(gdn_chunk_prep_tc_kernel, dim3(caps->max_chunks, H), dim3(kThreads), kSmem + 1024, st, mq, mk, mv,
-                  prm);
+  static std::atomic<int> sm_count[hsd::kMaxDevices];  // per device, 0 until read
+  int n_sm = sm_count[slot].load();
+  if (n_sm <= 0) {
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, slot) != cudaSuccess || n_sm <= 0)
+      return hs::fail(HS_ECUDA, "gdn_chunk_prep_tc: cannot read the SM count");
+    sm_count[slot].store(n_sm);
+  }
+  const long long items = (long long)caps->max_chunks * H;
+  const int grid = (int)(items < 2LL * n_sm ? items : 2LL * n_sm);  // persistent: two CTAs per SM
+  hsd::launch_pdl(gdn_chunk_prep_tc_kernel, dim3(grid), dim3(kThreads), kSmem + 1024, st, mq, mk, mv, prm);
   HS_LAUNCH_CHECK("gdn_chunk_prep_tc");
   return HS_OK;
 }
