@@ -20,6 +20,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -68,10 +69,26 @@ extern "C" hs_status hs_check_status(const int32_t* w) {
 struct hs_page_pool {
   int32_t n_pages = 0, page_size = 0;
   std::vector<int32_t> ref;
-  std::vector<int32_t> free_list;  // stack; pops yield ascending ids on a fresh pool
+  // Free pages, highest id first, so that an allocation takes the lowest free ids in ascending order: a
+  // node's pages form ascending runs wherever the free pages do, and the attention kernel moves a 128-key
+  // block of consecutive pages as one box.  Pages freed since the last allocation wait in `returned` and
+  // are merged in (sorted) before the next one.
+  std::vector<int32_t> free_list;
+  std::vector<int32_t> returned;
 
+  int32_t n_free() const { return (int32_t)(free_list.size() + returned.size()); }
+  void settle() {
+    if (returned.empty()) return;
+    std::sort(returned.begin(), returned.end(), std::greater<int32_t>());
+    std::vector<int32_t> merged(free_list.size() + returned.size());
+    std::merge(free_list.begin(), free_list.end(), returned.begin(), returned.end(), merged.begin(),
+               std::greater<int32_t>());
+    free_list.swap(merged);
+    returned.clear();
+  }
   bool alloc(int32_t n, std::vector<int32_t>& out) {
-    if ((int32_t)free_list.size() < n) return false;
+    if (n_free() < n) return false;
+    settle();
     for (int32_t i = 0; i < n; ++i) {
       int32_t p = free_list.back();
       free_list.pop_back();
@@ -82,7 +99,7 @@ struct hs_page_pool {
   }
   void decref(int32_t p) {
     if (p < 0 || p >= n_pages || ref[p] <= 0) return;
-    if (--ref[p] == 0) free_list.push_back(p);
+    if (--ref[p] == 0) returned.push_back(p);
   }
 };
 
@@ -104,8 +121,8 @@ extern "C" void hs_page_pool_destroy(hs_page_pool* p) { delete p; }
 
 extern "C" hs_status hs_page_pool_stats(const hs_page_pool* p, int32_t* n_free, int32_t* n_live) {
   HS_CHECK_ARG(p, "null pool");
-  if (n_free) *n_free = (int32_t)p->free_list.size();
-  if (n_live) *n_live = p->n_pages - (int32_t)p->free_list.size();
+  if (n_free) *n_free = p->n_free();
+  if (n_live) *n_live = p->n_pages - p->n_free();
   return HS_OK;
 }
 
@@ -400,8 +417,8 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
       for (int32_t p : s.hist_pages)
         if (p < 0 || p >= pool->n_pages || pool->ref[p] <= 0)
           return hs::fail(HS_EINVAL, "history page %d is not live in the pool", p);
-    if (n_own_pages > (int64_t)pool->free_list.size())
-      return hs::fail(HS_ENOPAGES, "need %lld pages, %d free", (long long)n_own_pages, (int)pool->free_list.size());
+    if (n_own_pages > (int64_t)pool->n_free())
+      return hs::fail(HS_ENOPAGES, "need %lld pages, %d free", (long long)n_own_pages, (int)pool->n_free());
   }
 
   std::vector<int32_t> page_ref;
@@ -719,8 +736,8 @@ extern "C" hs_status hs_round_finalize(hs_round* r, hs_page_pool* pool, int32_t 
   std::vector<int32_t> allocated;
   hs_status st = build(r, pool, temp_slot0, n_temp_slots, allocated);
   if (st != HS_OK) {
-    if (pool)  // in reverse, so that the free list is restored in its old order
-      for (auto it = allocated.rbegin(); it != allocated.rend(); ++it) pool->decref(*it);
+    if (pool)  // (the free list is kept sorted: it returns to its old order)
+      for (int32_t pg : allocated) pool->decref(pg);
     for (auto& s : r->segs) s.pages.clear();
     return st;
   }

@@ -94,6 +94,10 @@ hs_status hs_round_caps_for(int32_t n_tokens, int32_t n_segments, int32_t n_leve
 /* ForkServe README, "Copy-on-write context tree": a node's writes allocate  */
 /* pages for its own tokens; children alias ancestors' pages; abort decrefs. */
 /* Device pools are K and V arrays [Hkv][n_pages][page_size][d].             */
+/* Allocation takes the lowest free page ids, in ascending order, whatever   */
+/* order pages were freed in: a node's pages are consecutive wherever the    */
+/* free pages are, which the attention kernel's block copies rely on for     */
+/* speed (never for correctness).                                            */
 /* ------------------------------------------------------------------------ */
 typedef struct hs_page_pool hs_page_pool;
 

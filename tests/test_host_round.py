@@ -567,3 +567,33 @@ def test_split_at_requests():
     with pytest.raises(_lib.HsError) as e:
         rounds.split_at_requests(tree, api.round_caps_for(1000, 120, 2))
     assert e.value.code == _lib.HS_ECAPACITY
+
+
+def test_pool_allocates_lowest_free_pages_ascending():
+    """Whatever order rounds release their pages in, the next allocation takes the lowest free ids in
+    ascending order, so a node's pages stay consecutive across rounds (ForkServe README, "Copy-on-write
+    context tree": pages are reused once nothing references them)."""
+    pool = api.PagePool(300)
+    tree = synth.Tree([synth.fork_tree(1000, [40, 17, 64])])
+    first = None
+    for step in range(4):
+        R, seg_of = rounds.build_round(tree, pool)
+        pages = [list(R.segment_pages(s)) for s in range(R.info().n_segments)]
+        flat = [p for ps in pages for p in ps]
+        assert flat == sorted(flat) and flat == list(range(len(flat)))  # consecutive from page 0
+        if first is None:
+            first = pages
+        assert pages == first
+        R.release(pool)
+        assert pool.stats() == (300, 0)
+    # interleaved lifetimes: pages freed out of order are handed out lowest first
+    R1, _ = rounds.build_round(tree, pool)
+    R2, _ = rounds.build_round(tree, pool)
+    n1 = pool.stats()[1] // 2
+    R1.release(pool)
+    R3, _ = rounds.build_round(tree, pool)
+    flat3 = [p for s in range(R3.info().n_segments) for p in R3.segment_pages(s)]
+    assert flat3 == list(range(n1))
+    R2.release(pool)
+    R3.release(pool)
+    assert pool.stats() == (300, 0)
