@@ -622,7 +622,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tc::mbar_init(&bar_ve[s], 2);
       for (int h = 0; h < 2; ++h) {
         tc::mbar_init(&bar_sf[s][h], 1);    // [X][h]: S_X of a block's key half h done
-        tc::mbar_init(&bar_pf[s][h], 128);  // [X][h]: P_X of key half h written
+        tc::mbar_init(&bar_pf[s][h], 4);  // [X][h]: P_X of key half h written (one arrival per softmax warp)
       }
       tc::mbar_init(&bar_pv[s], 1);   // [X]: P.V_X of a key half done
     }
@@ -1018,7 +1018,7 @@ fork_attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
           tc::tmem_wait_st();
           tc::fence_before_sync();
-          tc::mbar_arrive(&bar_pf[x][h]);
+          tc::mbar_arrive_warp(&bar_pf[x][h]);
         }
         ++j;
         ++jg;

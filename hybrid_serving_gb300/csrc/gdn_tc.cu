@@ -238,13 +238,13 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       tc::mbar_init(&bar_full[s], 1);
       tc::mbar_init(&bar_empty[s], C::kEmptyCount);
     }
-    tc::mbar_init(&bar_s, 128);
-    tc::mbar_init(&bar_u, 128);
-    tc::mbar_init(&bar_of, 128);
+    tc::mbar_init(&bar_s, 4);  // (the four row warps, one arrival each; likewise every count of 4 below)
+    tc::mbar_init(&bar_u, 4);
+    tc::mbar_init(&bar_of, 4);
     tc::mbar_init(&bar_d1, 1);
     for (int c = 0; c < 2; ++c) {
-      tc::mbar_init(&bar_sc[c], 128);
-      tc::mbar_init(&bar_uc[c], 128);
+      tc::mbar_init(&bar_sc[c], 4);
+      tc::mbar_init(&bar_uc[c], 4);
       tc::mbar_init(&bar_d1c[c], 1);
       tc::mbar_init(&bar_d4c[c], 1);
     }
@@ -254,7 +254,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     tc::mbar_init(&bar_done, 1);
     tc::mbar_init(&bar_done2, 1);
     for (int b = 0; b < 3; ++b) tc::mbar_init(&bar_cb[b], 1);  // combine buffers (M or N images) filled
-    tc::mbar_init(&bar_ps, 128);
+    tc::mbar_init(&bar_ps, 4);
     tc::mbar_init(&bar_pd, 1);
     tc::fence_mbar_init();
   }
@@ -518,7 +518,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      for (int c = 0; c < nch; ++c) tc::mbar_arrive(&bar_sc[c]);
+      for (int c = 0; c < nch; ++c) tc::mbar_arrive_warp(&bar_sc[c]);
       for (int ci = 0; ci < n_c && ok; ++ci) {
         const int s = ci % C::kStages;
         const uint8_t* sb = stage(ci);
@@ -563,7 +563,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           }
           tc::tmem_wait_st();
           tc::fence_before_sync();
-          tc::mbar_arrive(&bar_uc[c]);
+          tc::mbar_arrive_warp(&bar_uc[c]);
         }
         if (!ok) break;
         __syncwarp();
@@ -578,7 +578,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
           state_to_bf16(tmem + lb + 256 * c + C::kTS32, tmem + lb + 256 * c + C::kTS16);
           tc::tmem_wait_st();
           tc::fence_before_sync();
-          tc::mbar_arrive(&bar_sc[c]);
+          tc::mbar_arrive_warp(&bar_sc[c]);
         }
       }
       if (!ok) {
@@ -714,7 +714,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bar_ps);
+      tc::mbar_arrive_warp(&bar_ps);
       if (!__all_sync(~0u, tc::mbar_wait_spin(&bar_pd, (q - 1) & 1, kWaitCycles))) {
         ok = false;
         break;
@@ -725,7 +725,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
     state_to_bf16(tmem + lb + C::kTS32, tmem + lb + C::kTS16);
     tc::tmem_wait_st();
     tc::fence_before_sync();
-    tc::mbar_arrive(&bar_s);
+    tc::mbar_arrive_warp(&bar_s);
     for (int ci = 0; ci < n_c; ++ci) {
       const int s = ci % C::kStages;
       const uint8_t* sb = stage(ci);
@@ -771,7 +771,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bar_u);
+      tc::mbar_arrive_warp(&bar_u);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar_empty[s]);  // Ut and the decay block are read
       // D4 done (new S), D2 done (the bf16 S may be overwritten)
@@ -785,7 +785,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       state_to_bf16(tmem + lb + C::kTS32, tmem + lb + C::kTS16);
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bar_s);
+      tc::mbar_arrive_warp(&bar_s);
     }
     if (!ok) {
       fail();
@@ -821,7 +821,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       }
       tc::fence_after_sync();
       if (!outputs) {  // no D2, D3 were formed: keep the hand-offs only
-        tc::mbar_arrive(&bar_of);
+        tc::mbar_arrive_warp(&bar_of);
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bar_empty[s]);
         continue;
@@ -837,7 +837,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const Prm p) {
       tc::tmem_ld32(tmem + lb + C::kTD3 + 32, *reinterpret_cast<uint32_t(*)[32]>(d3 + 32));
       tc::tmem_wait_ld();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bar_of);  // D2, D3 may be overwritten
+      tc::mbar_arrive_warp(&bar_of);  // D2, D3 may be overwritten
       float o[64];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
