@@ -79,6 +79,34 @@ def test_resumed_history_bf16():
     assert max_abs(got, ref) <= TOL_BF16
 
 
+def test_fragmented_pool_pages():
+    """A round whose pages are scattered over the pool (every other page held by an earlier round), so no
+    128-key block has consecutive pages and the kernel copies each page on its own: every row against its
+    isolated pass, and bit for bit equal to the same round on consecutive pages."""
+    from hybrid_serving_gb300 import rounds
+    tree = synth.Tree([synth.fork_tree(1024, [40, 64, 17])])
+    inp = synth.attn_inputs(tree, 8, 2, 128, seed=1500, bf16=True)
+    n_pages = 512
+    pool = api.PagePool(n_pages)
+    filler = synth.Tree([synth.fork_tree(16, [16] * 150)])  # one page per node
+    Rf, seg_f = rounds.build_round(filler, pool)
+    Rf.release(pool, keep=list(range(0, Rf.info().n_segments, 2)))  # every other page stays held
+    kp = torch.zeros((2, n_pages, 16, 128), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    run = AttnRun(tree, inp, torch.bfloat16, pool=pool, k_pages=kp, v_pages=vp).run()
+    api.check_status(run.status)
+    trunk_pages = run.R.segment_pages(run.seg_of[(0, 0)])
+    assert all(b != a + 1 for a, b in zip(trunk_pages, trunk_pages[1:]))  # no two consecutive
+    got = run.outputs()
+    ref = forward.attention_tree(tree, inp, 1 / math.sqrt(128))
+    err = max_abs(got, ref)
+    print(f"[margin] attention on scattered pages max-abs {err:.3e} (bar 2e-2)")
+    assert err <= TOL_BF16
+    dense = AttnRun(tree, inp, torch.bfloat16).run()  # fresh pool: consecutive pages
+    api.check_status(dense.status)
+    assert torch.equal(run.out, dense.out)
+
+
 def test_full_size_all_rows_and_choices():
     """The attention workload at full size (trunk 4096, 8 branches of
     U[16,64], GQA 32/8, d=128, bf16): every trunk row and every row of every
