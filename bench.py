@@ -41,12 +41,12 @@ N_OPT = 4
 METRIC = "tree-prefill tokens/s on 1 GB300 (ForkAttn + GDN); % of tensor/HBM roofline"
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of this
 # bench's workload, valid only while every listed kernel source still has the hash it was captured with.
-# fork_attn: the mean of three captures of one launch; gdn_fork: the sum over the launches of one call
-# (chunk-local pass, two state passes per tree level).
+# fork_attn: one capture of one launch; gdn_fork: the sum over the launches of one call (chunk-local pass,
+# two state passes per tree level).
 NCU_TRAFFIC = {
-    "fork_attn": ({"hybrid_serving_gb300/csrc/fork_attn_tc.cu": "fdc41de45030cdd0"}, 56.45e6),
+    "fork_attn": ({"hybrid_serving_gb300/csrc/fork_attn_tc.cu": "81576301c453ee55"}, 56.56e6),
     "gdn_fork": ({"hybrid_serving_gb300/csrc/gdn_prep_tc.cu": "81dca39759adefd7",
-                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "6b88e2b513537d34"}, 509.09e6),
+                  "hybrid_serving_gb300/csrc/gdn_tc.cu": "bb142092ba206c0c"}, 508.80e6),
 }
 
 
