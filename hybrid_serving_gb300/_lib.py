@@ -92,6 +92,7 @@ _SIGS = {
     "hs_choice_logprobs": (I32, [CAPSP, P, I32, P, C.c_int64, I32, P, I32, P, P, P]),
     "hs_round_set_conv_window": (I32, [P, I32, I32]),
     "hs_gemm_bf16": (I32, [I32, I32, I32, P, C.c_int64, P, C.c_int64, P, C.c_int64, P, C.c_int64, I32, P, P]),
+    "hs_gemm_bf16_swiglu": (I32, [I32, I32, I32, P, C.c_int64, P, C.c_int64, P, C.c_int64, P, P]),
     "hs_embed": (I32, [P, I32, P, I32, I32, P, I32, P, P]),
     "hs_rmsnorm": (I32, [P, C.c_int64, I32, I32, I32, P, C.c_float, P, C.c_int64, I32, P]),
     "hs_rope_table": (I32, [P, I32, I32, C.c_double]),

@@ -23,6 +23,11 @@
 // MMAs of the next tile fill the other accumulator.  Waits are bounded and
 // report HS_DEV_TIMEOUT through the status word; the epilogue warps take
 // every decision together, so a timeout never leaves one at a barrier.
+//
+// The SwiGLU variant (kGlu) takes B's rows in blocks of 128 gate rows followed
+// by the 128 up rows of the same output columns, so a 256-wide tile holds both
+// halves of 128 outputs: its epilogue writes silu(gate) * up, computed in fp32
+// from the two accumulator halves and rounded to bf16 once.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -53,29 +58,7 @@ struct GemmParams {
   int32_t* status;
 };
 
-// eight accumulator values (+ the residual's eight) into C
-__device__ __forceinline__ void epi8(float (&f)[8], const __nv_bfloat16* res, __nv_bfloat16* dst) {
-  if (res) {
-    float rr[8];
-    hsd::cvt16(*reinterpret_cast<const float4*>(res), rr, __nv_bfloat16());
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] += rr[i];
-  }
-  uint4 o;
-  o.x = tc::pack_bf16x2(f[0], f[1]);
-  o.y = tc::pack_bf16x2(f[2], f[3]);
-  o.z = tc::pack_bf16x2(f[4], f[5]);
-  o.w = tc::pack_bf16x2(f[6], f[7]);
-  *reinterpret_cast<uint4*>(dst) = o;
-}
-__device__ __forceinline__ void epi8(float (&f)[8], const float* res, float* dst) {
-  if (res) {
-    const float4 a = reinterpret_cast<const float4*>(res)[0], b = reinterpret_cast<const float4*>(res)[1];
-    f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w; f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
-  }
-  reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
-  reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
-}
+__device__ __forceinline__ float silu_f(float x) { return x / (1.f + expf(-x)); }
 
 // 64 bytes of a row: 16 fp32 or 32 bf16 values
 template <typename CT>
@@ -123,7 +106,7 @@ struct Piece<__nv_bfloat16> {
   }
 };
 
-template <typename CT>
+template <typename CT, bool kGlu>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_r,
@@ -243,7 +226,9 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5, barrier 1)
     using PC = Piece<CT>;
-    constexpr int kPieces = BN / PC::kCols;  // per tile (even)
+    static_assert(!kGlu || sizeof(CT) == 2, "the SwiGLU epilogue writes bf16");
+    constexpr int kOutCols = kGlu ? BN / 2 : BN;          // output columns per tile
+    constexpr int kPieces = kOutCols / PC::kCols;          // per tile (even)
     const int quarter = warp % 4;            // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
     const bool issuer = r == 0;
@@ -257,7 +242,8 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       if (!has_r || j >= n_mine) return;
       const int t = (int)blockIdx.x + j * (int)gridDim.x;
       tc::mbar_expect_tx(&bar_r[g & 1], kStg);
-      tc::tma_load_2d(rst + (g & 1) * kStg, &tm_r, (t % n_tn) * BN + c * PC::kCols, (t / n_tn) * BM, &bar_r[g & 1]);
+      tc::tma_load_2d(rst + (g & 1) * kStg, &tm_r, (t % n_tn) * kOutCols + c * PC::kCols, (t / n_tn) * BM,
+                      &bar_r[g & 1]);
     };
     if (issuer) {
       tc::prefetch_tmap(&tm_c);
@@ -273,7 +259,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
       if (!epi_go) break;
       const int b = j & 1;
       const int t = (int)blockIdx.x + j * (int)gridDim.x;
-      const int m0 = (t / n_tn) * BM, n0 = (t % n_tn) * BN;
+      const int m0 = (t / n_tn) * BM, n0 = (t % n_tn) * kOutCols;  // (n0: the tile's first output column)
       if (!__all_sync(~0u, tc::mbar_wait(&bar_acc[b], (j >> 1) & 1, kWaitCycles))) {  // warp-wide: ld is collective
         hsd::set_status(p.status, HS_DEV_TIMEOUT);
         atomicExch(&abort_flag, 1);  // (this tile goes on with whatever it holds; the next one stops)
@@ -282,8 +268,9 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 #pragma unroll 1
       for (int c = 0; c < kPieces; ++c, ++stored) {
         const int pb = stored & 1;
-        uint32_t v[32];
+        uint32_t v[32], vu[32];
         PC::load(tmem + lanes + 256 * b + c * PC::kCols, v);
+        if constexpr (kGlu) tc::tmem_ld32(tmem + lanes + 256 * b + BN / 2 + c * PC::kCols, vu);  // the up half
         tc::tmem_wait_ld();
         if (c == kPieces - 1) {  // the accumulator is read out: the MMAs of tile j + 2 may start
           tc::fence_before_sync();
@@ -295,11 +282,15 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         }
         if (issuer && stored >= 2) tc::bulk_wait_read_but1();  // the store of piece stored - 2 has read cst[pb]
         tc::named_sync(1, 128);
+        if constexpr (kGlu) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(silu_f(__uint_as_float(v[i])) * __uint_as_float(vu[i]));
+        }
         PC::put(v, has_r ? rst + pb * kStg + r * 64 : nullptr, cst + pb * kStg + r * 64);
         tc::fence_proxy_async_smem();
         tc::named_sync(1, 128);
         if (issuer) {
-          if (n0 + c * PC::kCols < p.N) {  // (a piece wholly past N is not stored)
+          if (n0 + c * PC::kCols < (kGlu ? p.N / 2 : p.N)) {  // (a piece wholly past the output is not stored)
             tc::tma_store_2d(&tm_c, n0 + c * PC::kCols, m0, cst + pb * kStg);
             tc::bulk_commit();
           }
@@ -362,15 +353,15 @@ bool map_piece(CUtensorMap* m, const void* base, long long rows, long long cols,
 
 }  // namespace
 
-extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B,
-                                  int64_t ldb, void* C, int64_t ldc, const void* R, int64_t ldr, hs_dtype c_dtype,
-                                  int32_t* dev_status, void* stream) {
-  HS_CHECK_ARG(A && B && C, "null argument");
-  if (c_dtype != HS_BF16 && c_dtype != HS_F32) return hs::fail(HS_EUNSUPPORTED, "gemm: C dtype %d", c_dtype);
-  HS_CHECK_ARG(M >= 0 && N > 0 && K > 0, "bad shape %d x %d x %d", M, N, K);
-  if (N % 128 != 0 || K % BK != 0)
-    return hs::fail(HS_EUNSUPPORTED, "N (%d) must be a multiple of 128 and K (%d) of %d", N, K, BK);
-  HS_CHECK_ARG(lda >= K && ldb >= K && ldc >= N && (!R || ldr >= N), "leading dimensions too small");
+namespace {
+
+// the launch shared by both entry points: C[M, Nout] from A[M, K] and B[N, K] (Nout = N, or N / 2 with kGlu)
+template <bool kGlu>
+hs_status gemm_launch(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      void* C, int64_t ldc, const void* R, int64_t ldr, hs_dtype c_dtype, int32_t* dev_status,
+                      void* stream) {
+  const int n_out = kGlu ? N / 2 : N;
+  HS_CHECK_ARG(lda >= K && ldb >= K && ldc >= n_out && (!R || ldr >= n_out), "leading dimensions too small");
   HS_CHECK_ARG(lda % 8 == 0 && ldb % 8 == 0 && ldc % 8 == 0 && (!R || ldr % 8 == 0),
                "leading dimensions must be multiples of 8 elements");
   HS_CHECK_ARG((((uintptr_t)A | (uintptr_t)B | (uintptr_t)C | (uintptr_t)R) & 15) == 0,
@@ -381,17 +372,17 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   CUtensorMap ma, mb;
   CUtensorMap mc, mr;
   const bool f32 = c_dtype == HS_F32;
-  if (!map_2d(&ma, A, M, K, lda, BM) || !map_2d(&mb, B, N, K, ldb, BN) || !map_piece(&mc, C, M, N, ldc, f32) ||
-      !map_piece(&mr, R ? R : C, M, N, R ? ldr : ldc, f32))
+  if (!map_2d(&ma, A, M, K, lda, BM) || !map_2d(&mb, B, N, K, ldb, BN) || !map_piece(&mc, C, M, n_out, ldc, f32) ||
+      !map_piece(&mr, R ? R : C, M, n_out, R ? ldr : ldc, f32))
     return hs::fail(HS_ECUDA, "gemm: tensor map encoding failed");
   static std::atomic<bool> configured[hsd::kMaxDevices];  // zero-initialised: per device
   const int slot = hsd::device_slot();
   if (slot < 0) return hs::fail(HS_ECUDA, "gemm: no usable CUDA device");
   if (!configured[slot].load()) {
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<__nv_bfloat16, kGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmem + 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_bf16_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem + 1024) !=
-            cudaSuccess)
+        (!kGlu && cudaFuncSetAttribute(gemm_bf16_tc_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmem + 1024) != cudaSuccess))
       return hs::fail(HS_ECUDA, "gemm: cannot raise the shared-memory limit");
     configured[slot].store(true);
   }
@@ -404,13 +395,36 @@ extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A
   }
   const long long n_tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const dim3 grid((unsigned)(n_tiles < n_sm ? n_tiles : n_sm));  // persistent: one CTA per SM
-  if (c_dtype == HS_F32) {
+  if (!kGlu && c_dtype == HS_F32) {
     GemmParams<float> prm{M, N, K, (float*)C, ldc, (const float*)R, ldr, dev_status};
-    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, mc, mr, prm);
+    gemm_bf16_tc_kernel<float, false><<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, mc, mr, prm);
   } else {
     GemmParams<__nv_bfloat16> prm{M, N, K, (__nv_bfloat16*)C, ldc, (const __nv_bfloat16*)R, ldr, dev_status};
-    gemm_bf16_tc_kernel<<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, mc, mr, prm);
+    gemm_bf16_tc_kernel<__nv_bfloat16, kGlu><<<grid, kThreads, kSmem + 1024, (cudaStream_t)stream>>>(ma, mb, mc, mr,
+                                                                                                    prm);
   }
   HS_LAUNCH_CHECK("gemm_bf16");
   return HS_OK;
+}
+
+}  // namespace
+
+extern "C" hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B,
+                                  int64_t ldb, void* C, int64_t ldc, const void* R, int64_t ldr, hs_dtype c_dtype,
+                                  int32_t* dev_status, void* stream) {
+  HS_CHECK_ARG(A && B && C, "null argument");
+  if (c_dtype != HS_BF16 && c_dtype != HS_F32) return hs::fail(HS_EUNSUPPORTED, "gemm: C dtype %d", c_dtype);
+  HS_CHECK_ARG(M >= 0 && N > 0 && K > 0, "bad shape %d x %d x %d", M, N, K);
+  if (N % 128 != 0 || K % BK != 0)
+    return hs::fail(HS_EUNSUPPORTED, "N (%d) must be a multiple of 128 and K (%d) of %d", N, K, BK);
+  return gemm_launch<false>(M, N, K, A, lda, B, ldb, C, ldc, R, ldr, c_dtype, dev_status, stream);
+}
+
+extern "C" hs_status hs_gemm_bf16_swiglu(int32_t M, int32_t N2, int32_t K, const void* A, int64_t lda, const void* B,
+                                         int64_t ldb, void* C, int64_t ldc, int32_t* dev_status, void* stream) {
+  HS_CHECK_ARG(A && B && C, "null argument");
+  HS_CHECK_ARG(M >= 0 && N2 > 0 && K > 0, "bad shape %d x %d x %d", M, N2, K);
+  if (N2 % BN != 0 || K % BK != 0)
+    return hs::fail(HS_EUNSUPPORTED, "N2 (%d) must be a multiple of %d and K (%d) of %d", N2, BN, K, BK);
+  return gemm_launch<true>(M, N2, K, A, lda, B, ldb, C, ldc, nullptr, 0, HS_BF16, dev_status, stream);
 }

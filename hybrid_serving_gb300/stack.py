@@ -4,14 +4,16 @@ Sequencing and argument marshalling only: every operation is a kernel of
 libhsfork.so (tcgen05 GEMMs with the residual fused into the epilogue,
 RMSNorm, rotary embedding at standalone positions, the GDN front end with
 predecessors across the fork, ForkAttention, Gated DeltaNet fork prefill,
-SwiGLU, option log-probs).  PyTorch only allocates device memory.
+the gate/up GEMM with SwiGLU in its epilogue, option log-probs).  PyTorch
+only allocates device memory.
 
 Layer definition (the pages give none; see the oracle for the same text):
 pre-norm residual blocks of a token mixer ('A' attention, 'G' Gated
 DeltaNet) and a SwiGLU MLP; final RMSNorm; option logits against embedding
 rows of the option tokens (Flide section 3.1, Eq. 1).  The residual stream
 and the final norm's output are kept in fp32; every other tensor between
-operations is stored in bf16 (gates fp32).
+operations is stored in bf16 (gates fp32), but the gate/up products enter
+SwiGLU straight from the GEMM's fp32 accumulators.
 """
 from __future__ import annotations
 
@@ -60,6 +62,23 @@ def gemm(A, B, Cout, M: int, R=None, status=None, stream=None):
                            R.stride(0) if R is not None else 0, _dt(Cout), status.data_ptr(), _s(stream)))
 
 
+def gemm_swiglu(A, B_il, Cout, M: int, status=None, stream=None):
+    """Cout[:M] = silu(A[:M] @ Bg^T) * (A[:M] @ Bu^T) through hs_gemm_bf16_swiglu (B_il: the gate and up
+    weights interleaved in blocks of 128 rows, see interleave_gate_up)."""
+    N2, K = B_il.shape
+    check(lib.hs_gemm_bf16_swiglu(M, N2, K, A.data_ptr(), A.stride(0), B_il.data_ptr(), B_il.stride(0),
+                                  Cout.data_ptr(), Cout.stride(0), status.data_ptr(), _s(stream)))
+
+
+def interleave_gate_up(w: np.ndarray) -> np.ndarray:
+    """[gate rows; up rows] ([2F, K]) in the row order hs_gemm_bf16_swiglu takes: per block of 128 outputs,
+    its 128 gate rows, then its 128 up rows (a weight layout chosen at load time)."""
+    F2, K = w.shape
+    F = F2 // 2
+    assert F2 % 2 == 0 and F % 128 == 0, "ffn must be a multiple of 128"
+    return np.ascontiguousarray(w.reshape(2, F // 128, 128, K).transpose(1, 0, 2, 3).reshape(F2, K))
+
+
 def rmsnorm(x, T: int, dim: int, eps: float, out, stream=None):
     """out[:T] = RMSNorm(x[:T]) with unit weight (x and out bf16 or fp32)."""
     check(lib.hs_rmsnorm(x.data_ptr(), x.stride(0), _dt(x), T, dim, None, eps, out.data_ptr(), out.stride(0),
@@ -69,7 +88,8 @@ def rmsnorm(x, T: int, dim: int, eps: float, out, stream=None):
 class HybridStack:
     def __init__(self, shape: StackShape, weights: Dict[str, np.ndarray], max_pos: int):
         self.sh = shape
-        self.W = {k: torch.from_numpy(np.ascontiguousarray(v)).to(DEV).to(torch.bfloat16)
+        self.W = {k: torch.from_numpy(interleave_gate_up(np.asarray(v)) if k.endswith("wgu")
+                                      else np.ascontiguousarray(v)).to(DEV).to(torch.bfloat16)
                   for k, v in weights.items()}
         opt = np.asarray(weights["embed"], np.float32)[list(shape.option_ids)]
         self.opt = torch.from_numpy(np.ascontiguousarray(opt)).to(DEV)
@@ -90,7 +110,7 @@ class HybridStack:
         self.a = torch.zeros((Tcap, sh.hidden), dtype=bf, device=DEV)             # normed GEMM input
         self.hf = torch.zeros((Tcap, sh.hidden), dtype=torch.float32, device=DEV)  # final norm
         wp_n = max(v.shape[0] for k, v in self.W.items() if k.endswith("wp")) if self.n_gdn else 0
-        self.proj = torch.zeros((Tcap, max(wp_n, 2 * sh.ffn)), dtype=bf, device=DEV)
+        self.proj = torch.zeros((Tcap, max(wp_n, 8)), dtype=bf, device=DEV)  # the GDN projection
         self.q = torch.zeros((Tcap, sh.attn_hq, sh.head_d), dtype=bf, device=DEV)
         self.k = torch.zeros((Tcap, sh.attn_hkv, sh.head_d), dtype=bf, device=DEV)
         self.v = torch.zeros_like(self.k)
@@ -143,7 +163,6 @@ class HybridStack:
             hr = torch.empty((n_readout, sh.hidden), dtype=torch.float32, device=DEV)
             ar = torch.empty((n_readout, sh.hidden), dtype=torch.bfloat16, device=DEV)
             fr = torch.empty_like(hr)
-            gur = torch.empty((n_readout, 2 * sh.ffn), dtype=torch.bfloat16, device=DEV)
             mr = torch.empty((n_readout, sh.ffn), dtype=torch.bfloat16, device=DEV)
         last = len(sh.pattern) - 1
         row_bytes = sh.hidden * 4  # (fp32 rows)
@@ -197,17 +216,14 @@ class HybridStack:
                 check(lib.hs_copy_rows(self.h.data_ptr(), row_bytes, ro_rows.data_ptr(), hr.data_ptr(), row_bytes,
                                        ro_idx.data_ptr(), n_readout, row_bytes, s))
                 rmsnorm(hr, n_readout, sh.hidden, sh.eps, ar, stream)
-                gemm(ar, self.W[p + "wgu"], gur, n_readout, status=st, stream=stream)
-                check(lib.hs_swiglu(gur.data_ptr(), gur.stride(0), n_readout, sh.ffn, mr.data_ptr(), sh.ffn, s))
+                gemm_swiglu(ar, self.W[p + "wgu"], mr, n_readout, status=st, stream=stream)
                 gemm(mr, self.W[p + "wd"], hr, n_readout, R=hr, status=st, stream=stream)
                 rmsnorm(hr, n_readout, sh.hidden, sh.eps, fr, stream)
                 check(lib.hs_copy_rows(fr.data_ptr(), row_bytes, ro_idx.data_ptr(), self.hf.data_ptr(), row_bytes,
                                        ro_rows.data_ptr(), n_readout, row_bytes, s))
                 break
             rmsnorm(self.h, T, sh.hidden, sh.eps, self.a, stream)
-            gu = self.proj[:, :2 * sh.ffn]
-            gemm(self.a, self.W[p + "wgu"], gu, T, status=st, stream=stream)
-            check(lib.hs_swiglu(gu.data_ptr(), gu.stride(0), T, sh.ffn, self.m.data_ptr(), sh.ffn, s))
+            gemm_swiglu(self.a, self.W[p + "wgu"], self.m, T, status=st, stream=stream)
             gemm(self.m, self.W[p + "wd"], self.h, T, R=self.h, status=st, stream=stream)
         else:
             rmsnorm(self.h, T, sh.hidden, sh.eps, self.hf, stream)

@@ -367,14 +367,26 @@ hs_status hs_choice_logprobs(const hs_round_caps* caps, const void* dev_meta, hs
 /* ------------------------------------------------------------------------ */
 
 /* C[M,N] = A[M,K] . B[N,K]^T (+ R[M,N]), A and B bf16, fp32 accumulation in
- * a fixed order for any M (one 128x128 tile per CTA, no split-K; Flide
- * section 3.5); C and R in c_dtype (HS_BF16, rounded to nearest even, or
- * HS_F32: a residual stream kept in fp32).  N % 128 == 0, K % 64 == 0,
- * leading dimensions % 8 == 0, 16-byte aligned pointers.  R may be NULL; R
- * may alias C.  HS_EUNSUPPORTED: another c_dtype or shape. */
+ * a fixed order for any M (128x256 output tiles walked by persistent CTAs,
+ * the same K steps for every tile, no split-K; Flide section 3.5); C and R in
+ * c_dtype (HS_BF16, rounded to nearest even, or HS_F32: a residual stream
+ * kept in fp32).  N % 128 == 0, K % 64 == 0, leading dimensions % 8 == 0,
+ * 16-byte aligned pointers.  R may be NULL; R may alias C.
+ * HS_EUNSUPPORTED: another c_dtype or shape. */
 hs_status hs_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                        void* C, int64_t ldc, const void* R, int64_t ldr, hs_dtype c_dtype, int32_t* dev_status,
                        void* stream);
+/* The gate/up projection of a SwiGLU MLP with the activation applied in the
+ * GEMM's epilogue:
+ *   C[M, N2/2] = silu(A . Bg^T) * (A . Bu^T),   silu(x) = x / (1 + e^-x)
+ * B [N2, K] bf16 holds the two weight matrices interleaved in blocks of 128
+ * rows: rows 256j .. 256j+127 are Bg's rows 128j .. 128j+127 and rows
+ * 256j+128 .. 256j+255 are Bu's same rows.  Both products accumulate in fp32
+ * exactly as hs_gemm_bf16's do; silu and the product are taken in fp32 and
+ * rounded to bf16 once.  N2 % 256 == 0, K % 64 == 0, ldc >= N2/2; the other
+ * rules as for hs_gemm_bf16.  HS_EUNSUPPORTED: another shape. */
+hs_status hs_gemm_bf16_swiglu(int32_t M, int32_t N2, int32_t K, const void* A, int64_t lda, const void* B,
+                              int64_t ldb, void* C, int64_t ldc, int32_t* dev_status, void* stream);
 /* out[t] = table[ids[t]], table bf16 [vocab, dim], out in out_dtype (HS_BF16
  * or HS_F32) [T, dim] (ids: device int32 [T]; an id outside [0,vocab)
  * gives a zero row and HS_DEV_BAD_META). */

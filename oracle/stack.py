@@ -25,7 +25,9 @@ mixer followed by a SwiGLU MLP.
   rows of the option tokens (Flide section 3.1, Eq. 1).
 
 The model keeps its residual stream and the final norm's output in fp32 and
-stores every other tensor between operations in bf16 (the gates in fp32):
+stores every other tensor between operations in bf16 (the gates in fp32);
+the gate and up projections go into SwiGLU unrounded (the library applies
+SwiGLU to the fp32 accumulators of the projection that forms them):
 the oracle computes each operation in fp64 and rounds its stored result to
 the same precision at the same points, so that it defines the model itself.
 
@@ -139,7 +141,7 @@ def forward(cfg: StackConfig, W: Dict[str, np.ndarray], ids, rows=None, gemm_dty
             o = round_bf16(o)
             h = round_f32(h + mm(o.reshape(n, H * d), W[p + "wo"]))
         b = round_bf16(rmsnorm(h, cfg.eps))
-        gu = round_bf16(mm(b, W[p + "wgu"]))
+        gu = mm(b, W[p + "wgu"])
         F = cfg.ffn
         m = round_bf16(silu(gu[:, :F]) * gu[:, F:])
         h = round_f32(h + mm(m, W[p + "wd"]))

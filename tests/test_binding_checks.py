@@ -26,7 +26,7 @@ import harness  # noqa: E402
 DEVICE_CALLS = {"hs_fork_attn_prefill", "hs_kv_page_write", "hs_fork_attn", "hs_gdn_fork_prefill",
                 "hs_gdn_fork_prefill_noalloc", "hs_gdn_state_checkpoint", "hs_choice_logprobs",
                 "hs_round_upload", "hs_embed", "hs_rmsnorm", "hs_gemm_bf16", "hs_rope_apply", "hs_gdn_prep",
-                "hs_swiglu", "hs_copy_rows"}
+                "hs_swiglu", "hs_copy_rows", "hs_gemm_bf16_swiglu"}
 
 
 class Recorder:
