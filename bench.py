@@ -802,7 +802,7 @@ def run_reference(args):
 def profile_gemm():
     import torch
     from hybrid_serving_gb300 import api
-    from hybrid_serving_gb300.stack import gemm
+    from hybrid_serving_gb300.stack import gemm, gemm_swiglu
     M = 65536
     g = torch.Generator(device="cuda").manual_seed(7)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -815,6 +815,9 @@ def profile_gemm():
         gemm(A[:, :2048], Wgu, gu, M, status=st)
     for _ in range(3):
         gemm(A, Wd, h, M, R=h, status=st)
+    m = torch.empty(M, 4096, device="cuda", dtype=torch.bfloat16)
+    for _ in range(3):  # the same gate/up weights (any row order) with SwiGLU in the epilogue
+        gemm_swiglu(A[:, :2048], Wgu, m, M, status=st)
     torch.cuda.synchronize()
     api.check_status(st)
     print(f"profile gemm: device memory held {torch.cuda.max_memory_allocated() / 2**20:.0f} MiB", flush=True)
@@ -831,8 +834,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the resume / stack / agent-tree lines")
     ap.add_argument("--profile-gemm", action="store_true",
                     help="three launches of the hybrid stack's gate/up projection (M=65536, N=8192, K=2048, bf16 "
-                         "out) and three of its down projection with the fp32 residual (N=2048, K=4096): the "
-                         "case that ncu captures of the GEMM run (about 2 GB on the device)")
+                         "out), three of its down projection with the fp32 residual (N=2048, K=4096) and three "
+                         "of the gate/up projection with SwiGLU in the epilogue (4096 outputs): the case that "
+                         "ncu captures of the GEMM run (about 2.5 GB on the device)")
     ap.add_argument("--profile-case", action="store_true",
                     help="one input set, the warm-up steps only, no timing and no JSON line: the case that ncu "
                          "captures of single kernels run (a few hundred MB on the device)")
