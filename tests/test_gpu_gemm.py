@@ -119,3 +119,20 @@ def test_gemm_swiglu_refuses_bad_shapes():
     with pytest.raises(_lib.HsError) as e:
         gemm_swiglu(A, B, C, 8, status=st)
     assert e.value.code == _lib.HS_EUNSUPPORTED
+
+
+def test_standalone_swiglu_kernel():
+    """hs_swiglu (the unfused activation over a stored [T, 2F] gate | up tensor) against silu(g) * u in fp32
+    from the same bf16 inputs, each element within its bf16 rounding."""
+    from hybrid_serving_gb300._lib import check, lib
+    g = torch.Generator(device="cuda").manual_seed(13)
+    T, F = 333, 512
+    gu = (torch.randn(T, 2 * F, device="cuda", generator=g) * 3).to(torch.bfloat16)
+    out = torch.full((T, F), float("nan"), device="cuda", dtype=torch.bfloat16)
+    check(lib.hs_swiglu(gu.data_ptr(), gu.stride(0), T, F, out.data_ptr(), out.stride(0),
+                        torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    gt, up = gu[:, :F].float(), gu[:, F:].float()
+    want = gt * torch.sigmoid(gt) * up
+    err = (out.float() - want).abs()
+    assert bool((err <= 2.0 ** -8 * want.abs() + 1e-6).all()), float(err.max())
