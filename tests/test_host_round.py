@@ -597,3 +597,24 @@ def test_pool_allocates_lowest_free_pages_ascending():
     R2.release(pool)
     R3.release(pool)
     assert pool.stats() == (300, 0)
+
+
+def test_gate_up_interleave_and_swiglu_gemm_argument_checks():
+    """The gate/up weight layout of hs_gemm_bf16_swiglu (per 128 outputs: their gate rows, then their up rows),
+    and the entry point's refusals, which it decides before touching a device."""
+    import ctypes as C
+    from hybrid_serving_gb300.stack import interleave_gate_up
+    F, K = 384, 3
+    w = np.arange(2 * F * K, dtype=np.float64).reshape(2 * F, K)
+    il = interleave_gate_up(w)
+    for j in range(F // 128):
+        assert np.array_equal(il[256 * j:256 * j + 128], w[128 * j:128 * j + 128])          # gate rows
+        assert np.array_equal(il[256 * j + 128:256 * j + 256], w[F + 128 * j:F + 128 * j + 128])  # up rows
+    assert sorted(map(tuple, il)) == sorted(map(tuple, w))
+    buf = (C.c_uint8 * 4096)()
+    p = C.cast(buf, C.c_void_p)
+    lib = _lib.lib
+    assert lib.hs_gemm_bf16_swiglu(8, 384, 64, p, 64, p, 64, p, 192, None, None) == _lib.HS_EUNSUPPORTED  # N2 % 256
+    assert lib.hs_gemm_bf16_swiglu(8, 512, 48, p, 64, p, 64, p, 256, None, None) == _lib.HS_EUNSUPPORTED  # K % 64
+    assert lib.hs_gemm_bf16_swiglu(8, 512, 64, None, 64, p, 64, p, 256, None, None) == _lib.HS_EINVAL    # null A
+    assert lib.hs_gemm_bf16_swiglu(8, 512, 64, p, 64, p, 64, p, 128, None, None) == _lib.HS_EINVAL       # ldc < N2/2
