@@ -420,7 +420,8 @@ hs_status hs_gdn_prep(const hs_round_caps* caps, const void* dev_meta, const voi
                       const void* window, int64_t ldw, int32_t n_window_rows, const void* conv_w, int32_t h, int32_t d,
                       void* q, void* k, void* v, float* alpha, float* beta, int32_t* dev_status, void* stream);
 /* out[t, i] = silu(gu[t, i]) * gu[t, F + i]; bf16, F, ldg, ldo multiples
- * of 8, gu and out 16-byte aligned. */
+ * of 8, gu and out 16-byte aligned.  (The activation over a stored gate | up
+ * tensor; hs_gemm_bf16_swiglu applies it inside the projection instead.) */
 hs_status hs_swiglu(const void* gu, int64_t ldg, int32_t T, int32_t F, void* out, int64_t ldo, void* stream);
 /* dst row dst_rows[i] = src row src_rows[i] (device int32 row lists; row
  * strides lds, ldd and width_bytes in BYTES, multiples of 16; src and dst
