@@ -687,11 +687,18 @@ static hs_status build(hs_round* r, hs_page_pool* pool, int32_t temp0, int32_t n
     }
   }
   {
+    // a level's nodes, most chunks first (stream order among equals): the state pass hands its CTAs out
+    // in this order, so when a level needs more than one wave the short nodes fill the last one
     int32_t k = 0;
+    std::vector<int32_t> lev_ids;
     for (int32_t lev = 0; lev < n_levels; ++lev) {
       h[L.off_level + lev] = k;
+      lev_ids.clear();
       for (int32_t id : order)
-        if (S[id].level == lev) h[L.off_level_seg + k++] = id;
+        if (S[id].level == lev) lev_ids.push_back(id);
+      std::stable_sort(lev_ids.begin(), lev_ids.end(),
+                       [&](int32_t a, int32_t b) { return S[a].n_chunk > S[b].n_chunk; });
+      for (int32_t id : lev_ids) h[L.off_level_seg + k++] = id;
     }
     for (int32_t lev = n_levels; lev <= C.max_levels; ++lev) h[L.off_level + lev] = k;
   }
