@@ -618,3 +618,21 @@ def test_gate_up_interleave_and_swiglu_gemm_argument_checks():
     assert lib.hs_gemm_bf16_swiglu(8, 512, 48, p, 64, p, 64, p, 256, None, None) == _lib.HS_EUNSUPPORTED  # K % 64
     assert lib.hs_gemm_bf16_swiglu(8, 512, 64, None, 64, p, 64, p, 256, None, None) == _lib.HS_EINVAL    # null A
     assert lib.hs_gemm_bf16_swiglu(8, 512, 64, p, 64, p, 64, p, 128, None, None) == _lib.HS_EINVAL       # ldc < N2/2
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_level_lists_longest_first(seed):
+    """Each level's node list (the GDN state pass's task order) holds exactly that level's nodes, by chunk
+    count, most first, in stream order among equals."""
+    tree = _random_tree(4000 + seed)
+    R, seg_of, pool, b = make(tree)
+    segs = b.segs
+    n_lev = b.h("N_LEVEL")
+    lev_off = b.arr("OFF_LEVEL", n_lev + 1, 1)
+    lst = b.w[b.h("OFF_LEVEL_SEG"):b.h("OFF_LEVEL_SEG") + b.h("N_SEG")]
+    S_STREAM_OFF, S_LEVEL, S_N_CHUNK = 0, 5, 10
+    for lev in range(n_lev):
+        ids = [int(x) for x in lst[lev_off[lev]:lev_off[lev + 1]]]
+        assert sorted(ids) == [i for i in range(b.h("N_SEG")) if segs[i][S_LEVEL] == lev]
+        key = [(-int(segs[i][S_N_CHUNK]), int(segs[i][S_STREAM_OFF])) for i in ids]
+        assert key == sorted(key), (lev, key)
